@@ -1,0 +1,359 @@
+"""fp64 CPU oracle of the routed mixture-of-experts forward layer.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and its reference arm) may import this
+module. The CUDA library (``sparse_expert_router_gb300``) never imports, links
+or runs anything here, and nothing here imports from it. The two share only
+the seeded input generators of ``moe_workloads``.
+
+The layer, as the pages state it:
+  * "Marin 535B-A23B: the half of a training run nobody usually shows you",
+    section "What is actually being trained": every layer's MLP is a mixture of
+    384 routed experts of width 3,072, eight chosen per token, plus two shared
+    experts every token goes through; routed experts run in a 3,072-wide
+    latent: each token is projected down, normalised, sent to its experts and
+    projected back up after the weighted combine.
+  * "Marin Begins Open Training of a 535B-Parameter MoE Model", section 2: the
+    same, and the two shared experts process every token independently of the
+    routed path; the output is projected back to model width before it is
+    combined with the shared path.
+  * Teardown, section "The one knob nobody pinned": the router has a weight
+    and a bias.
+  * Teardown, section "A sphere for every matrix": expert banks are stacked
+    [experts, d_in, d_out].
+
+Readings taken where the pages are silent (each is listed in the design doc):
+  R1 the router reads the block input x (width d);
+  R2 routing is the top-k of the EXACT real-valued logits x.W_r + b of the
+     stored inputs, ties to the lowest expert index; indices are reported in
+     ascending expert order;
+  R3 gates are the softmax over the k selected logits (equal to the full
+     softmax renormalised over the selection);
+  R4 capacity C = ceil(cf * T * k / E), computed in integers from cf = num/den;
+     assignments of expert e beyond C, in token order, are dropped, contribute
+     nothing, and the other gates are NOT renormalised ("the token skips that
+     expert": teardown section "21% to 27% MFU without stopping the run";
+     open-training page section 2);
+  R5 RMSNorm h = z / sqrt(mean(z^2) + eps) * gamma, no bias;
+  R6 experts are SwiGLU: a = silu(h W1) * (h W3), o = a W2, silu(v) = v / (1 + e^-v)
+     computed exactly (the July summary records a ~2.6% mismatch caused by an
+     approximate fused SwiGLU epilogue);
+  R7 shared experts read x and are summed unweighted;
+  R8 y = c W_up + sum_s SwiGLU_s(x).
+
+All arithmetic is fp64 on exactly promoted inputs (bf16 and fp32 values are
+exact in fp64, and so is every product of two of them). Nothing is rounded
+to a lower precision anywhere in this module.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import torch
+
+F64 = torch.float64
+U64 = 2.0 ** -53          # unit roundoff of fp64
+
+
+def to64(t: torch.Tensor) -> torch.Tensor:
+    """Exact promotion of a stored bf16/fp32 tensor to fp64 on the CPU."""
+    return t.detach().to(device="cpu").to(F64)
+
+
+# ---------------------------------------------------------------- router ----
+
+def router_logits(x: torch.Tensor, w_router: torch.Tensor,
+                  b_router: Optional[torch.Tensor]) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Router logits l[t, e] = sum_i x[t, i] W_r[i, e] + b[e] in fp64, and a bound on their error.
+
+    Every product is exact in fp64, so the only error is the summation of d+1
+    terms, bounded for any summation order by gamma_{d+1} * sum|terms| with
+    gamma_n = n u / (1 - n u). The sum of |x_i||w_i| is bounded above by
+    Cauchy-Schwarz, ||x_t||_2 ||w_e||_2, itself inflated for its own rounding.
+    """
+    x64, w64 = to64(x), to64(w_router)
+    T, d = x64.shape
+    logits = x64 @ w64
+    babs = torch.zeros(w64.shape[1], dtype=F64)
+    if b_router is not None:
+        b64 = to64(b_router)
+        logits = logits + b64
+        babs = b64.abs()
+    n = d + 1
+    gamma = n * U64 / (1.0 - n * U64)
+    cs = x64.norm(dim=1, keepdim=True) * w64.norm(dim=0, keepdim=True)
+    bound = (2.0 * gamma) * (cs * (1.0 + 1e-12) + babs) + 1e-300
+    return logits, bound
+
+
+def exact_logit(x_row: Sequence[float], w_col: Sequence[float], b: float) -> Fraction:
+    """The exact rational value of one logit: sum of exact products plus the bias."""
+    acc = Fraction(b)
+    for xi, wi in zip(x_row, w_col):
+        if xi != 0.0 and wi != 0.0:
+            acc += Fraction(xi) * Fraction(wi)
+    return acc
+
+
+def topk_exact(logits: torch.Tensor, bound: torch.Tensor, k: int,
+               exact_fn) -> torch.Tensor:
+    """Per token, the k experts with the largest exact logits; ties to the lowest index.
+
+    The fp64 logits decide a token unless the k-th selected and some
+    unselected expert overlap within their error bounds; then every expert
+    that could still enter the top-k gets its exact value from
+    ``exact_fn(t, e)`` and the selection is re-taken on exact values.
+    Returns idx [T, k] int64 in ascending expert order (reading R2).
+    """
+    T, E = logits.shape
+    # descending by value; a stable sort keeps equal values in ascending index order
+    order = torch.sort(logits, dim=1, descending=True, stable=True).indices
+    sel = order[:, :k]
+    lo = (logits - bound).gather(1, sel).min(dim=1).values
+    if k < E:
+        hi = (logits + bound).gather(1, order[:, k:]).max(dim=1).values
+    else:
+        hi = torch.full((T,), -math.inf, dtype=F64)
+    out = sel.clone()
+    for t in torch.nonzero(lo <= hi).flatten().tolist():
+        cand = torch.nonzero(logits[t] + bound[t] >= lo[t]).flatten().tolist()
+        vals = {e: exact_fn(t, e) for e in cand}
+        ranked = sorted(cand, key=lambda e: (-vals[e], e))
+        out[t] = torch.tensor(ranked[:k])
+    return torch.sort(out, dim=1).values
+
+
+def route(x: torch.Tensor, w_router: torch.Tensor, b_router: Optional[torch.Tensor],
+          k: int) -> Dict[str, torch.Tensor]:
+    """Router: logits, exact top-k indices (ascending), renormalised softmax gates."""
+    logits, bound = router_logits(x, w_router, b_router)
+    xs = to64(x)
+    ws = to64(w_router)
+    bs = to64(b_router) if b_router is not None else torch.zeros(ws.shape[1], dtype=F64)
+
+    def exact_fn(t: int, e: int) -> Fraction:
+        return exact_logit(xs[t].tolist(), ws[:, e].tolist(), float(bs[e]))
+
+    idx = topk_exact(logits, bound, k, exact_fn)
+    return {"logits": logits, "bound": bound, "idx": idx, "gate": softmax_gates(logits, idx)}
+
+
+def softmax_gates(logits: torch.Tensor, idx: torch.Tensor) -> torch.Tensor:
+    """g[t, j] = exp(l_j - m) / sum_{j'} exp(l_j' - m) over the k selected logits (reading R3)."""
+    sl = logits.gather(1, idx)
+    m = sl.max(dim=1, keepdim=True).values
+    ex = torch.exp(sl - m)
+    return ex / ex.sum(dim=1, keepdim=True)
+
+
+# -------------------------------------------------------------- dispatch ----
+
+def capacity(T: int, k: int, E: int, cf: Optional[Tuple[int, int]]) -> Optional[int]:
+    """Per-expert capacity C = ceil(num * T * k / (den * E)) in integer arithmetic; None = no limit.
+
+    The open-training page, section 2, gives capacity factors of 1.10 and 1.15;
+    the September 14 summary records a capacity rounding that could exceed its
+    buffer by one row (#9159). The formula is reading R4.
+    """
+    if cf is None:
+        return None
+    num, den = cf
+    if num <= 0:
+        return None
+    return -(-(num * T * k) // (den * E))
+
+
+def dispatch(idx: torch.Tensor, E: int, cap: Optional[int]) -> Dict[str, torch.Tensor]:
+    """Expert counts, capacity clamp, group offsets and the stable permutation.
+
+    counts[e] = number of assignments to e; kept[e] = min(counts[e], C);
+    offsets = exclusive prefix sum of kept (E+1 entries). Assignment (t, j) to
+    e gets slot offsets[e] + r, r = number of tokens t' < t that chose e, if
+    r < C, else slot -1 (dropped). perm[slot] = t * k + j. Rows of one expert
+    therefore sit together in ascending token order, as the ragged transport
+    delivers them (teardown, section "21% to 27% MFU without stopping the run").
+    """
+    T, k = idx.shape
+    il = idx.tolist()
+    counts = [0] * E
+    for row in il:
+        for e in row:
+            counts[e] += 1
+    kept = [c if cap is None else min(c, cap) for c in counts]
+    offsets = [0] * (E + 1)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + kept[e]
+    seen = [0] * E
+    slot_of = [[-1] * k for _ in range(T)]
+    perm = [-1] * offsets[E]
+    for t in range(T):
+        for j in range(k):
+            e = il[t][j]
+            r = seen[e]
+            seen[e] += 1
+            if cap is None or r < cap:
+                s = offsets[e] + r
+                slot_of[t][j] = s
+                perm[s] = t * k + j
+    return {
+        "counts": torch.tensor(counts, dtype=torch.int64),
+        "kept": torch.tensor(kept, dtype=torch.int64),
+        "offsets": torch.tensor(offsets, dtype=torch.int64),
+        "slot_of": torch.tensor(slot_of, dtype=torch.int64).reshape(T, k),
+        "perm": torch.tensor(perm, dtype=torch.int64),
+        "n_dropped": torch.tensor(sum(counts) - sum(kept), dtype=torch.int64),
+    }
+
+
+# --------------------------------------------------------------- latent ----
+
+def latent(x: torch.Tensor, w_down: torch.Tensor, gamma: torch.Tensor,
+           eps: float) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Latent down-projection z = x W_down and RMSNorm h = z / sqrt(mean(z^2) + eps) * gamma (R5)."""
+    z = to64(x) @ to64(w_down)
+    ms = (z * z).mean(dim=1, keepdim=True)
+    h = z / torch.sqrt(ms + eps) * to64(gamma)
+    return z, h
+
+
+# --------------------------------------------------------------- experts ----
+
+def silu(v: torch.Tensor) -> torch.Tensor:
+    """silu(v) = v / (1 + exp(-v)), exact fp64 (reading R6)."""
+    return v / (1.0 + torch.exp(-v))
+
+
+def swiglu_mlp(h: torch.Tensor, w1: torch.Tensor, w3: torch.Tensor,
+               w2: torch.Tensor) -> torch.Tensor:
+    """One SwiGLU expert: (silu(h W1) * (h W3)) W2, all operands fp64."""
+    return (silu(h @ w1) * (h @ w3)) @ w2
+
+
+def swiglu_hidden(h: torch.Tensor, w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    """The SwiGLU hidden activation silu(h W1) * (h W3)."""
+    return silu(h @ w1) * (h @ w3)
+
+
+def shared_experts(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor,
+                   w2_s: torch.Tensor) -> torch.Tensor:
+    """Sum over the S shared experts of SwiGLU_s(x); they read x, not the latent (R7)."""
+    x64 = to64(x)
+    out = torch.zeros((x64.shape[0], to64(w2_s[0]).shape[1]), dtype=F64)
+    for s in range(w1_s.shape[0]):
+        out += swiglu_mlp(x64, to64(w1_s[s]), to64(w3_s[s]), to64(w2_s[s]))
+    return out
+
+
+def shared_hidden(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor) -> torch.Tensor:
+    """Shared experts' hidden activations, concatenated along the feature axis [T, S*F_s]."""
+    x64 = to64(x)
+    return torch.cat([swiglu_hidden(x64, to64(w1_s[s]), to64(w3_s[s]))
+                      for s in range(w1_s.shape[0])], dim=1)
+
+
+def grouped_experts(rows: torch.Tensor, offsets: Sequence[int], w1: torch.Tensor,
+                    w3: torch.Tensor, w2: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Expert MLPs over expert-grouped rows: rows offsets[e]:offsets[e+1] go through expert e.
+
+    Returns (hidden a [R, F], output o [R, L]) in fp64 for the active rows
+    only; rows past offsets[-1] (pool padding) are never computed, matching
+    the "mask-free" ragged expert MLP of the teardown's section
+    "21% to 27% MFU without stopping the run".
+    """
+    r64 = to64(rows)
+    n_act = int(offsets[-1])
+    F = w1.shape[2]
+    a = torch.zeros((n_act, F), dtype=F64)
+    o = torch.zeros((n_act, w2.shape[2]), dtype=F64)
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            a[lo:hi] = swiglu_hidden(r64[lo:hi], to64(w1[e]), to64(w3[e]))
+            o[lo:hi] = a[lo:hi] @ to64(w2[e])
+    return a, o
+
+
+def combine(y_perm: torch.Tensor, slot_of: torch.Tensor, gate: torch.Tensor) -> torch.Tensor:
+    """c[t] = sum over kept j, in ascending expert order, of gate[t, j] * y_perm[slot_of[t, j]].
+
+    A dropped assignment (slot -1) contributes nothing and the other gates are
+    not renormalised (reading R4). The fixed j order is the ordered-gather
+    combine that made repeated scoring bitwise exact (September 14 summary,
+    post-training epic, #9144).
+    """
+    yp = to64(y_perm)
+    g = to64(gate)
+    T, k = slot_of.shape
+    c = torch.zeros((T, yp.shape[1]), dtype=F64)
+    for j in range(k):
+        s = slot_of[:, j]
+        keep = s >= 0
+        if keep.any():
+            c[keep] += g[keep, j:j + 1] * yp[s[keep]]
+    return c
+
+
+# --------------------------------------------------------------- forward ----
+
+def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
+            capacity_factor: Optional[Tuple[int, int]] = None,
+            tokens: Optional[Sequence[int]] = None) -> Dict[str, torch.Tensor]:
+    """The whole layer: route, dispatch, latent, experts, combine, up-projection + shared.
+
+    Routing and dispatch are always computed for every token (capacity drops
+    depend on all earlier tokens). The expert, combine and output stages are
+    computed for ``tokens`` only when given (each token's output depends only
+    on its own row and its own routing), else for all tokens.
+    Returned tensors for those stages are indexed by position in ``tokens``.
+    """
+    x = inp["x"]
+    T = x.shape[0]
+    E = inp["w_router"].shape[1]
+    r = route(x, inp["w_router"], inp.get("b_router"), top_k)
+    cap = capacity(T, top_k, E, capacity_factor)
+    dsp = dispatch(r["idx"], E, cap)
+    toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    xt = x[toks]
+    z, h = latent(xt, inp["w_down"], inp["rms_gamma"], rms_eps)
+    w1, w3, w2 = inp["w1"], inp["w3"], inp["w2"]
+    L = w2.shape[2]
+    idx = r["idx"][toks]
+    slot = dsp["slot_of"][toks]
+    gate = r["gate"][toks]
+    # per assignment expert output o[t, j] (zero when dropped)
+    o = torch.zeros((len(toks), top_k, L), dtype=F64)
+    by_expert: Dict[int, List[Tuple[int, int]]] = {}
+    for i in range(len(toks)):
+        for j in range(top_k):
+            if int(slot[i, j]) >= 0:
+                by_expert.setdefault(int(idx[i, j]), []).append((i, j))
+    for e in sorted(by_expert):
+        pairs = by_expert[e]
+        rows = torch.stack([h[i] for i, _ in pairs])
+        out_e = swiglu_mlp(rows, to64(w1[e]), to64(w3[e]), to64(w2[e]))
+        for n, (i, j) in enumerate(pairs):
+            o[i, j] = out_e[n]
+    c = torch.zeros((len(toks), L), dtype=F64)
+    for j in range(top_k):
+        kept = slot[:, j] >= 0
+        c[kept] += gate[kept, j:j + 1] * o[kept, j]
+    a_s = shared_hidden(xt, inp["w1_s"], inp["w3_s"])
+    w2s = to64(inp["w2_s"]).reshape(-1, to64(inp["w2_s"]).shape[-1])
+    y = c @ to64(inp["w_up"]) + a_s @ w2s
+    out = dict(r)
+    out.update(dsp)
+    out.update({"tokens": torch.tensor(toks, dtype=torch.int64), "z": z, "h": h, "o": o,
+                "c": c, "a_s": a_s, "y": y, "capacity": torch.tensor(-1 if cap is None else cap)})
+    return out
+
+
+def slice_forward(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
+    """One expert-parallel rank's slice: grouped SwiGLU experts over the pool, then the
+    gate-weighted un-permute back to arrival order: out[i] = gate[i] * o[slot_of[i]]."""
+    offs = [int(v) for v in inp["expert_offsets"].tolist()]
+    a, o = grouped_experts(inp["pool"], offs, inp["w1"], inp["w3"], inp["w2"])
+    s = inp["slot_of"].to(torch.int64)
+    out = to64(inp["gate"]).unsqueeze(1) * o[s]
+    return {"a": a, "y_perm": o, "out": out}

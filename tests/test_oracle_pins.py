@@ -1,0 +1,387 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than the oracle itself:
+brute-force enumeration, closed forms, hand-derived fixtures under
+tests/golden/, invariants of the layer, and an independently written dense
+pipeline. test_planted_mistakes_are_caught plants plausible mistakes in the
+oracle (on the CPU) and shows that some pin fails for each.
+"""
+import itertools
+import json
+import math
+import os
+
+import pytest
+import torch
+import torch.nn.functional as Fn
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F64 = torch.float64
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand_layer(T=24, d=12, L=8, E=6, F=5, S=2, Fs=7, seed=0, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s, sc=1.0: (torch.randn(*s, generator=g) * sc).to(dtype)
+    return {
+        "x": r(T, d), "w_router": r(d, E, sc=d ** -0.5), "b_router": torch.zeros(E),
+        "w_down": r(d, L, sc=d ** -0.5), "rms_gamma": (1.0 + 0.1 * torch.randn(L, generator=g)),
+        "w1": r(E, L, F, sc=L ** -0.5), "w3": r(E, L, F, sc=L ** -0.5), "w2": r(E, F, L, sc=F ** -0.5),
+        "w1_s": r(S, d, Fs, sc=d ** -0.5), "w3_s": r(S, d, Fs, sc=d ** -0.5),
+        "w2_s": r(S, Fs, d, sc=Fs ** -0.5), "w_up": r(L, d, sc=L ** -0.5),
+    }
+
+
+# ------------------------------------------------------------ pin functions ----
+# Written as plain functions so that the planted-mistake test can re-run them.
+
+def pin_topk_bruteforce(seed=0):
+    """Top-k with ties to the lowest index == the max-sum k-subset, ties to the
+    lexicographically smallest sorted tuple, enumerated over all C(E, k) subsets.
+    Integer-valued inputs make exact integer logits with many ties."""
+    g = torch.Generator().manual_seed(seed)
+    for (E, k, d) in [(16, 2, 5), (10, 3, 4), (8, 1, 3), (7, 7, 3), (12, 4, 2)]:
+        x = torch.randint(-2, 3, (12, d), generator=g).float()
+        w = torch.randint(-1, 2, (d, E), generator=g).float()
+        b = torch.randint(-1, 2, (E,), generator=g).float()
+        got = O.route(x, w, b, k)["idx"]
+        xi, wi, bi = x.long().tolist(), w.long().tolist(), b.long().tolist()
+        for t in range(x.shape[0]):
+            logit = [sum(xi[t][i] * wi[i][e] for i in range(d)) + bi[e] for e in range(E)]
+            best = max(itertools.combinations(range(E), k),
+                       key=lambda c: (sum(logit[e] for e in c), [-e for e in c]))
+            assert got[t].tolist() == list(best), (E, k, t, logit, got[t].tolist(), best)
+
+
+def pin_topk_exact_near_tie():
+    """Two experts whose exact logits differ by far less than fp64 resolves: the
+    exact value must decide, and a true tie must go to the lower index."""
+    d = 6
+    x = torch.tensor([[1.0, 1.0, 1.0, 1.0, 1.0, 2.0 ** -60]], dtype=torch.float32)
+    base = torch.tensor([0.5, -0.25, 0.125, 1.0, 0.75, 0.0])
+    cols = []
+    for e in range(5):
+        cols.append(base - 4.0 * (e + 1))        # clearly smaller experts
+    hi_a = base.clone()
+    hi_b = base.clone()
+    hi_b[5] = 1.0                                 # exact logit larger by 2^-60
+    w = torch.stack([hi_a] + cols + [hi_b], dim=1).float()   # expert 0 = a, expert 6 = b
+    idx = O.route(x, w, None, 1)["idx"]
+    assert idx.tolist() == [[6]], idx
+    w2 = torch.stack([hi_a] + cols + [hi_a], dim=1).float()  # exact tie: lower index wins
+    assert O.route(x, w2, None, 1)["idx"].tolist() == [[0]]
+    _ = d
+
+
+def pin_logit_bound_holds(seed=1):
+    """The fp64 logit error stays inside the oracle's bound (exact values by rationals)."""
+    lay = _rand_layer(T=6, d=40, E=5, seed=seed, dtype=torch.bfloat16)
+    logits, bound = O.router_logits(lay["x"], lay["w_router"], lay["b_router"])
+    xs, ws = O.to64(lay["x"]), O.to64(lay["w_router"])
+    for t in range(6):
+        for e in range(5):
+            ex = O.exact_logit(xs[t].tolist(), ws[:, e].tolist(), 0.0)
+            assert abs(float(ex - __import__("fractions").Fraction(float(logits[t, e])))) <= float(bound[t, e])
+
+
+def pin_gates():
+    """Gates sum to 1; for k=2 they are sigmoid(l1 - l2); they equal the full softmax
+    renormalised over the selected experts."""
+    lay = _rand_layer(T=32, d=16, E=9, seed=3)
+    for k in (1, 2, 4):
+        r = O.route(lay["x"], lay["w_router"], lay["b_router"], k)
+        g = r["gate"]
+        assert torch.allclose(g.sum(1), torch.ones(32, dtype=F64), atol=1e-15, rtol=0)
+        full = torch.softmax(r["logits"], dim=1).gather(1, r["idx"])
+        assert torch.allclose(g, full / full.sum(1, keepdim=True), atol=1e-15, rtol=0)
+        if k == 1:
+            assert torch.equal(g, torch.ones_like(g))
+        if k == 2:
+            l = r["logits"].gather(1, r["idx"])
+            assert torch.allclose(g[:, 0], torch.sigmoid(l[:, 0] - l[:, 1]), atol=1e-15, rtol=0)
+
+
+def pin_capacity():
+    """Integer ceiling of cf*T*k/E; a float product would overshoot by one row."""
+    assert O.capacity(16384, 8, 384, (11, 10)) == 376           # ceil(375.47)
+    assert O.capacity(50, 1, 1, (11, 10)) == 55                 # 1.1*50 in floats is 55.00000000000001
+    assert O.capacity(100, 8, 8, (11, 10)) == 110               # 1.1*100 in floats is 110.00000000000001
+    assert O.capacity(100, 1, 10, (1, 1)) == 10
+    assert O.capacity(7, 2, 3, (1, 1)) == 5                     # ceil(14/3)
+    assert O.capacity(5, 2, 3, None) is None
+    assert O.capacity(5, 2, 3, (0, 1)) is None
+
+
+def pin_dispatch_golden():
+    gd = _load("dispatch_capacity.json")
+    idx = torch.tensor(gd["idx"])
+    cap = O.capacity(idx.shape[0], idx.shape[1], gd["n_experts"], tuple(gd["capacity_factor"]))
+    assert cap == gd["expected_capacity"]
+    d = O.dispatch(idx, gd["n_experts"], cap)
+    assert d["counts"].tolist() == gd["expected_counts"]
+    assert d["kept"].tolist() == gd["expected_kept"]
+    assert d["offsets"].tolist() == gd["expected_offsets"]
+    assert d["slot_of"].tolist() == gd["expected_slot_of"]
+    assert d["perm"].tolist() == gd["expected_perm"]
+    assert int(d["n_dropped"]) == gd["expected_n_dropped"]
+
+
+def pin_dispatch_invariants(seed=5):
+    """Counts sum to T*k; slots are a bijection onto [0, sum kept); perm inverts slot_of;
+    within an expert slots ascend with t; the dropped assignments are exactly those past
+    capacity in token order (checked against a sort-based recomputation)."""
+    g = torch.Generator().manual_seed(seed)
+    T, E, k = 200, 11, 3
+    idx = torch.stack([torch.randperm(E, generator=g)[:k].sort().values for _ in range(T)])
+    for cap in (None, 40, 55, 1):
+        d = O.dispatch(idx, E, cap)
+        assert int(d["counts"].sum()) == T * k
+        slots = d["slot_of"].flatten()
+        kept = slots[slots >= 0]
+        assert sorted(kept.tolist()) == list(range(int(d["kept"].sum())))
+        for t in range(T):
+            for j in range(k):
+                s = int(d["slot_of"][t, j])
+                if s >= 0:
+                    assert int(d["perm"][s]) == t * k + j
+        # sort-based: all assignments ordered by (expert, token)
+        order = sorted(((int(idx[t, j]), t, j) for t in range(T) for j in range(k)))
+        pos, rank = 0, {}
+        for e, t, j in order:
+            rank[(t, j)] = sum(1 for (e2, t2, _) in order if e2 == e and t2 < t)
+        off = d["offsets"].tolist()
+        for e, t, j in order:
+            r = rank[(t, j)]
+            exp = off[e] + r if (cap is None or r < cap) else -1
+            assert int(d["slot_of"][t, j]) == exp
+            pos += 1
+        assert int(d["n_dropped"]) == int((slots < 0).sum())
+
+
+def _dense_pipeline(lay, e, eps):
+    """An independently written dense layer: up(SwiGLU_e(RMSNorm(down(x)))) + shared(x)."""
+    x = lay["x"].double()
+    z = torch.einsum("td,dl->tl", x, lay["w_down"].double())
+    h = z * torch.rsqrt(z.pow(2).mean(-1, keepdim=True) + eps) * lay["rms_gamma"].double()
+    hid = Fn.silu(torch.einsum("tl,lf->tf", h, lay["w1"][e].double())) * \
+        torch.einsum("tl,lf->tf", h, lay["w3"][e].double())
+    routed = torch.einsum("tf,fl->tl", hid, lay["w2"][e].double())
+    y = torch.einsum("tl,ld->td", routed, lay["w_up"].double())
+    for s in range(lay["w1_s"].shape[0]):
+        hs = Fn.silu(x @ lay["w1_s"][s].double()) * (x @ lay["w3_s"][s].double())
+        y = y + hs @ lay["w2_s"][s].double()
+    return y
+
+
+def pin_forced_single_expert():
+    """k=1 and a +1e4 bias on one expert: every gate is 1 and the layer equals a dense MLP."""
+    for e_star in (0, 4):
+        lay = _rand_layer(T=20, seed=11 + e_star)
+        lay["b_router"] = torch.zeros(6)
+        lay["b_router"][e_star] = 1e4
+        out = O.forward(lay, top_k=1, rms_eps=1e-6)
+        assert (out["idx"] == e_star).all()
+        ref = _dense_pipeline(lay, e_star, 1e-6)
+        err = (out["y"] - ref).norm() / ref.norm()
+        assert err <= 1e-12, float(err)
+
+
+def pin_identical_experts():
+    """All routed experts equal and no drop: gates sum to 1, so the output does not depend
+    on the routing and equals the dense pipeline with that one expert."""
+    lay = _rand_layer(T=16, seed=21)
+    for name in ("w1", "w3", "w2"):
+        lay[name] = lay[name][:1].expand_as(lay[name]).clone()
+    for k in (2, 3):
+        out = O.forward(lay, top_k=k, rms_eps=1e-6)
+        ref = _dense_pipeline(lay, 0, 1e-6)
+        assert ((out["y"] - ref).norm() / ref.norm()) <= 1e-12
+
+
+def pin_two_token_golden():
+    gd = _load("two_token_layer.json")
+    lay = {kk: torch.tensor(gd[kk], dtype=torch.float32) for kk in
+           ("x", "w_router", "b_router", "w_down", "rms_gamma", "w1", "w3", "w2", "w1_s",
+            "w3_s", "w2_s", "w_up")}
+    out = O.forward(lay, top_k=gd["top_k"], rms_eps=gd["rms_eps"])
+    assert out["idx"].tolist() == gd["expected_idx"]
+    env = {"sig": lambda v: 1.0 / (1.0 + math.exp(-v)), "sqrt": math.sqrt}
+    exp = torch.tensor([[eval(s, {"__builtins__": {}}, env) for s in row]
+                        for row in gd["expected_y"]], dtype=F64)
+    assert torch.allclose(out["y"], exp, atol=1e-14, rtol=0), (out["y"], exp)
+
+
+def pin_rmsnorm():
+    """With gamma = 1 and eps = 0, mean(h^2) = 1 and h is invariant to scaling z by c > 0."""
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(10, 12, generator=g)
+    w = torch.randn(12, 8, generator=g)
+    _, h = O.latent(x, w, torch.ones(8), 0.0)
+    assert torch.allclose((h * h).mean(1), torch.ones(10, dtype=F64), atol=1e-14, rtol=0)
+    _, h2 = O.latent(x * 4.0, w, torch.ones(8), 0.0)
+    assert torch.allclose(h, h2, atol=1e-14, rtol=0)
+
+
+def pin_combine_drop_not_renormalised():
+    """A dropped assignment contributes nothing and the kept gates keep their values."""
+    yp = torch.tensor([[1.0, 2.0], [10.0, 20.0]])
+    slot = torch.tensor([[0, -1], [1, 0]])
+    gate = torch.tensor([[0.25, 0.75], [0.5, 0.5]])
+    c = O.combine(yp, slot, gate)
+    assert c.tolist() == [[0.25, 0.5], [5.5, 11.0]]
+
+
+def pin_slice_rowwise():
+    """The grouped slice equals a per-row loop that looks up each row's expert."""
+    g = torch.Generator().manual_seed(9)
+    E, L, F, P = 3, 6, 5, 14
+    offs = [0, 4, 4, 10]                      # an empty expert; rows 10..13 are padding
+    inp = {"pool": torch.randn(P, L, generator=g), "expert_offsets": torch.tensor(offs),
+           "w1": torch.randn(E, L, F, generator=g), "w3": torch.randn(E, L, F, generator=g),
+           "w2": torch.randn(E, F, L, generator=g),
+           "gate": torch.rand(10, generator=g), "slot_of": torch.randperm(10, generator=g)}
+    out = O.slice_forward(inp)["out"]
+    for i in range(10):
+        r = int(inp["slot_of"][i])
+        e = max(ee for ee in range(E) if offs[ee] <= r < offs[ee + 1])
+        v = inp["pool"][r].double()
+        hid = Fn.silu(v @ inp["w1"][e].double()) * (v @ inp["w3"][e].double())
+        ref = float(inp["gate"][i]) * (hid @ inp["w2"][e].double())
+        assert torch.allclose(out[i], ref, atol=1e-12, rtol=0)
+
+
+def pin_forward_drop_skips_expert():
+    """With a capacity, each dropped assignment removes exactly gate * expert output from
+    the token's routed sum; kept gates are unchanged (the token skips that expert)."""
+    lay = _rand_layer(T=40, E=4, seed=31)
+    k = 2
+    full = O.forward(lay, top_k=k, rms_eps=1e-6)
+    capd = O.forward(lay, top_k=k, rms_eps=1e-6, capacity_factor=(1, 2))   # C = 10 of ~20 per expert
+    assert int(capd["n_dropped"]) > 0
+    x = lay["x"].double()
+    z = x @ lay["w_down"].double()
+    h = z * torch.rsqrt(z.pow(2).mean(-1, keepdim=True) + 1e-6) * lay["rms_gamma"].double()
+    for t in range(40):
+        diff = full["y"][t] - capd["y"][t]
+        exp = torch.zeros_like(diff)
+        for j in range(k):
+            if int(capd["slot_of"][t, j]) < 0:
+                e = int(full["idx"][t, j])
+                hid = Fn.silu(h[t] @ lay["w1"][e].double()) * (h[t] @ lay["w3"][e].double())
+                exp += float(full["gate"][t, j]) * ((hid @ lay["w2"][e].double()) @ lay["w_up"].double())
+        assert torch.allclose(diff, exp, atol=1e-12, rtol=0), t
+
+
+ALL_PINS = [pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
+            pin_capacity, pin_dispatch_golden, pin_dispatch_invariants, pin_forced_single_expert,
+            pin_identical_experts, pin_two_token_golden, pin_rmsnorm,
+            pin_combine_drop_not_renormalised, pin_slice_rowwise]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
+def test_oracle_pin(pin):
+    pin()
+
+
+# -------------------------------------------------------- planted mistakes ----
+
+def _mut_silu_no_sigmoid(monkeypatch):
+    monkeypatch.setattr(O, "silu", lambda v: v * torch.exp(-v))
+
+
+def _mut_tie_high_index(monkeypatch):
+    orig = O.topk_exact
+
+    def bad(logits, bound, k, exact_fn):
+        E = logits.shape[1]
+        flipped = orig(logits.flip(1), bound.flip(1), k, lambda t, e: exact_fn(t, E - 1 - e))
+        return torch.sort(E - 1 - flipped, dim=1).values
+    monkeypatch.setattr(O, "topk_exact", bad)
+
+
+def _mut_float_capacity(monkeypatch):
+    monkeypatch.setattr(O, "capacity", lambda T, k, E, cf: None if cf is None or cf[0] <= 0
+                        else math.ceil(cf[0] / cf[1] * T * k / E))
+
+
+def _mut_no_shared(monkeypatch):
+    monkeypatch.setattr(O, "shared_hidden", lambda x, w1, w3: torch.zeros(
+        x.shape[0], w1.shape[0] * w1.shape[2], dtype=F64))
+
+
+def _mut_rms_sum(monkeypatch):
+    def bad(x, w_down, gamma, eps):
+        z = O.to64(x) @ O.to64(w_down)
+        return z, z / torch.sqrt((z * z).sum(1, keepdim=True) + eps) * O.to64(gamma)
+    monkeypatch.setattr(O, "latent", bad)
+
+
+def _mut_full_softmax(monkeypatch):
+    monkeypatch.setattr(O, "softmax_gates",
+                        lambda logits, idx: torch.softmax(logits, 1).gather(1, idx))
+
+
+def _mut_renorm_after_drop(monkeypatch):
+    orig = O.combine
+
+    def bad(y_perm, slot_of, gate):
+        g = gate.clone().double() * (slot_of >= 0)
+        g = g / g.sum(1, keepdim=True).clamp_min(1e-300)
+        return orig(y_perm, slot_of, g)
+    monkeypatch.setattr(O, "combine", bad)
+
+
+def _mut_forward_renorm(monkeypatch):
+    orig = O.softmax_gates
+
+    def bad(logits, idx):                   # gates computed as if dropped experts never existed
+        g = orig(logits, idx)
+        return g * 0.5 + 0.5 / idx.shape[1]
+    monkeypatch.setattr(O, "softmax_gates", bad)
+
+
+def _mut_unstable_perm(monkeypatch):
+    orig = O.dispatch
+
+    def bad(idx, E, cap):
+        d = orig(idx.flip(0), E, cap)          # ranks taken in reverse token order
+        d["slot_of"] = d["slot_of"].flip(0)
+        T, k = idx.shape
+        d["perm"] = torch.where(d["perm"] >= 0, (T - 1 - d["perm"] // k) * k + d["perm"] % k,
+                                d["perm"])
+        return d
+    monkeypatch.setattr(O, "dispatch", bad)
+
+
+def _mut_transposed_up(monkeypatch):
+    orig = O.forward
+
+    def bad(inp, **kw):
+        inp = dict(inp)
+        L, d = inp["w_up"].shape
+        inp["w_up"] = inp["w_up"].t().reshape(L, d) if L != d else inp["w_up"].t()
+        return orig(inp, **kw)
+    monkeypatch.setattr(O, "forward", bad)
+
+
+MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mut_no_shared,
+             _mut_rms_sum, _mut_full_softmax, _mut_renorm_after_drop, _mut_forward_renorm, _mut_unstable_perm,
+             _mut_transposed_up]
+
+
+@pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__[5:] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(mutate, monkeypatch):
+    mutate(monkeypatch)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {mutate.__name__}"
