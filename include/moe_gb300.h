@@ -1,0 +1,216 @@
+/*
+ * moe_gb300.h -- C ABI of the routed mixture-of-experts forward layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (pages: "Marin 535B-A23B: the half of a training run nobody usually shows you",
+ * section "What is actually being trained"; "Marin Begins Open Training of a 535B-Parameter
+ * MoE Model", section 2): a router picks top_k of n_experts routed experts per token; the
+ * token is projected from d_model down to a d_latent-wide latent and RMS-normalised; each
+ * chosen expert (a SwiGLU MLP of width d_ff in the latent) processes it; the expert outputs
+ * are combined with the router's gates, projected back up to d_model and added to the output
+ * of n_shared shared SwiGLU experts (width d_ff_shared) that read every token.
+ *
+ *   logits = x W_r + b_r                      router, [T, E]
+ *   idx, gate = top_k(logits), softmax over the selected logits
+ *   z = x W_down;  h = z / sqrt(mean(z^2) + eps) * gamma
+ *   o_{t,j} = (silu(h_t W1_e) * (h_t W3_e)) W2_e,  e = idx[t, j]
+ *   c_t = sum_j gate[t, j] o_{t,j}            (ascending expert order, dropped terms skipped)
+ *   y = c W_up + sum_s (silu(x W1_s[s]) * (x W3_s[s])) W2_s[s]
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every buffer (device memory unless stated) and the workspace.
+ *     The library allocates no device memory, keeps no pointer after a call returns and frees
+ *     nothing.
+ *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Every call only
+ *     enqueues work on it and returns; nothing synchronises the host except
+ *     moe_get_device_status().
+ *   - Layouts: all matrices are row-major and densely packed. Activations and weights have
+ *     the element type cfg->dtype (bf16 or fp32); b_router, rms_gamma and gates are fp32;
+ *     indices, counts, offsets and slots are int32.
+ *   - Alignment: every pointer must be 16-byte aligned and, for bf16, d_model, d_latent, d_ff,
+ *     d_ff_shared and n_experts must be multiples of 8 (MOE_ERR_ALIGNMENT otherwise).
+ *   - Errors: argument errors return before anything is enqueued. A failed launch returns
+ *     MOE_ERR_CUDA. Errors found on the device (an out-of-range expert id or slot, offsets that
+ *     are not monotone, a device wait that timed out) are recorded in a status word inside the
+ *     workspace and read by moe_get_device_status(); the kernels then skip the offending item
+ *     instead of touching memory out of range. No call aborts the process.
+ *   - Determinism: outputs are bitwise identical for identical inputs and configuration (the
+ *     combine sums each token's terms in a fixed order, as the ordered-gather combine of the
+ *     Marin summary for the week of 2026-09-14, post-training epic (#9144), does).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* a NULL required pointer, a non-positive size, top_k > n_experts */
+  MOE_ERR_UNSUPPORTED = 2,    /* a size beyond the limits below */
+  MOE_ERR_WORKSPACE = 3,      /* ws_bytes smaller than moe_workspace_size() */
+  MOE_ERR_ALIGNMENT = 4,      /* a pointer not 16-byte aligned, or a bf16 width not a multiple of 8 */
+  MOE_ERR_CUDA = 5,           /* a CUDA launch or runtime call failed */
+  MOE_ERR_BAD_ROUTING = 6,    /* device: an expert id, slot or offset out of range or unordered */
+  MOE_ERR_DEVICE_TIMEOUT = 7  /* device: a bounded wait inside a kernel gave up */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype_t;
+
+/* cfg->flags */
+#define MOE_FLAG_PDL  (1u << 0)  /* launch dependent kernels with programmatic dependent launch */
+#define MOE_FLAG_SIMT (1u << 1)  /* bf16: run every GEMM on CUDA cores (fp32 FMA) instead of tcgen05 */
+
+/* Limits: 1 <= top_k <= 32, top_k <= n_experts <= 1024, T * top_k < 2^31. */
+
+typedef struct {
+  int64_t  T;            /* tokens */
+  int32_t  d_model;      /* d */
+  int32_t  d_latent;     /* L */
+  int32_t  n_experts;    /* E */
+  int32_t  top_k;        /* k */
+  int32_t  d_ff;         /* F, routed expert SwiGLU width */
+  int32_t  n_shared;     /* S, shared experts (0 allowed) */
+  int32_t  d_ff_shared;  /* F_s */
+  /* Per-expert capacity C = ceil(capacity_num * T * top_k / (capacity_den * n_experts)),
+   * computed in integers; capacity_num <= 0 means no capacity (nothing is dropped). The
+   * capacity factors 1.10 / 1.15 and the drop of assignments past a fixed buffer are those of
+   * the open-training page, section 2; a dropped assignment contributes nothing and the other
+   * gates are not renormalised ("the token skips that expert", teardown section "21% to 27%
+   * MFU without stopping the run"). */
+  int32_t  capacity_num;
+  int32_t  capacity_den;
+  float    rms_eps;      /* RMSNorm epsilon */
+  int32_t  dtype;        /* moe_dtype_t */
+  uint32_t flags;        /* MOE_FLAG_* */
+  /* Physical rows of the expert-grouped buffers x_perm / y_perm passed to moe_expert_ffn and
+   * moe_combine; 0 means T * top_k. Rows past expert_offsets[E] are padding that no kernel
+   * reads or writes (the "mask-free" ragged expert MLP with physical vs active group sizes,
+   * teardown section "21% to 27% MFU without stopping the run"). */
+  int64_t  pool_rows;
+} moe_config_t;
+
+/* Weights of one layer. Expert banks are stacked [experts, d_in, d_out] (teardown section
+ * "A sphere for every matrix"). */
+typedef struct {
+  const void*  w_router;   /* [d, E] */
+  const float* b_router;   /* [E] fp32, may be NULL (zero bias) */
+  const void*  w_down;     /* [d, L] */
+  const float* rms_gamma;  /* [L] fp32 */
+  const void*  w1;         /* [E, L, F] gate projection */
+  const void*  w3;         /* [E, L, F] up projection */
+  const void*  w2;         /* [E, F, L] down projection */
+  const void*  w1_s;       /* [S, d, F_s] */
+  const void*  w3_s;       /* [S, d, F_s] */
+  const void*  w2_s;       /* [S, F_s, d] */
+  const void*  w_up;       /* [L, d] */
+} moe_weights_t;
+
+/* Optional extras of moe_forward; every pointer may be NULL. Device buffers receive copies of
+ * the routing results. stage_events, when not NULL, holds MOE_FORWARD_STAGES + 1 cudaEvent_t
+ * handles created by the caller; event i is recorded on `stream` before stage i and the last
+ * one after the final stage, so that the caller can time stages without a profiler. */
+#define MOE_FORWARD_STAGES 8   /* prep, front GEMM, router select, dispatch, expert GEMM 1,
+                                  expert GEMM 2, combine, back GEMM */
+typedef struct {
+  int32_t* topk_idx;        /* [T, k] */
+  float*   topk_gate;       /* [T, k] */
+  int32_t* expert_counts;   /* [E] assignments per expert before the capacity clamp */
+  int32_t* expert_offsets;  /* [E + 1] */
+  int32_t* slot_of;         /* [T, k] */
+  int32_t* n_dropped;       /* [1] */
+  void* const* stage_events;
+} moe_forward_aux_t;
+
+/* Diagnostics recorded on the device by the last calls (see moe_get_device_status). */
+typedef struct {
+  int32_t status;          /* moe_status_t of the first device-detected error, MOE_OK if none */
+  int32_t detail;          /* error-specific detail (e.g. the offending token or expert) */
+  int32_t n_refined;       /* tokens whose top-k needed the compensated re-evaluation */
+  int32_t n_exact;         /* tokens whose top-k needed exact (integer) logits */
+} moe_device_report_t;
+
+MOE_API int32_t     moe_abi_version(void);
+MOE_API const char* moe_status_string(moe_status_t status);
+
+/* Bytes of workspace every call below needs for this configuration (one size fits all calls).
+ * The workspace must be 256-byte aligned device memory owned by the caller. */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Router: logits = x W_r + b_r, then per token the top_k experts by the exact real value of
+ * the logit (ties to the lowest index), written in ascending expert order to topk_idx [T, k],
+ * and gates topk_gate [T, k] = softmax over the selected logits. The router weight and bias
+ * are those of the teardown's section "The one knob nobody pinned". The selection is exact:
+ * fp32 logits decide a token when their rigorous error bounds separate the k-th from the
+ * (k+1)-th expert; otherwise the candidates are re-evaluated with a compensated dot product
+ * and, if still too close, with exact integer arithmetic (the teardown's section "What I'd
+ * take from it" reports that router arithmetic alone changed the top-8 of ~9% of tokens). */
+MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* b_router, int32_t* topk_idx, float* topk_gate,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch: z = x W_down, h = RMSNorm(z) * gamma; expert_counts [E] (before capacity);
+ * expert_offsets [E+1] = exclusive prefix sum of min(counts, C); slot_of [T, k] = the row of
+ * assignment (t, j) in the expert-grouped buffer (rows of one expert in ascending token order,
+ * as the ragged transport delivers them), -1 if dropped; perm [T*k] = t*k + j at each used
+ * row (entries past expert_offsets[E] are left untouched); n_dropped [1];
+ * x_perm [pool_rows, L] receives h at every used row. topk_idx must hold ascending, distinct
+ * expert ids (as moe_route writes them). */
+MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
+                         const float* rms_gamma, const int32_t* topk_idx,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                         int32_t* slot_of, int32_t* n_dropped, void* x_perm,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Experts: for every expert e and every row r in [expert_offsets[e], expert_offsets[e+1]):
+ * y_perm[r] = (silu(x_perm[r] W1_e) * (x_perm[r] W3_e)) W2_e. Rows past expert_offsets[E]
+ * (pool padding) are neither read nor written; an expert with no rows loads no weights.
+ * The grouped GEMM reads expert_offsets only after the kernel that wrote them has completed
+ * (the hang of the weekly summary of 2026-09-14, hero-run epic, came from warps that read
+ * the group boundaries early under programmatic dependent launch).
+ * When x is not NULL, also the shared experts' hidden activations
+ * a_shared [T, S*F_s] = concat_s silu(x W1_s[s]) * (x W3_s[s]). */
+MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
+                            const int32_t* expert_offsets, const void* w1, const void* w3,
+                            const void* w2, void* y_perm, const void* x, const void* w1_s,
+                            const void* w3_s, void* a_shared, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* Combine: c[t] = sum over j with slot_of[t, j] >= 0, in order j = 0..k-1, of
+ * topk_gate[t, j] * y_perm[slot_of[t, j]] (fp32 accumulation). When w_up is NULL, out [T, L]
+ * receives c (the gate-weighted un-permute back to arrival order, e.g. of one expert-parallel
+ * rank's slice with k = 1); otherwise out [T, d] receives y = c W_up + a_shared W2_s
+ * (a_shared / w2_s may be NULL when n_shared == 0). */
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* slot_of,
+                         const float* topk_gate, const void* a_shared, const void* w_up,
+                         const void* w2_s, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer: y [T, d] from x [T, d], all stages enqueued on `stream` with no host
+ * synchronisation. aux may be NULL. */
+MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, void* y,
+                         void* ws, size_t ws_bytes, void* stream, const moe_forward_aux_t* aux);
+
+/* Waits for `stream`, then copies the device report out of the workspace into *out (host
+ * memory). Returns MOE_ERR_CUDA if the wait or the copy fails. */
+MOE_API moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream,
+                                   moe_device_report_t* out);
+
+/* Enqueues a reset of the device report (status, detail and counters) to zero. */
+MOE_API moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

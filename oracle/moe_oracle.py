@@ -129,12 +129,11 @@ def route(x: torch.Tensor, w_router: torch.Tensor, b_router: Optional[torch.Tens
           k: int) -> Dict[str, torch.Tensor]:
     """Router: logits, exact top-k indices (ascending), renormalised softmax gates."""
     logits, bound = router_logits(x, w_router, b_router)
-    xs = to64(x)
     ws = to64(w_router)
     bs = to64(b_router) if b_router is not None else torch.zeros(ws.shape[1], dtype=F64)
 
     def exact_fn(t: int, e: int) -> Fraction:
-        return exact_logit(xs[t].tolist(), ws[:, e].tolist(), float(bs[e]))
+        return exact_logit(to64(x[t]).tolist(), ws[:, e].tolist(), float(bs[e]))
 
     idx = topk_exact(logits, bound, k, exact_fn)
     return {"logits": logits, "bound": bound, "idx": idx, "gate": softmax_gates(logits, idx)}
@@ -357,3 +356,23 @@ def slice_forward(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
     s = inp["slot_of"].to(torch.int64)
     out = to64(inp["gate"]).unsqueeze(1) * o[s]
     return {"a": a, "y_perm": o, "out": out}
+
+
+def slice_rows(inp: Dict[str, torch.Tensor], positions: Sequence[int]) -> Dict[str, torch.Tensor]:
+    """The slice workload for selected arrival positions only (each row is independent):
+    for position i, pool row r = slot_of[i] of expert e (offsets[e] <= r < offsets[e+1]),
+    o = SwiGLU_e(pool[r]) and out[i] = gate[i] * o."""
+    offs = [int(v) for v in inp["expert_offsets"].tolist()]
+    pos = [int(p) for p in positions]
+    rows = [int(inp["slot_of"][p]) for p in pos]
+    groups: Dict[int, List[int]] = {}
+    for n, r in enumerate(rows):
+        e = max(g for g in range(len(offs) - 1) if offs[g] <= r < offs[g + 1])
+        groups.setdefault(e, []).append(n)
+    L = inp["w2"].shape[2]
+    o = torch.zeros((len(pos), L), dtype=F64)
+    for e, ns in groups.items():
+        v = to64(inp["pool"][[rows[n] for n in ns]])
+        o[ns] = swiglu_mlp(v, to64(inp["w1"][e]), to64(inp["w3"][e]), to64(inp["w2"][e]))
+    g = to64(inp["gate"][pos]).unsqueeze(1)
+    return {"rows": torch.tensor(rows), "y_perm": o, "out": g * o}

@@ -1,0 +1,160 @@
+"""GB300-native routed mixture-of-experts forward layer.
+
+A thin Python binding over the C ABI of ``libmoe_gb300.so`` (include/moe_gb300.h): every
+function here marshals torch tensors into pointers and sizes and calls the C entry point of
+the same name; every step of the layer runs in the library's CUDA kernels. PyTorch supplies
+device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Dict, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_PDL, MOE_FLAG_SIMT, MOE_FORWARD_STAGES,
+                   moe_config_t, moe_device_report_t, moe_forward_aux_t, moe_weights_t)
+
+__all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
+           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+           "moe_get_device_status", "moe_clear_device_status", "MOE_FLAG_PDL", "MOE_FLAG_SIMT",
+           "MOE_FORWARD_STAGES", "WEIGHT_NAMES"]
+
+WEIGHT_NAMES = ("w_router", "b_router", "w_down", "rms_gamma", "w1", "w3", "w2", "w1_s", "w3_s",
+                "w2_s", "w_up")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {_lib.STATUS_NAMES.get(status, status)}")
+
+
+@dataclass
+class LayerConfig:
+    T: int
+    d_model: int
+    d_latent: int
+    n_experts: int
+    top_k: int
+    d_ff: int
+    n_shared: int
+    d_ff_shared: int
+    dtype: str = "bf16"            # "bf16" or "f32"
+    capacity: Optional[Sequence[int]] = None   # (num, den) or None
+    rms_eps: float = 1e-6
+    flags: int = 0
+    pool_rows: int = 0
+
+    @classmethod
+    def from_shape(cls, shape, **kw) -> "LayerConfig":
+        return cls(T=shape.T, d_model=shape.d_model, d_latent=shape.d_latent,
+                   n_experts=shape.n_experts, top_k=shape.top_k, d_ff=shape.d_ff,
+                   n_shared=shape.n_shared, d_ff_shared=shape.d_ff_shared, dtype=shape.dtype,
+                   capacity=shape.capacity, rms_eps=shape.rms_eps, **kw)
+
+    def c(self) -> moe_config_t:
+        num, den = (self.capacity if self.capacity else (0, 1))
+        return moe_config_t(T=self.T, d_model=self.d_model, d_latent=self.d_latent,
+                            n_experts=self.n_experts, top_k=self.top_k, d_ff=self.d_ff,
+                            n_shared=self.n_shared, d_ff_shared=self.d_ff_shared,
+                            capacity_num=num, capacity_den=den, rms_eps=self.rms_eps,
+                            dtype=MOE_BF16 if self.dtype == "bf16" else MOE_F32,
+                            flags=self.flags, pool_rows=self.pool_rows)
+
+
+def load():
+    return _lib.load()
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MoEError(fn, status)
+
+
+def workspace_size(cfg: LayerConfig) -> int:
+    n = C.c_size_t(0)
+    _check("moe_workspace_size", load().moe_workspace_size(C.byref(cfg.c()), C.byref(n)))
+    return n.value
+
+
+def alloc_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
+    """A caller-owned workspace of the right size (torch's allocator aligns it to 256 bytes)."""
+    return torch.empty(workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def moe_route(cfg, x, w_router, b_router, topk_idx, topk_gate, ws, stream=None):
+    _check("moe_route", load().moe_route(C.byref(cfg.c()), _p(x), _p(w_router), _p(b_router),
+                                          _p(topk_idx), _p(topk_gate), _p(ws), ws.numel(),
+                                          _stream(stream)))
+
+
+def moe_permute(cfg, x, w_down, rms_gamma, topk_idx, expert_counts, expert_offsets, perm,
+                slot_of, n_dropped, x_perm, ws, stream=None):
+    _check("moe_permute", load().moe_permute(
+        C.byref(cfg.c()), _p(x), _p(w_down), _p(rms_gamma), _p(topk_idx), _p(expert_counts),
+        _p(expert_offsets), _p(perm), _p(slot_of), _p(n_dropped), _p(x_perm), _p(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn(cfg, x_perm, expert_offsets, w1, w3, w2, y_perm, x=None, w1_s=None,
+                   w3_s=None, a_shared=None, ws=None, stream=None):
+    _check("moe_expert_ffn", load().moe_expert_ffn(
+        C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _p(y_perm),
+        _p(x), _p(w1_s), _p(w3_s), _p(a_shared), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_combine(cfg, y_perm, slot_of, topk_gate, out, ws, a_shared=None, w_up=None, w2_s=None,
+                stream=None):
+    _check("moe_combine", load().moe_combine(
+        C.byref(cfg.c()), _p(y_perm), _p(slot_of), _p(topk_gate), _p(a_shared), _p(w_up),
+        _p(w2_s), _p(out), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_forward(cfg, weights: Dict[str, torch.Tensor], x, y, ws, stream=None,
+                aux: Optional[Dict[str, object]] = None):
+    """y = layer(x). ``aux`` may map topk_idx / topk_gate / expert_counts / expert_offsets /
+    slot_of / n_dropped to device tensors, and stage_events to MOE_FORWARD_STAGES + 1
+    torch.cuda.Event objects (created with enable_timing=True)."""
+    w = moe_weights_t(**{n: (weights[n].data_ptr() if weights.get(n) is not None else None)
+                         for n in WEIGHT_NAMES})
+    a = None
+    keep = None
+    if aux:
+        fields = {n: (aux[n].data_ptr() if aux.get(n) is not None else None)
+                  for n in ("topk_idx", "topk_gate", "expert_counts", "expert_offsets",
+                            "slot_of", "n_dropped")}
+        if aux.get("stage_events") is not None:
+            evs = aux["stage_events"]
+            keep = (C.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+            fields["stage_events"] = C.cast(keep, C.c_void_p).value
+        a = moe_forward_aux_t(**fields)
+    _check("moe_forward", load().moe_forward(C.byref(cfg.c()), C.byref(w), _p(x), _p(y), _p(ws),
+                                             ws.numel(), _stream(stream),
+                                             C.byref(a) if a is not None else None))
+    del keep
+
+
+def moe_get_device_status(ws, stream=None) -> Dict[str, int]:
+    r = moe_device_report_t()
+    _check("moe_get_device_status",
+           load().moe_get_device_status(_p(ws), ws.numel(), _stream(stream), C.byref(r)))
+    return {"status": r.status, "detail": r.detail, "n_refined": r.n_refined,
+            "n_exact": r.n_exact}
+
+
+def moe_clear_device_status(ws, stream=None):
+    _check("moe_clear_device_status",
+           load().moe_clear_device_status(_p(ws), ws.numel(), _stream(stream)))

@@ -1,0 +1,573 @@
+// The C ABI: argument validation, workspace layout and the stage sequence of the layer.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "dispatch.h"
+#include "gemm.h"
+#include "router.h"
+
+using namespace moe;
+
+namespace {
+
+// Safety factor on the fp32 accumulation error bound of the tensor-core router logits
+// (the CUDA-core GEMM accumulates sequentially with FMA and uses 1). Certification
+// correctness needs only a valid bound; a looser bound sends more tokens to the
+// compensated stage.
+constexpr float TC_BOUND_FACTOR = 4.0f;
+
+int64_t pool_rows_of(const moe_config_t& c) {
+  return c.pool_rows > 0 ? c.pool_rows : c.T * (int64_t)c.top_k;
+}
+
+size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, idx, gate, z, chist, cbase, counts,
+      offsets, ndrop, slot_of, perm, x_perm, hid, y_perm, a_s, c, total;
+};
+
+Layout make_layout(const moe_config_t& c) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    size_t o = off;
+    off = al256(off + (size_t)bytes);
+    return o;
+  };
+  const int64_t es = (c.dtype == MOE_BF16) ? 2 : 4;
+  const int64_t T = c.T, E = c.n_experts, k = c.top_k, d = c.d_model, Lt = c.d_latent,
+                F = c.d_ff, SF = (int64_t)c.n_shared * c.d_ff_shared, P = pool_rows_of(c),
+                nch = dispatch_chunks(T);
+  L.hdr = take(sizeof(DeviceHeader));
+  L.logits = take(T * E * 4);
+  L.wrT = take(E * d * es);
+  L.wnorm = take(E * 4);
+  L.xnorm = take(T * 4);
+  L.rlist = take(T * 4);
+  L.elist = take(T * 4);
+  L.idx = take(T * k * 4);
+  L.gate = take(T * k * 4);
+  L.z = take(T * Lt * 4);
+  L.chist = take(nch * E * 4);
+  L.cbase = take(nch * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.ndrop = take(4);
+  L.slot_of = take(T * k * 4);
+  L.perm = take(P * 4);
+  L.x_perm = take(P * Lt * es);
+  L.hid = take(P * F * es);
+  L.y_perm = take(P * Lt * es);
+  L.a_s = take(T * (SF > 0 ? SF : 1) * es);
+  L.c = take(T * Lt * es);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status_t check_cfg(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d_model < 1 || c->d_latent < 1 || c->n_experts < 1 || c->top_k < 1 ||
+      c->d_ff < 1 || c->n_shared < 0 || (c->n_shared > 0 && c->d_ff_shared < 1))
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->capacity_num > 0 && c->capacity_den < 1) return MOE_ERR_INVALID_ARG;
+  if (c->pool_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (!(c->rms_eps >= 0.0f) || !isfinite(c->rms_eps)) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > 32 || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c->T * (int64_t)c->top_k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (pool_rows_of(*c) >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if ((c->d_model % 8) || (c->d_latent % 8) || (c->d_ff % 8) ||
+      (c->n_shared > 0 && (c->d_ff_shared % 8)))
+    return MOE_ERR_ALIGNMENT;
+  if (c->dtype == MOE_BF16 && (c->n_experts % 8)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+moe_status_t check_ptrs(std::initializer_list<const void*> req,
+                        std::initializer_list<const void*> opt) {
+  for (const void* p : req) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGNMENT;
+  }
+  for (const void* p : opt)
+    if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t& c, const void* ws, size_t ws_bytes) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((uintptr_t)ws & 255u) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < make_layout(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int capacity_of(const moe_config_t& c) {
+  if (c.capacity_num <= 0) return -1;
+  int64_t num = (int64_t)c.capacity_num * c.T * c.top_k;
+  int64_t den = (int64_t)c.capacity_den * c.n_experts;
+  int64_t C = (num + den - 1) / den;
+  return (int)(C > (int64_t)INT32_MAX ? INT32_MAX : C);
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+float round_up_f(double v) {
+  float f = (float)v;
+  if ((double)f < v) f = nextafterf(f, INFINITY);
+  return f;
+}
+
+// One call's resolved state.
+struct Call {
+  moe_config_t c;
+  cudaStream_t st;
+  bool pdl, tc;
+  unsigned char* ws;
+  Layout L;
+  template <typename P> P* at(size_t off) const { return reinterpret_cast<P*>(ws + off); }
+  DeviceHeader* hdr() const { return at<DeviceHeader>(L.hdr); }
+};
+
+Call make_call(const moe_config_t* cfg, void* ws, void* stream) {
+  Call k;
+  k.c = *cfg;
+  k.st = static_cast<cudaStream_t>(stream);
+  k.pdl = (cfg->flags & MOE_FLAG_PDL) != 0;
+  k.tc = cfg->dtype == MOE_BF16 && !(cfg->flags & MOE_FLAG_SIMT);
+  k.ws = static_cast<unsigned char*>(ws);
+  k.L = make_layout(*cfg);
+  return k;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY_CUDA(expr)                         \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;    \
+  } while (0)
+
+cudaError_t run_gemms(const Call& k, GemmProblem* probs, int n) {
+  if (n == 0) return cudaSuccess;
+  if (k.tc) return gemm_tc(probs, n, k.hdr(), k.st, k.pdl);
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = gemm_simt(probs[i], k.st, k.pdl);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+moe_status_t check_tc(const Call& k, const GemmProblem* probs, int n) {
+  if (!k.tc) return MOE_OK;
+  for (int i = 0; i < n; ++i)
+    if (!gemm_tc_supported(probs[i])) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+RouterArgs router_args(const Call& k, const void* x, const void* w_router, const float* b,
+                       int32_t* idx, float* gate) {
+  const moe_config_t& c = k.c;
+  RouterArgs a{};
+  a.x = x;
+  a.w_router = w_router;
+  a.bias = b;
+  a.logits = k.at<float>(k.L.logits);
+  a.wrT = k.at<void>(k.L.wrT);
+  a.wnorm = k.at<float>(k.L.wnorm);
+  a.xnorm = k.at<float>(k.L.xnorm);
+  a.T = c.T;
+  a.d = c.d_model;
+  a.E = c.n_experts;
+  a.k = c.top_k;
+  const double u = ldexp(1.0, -24);
+  const double gd = c.d_model * u / (1.0 - c.d_model * u);
+  a.gam_d = round_up_f(gd);
+  a.cgam = round_up_f(gd * (k.tc ? TC_BOUND_FACTOR : 1.0));
+  const double n2 = (c.dtype == MOE_F32 ? 2.0 : 1.0) * (c.d_model + 1) + 64.0;
+  const double gn = n2 * u / (1.0 - n2 * u);
+  a.g2 = round_up_f(gn * gn);
+  a.idx = idx;
+  a.gate = gate;
+  a.refine_list = k.at<int32_t>(k.L.rlist);
+  a.exact_list = k.at<int32_t>(k.L.elist);
+  a.hdr = k.hdr();
+  return a;
+}
+
+GemmProblem router_problem(const Call& k, const void* x, const void* w_router, const float* b) {
+  GemmProblem p;
+  p.epi = EPI_F32;
+  p.group = GROUP_NONE;
+  p.M = k.c.n_experts;
+  p.seg[0] = {x, w_router, nullptr, k.c.d_model};
+  p.rows = k.c.T;
+  p.out = k.at<void>(k.L.logits);
+  p.ld_out = k.c.n_experts;
+  p.bias = b;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+GemmProblem down_problem(const Call& k, const void* x, const void* w_down) {
+  GemmProblem p;
+  p.epi = EPI_F32;
+  p.group = GROUP_NONE;
+  p.M = k.c.d_latent;
+  p.seg[0] = {x, w_down, nullptr, k.c.d_model};
+  p.rows = k.c.T;
+  p.out = k.at<void>(k.L.z);
+  p.ld_out = k.c.d_latent;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+GemmProblem shared_problem(const Call& k, const void* x, const void* w1_s, const void* w3_s,
+                           void* a_s) {
+  GemmProblem p;
+  p.epi = EPI_SWIGLU;
+  p.group = GROUP_COLS;
+  p.M = k.c.n_shared * k.c.d_ff_shared;
+  p.Mg = k.c.d_ff_shared;
+  p.seg[0] = {x, w1_s, w3_s, k.c.d_model};
+  p.rows = k.c.T;
+  p.out = a_s;
+  p.ld_out = p.M;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+GemmProblem expert_up_problem(const Call& k, const void* x_perm, const int32_t* offsets,
+                              const void* w1, const void* w3) {
+  GemmProblem p;
+  p.epi = EPI_SWIGLU;
+  p.group = GROUP_ROWS;
+  p.M = k.c.d_ff;
+  p.seg[0] = {x_perm, w1, w3, k.c.d_latent};
+  p.offsets = offsets;
+  p.G = k.c.n_experts;
+  p.rows = pool_rows_of(k.c);
+  p.out = k.at<void>(k.L.hid);
+  p.ld_out = k.c.d_ff;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+GemmProblem expert_down_problem(const Call& k, const int32_t* offsets, const void* w2,
+                                void* y_perm) {
+  GemmProblem p;
+  p.epi = EPI_STORE;
+  p.group = GROUP_ROWS;
+  p.M = k.c.d_latent;
+  p.seg[0] = {k.at<void>(k.L.hid), w2, nullptr, k.c.d_ff};
+  p.offsets = offsets;
+  p.G = k.c.n_experts;
+  p.rows = pool_rows_of(k.c);
+  p.out = y_perm;
+  p.ld_out = k.c.d_latent;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+GemmProblem back_problem(const Call& k, const void* c_buf, const void* w_up, const void* a_s,
+                         const void* w2_s, void* y) {
+  GemmProblem p;
+  p.epi = EPI_STORE;
+  p.group = GROUP_NONE;
+  p.M = k.c.d_model;
+  p.seg[0] = {c_buf, w_up, nullptr, k.c.d_latent};
+  p.n_seg = 1;
+  if (k.c.n_shared > 0 && a_s && w2_s) {
+    p.seg[1] = {a_s, w2_s, nullptr, k.c.n_shared * k.c.d_ff_shared};
+    p.n_seg = 2;
+  }
+  p.rows = k.c.T;
+  p.out = y;
+  p.ld_out = k.c.d_model;
+  p.dtype = k.c.dtype;
+  return p;
+}
+
+DispatchArgs dispatch_args(const Call& k, const int32_t* idx, const float* gamma,
+                           int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
+                           int32_t* n_dropped, void* x_perm) {
+  const moe_config_t& c = k.c;
+  DispatchArgs a{};
+  a.idx = idx;
+  a.T = c.T;
+  a.k = c.top_k;
+  a.E = c.n_experts;
+  a.L = c.d_latent;
+  a.cap = capacity_of(c);
+  a.n_chunks = dispatch_chunks(c.T);
+  a.chunk_hist = k.at<int32_t>(k.L.chist);
+  a.chunk_base = k.at<int32_t>(k.L.cbase);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.n_dropped = n_dropped;
+  a.slot_of = slot_of;
+  a.perm = perm;
+  a.pool_rows = pool_rows_of(c);
+  a.z = k.at<float>(k.L.z);
+  a.gamma = gamma;
+  a.eps = c.rms_eps;
+  a.x_perm = x_perm;
+  a.hdr = k.hdr();
+  return a;
+}
+
+CombineArgs combine_args(const Call& k, const void* y_perm, const int32_t* slot_of,
+                         const float* gate, void* out) {
+  CombineArgs a{};
+  a.y_perm = y_perm;
+  a.slot_of = slot_of;
+  a.gate = gate;
+  a.T = k.c.T;
+  a.k = k.c.top_k;
+  a.L = k.c.d_latent;
+  a.pool_rows = pool_rows_of(k.c);
+  a.out = out;
+  a.ld_out = k.c.d_latent;
+  a.hdr = k.hdr();
+  return a;
+}
+
+void record(const moe_forward_aux_t* aux, int i, cudaStream_t st) {
+  if (aux && aux->stage_events && aux->stage_events[i])
+    cudaEventRecord(static_cast<cudaEvent_t>(aux->stage_events[i]), st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer or width";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_ROUTING: return "bad routing data on the device";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* b_router, int32_t* topk_idx, float* topk_gate, void* ws,
+                       size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptrs({x, w_router, topk_idx, topk_gate}, {b_router})) != MOE_OK) return s;
+  if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
+  Call k = make_call(cfg, ws, stream);
+  GemmProblem p = router_problem(k, x, w_router, b_router);
+  if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+  RouterArgs ra = router_args(k, x, w_router, b_router, topk_idx, topk_gate);
+  MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false));
+  MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
+  MOE_TRY_CUDA(run_gemms(k, &p, 1));
+  MOE_TRY_CUDA(router_select(ra, cfg->dtype, num_sms(), k.st, k.pdl));
+  return MOE_OK;
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
+                         const float* rms_gamma, const int32_t* topk_idx, int32_t* expert_counts,
+                         int32_t* expert_offsets, int32_t* perm, int32_t* slot_of,
+                         int32_t* n_dropped, void* x_perm, void* ws, size_t ws_bytes,
+                         void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptrs({x, w_down, rms_gamma, topk_idx, expert_counts, expert_offsets, perm,
+                       slot_of, x_perm},
+                      {n_dropped})) != MOE_OK)
+    return s;
+  if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
+  Call k = make_call(cfg, ws, stream);
+  GemmProblem p = down_problem(k, x, w_down);
+  if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+  MOE_TRY_CUDA(run_gemms(k, &p, 1));
+  DispatchArgs da = dispatch_args(k, topk_idx, rms_gamma, expert_counts, expert_offsets, perm,
+                                  slot_of, n_dropped, x_perm);
+  MOE_TRY_CUDA(dispatch_run(da, cfg->dtype, k.st, k.pdl));
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
+                            const int32_t* expert_offsets, const void* w1, const void* w3,
+                            const void* w2, void* y_perm, const void* x, const void* w1_s,
+                            const void* w3_s, void* a_shared, void* ws, size_t ws_bytes,
+                            void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptrs({x_perm, expert_offsets, w1, w3, w2, y_perm}, {x, w1_s, w3_s, a_shared})) !=
+      MOE_OK)
+    return s;
+  const bool shared = x && cfg->n_shared > 0;
+  if (shared && (!w1_s || !w3_s || !a_shared)) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
+  Call k = make_call(cfg, ws, stream);
+  GemmProblem up[2] = {expert_up_problem(k, x_perm, expert_offsets, w1, w3)};
+  int n_up = 1;
+  if (shared) up[n_up++] = shared_problem(k, x, w1_s, w3_s, a_shared);
+  GemmProblem down = expert_down_problem(k, expert_offsets, w2, y_perm);
+  if ((s = check_tc(k, up, n_up)) != MOE_OK) return s;
+  if ((s = check_tc(k, &down, 1)) != MOE_OK) return s;
+  MOE_TRY_CUDA(validate_offsets(expert_offsets, cfg->n_experts, pool_rows_of(*cfg), k.hdr(), k.st,
+                                false));
+  MOE_TRY_CUDA(run_gemms(k, up, n_up));
+  MOE_TRY_CUDA(run_gemms(k, &down, 1));
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* slot_of,
+                         const float* topk_gate, const void* a_shared, const void* w_up,
+                         const void* w2_s, void* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptrs({y_perm, slot_of, topk_gate, out}, {a_shared, w_up, w2_s})) != MOE_OK)
+    return s;
+  if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
+  Call k = make_call(cfg, ws, stream);
+  if (!w_up) {
+    CombineArgs ca = combine_args(k, y_perm, slot_of, topk_gate, out);
+    MOE_TRY_CUDA(combine_run(ca, cfg->dtype, k.st, k.pdl));
+    return MOE_OK;
+  }
+  if (cfg->n_shared > 0 && (!a_shared || !w2_s)) return MOE_ERR_INVALID_ARG;
+  GemmProblem p = back_problem(k, k.at<void>(k.L.c), w_up, a_shared, w2_s, out);
+  if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+  CombineArgs ca = combine_args(k, y_perm, slot_of, topk_gate, k.at<void>(k.L.c));
+  MOE_TRY_CUDA(combine_run(ca, cfg->dtype, k.st, k.pdl));
+  MOE_TRY_CUDA(run_gemms(k, &p, 1));
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, void* y,
+                         void* ws, size_t ws_bytes, void* stream, const moe_forward_aux_t* aux) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ptrs({x, y, w->w_router, w->w_down, w->rms_gamma, w->w1, w->w3, w->w2, w->w_up},
+                      {w->b_router})) != MOE_OK)
+    return s;
+  if (cfg->n_shared > 0 && (s = check_ptrs({w->w1_s, w->w3_s, w->w2_s}, {})) != MOE_OK) return s;
+  if (cfg->pool_rows != 0 && cfg->pool_rows < cfg->T * (int64_t)cfg->top_k)
+    return MOE_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
+  if (aux) {
+    if ((s = check_ptrs({}, {aux->topk_idx, aux->topk_gate, aux->expert_counts,
+                             aux->expert_offsets, aux->slot_of, aux->n_dropped})) != MOE_OK)
+      return s;
+  }
+  Call k = make_call(cfg, ws, stream);
+  const Layout& L = k.L;
+  const bool shared = cfg->n_shared > 0;
+  void* a_s = k.at<void>(L.a_s);
+  int32_t* idx = k.at<int32_t>(L.idx);
+  float* gate = k.at<float>(L.gate);
+  int32_t* offsets = k.at<int32_t>(L.offsets);
+  int32_t* slot_of = k.at<int32_t>(L.slot_of);
+
+  GemmProblem front[3] = {router_problem(k, x, w->w_router, w->b_router),
+                          down_problem(k, x, w->w_down)};
+  int n_front = 2;
+  if (shared) front[n_front++] = shared_problem(k, x, w->w1_s, w->w3_s, a_s);
+  GemmProblem up = expert_up_problem(k, k.at<void>(L.x_perm), offsets, w->w1, w->w3);
+  GemmProblem down = expert_down_problem(k, offsets, w->w2, k.at<void>(L.y_perm));
+  GemmProblem back = back_problem(k, k.at<void>(L.c), w->w_up, shared ? a_s : nullptr,
+                                  shared ? w->w2_s : nullptr, y);
+  if ((s = check_tc(k, front, n_front)) != MOE_OK) return s;
+  if ((s = check_tc(k, &up, 1)) != MOE_OK) return s;
+  if ((s = check_tc(k, &down, 1)) != MOE_OK) return s;
+  if ((s = check_tc(k, &back, 1)) != MOE_OK) return s;
+
+  RouterArgs ra = router_args(k, x, w->w_router, w->b_router, idx, gate);
+  DispatchArgs da = dispatch_args(k, idx, w->rms_gamma, k.at<int32_t>(L.counts), offsets,
+                                  k.at<int32_t>(L.perm), slot_of, k.at<int32_t>(L.ndrop),
+                                  k.at<void>(L.x_perm));
+  CombineArgs ca = combine_args(k, k.at<void>(L.y_perm), slot_of, gate, k.at<void>(L.c));
+
+  record(aux, 0, k.st);
+  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false));
+  MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
+  record(aux, 1, k.st);
+  MOE_TRY_CUDA(run_gemms(k, front, n_front));
+  record(aux, 2, k.st);
+  MOE_TRY_CUDA(router_select(ra, cfg->dtype, num_sms(), k.st, k.pdl));
+  record(aux, 3, k.st);
+  MOE_TRY_CUDA(dispatch_run(da, cfg->dtype, k.st, k.pdl));
+  record(aux, 4, k.st);
+  MOE_TRY_CUDA(run_gemms(k, &up, 1));
+  record(aux, 5, k.st);
+  MOE_TRY_CUDA(run_gemms(k, &down, 1));
+  record(aux, 6, k.st);
+  MOE_TRY_CUDA(combine_run(ca, cfg->dtype, k.st, k.pdl));
+  record(aux, 7, k.st);
+  MOE_TRY_CUDA(run_gemms(k, &back, 1));
+  record(aux, 8, k.st);
+
+  if (aux) {
+    const int64_t Tk = cfg->T * (int64_t)cfg->top_k;
+    auto cp = [&](void* dst, size_t off, size_t bytes) -> cudaError_t {
+      if (!dst) return cudaSuccess;
+      return cudaMemcpyAsync(dst, k.ws + off, bytes, cudaMemcpyDeviceToDevice, k.st);
+    };
+    MOE_TRY_CUDA(cp(aux->topk_idx, L.idx, Tk * 4));
+    MOE_TRY_CUDA(cp(aux->topk_gate, L.gate, Tk * 4));
+    MOE_TRY_CUDA(cp(aux->expert_counts, L.counts, (size_t)cfg->n_experts * 4));
+    MOE_TRY_CUDA(cp(aux->expert_offsets, L.offsets, ((size_t)cfg->n_experts + 1) * 4));
+    MOE_TRY_CUDA(cp(aux->slot_of, L.slot_of, Tk * 4));
+    MOE_TRY_CUDA(cp(aux->n_dropped, L.ndrop, 4));
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream,
+                                   moe_device_report_t* out) {
+  if (!ws || !out || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
+  DeviceHeader h;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  out->status = h.status;
+  out->detail = h.detail;
+  out->n_refined = h.n_refine;
+  out->n_exact = h.n_exact;
+  return MOE_OK;
+}
+
+moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(header_reset(static_cast<DeviceHeader*>(ws), true,
+                                  static_cast<cudaStream_t>(stream), false));
+}
+
+}  // extern "C"

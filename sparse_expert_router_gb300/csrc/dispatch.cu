@@ -1,0 +1,246 @@
+// Dispatch and combine: expert histogram, capacity clamp and exclusive scan (group offsets),
+// stable token permutation, RMSNorm-and-scatter of the latent rows, and the gate-weighted
+// ordered gather that combines expert outputs.
+//
+// The layer sends each token, projected down and normalised, to its experts and combines
+// their outputs with the gates ("Marin 535B-A23B: the half of a training run nobody usually
+// shows you", section "What is actually being trained"). Rows reach the expert GEMMs grouped
+// by expert, in token order within an expert (section "21% to 27% MFU without stopping the
+// run"); assignments past an expert's capacity are dropped and the token skips that expert
+// ("Marin Begins Open Training of a 535B-Parameter MoE Model", section 2). The combine is an
+// ordered gather rather than an atomic scatter-add, so repeated runs are bitwise identical
+// (weekly summary of 2026-09-14, post-training epic, #9144).
+#include "common.cuh"
+#include "dispatch.h"
+
+namespace moe {
+namespace {
+
+constexpr int CH = 128;   // tokens per dispatch chunk (one thread per token)
+
+__global__ void header_reset_kernel(DeviceHeader* h, int clear_status) {
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    if (clear_status) { h->status = 0; h->detail = 0; }
+    h->n_refine = 0;
+    h->n_exact = 0;
+  }
+}
+
+// An assignment (t, j) is valid when its expert id is in range and the token's ids ascend.
+__device__ __forceinline__ bool valid_assignment(const int32_t* row, int j, int E) {
+  int e = row[j];
+  return e >= 0 && e < E && (j == 0 || row[j - 1] < e);
+}
+
+__global__ void __launch_bounds__(CH) hist_kernel(DispatchArgs a) {
+  pdl_wait();
+  extern __shared__ int s_cnt[];
+  for (int e = threadIdx.x; e < a.E; e += CH) s_cnt[e] = 0;
+  __syncthreads();
+  int64_t t = (int64_t)blockIdx.x * CH + threadIdx.x;
+  if (t < a.T) {
+    const int32_t* row = a.idx + t * a.k;
+    for (int j = 0; j < a.k; ++j) {
+      if (valid_assignment(row, j, a.E)) atomicAdd(&s_cnt[row[j]], 1);
+      else report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += CH)
+    a.chunk_hist[(int64_t)blockIdx.x * a.E + e] = s_cnt[e];
+}
+
+// One block: per-expert walk over chunks (chunk bases, counts), capacity clamp, scan.
+__global__ void __launch_bounds__(1024) scan_kernel(DispatchArgs a) {
+  pdl_wait();
+  __shared__ int s_warp[32];
+  __shared__ int s_drop[32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int cnt = 0;
+  if (e < a.E) {
+    for (int c = 0; c < a.n_chunks; ++c) {
+      int64_t o = (int64_t)c * a.E + e;
+      int v = a.chunk_hist[o];
+      a.chunk_base[o] = cnt;
+      cnt += v;
+    }
+    a.counts[e] = cnt;
+  }
+  int kept = (a.cap >= 0) ? min(cnt, a.cap) : cnt;
+  int drop = cnt - kept;
+  // block exclusive scan of kept over experts
+  int incl = kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int wdrop = drop;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) wdrop += __shfl_xor_sync(~0u, wdrop, o);
+  if (lane == 31) s_warp[warp] = incl;
+  if (lane == 0) s_drop[warp] = wdrop;
+  __syncthreads();
+  if (warp == 0) {
+    int v = s_warp[lane], dv = s_drop[lane];
+    int iv = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(~0u, iv, o);
+      if (lane >= o) iv += u;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) dv += __shfl_xor_sync(~0u, dv, o);
+    s_warp[lane] = iv - v;   // exclusive prefix of warp totals
+    if (lane == 0) s_drop[0] = dv;
+  }
+  __syncthreads();
+  int excl = s_warp[warp] + incl - kept;
+  if (e < a.E) a.offsets[e] = excl;
+  if (e == a.E - 1) a.offsets[a.E] = excl + kept;
+  if (e == 0 && a.n_dropped) *a.n_dropped = s_drop[0];
+}
+
+// Slots: stable rank of each token among the tokens of its chunk that chose the same expert
+// (bitmask per expert and popcount), plus the chunk's base.
+__global__ void __launch_bounds__(CH) rank_kernel(DispatchArgs a) {
+  pdl_wait();
+  extern __shared__ uint32_t s_mask[];   // [E][CH / 32]
+  constexpr int W = CH / 32;
+  for (int i = threadIdx.x; i < a.E * W; i += CH) s_mask[i] = 0u;
+  __syncthreads();
+  const int tl = threadIdx.x;
+  const int64_t t = (int64_t)blockIdx.x * CH + tl;
+  const int32_t* row = a.idx + t * a.k;
+  if (t < a.T)
+    for (int j = 0; j < a.k; ++j)
+      if (valid_assignment(row, j, a.E)) atomicOr(&s_mask[row[j] * W + (tl >> 5)], 1u << (tl & 31));
+  __syncthreads();
+  if (t >= a.T) return;
+  for (int j = 0; j < a.k; ++j) {
+    int32_t slot = -1;
+    if (valid_assignment(row, j, a.E)) {
+      const int e = row[j];
+      int r = __popc(s_mask[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u));
+      for (int w = 0; w < (tl >> 5); ++w) r += __popc(s_mask[e * W + w]);
+      r += a.chunk_base[(int64_t)blockIdx.x * a.E + e];
+      if (a.cap < 0 || r < a.cap) {
+        slot = a.offsets[e] + r;
+        if (slot >= a.pool_rows) { report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t); slot = -1; }
+        else a.perm[slot] = (int32_t)(t * a.k + j);
+      }
+    }
+    a.slot_of[t * a.k + j] = slot;
+  }
+}
+
+// h = z * rsqrt(mean(z^2) + eps) * gamma written to every kept slot of the token.
+template <typename T>
+__global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
+  pdl_wait();
+  __shared__ float s_red[4];
+  const int64_t t = blockIdx.x;
+  const float* z = a.z + t * a.L;
+  float ss = 0.0f;
+  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+    float v[8];
+    ld8(z + i, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(~0u, ss, o);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  ss = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+  const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)a.L), a.eps)));
+  int32_t slots[32];
+  int ns = 0;
+  for (int j = 0; j < a.k; ++j) {
+    int32_t s = a.slot_of[t * a.k + j];
+    if (s >= 0 && s < a.pool_rows) slots[ns++] = s;
+  }
+  T* xp = static_cast<T*>(a.x_perm);
+  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+    float v[8], g[8];
+    ld8(z + i, v);
+    ld8(a.gamma + i, g);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = v[q] * rstd * g[q];
+    for (int j = 0; j < ns; ++j) st8(xp + (int64_t)slots[j] * a.L + i, v);
+  }
+}
+
+// c[t] = sum_j gate[t, j] * y_perm[slot_of[t, j]] over kept j, in order j = 0..k-1.
+template <typename T>
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  pdl_wait();
+  const int64_t t = blockIdx.x;
+  int32_t slots[32];
+  float gates[32];
+  int ns = 0;
+  for (int j = 0; j < a.k; ++j) {
+    int32_t s = a.slot_of[t * a.k + j];
+    if (s >= a.pool_rows || s < -1) {
+      if (threadIdx.x == 0) report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
+      continue;
+    }
+    if (s >= 0) { slots[ns] = s; gates[ns] = a.gate[t * a.k + j]; ++ns; }
+  }
+  const T* yp = static_cast<const T*>(a.y_perm);
+  T* out = static_cast<T*>(a.out);
+  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < ns; ++j) {
+      float v[8];
+      ld8(yp + (int64_t)slots[j] * a.L + i, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(gates[j], v[q], acc[q]);
+    }
+    st8(out + t * a.ld_out + i, acc);
+  }
+}
+
+__global__ void validate_offsets_kernel(const int32_t* off, int G, int64_t rows, DeviceHeader* h) {
+  pdl_wait();
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+    int v = off[g];
+    bool bad = v < 0 || v > rows || (g > 0 && off[g - 1] > v);
+    if (bad) report_error(h, MOE_ERR_BAD_ROUTING, g);
+  }
+}
+
+}  // namespace
+
+cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl) {
+  return launch(header_reset_kernel, dim3(1), dim3(32), 0, st, pdl, h, clear_status ? 1 : 0);
+}
+
+int64_t dispatch_chunks(int64_t T) { return cdiv(T, CH); }
+
+cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool pdl) {
+  cudaError_t err;
+  const unsigned nch = (unsigned)a.n_chunks;
+  err = launch(hist_kernel, dim3(nch), dim3(CH), (size_t)a.E * 4, st, pdl, a);
+  if (err != cudaSuccess) return err;
+  err = launch(scan_kernel, dim3(1), dim3(1024), 0, st, pdl, a);
+  if (err != cudaSuccess) return err;
+  err = launch(rank_kernel, dim3(nch), dim3(CH), (size_t)a.E * (CH / 32) * 4, st, pdl, a);
+  if (err != cudaSuccess) return err;
+  if (a.x_perm == nullptr) return cudaSuccess;
+  if (dtype == DT_BF16) return launch(gather_kernel<bf16>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
+  return launch(gather_kernel<float>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
+}
+
+cudaError_t combine_run(const CombineArgs& a, int dtype, cudaStream_t st, bool pdl) {
+  if (dtype == DT_BF16) return launch(combine_kernel<bf16>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
+  return launch(combine_kernel<float>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
+}
+
+cudaError_t validate_offsets(const int32_t* off, int G, int64_t rows, DeviceHeader* h,
+                             cudaStream_t st, bool pdl) {
+  return launch(validate_offsets_kernel, dim3(1), dim3(256), 0, st, pdl, off, G, rows, h);
+}
+
+}  // namespace moe

@@ -1,0 +1,53 @@
+// GEMM problem description shared by the CUDA-core and the tcgen05 GEMM kernels.
+//
+// One problem computes, for every row r and output column c in [0, M):
+//   acc(r, c) = sum over segments s of  sum_k act_s[r, k] * W_s[group][k, col]
+// and writes an epilogue of acc to out[r, out_col0 + c]. Row grouping follows the expert
+// layout of the layer: GROUP_ROWS takes the rows of group g from offsets[g]..offsets[g+1]
+// and uses expert g's weights (the grouped expert GEMM over ragged groups); GROUP_COLS uses
+// one weight matrix per block of Mg output columns for every row (the shared experts, stacked
+// [S, d, F_s]); GROUP_NONE is a plain dense GEMM.
+#pragma once
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+enum Epi { EPI_F32 = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
+enum GroupMode { GROUP_NONE = 0, GROUP_ROWS = 1, GROUP_COLS = 2 };
+
+struct GemmSeg {
+  const void* act;   // [rows, K] row-major (leading dimension K)
+  const void* w;     // NONE: [K, M]; ROWS: [G, K, M]; COLS: [M / Mg, K, Mg]
+  const void* w3;    // EPI_SWIGLU: the up-projection weights, same layout as w
+  int K;
+};
+
+struct GemmProblem {
+  int epi = EPI_STORE;
+  int group = GROUP_NONE;
+  int M = 0;                 // output columns
+  int Mg = 0;                // GROUP_COLS: columns per weight matrix
+  int n_seg = 1;
+  GemmSeg seg[2] = {};
+  const int32_t* offsets = nullptr;  // GROUP_ROWS: [G + 1], device
+  int G = 1;
+  int64_t rows = 0;          // rows of act and out (GROUP_ROWS: physical rows; offsets clamp to it)
+  void* out = nullptr;
+  int64_t ld_out = 0;        // elements per output row
+  int out_col0 = 0;
+  const float* bias = nullptr;  // EPI_F32: [M] or NULL
+  int dtype = 0;             // DT_BF16 / DT_F32: act, weights and EPI_STORE/EPI_SWIGLU output
+};
+
+// CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).
+cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl);
+
+// tcgen05 GEMM (bf16 operands, fp32 accumulation in tensor memory). Up to 3 problems share
+// one persistent launch. Returns cudaErrorNotSupported when a problem does not fit its rules.
+cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cudaStream_t stream,
+                    bool pdl);
+bool gemm_tc_supported(const GemmProblem& p);
+
+}  // namespace moe

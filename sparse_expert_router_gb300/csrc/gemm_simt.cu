@@ -1,0 +1,133 @@
+// CUDA-core GEMM for the fp32 configuration and as the bf16 cross-check path.
+//
+// 64 x 64 output tile per 256-thread block, 4 x 4 outputs per thread, k staged 16 at a time
+// through shared memory. Every output is accumulated sequentially over k with fused
+// multiply-adds, so its rounding error is bounded by gamma_K * sum_k |a_k w_k| (the router's
+// certified top-k relies on this bound).
+#include "common.cuh"
+#include "gemm.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
+
+template <typename T>
+__device__ __forceinline__ const T* weight_ptr(const GemmProblem& p, const GemmSeg& s,
+                                               const void* base, int g, int k, int c) {
+  const T* w = static_cast<const T*>(base);
+  if (p.group == GROUP_ROWS) return w + ((int64_t)g * s.K + k) * p.M + c;
+  if (p.group == GROUP_COLS) return w + ((int64_t)(c / p.Mg) * s.K + k) * p.Mg + (c % p.Mg);
+  return w + (int64_t)k * p.M + c;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
+  pdl_wait();
+  __shared__ float sA[BK][BM + 4];
+  __shared__ float sW[BK][BN];
+  __shared__ float sW3[BK][BN];
+  __shared__ int s_g, s_r0, s_r1;
+
+  const int tid = threadIdx.x;
+  const int c0 = blockIdx.y * BN;
+  if (tid == 0) {
+    int g = 0, r0 = 0, r1 = 0;
+    if (p.group == GROUP_ROWS) {
+      // map the linear tile index onto (group, row tile) with clamped, monotone offsets
+      int64_t want = blockIdx.x, prev = 0;
+      g = -1;
+      for (int gg = 0; gg < p.G; ++gg) {
+        int64_t lo = imin64(imax64((int64_t)p.offsets[gg], prev), p.rows);
+        int64_t hi = imin64(imax64((int64_t)p.offsets[gg + 1], lo), p.rows);
+        prev = hi;
+        int64_t nt = (hi - lo + BM - 1) / BM;
+        if (want < nt) { g = gg; r0 = (int)(lo + want * BM); r1 = (int)imin64(hi, (int64_t)r0 + BM); break; }
+        want -= nt;
+      }
+    } else {
+      r0 = blockIdx.x * BM;
+      r1 = (int)imin64(p.rows, (int64_t)r0 + BM);
+    }
+    s_g = g; s_r0 = r0; s_r1 = r1;
+  }
+  __syncthreads();
+  const int g = s_g, r0 = s_r0, r1 = s_r1;
+  if (g < 0 || r0 >= r1) return;
+
+  const bool glu = (p.epi == EPI_SWIGLU);
+  const int tx = tid % 16, ty = tid / 16;   // thread owns rows ty*4.., cols tx*4..
+  float acc[4][4] = {}, acc3[4][4] = {};
+
+  for (int si = 0; si < p.n_seg; ++si) {
+    const GemmSeg& s = p.seg[si];
+    const T* act = static_cast<const T*>(s.act);
+    for (int k0 = 0; k0 < s.K; k0 += BK) {
+      // stage A: 64 rows x 16 k (4 elements per thread)
+      for (int i = tid; i < BM * BK; i += NT) {
+        int rr = i / BK, kk = i % BK;
+        int r = r0 + rr, k = k0 + kk;
+        sA[kk][rr] = (r < r1 && k < s.K) ? ld_f(act, (int64_t)r * s.K + k) : 0.0f;
+      }
+      // stage W (and W3): 16 k x 64 columns
+      for (int i = tid; i < BK * BN; i += NT) {
+        int kk = i / BN, cc = i % BN;
+        int k = k0 + kk, c = c0 + cc;
+        bool ok = (k < s.K && c < p.M);
+        sW[kk][cc] = ok ? ld_f(weight_ptr<T>(p, s, s.w, g, k, c), 0) : 0.0f;
+        if (glu) sW3[kk][cc] = ok ? ld_f(weight_ptr<T>(p, s, s.w3, g, k, c), 0) : 0.0f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) {
+        float a[4], w[4], w3[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = sA[kk][ty * 4 + i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { w[j] = sW[kk][tx * 4 + j]; w3[j] = glu ? sW3[kk][tx * 4 + j] : 0.0f; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+            if (glu) acc3[i][j] = fmaf(a[i], w3[j], acc3[i][j]);
+          }
+      }
+      __syncthreads();
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int r = r0 + ty * 4 + i;
+    if (r >= r1) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int c = c0 + tx * 4 + j;
+      if (c >= p.M) continue;
+      int64_t o = (int64_t)r * p.ld_out + p.out_col0 + c;
+      if (p.epi == EPI_F32) {
+        float v = acc[i][j];
+        if (p.bias) v = __fadd_rn(v, p.bias[c]);
+        static_cast<float*>(p.out)[o] = v;
+      } else if (p.epi == EPI_SWIGLU) {
+        st_f(static_cast<T*>(p.out), o, swiglu(acc[i][j], acc3[i][j]));
+      } else {
+        st_f(static_cast<T*>(p.out), o, acc[i][j]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl) {
+  if (p.rows <= 0 || p.M <= 0) return cudaSuccess;
+  int64_t tiles = cdiv(p.rows, BM) + (p.group == GROUP_ROWS ? p.G : 0);
+  dim3 grid((unsigned)tiles, (unsigned)cdiv(p.M, BN));
+  if (p.dtype == DT_BF16)
+    return launch(simt_gemm_kernel<bf16>, grid, dim3(NT), 0, stream, pdl, p);
+  return launch(simt_gemm_kernel<float>, grid, dim3(NT), 0, stream, pdl, p);
+}
+
+}  // namespace moe

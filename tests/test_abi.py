@@ -1,0 +1,121 @@
+"""The C-ABI library: loads without a GPU, exports every declared symbol, and rejects bad
+arguments with status codes before touching the device (CPU only)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_expert_router_gb300.build import build_library
+    build_library()
+    import sparse_expert_router_gb300 as m
+    return m.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_api():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_workspace_size", "moe_get_device_status"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    from sparse_expert_router_gb300 import _lib
+    path = _lib.LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (moe_\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+    # nothing else of ours leaks out of the library
+    assert exported == set(declared_functions())
+    # the binding wraps every declared entry point under the same name
+    assert set(_lib.SIGNATURES) == set(declared_functions())
+
+
+def _cfg(**kw):
+    import sparse_expert_router_gb300 as m
+    base = dict(T=256, d_model=256, d_latent=128, n_experts=16, top_k=2, d_ff=128, n_shared=1,
+                d_ff_shared=256, dtype="f32")
+    base.update(kw)
+    return m.LayerConfig(**base)
+
+
+def _ws(lib, cfg):
+    n = C.c_size_t(0)
+    assert lib.moe_workspace_size(C.byref(cfg.c()), C.byref(n)) == 0
+    return n.value
+
+
+def test_workspace_size_and_config_errors(lib):
+    from sparse_expert_router_gb300 import _lib as L
+    n = _ws(lib, _cfg())
+    assert n > 0 and n % 256 == 0
+    assert _ws(lib, _cfg(T=512)) > n
+    bad = [(dict(top_k=17), L.MOE_ERR_INVALID_ARG), (dict(T=0), L.MOE_ERR_INVALID_ARG),
+           (dict(n_experts=2048, top_k=2), L.MOE_ERR_UNSUPPORTED),
+           (dict(top_k=33, n_experts=64), L.MOE_ERR_UNSUPPORTED),
+           (dict(d_model=250), L.MOE_ERR_ALIGNMENT),
+           (dict(dtype="bf16", n_experts=12), L.MOE_ERR_ALIGNMENT),
+           (dict(capacity=(11, 0)), L.MOE_ERR_INVALID_ARG)]
+    for kw, code in bad:
+        c = _cfg(**kw)
+        assert lib.moe_workspace_size(C.byref(c.c()), C.byref(C.c_size_t())) == code, kw
+    assert lib.moe_workspace_size(None, C.byref(C.c_size_t())) == L.MOE_ERR_INVALID_ARG
+
+
+def test_argument_errors_before_any_launch(lib):
+    """Fake but aligned pointers: every call must fail validation without dereferencing them."""
+    from sparse_expert_router_gb300 import _lib as L
+    cfg = _cfg()
+    c = C.byref(cfg.c())
+    n = _ws(lib, cfg)
+    P = lambda v: C.c_void_p(v)
+    good, odd, ws = P(0x10000), P(0x10008), P(0x100000)
+    # NULL required pointer
+    assert lib.moe_route(c, None, good, None, good, good, ws, n, None) == L.MOE_ERR_INVALID_ARG
+    # misaligned pointer
+    assert lib.moe_route(c, odd, good, None, good, good, ws, n, None) == L.MOE_ERR_ALIGNMENT
+    # workspace too small / misaligned
+    assert lib.moe_route(c, good, good, None, good, good, ws, n - 256, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_route(c, good, good, None, good, good, P(0x100080), n, None) == L.MOE_ERR_ALIGNMENT
+    assert lib.moe_permute(c, good, good, good, good, good, good, good, good, None, None, ws, n,
+                           None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_ffn(c, good, good, good, good, None, good, None, None, None, None, ws, n,
+                              None) == L.MOE_ERR_INVALID_ARG
+    # shared experts requested without their weights
+    assert lib.moe_expert_ffn(c, good, good, good, good, good, good, good, None, None, good, ws,
+                              n, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(c, good, good, None, None, None, None, good, ws, n, None) == \
+        L.MOE_ERR_INVALID_ARG
+    w = L.moe_weights_t(w_router=0x10000, w_down=0x10000, rms_gamma=0x10000, w1=0x10000,
+                        w3=0x10000, w2=0x10000, w1_s=0x10000, w3_s=0x10000, w2_s=None,
+                        w_up=0x10000)
+    assert lib.moe_forward(c, C.byref(w), good, good, ws, n, None, None) == L.MOE_ERR_INVALID_ARG
+    cfg2 = _cfg(pool_rows=100)                      # fewer pool rows than T * k
+    assert lib.moe_forward(C.byref(cfg2.c()), C.byref(w), good, good, ws, n, None, None) == \
+        L.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_device_status(None, 256, None, None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    from sparse_expert_router_gb300 import _lib
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            _lib.load(str(tmp_path / "nope.so"))
+    finally:
+        _lib._lib = saved

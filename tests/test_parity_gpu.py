@@ -1,0 +1,273 @@
+"""Parity of the CUDA library (through its C ABI) with the fp64 oracle on seeded inputs.
+
+Bar: routing indices, expert counts, offsets, slots and drops bit-exact; gates within 1e-6
+(fp32 configuration) / 1e-5 (bf16); outputs within a normwise relative error of 1e-5 (fp32)
+and 2e-2 (bf16 storage of the intermediates, fp32 accumulation).
+"""
+import pytest
+import torch
+
+import sparse_expert_router_gb300 as m
+from moe_workloads import SHAPES, SLICE_C5B, make_layer_inputs, make_slice_inputs
+from oracle import moe_oracle
+
+from gpu_cases import (DEV, check_routing, gpu_inputs, normwise, oracle_forward, run_forward,
+                       sample_tokens)
+
+pytestmark = pytest.mark.gpu
+
+# the bf16 GEMM paths under test: tensor cores (default) and the CUDA-core cross-check
+BF16_PATHS = {"simt": m.MOE_FLAG_SIMT}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# ------------------------------------------------------------------ full layer, small ----
+
+@pytest.mark.parametrize("cap", [None, (11, 10), (1, 2)], ids=["nocap", "cf110", "cf050"])
+def test_tiny_f32_forward(cap):
+    shape = SHAPES["tiny_f32"].with_(capacity=cap)
+    inp = gpu_inputs(shape)
+    got = run_forward(shape, inp)
+    ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()})
+    check_routing(got, ref, shape)
+    if cap == (1, 2):
+        assert int(ref["n_dropped"]) > 0
+    err = normwise(got["y"], ref["y"])
+    assert err <= 1e-5, err
+    assert got["report"]["status"] == 0
+
+
+@pytest.mark.parametrize("path", list(BF16_PATHS))
+def test_small_bf16_forward(path):
+    shape = SHAPES["small_bf16"]
+    inp = gpu_inputs(shape)
+    got = run_forward(shape, inp, BF16_PATHS[path])
+    toks = sample_tokens(shape.T, 256)
+    ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()}, tokens=toks)
+    check_routing(got, ref, shape)
+    err = normwise(got["y"][toks], ref["y"])
+    assert err <= 2e-2, err
+    assert got["report"]["status"] == 0
+
+
+def test_forward_deterministic():
+    shape = SHAPES["small_bf16"].with_(T=1024)
+    inp = gpu_inputs(shape)
+    for flags in BF16_PATHS.values():
+        a = run_forward(shape, inp, flags)
+        b = run_forward(shape, inp, flags)
+        assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
+        assert torch.equal(a["topk_gate"], b["topk_gate"])
+
+
+# ---------------------------------------------------------------------- split calls ----
+
+def test_split_calls_tiny_f32():
+    shape = SHAPES["tiny_f32"].with_(capacity=(1, 2))
+    cfg = m.LayerConfig.from_shape(shape)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    T, k, E, L, F = shape.T, shape.top_k, shape.n_experts, shape.d_latent, shape.d_ff
+    ws = m.alloc_workspace(cfg, DEV)
+    ref = oracle_forward(shape, cpu)
+
+    # moe_route
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(cfg, inp["x"], inp["w_router"], inp["b_router"], idx, gate, ws)
+    assert torch.equal(idx.cpu().long(), ref["idx"])
+    assert float((gate.cpu().double() - ref["gate"]).abs().max()) <= 1e-6
+
+    # moe_permute on the oracle's routing
+    oidx = ref["idx"].to(torch.int32).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.full((T * k,), -5, dtype=torch.int32, device=DEV)
+    slot = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ndrop = torch.empty(1, dtype=torch.int32, device=DEV)
+    x_perm = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], oidx, counts, offs, perm, slot,
+                  ndrop, x_perm, ws)
+    assert torch.equal(counts.cpu().long(), ref["counts"])
+    assert torch.equal(offs.cpu().long(), ref["offsets"])
+    assert torch.equal(slot.cpu().long(), ref["slot_of"])
+    R = int(ref["offsets"][-1])
+    assert torch.equal(perm.cpu().long()[:R], ref["perm"])
+    assert int(ndrop.cpu()) == int(ref["n_dropped"])
+    # rows of x_perm are the normalised latent of their token
+    tok = ref["perm"] // k
+    assert normwise(x_perm[:R], ref["h"][tok]) <= 1e-5
+
+    # moe_expert_ffn on the oracle's grouped rows (rounded to the storage type)
+    xp = ref["h"][tok].float().to(DEV)
+    y_perm = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    a_s = torch.empty((T, shape.n_shared * shape.d_ff_shared), dtype=torch.float32, device=DEV)
+    offs_in = ref["offsets"].to(torch.int32).to(DEV)
+    xp_full = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    xp_full[:R] = xp
+    m.moe_expert_ffn(cfg, xp_full, offs_in, inp["w1"], inp["w3"], inp["w2"], y_perm, inp["x"],
+                     inp["w1_s"], inp["w3_s"], a_s, ws)
+    _, o_ref = moe_oracle.grouped_experts(xp_full.cpu(), ref["offsets"].tolist(), cpu["w1"],
+                                          cpu["w3"], cpu["w2"])
+    assert normwise(y_perm[:R], o_ref) <= 1e-5
+    assert float(y_perm[R:].abs().max()) == 0.0          # rows past the groups untouched
+    assert normwise(a_s, ref["a_s"]) <= 1e-5
+
+    # moe_combine without and with the up-projection
+    yp_in = o_ref.float().to(DEV)
+    yp_full = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    yp_full[:R] = yp_in
+    c = torch.empty((T, L), dtype=torch.float32, device=DEV)
+    ogate = ref["gate"].float().to(DEV)
+    oslot = ref["slot_of"].to(torch.int32).to(DEV)
+    m.moe_combine(cfg, yp_full, oslot, ogate, c, ws)
+    c_ref = moe_oracle.combine(yp_full.cpu(), ref["slot_of"], ogate.cpu())
+    assert normwise(c, c_ref) <= 1e-6
+    y = torch.empty((T, shape.d_model), dtype=torch.float32, device=DEV)
+    m.moe_combine(cfg, yp_full, oslot, ogate, y, ws, a_shared=ref["a_s"].float().to(DEV),
+                  w_up=inp["w_up"], w2_s=inp["w2_s"])
+    y_ref = c_ref @ cpu["w_up"].double() + ref["a_s"] @ cpu["w2_s"].double().reshape(-1, shape.d_model)
+    assert normwise(y, y_ref) <= 1e-5
+    assert m.moe_get_device_status(ws)["status"] == 0
+
+
+# ----------------------------------------------------------- router exactness stress ----
+
+def _near_tie_router(T=512, d=256, E=64, seed=3):
+    """bf16 router inputs built to defeat fp32 logits: duplicated expert columns (exact
+    ties, to be broken by the lower index) and columns that differ only in an element
+    weighted by 2^-30 (gaps far below fp32 resolution), plus reordered columns."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, d, generator=g)
+    x[:, -1] = 2.0 ** -30                           # a tiny coordinate shared by all tokens
+    x = x.to(torch.bfloat16)
+    base = torch.randn(d, 8, generator=g) * d ** -0.5
+    cols = []
+    for e in range(E):
+        c = base[:, e % 8].clone()
+        if e % 3 == 1:
+            c[-1] += 1.0                          # larger by 2^-30 in exact arithmetic
+        if e % 5 == 2:
+            c[:-1] = c[:-1][torch.randperm(d - 1, generator=g)]
+        cols.append(c)
+    w = torch.stack(cols, 1).to(torch.bfloat16)
+    return x, w
+
+
+@pytest.mark.parametrize("path", list(BF16_PATHS))
+def test_router_exact_on_near_ties(path):
+    x, w = _near_tie_router()
+    T, d = x.shape
+    E, k = w.shape[1], 8
+    cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,
+                        d_ff_shared=0, dtype="bf16", flags=BF16_PATHS[path])
+    ws = m.alloc_workspace(cfg, DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(cfg, x.to(DEV), w.to(DEV), None, idx, gate, ws)
+    rep = m.moe_get_device_status(ws)
+    ref = moe_oracle.route(x, w, None, k)
+    assert torch.equal(idx.cpu().long(), ref["idx"])
+    assert rep["status"] == 0
+    assert rep["n_refined"] > 0 and rep["n_exact"] > 0, rep      # every stage exercised
+
+
+# ------------------------------------------------------------ device-detected errors ----
+
+def test_bad_routing_is_reported_not_faulted():
+    shape = SHAPES["tiny_f32"]
+    cfg = m.LayerConfig.from_shape(shape)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    T, k, E, L = shape.T, shape.top_k, shape.n_experts, shape.d_latent
+    ws = m.alloc_workspace(cfg, DEV)
+    bad = torch.stack([torch.arange(k) for _ in range(T)]).to(torch.int32)
+    bad[5, 1] = E + 3                                # out of range
+    bad[9] = torch.tensor([4, 4])                    # repeated expert
+    bad = bad.to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    slot = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    x_perm = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    m.moe_clear_device_status(ws)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], bad, counts, offs, perm, slot,
+                  None, x_perm, ws)
+    rep = m.moe_get_device_status(ws)
+    assert rep["status"] == 6, rep                   # MOE_ERR_BAD_ROUTING
+    assert int(slot[5, 1]) == -1 and int(slot[9, 1]) == -1
+    assert int(counts.sum()) == T * k - 2
+
+    # non-monotone offsets into the grouped GEMM: reported, and nothing out of range runs
+    m.moe_clear_device_status(ws)
+    offs_bad = torch.tensor([0, 40, 20, 10**6] + [10**6] * (E - 3), dtype=torch.int32, device=DEV)
+    y_perm = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    m.moe_expert_ffn(cfg, x_perm, offs_bad, inp["w1"], inp["w3"], inp["w2"], y_perm, ws=ws)
+    rep = m.moe_get_device_status(ws)
+    assert rep["status"] == 6, rep
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------- 535B-shaped ----
+
+LARGE = ["l535b_t8192", "l535b_zipf_t16384", "l535b_zipf_t16384_cf110", "l535b_t65536"]
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_large_layer(name):
+    """Full routing and dispatch checked bit-exactly on every token; outputs on a seeded
+    sample of tokens (each token's output depends only on its own row and routing), with the
+    hottest expert's first tokens and dropped tokens added to the sample."""
+    shape = SHAPES[name]
+    inp = gpu_inputs(shape)
+    path = "tc" if "tc" in BF16_PATHS else "simt"
+    got = run_forward(shape, inp, BF16_PATHS[path])
+    counts = got["expert_counts"].cpu()
+    hot = int(counts.argmax())
+    hot_tokens = (got["topk_idx"].cpu() == hot).any(1).nonzero().flatten()[:4].tolist()
+    dropped = (got["slot_of"].cpu() < 0).any(1).nonzero().flatten()[:4].tolist()
+    toks = sample_tokens(shape.T, 12, extra=hot_tokens + dropped)
+    ref = oracle_forward(shape, inp, tokens=toks)
+    check_routing(got, ref, shape)
+    if shape.routing == "zipf":
+        assert int((counts == 0).sum()) > 0                      # experts with no rows
+        assert float(counts.max()) > 20 * shape.T * shape.top_k / shape.n_experts
+    if shape.capacity:
+        assert int(ref["n_dropped"]) > 0
+    err = normwise(got["y"][toks], ref["y"])
+    assert err <= 2e-2, err
+    assert got["report"]["status"] == 0
+    del inp, got
+    torch.cuda.empty_cache()
+
+
+def test_expert_slice():
+    """One expert-parallel rank's slice: grouped GEMMs over the active rows of a padded pool,
+    then the gate-weighted un-permute back to arrival order."""
+    sh = SLICE_C5B
+    inp = make_slice_inputs(sh, DEV)
+    cfg = m.LayerConfig(T=sh.rows, d_model=sh.d_latent, d_latent=sh.d_latent, n_experts=sh.n_local,
+                        top_k=1, d_ff=sh.d_ff, n_shared=0, d_ff_shared=0, dtype=sh.dtype,
+                        pool_rows=sh.pool_rows,
+                        flags=BF16_PATHS["tc" if "tc" in BF16_PATHS else "simt"])
+    ws = m.alloc_workspace(cfg, DEV)
+    y_perm = torch.full((sh.pool_rows, sh.d_latent), 7.0, dtype=torch.bfloat16, device=DEV)
+    m.moe_expert_ffn(cfg, inp["pool"], inp["expert_offsets"], inp["w1"], inp["w3"], inp["w2"],
+                     y_perm, ws=ws)
+    out = torch.empty((sh.rows, sh.d_latent), dtype=torch.bfloat16, device=DEV)
+    m.moe_combine(cfg, y_perm, inp["slot_of"].view(-1, 1), inp["gate"].view(-1, 1), out, ws)
+    torch.cuda.synchronize()
+    n_act = int(inp["expert_offsets"][-1])
+    assert bool((y_perm[n_act:] == 7.0).all())                  # padding never computed
+    pos = sample_tokens(sh.rows, 24)
+    ref = moe_oracle.slice_rows(inp, pos)
+    assert normwise(y_perm[ref["rows"].to(DEV)], ref["y_perm"]) <= 2e-2
+    assert normwise(out[pos], ref["out"]) <= 2e-2
+    assert m.moe_get_device_status(ws)["status"] == 0
