@@ -26,8 +26,13 @@
  *   - Layouts: all matrices are row-major and densely packed. Activations and weights have
  *     the element type cfg->dtype (bf16 or fp32); b_router, rms_gamma and gates are fp32;
  *     indices, counts, offsets and slots are int32.
- *   - Alignment: every pointer must be 16-byte aligned and, for bf16, d_model, d_latent, d_ff,
- *     d_ff_shared and n_experts must be multiples of 8 (MOE_ERR_ALIGNMENT otherwise).
+ *   - Alignment: every pointer must be 16-byte aligned; d_model, d_latent, d_ff and d_ff_shared
+ *     must be multiples of 8, and so must n_experts for the bf16 router (moe_route,
+ *     moe_forward); MOE_ERR_ALIGNMENT otherwise.
+ *   - Workspace: caller-owned device memory of moe_workspace_size() bytes, 256-byte aligned. Its
+ *     first 256 bytes hold the device report; clear them once after allocating the workspace
+ *     (moe_clear_device_status, or zero-filled memory). moe_forward clears the report itself;
+ *     the split calls accumulate into it.
  *   - Errors: argument errors return before anything is enqueued. A failed launch returns
  *     MOE_ERR_CUDA. Errors found on the device (an out-of-range expert id or slot, offsets that
  *     are not monotone, a device wait that timed out) are recorded in a status word inside the

@@ -91,8 +91,9 @@ def workspace_size(cfg: LayerConfig) -> int:
 
 
 def alloc_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
-    """A caller-owned workspace of the right size (torch's allocator aligns it to 256 bytes)."""
-    return torch.empty(workspace_size(cfg), dtype=torch.uint8, device=device)
+    """A caller-owned, zero-filled workspace of the right size (torch's allocator aligns it to
+    256 bytes); zero fill clears the device report it starts with."""
+    return torch.zeros(workspace_size(cfg), dtype=torch.uint8, device=device)
 
 
 def moe_route(cfg, x, w_router, b_router, topk_idx, topk_gate, ws, stream=None):

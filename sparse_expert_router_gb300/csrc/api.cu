@@ -84,8 +84,12 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if ((c->d_model % 8) || (c->d_latent % 8) || (c->d_ff % 8) ||
       (c->n_shared > 0 && (c->d_ff_shared % 8)))
     return MOE_ERR_ALIGNMENT;
-  if (c->dtype == MOE_BF16 && (c->n_experts % 8)) return MOE_ERR_ALIGNMENT;
   return MOE_OK;
+}
+
+// The router weight [d, E] is read by TMA in the bf16 tensor-core path: 16-byte row pitch.
+moe_status_t check_router_width(const moe_config_t* c) {
+  return (c->dtype == MOE_BF16 && (c->n_experts % 8)) ? MOE_ERR_ALIGNMENT : MOE_OK;
 }
 
 moe_status_t check_ptrs(std::initializer_list<const void*> req,
@@ -384,6 +388,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
                        size_t ws_bytes, void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
+  if ((s = check_router_width(cfg)) != MOE_OK) return s;
   if ((s = check_ptrs({x, w_router, topk_idx, topk_gate}, {b_router})) != MOE_OK) return s;
   if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
   Call k = make_call(cfg, ws, stream);
@@ -474,6 +479,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!w) return MOE_ERR_INVALID_ARG;
+  if ((s = check_router_width(cfg)) != MOE_OK) return s;
   if ((s = check_ptrs({x, y, w->w_router, w->w_down, w->rms_gamma, w->w1, w->w3, w->w2, w->w_up},
                       {w->b_router})) != MOE_OK)
     return s;

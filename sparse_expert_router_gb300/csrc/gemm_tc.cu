@@ -1,10 +1,585 @@
-// tcgen05 GEMM (placeholder until the tensor-core kernel lands).
+// tcgen05 / TMEM / TMA GEMM for sm_103a: the grouped expert GEMMs over ragged expert groups
+// and the dense GEMMs of the layer.
+//
+// Orientation ("swap AB"): the MMA's A operand is a 128-feature tile of a weight matrix
+// (weights are stored [d_in, d_out], so the tile is MN-major) and its B operand is a tile of
+// up to 256 token rows of the activations (K-major). The accumulator in tensor memory holds
+// features in its 128 lanes and tokens in its columns, so a ragged expert group of ~171 rows
+// is one N = 176 tile instead of two 128-row tiles, and every weight tile is streamed from HBM
+// once per token tile. The grouped GEMM reads the expert group boundaries (the pages' cu_seqlens)
+// only after every thread of the kernel has executed griddepcontrol.wait: the Marin summary
+// of the week of 2026-09-14 (hero-run epic, #9183) traces a hang to MMA and epilogue warps
+// that decoded their tiles from group boundaries before the producing kernel had written them.
+//
+// Roles of the 6 warps of a CTA (one CTA per SM, persistent over work items):
+//   warp 0: TMA producer (one thread) filling a ring of shared-memory stages;
+//   warp 1: TMEM allocator and MMA issuer (one thread issues tcgen05.mma, commits to barriers);
+//   warps 2-5: epilogue, tcgen05.ld from tensor memory, fused epilogue, global stores.
+// Every wait on an mbarrier is bounded: after a few seconds the kernel records
+// MOE_ERR_DEVICE_TIMEOUT, stops issuing work, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "gemm.h"
 
 namespace moe {
-bool gemm_tc_supported(const GemmProblem&) { return false; }
-cudaError_t gemm_tc(const GemmProblem*, int, void*, cudaStream_t, bool) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
+constexpr int BN = 256;        // max token rows per tile (MMA N)
+constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
+constexpr int NTHREADS = 192;
+constexpr int MAX_PROBS = 3;
+constexpr int MAX_GROUPS = 1024;
+constexpr int A_HALF = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int B_BOX_ROWS = 32;
+constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;   // 4 KB
+constexpr unsigned long long TIMEOUT_NS = 5000000000ull;
+
+struct TcSeg {
+  CUtensorMap a1, a3, b;
+  int kblocks;
+};
+
+struct TcProblem {
+  TcSeg seg[2];
+  int n_seg;
+  int epi, group, M, Mg, m_tiles;
+  int n_fastest;               // dense problems: token tiles vary fastest
+  int64_t rows;
+  void* out;
+  int64_t ld_out;
+  int out_col0;
+  const float* bias;
+  const int32_t* offsets;
+  int G;
+  int64_t item_base;           // first item of this problem (grouped: filled on device)
+  int64_t n_items;             // dense: m_tiles * n_tiles (grouped: filled on device)
+};
+
+struct TcParams {
+  TcProblem p[MAX_PROBS];
+  int n_probs;
+  int grouped;                 // index of the grouped problem (always the last) or -1
+  int glu;                     // any problem has the SwiGLU epilogue (two A tiles per stage)
+  int stages;
+  int desc_swap;
+  DeviceHeader* hdr;
+};
+
+// ---- PTX wrappers -------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false when the kernel is aborting (timeout here or elsewhere in the CTA).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                          DeviceHeader* hdr, int where) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*abort_flag) return false;
+      uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TIMEOUT_NS) {
+        report_error(hdr, MOE_ERR_DEVICE_TIMEOUT, where);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte offsets,
+// the fixed version bits 0b001 at 46..48, 128-byte swizzle (2) at 61..63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A MN-major
+// (transposed), B K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
+__device__ __forceinline__ uint32_t make_idesc(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- work decomposition -----------------------------------------------------------------
+
+struct Item {
+  int p;           // problem
+  int wg;          // weight group (expert for grouped problems, shared expert for GROUP_COLS)
+  int m_w;         // first feature within the weight group's matrix
+  int m0;          // first output column (relative to the problem's M)
+  int64_t row0;
+  int nrows;
+};
+
+struct Sched {
+  int32_t glo[MAX_GROUPS];
+  int32_t ghi[MAX_GROUPS];
+  int64_t gitem[MAX_GROUPS + 1];
+  int64_t total;
+};
+
+__device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_t w) {
+  Item it;
+  int p = 0;
+  while (p + 1 < P.n_probs && w >= P.p[p + 1].item_base) ++p;
+  if (p == P.grouped) {
+    // the grouped problem keeps its item base on the device schedule
+  }
+  const TcProblem& q = P.p[p];
+  int64_t local = w - (p == P.grouped ? (S.gitem[0]) : q.item_base);
+  it.p = p;
+  if (q.group == GROUP_ROWS) {
+    int lo = 0, hi = q.G;   // largest g with gitem[g] <= local
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (S.gitem[mid] - S.gitem[0] <= local) lo = mid; else hi = mid;
+    }
+    int g = lo;
+    int64_t within = local - (S.gitem[g] - S.gitem[0]);
+    int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
+    it.wg = g;
+    it.m0 = m_t * BM;
+    it.m_w = it.m0;
+    it.row0 = S.glo[g] + (int64_t)n_t * BN;
+    it.nrows = (int)imin64(BN, (int64_t)S.ghi[g] - it.row0);
+  } else {
+    int64_t n_tiles = cdiv(q.rows, BN);
+    int n_t, m_t;
+    if (q.n_fastest) { n_t = (int)(local % n_tiles); m_t = (int)(local / n_tiles); }
+    else { n_t = (int)(local / q.m_tiles); m_t = (int)(local % q.m_tiles); }
+    it.m0 = m_t * BM;
+    if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
+    else { it.wg = 0; it.m_w = it.m0; }
+    it.row0 = (int64_t)n_t * BN;
+    it.nrows = (int)imin64(BN, q.rows - it.row0);
+  }
+  return it;
+}
+
+// ---- the kernel ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ Sched S;
+  __shared__ __align__(8) uint64_t bars[2 * 4 + 2];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stages = P.stages;
+  const bool glu = P.glu != 0;
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int stage_bytes = (glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
+  auto sA1 = [&](int s) { return base + s * stage_bytes; };
+  auto sA3 = [&](int s) { return base + s * stage_bytes + A_BYTES; };
+  auto sB = [&](int s) { return base + s * stage_bytes + (glu ? 2 * A_BYTES : A_BYTES); };
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[4]);
+  const uint32_t tmem_full = smem_u32(&bars[8]), tmem_empty = smem_u32(&bars[9]);
+  auto full = [&](int s) { return full0 + 8u * s; };
+  auto empty = [&](int s) { return empty0 + 8u * s; };
+
+  // set-up that reads nothing a preceding kernel writes
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 128);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int p = 0; p < P.n_probs; ++p)
+      for (int s = 0; s < P.p[p].n_seg; ++s) {
+        prefetch_map(&P.p[p].seg[s].a1);
+        prefetch_map(&P.p[p].seg[s].b);
+        if (glu) prefetch_map(&P.p[p].seg[s].a3);
+      }
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // Every thread waits for the preceding kernel before it reads the group offsets.
+  pdl_wait();
+
+  // schedule of the grouped problem: clamped group bounds and the prefix of its items
+  if (P.grouped >= 0) {
+    const TcProblem& q = P.p[P.grouped];
+    if (warp == 0) {
+      const int G = q.G;
+      const int per = (G + 31) / 32;
+      int64_t sum = 0;
+      for (int i = 0; i < per; ++i) {
+        int g = lane * per + i;
+        if (g < G) {
+          int64_t lo = imin64(imax64(q.offsets[g], 0), q.rows);
+          int64_t hi = imin64(imax64(q.offsets[g + 1], lo), q.rows);
+          S.glo[g] = (int32_t)lo;
+          S.ghi[g] = (int32_t)hi;
+          sum += cdiv(hi - lo, BN) * q.m_tiles;
+        }
+      }
+      int64_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int64_t v = __shfl_up_sync(~0u, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int64_t run = incl - sum + q.item_base;
+      for (int i = 0; i < per; ++i) {
+        int g = lane * per + i;
+        if (g < G) {
+          S.gitem[g] = run;
+          run += cdiv((int64_t)S.ghi[g] - S.glo[g], BN) * q.m_tiles;
+        }
+      }
+      if (lane == 31) { S.gitem[G] = run; S.total = run; }
+    }
+  } else if (threadIdx.x == 0) {
+    const TcProblem& q = P.p[P.n_probs - 1];
+    S.total = q.item_base + q.n_items;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int64_t total = S.total;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const int nb = (it.nrows + B_BOX_ROWS - 1) / B_BOX_ROWS;
+      const uint32_t bytes = (glu && q.epi == EPI_SWIGLU ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
+      for (int s = 0; s < q.n_seg && ok; ++s) {
+        const TcSeg& sg = q.seg[s];
+        for (int kb = 0; kb < sg.kblocks; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
+          mbar_expect_tx(full(stage), bytes);
+          const int k0 = kb * BK;
+          tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
+          tma_load_3d(smem_u32(sA1(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + 64, k0, it.wg);
+          if (q.epi == EPI_SWIGLU) {
+            tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
+            tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a3, full(stage), it.m_w + 64, k0, it.wg);
+          }
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, full(stage), k0,
+                        (int)(it.row0 + b * B_BOX_ROWS));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const bool sw = (q.epi == EPI_SWIGLU);
+      const int n = ((it.nrows + 15) / 16) * 16;
+      const uint32_t idesc = make_idesc(n);
+      if (!mbar_wait(tmem_empty, acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
+      tc_fence_after();
+      uint32_t accumulate = 0;
+      for (int s = 0; s < q.n_seg && ok; ++s) {
+        for (int kb = 0; kb < q.seg[s].kblocks; ++kb) {
+          if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)), b = smem_u32(sB(stage));
+          const uint32_t albo = P.desc_swap ? 1024u : (uint32_t)A_HALF;
+          const uint32_t asbo = P.desc_swap ? (uint32_t)A_HALF : 1024u;
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
+            mma_bf16(tmem_base, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
+            if (sw)
+              mma_bf16(tmem_base + BN, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
+                       accumulate);
+            accumulate = 1;
+          }
+          mma_commit(empty(stage));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      mma_commit(tmem_full);
+      acc_phase ^= 1u;
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int quad = warp & 3;
+    const int f_local = quad * 32 + lane;
+    uint32_t acc_phase = 0;
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      if (!mbar_wait(tmem_full, acc_phase, &s_abort, P.hdr, 4)) break;
+      tc_fence_after();
+      const int f = it.m0 + f_local;
+      const bool fok = f < q.M;
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+      const float bias = (q.epi == EPI_F32 && q.bias && fok) ? q.bias[f] : 0.0f;
+      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+        float v[16], v3[16];
+        tmem_ld16(lane_addr + c0, v);
+        if (q.epi == EPI_SWIGLU) tmem_ld16(lane_addr + BN + c0, v3);
+        tmem_wait_ld();
+        if (fok) {
+          const int cmax = min(16, it.nrows - c0);
+          for (int j = 0; j < cmax; ++j) {
+            const int64_t o = (it.row0 + c0 + j) * q.ld_out + q.out_col0 + f;
+            if (q.epi == EPI_F32) {
+              static_cast<float*>(q.out)[o] = __fadd_rn(v[j], bias);
+            } else if (q.epi == EPI_SWIGLU) {
+              static_cast<bf16*>(q.out)[o] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
+            } else {
+              static_cast<bf16*>(q.out)[o] = __float2bfloat16_rn(v[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                 : "memory");
+  }
+}
+
+// ---- host side ----------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Weights [G, K, Mw] (Mw contiguous): 3-D map with a 64 x 64 x 1 box, 128-byte swizzle.
+bool map_weights(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, int64_t G) {
+  cuuint64_t dims[3] = {(cuuint64_t)Mw, (cuuint64_t)K, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)(Mw * 2), (cuuint64_t)(Mw * K * 2)};
+  cuuint32_t box[3] = {64, BK, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Activations [rows, K] (K contiguous): 2-D map with a 64 x 32 box, 128-byte swizzle.
+bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+  cuuint32_t box[2] = {BK, B_BOX_ROWS};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms_tc() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmProblem& p) {
+  if (p.dtype != DT_BF16) return false;
+  const int Mw = (p.group == GROUP_COLS) ? p.Mg : p.M;
+  if (Mw < 64 || (Mw % 8)) return false;
+  if (p.group == GROUP_COLS && (p.Mg % BM || p.M % p.Mg)) return false;
+  if (p.group == GROUP_ROWS && (p.G < 1 || p.G > MAX_GROUPS)) return false;
+  if (p.n_seg < 1 || p.n_seg > 2) return false;
+  for (int s = 0; s < p.n_seg; ++s)
+    if (p.seg[s].K < 8 || (p.seg[s].K % 8)) return false;
+  if (p.epi != EPI_F32 && p.epi != EPI_STORE && p.epi != EPI_SWIGLU) return false;
+  return true;
+}
+
+cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cudaStream_t stream,
+                    bool pdl) {
+  if (n_probs < 1 || n_probs > MAX_PROBS) return cudaErrorInvalidValue;
+  if (!encode_fn()) return cudaErrorNotSupported;
+  static TcParams P;   // large; filled on the host for each launch (launches copy it)
+  memset(&P, 0, sizeof(P));
+  P.hdr = static_cast<DeviceHeader*>(dev_header);
+  P.grouped = -1;
+  // dense problems first, the (single) grouped problem last
+  int order[MAX_PROBS], n = 0;
+  for (int i = 0; i < n_probs; ++i) if (probs[i].group != GROUP_ROWS) order[n++] = i;
+  for (int i = 0; i < n_probs; ++i) if (probs[i].group == GROUP_ROWS) order[n++] = i;
+  int64_t base = 0;
+  for (int j = 0; j < n_probs; ++j) {
+    const GemmProblem& g = probs[order[j]];
+    if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
+    if (g.group == GROUP_ROWS && j != n_probs - 1) return cudaErrorNotSupported;
+    TcProblem& q = P.p[j];
+    q.n_seg = g.n_seg;
+    q.epi = g.epi;
+    q.group = g.group;
+    q.M = g.M;
+    q.Mg = g.Mg;
+    q.m_tiles = (int)cdiv(g.M, BM);
+    q.n_fastest = (g.group != GROUP_ROWS);
+    q.rows = g.rows;
+    q.out = g.out;
+    q.ld_out = g.ld_out;
+    q.out_col0 = g.out_col0;
+    q.bias = g.bias;
+    q.offsets = g.offsets;
+    q.G = g.G;
+    const int64_t Mw = (g.group == GROUP_COLS) ? g.Mg : g.M;
+    const int64_t Gw = (g.group == GROUP_ROWS) ? g.G : (g.group == GROUP_COLS ? g.M / g.Mg : 1);
+    for (int s = 0; s < g.n_seg; ++s) {
+      const GemmSeg& sg = g.seg[s];
+      TcSeg& ts = q.seg[s];
+      ts.kblocks = (int)cdiv(sg.K, BK);
+      if (!map_weights(&ts.a1, sg.w, Mw, sg.K, Gw)) return cudaErrorInvalidValue;
+      if (g.epi == EPI_SWIGLU && !map_weights(&ts.a3, sg.w3, Mw, sg.K, Gw))
+        return cudaErrorInvalidValue;
+      if (!map_act(&ts.b, sg.act, sg.K, g.rows)) return cudaErrorInvalidValue;
+    }
+    q.item_base = base;
+    if (g.group == GROUP_ROWS) {
+      P.grouped = j;
+      q.n_items = 0;
+    } else {
+      q.n_items = q.m_tiles * cdiv(g.rows, BN);
+      base += q.n_items;
+    }
+    if (g.epi == EPI_SWIGLU) P.glu = 1;
+  }
+  P.n_probs = n_probs;
+  P.desc_swap = getenv("MOE_TC_DESC_SWAP") ? 1 : 0;
+  const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
+  P.stages = P.glu ? 3 : 4;
+  const size_t smem = (size_t)P.stages * stage_bytes + 1024;
+  cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int grid = num_sms_tc();
+  if (P.grouped < 0) grid = (int)imin64(grid, base);
+  if (grid < 1) return cudaSuccess;
+  return launch(tc_gemm_kernel, dim3(grid), dim3(NTHREADS), smem, stream, pdl, P);
+}
+
 }  // namespace moe

@@ -68,7 +68,6 @@ def test_workspace_size_and_config_errors(lib):
            (dict(n_experts=2048, top_k=2), L.MOE_ERR_UNSUPPORTED),
            (dict(top_k=33, n_experts=64), L.MOE_ERR_UNSUPPORTED),
            (dict(d_model=250), L.MOE_ERR_ALIGNMENT),
-           (dict(dtype="bf16", n_experts=12), L.MOE_ERR_ALIGNMENT),
            (dict(capacity=(11, 0)), L.MOE_ERR_INVALID_ARG)]
     for kw, code in bad:
         c = _cfg(**kw)
@@ -108,6 +107,11 @@ def test_argument_errors_before_any_launch(lib):
     assert lib.moe_forward(C.byref(cfg2.c()), C.byref(w), good, good, ws, n, None, None) == \
         L.MOE_ERR_INVALID_ARG
     assert lib.moe_get_device_status(None, 256, None, None) == L.MOE_ERR_INVALID_ARG
+    # a bf16 router needs a 16-byte row pitch of W_r (E a multiple of 8); the expert calls do not
+    c12 = _cfg(dtype="bf16", n_experts=12)
+    n12 = _ws(lib, c12)
+    assert lib.moe_route(C.byref(c12.c()), good, good, None, good, good, ws, n12, None) == \
+        L.MOE_ERR_ALIGNMENT
 
 
 def test_binding_refuses_missing_library(tmp_path):

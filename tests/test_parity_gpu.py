@@ -17,7 +17,7 @@ from gpu_cases import (DEV, check_routing, gpu_inputs, normwise, oracle_forward,
 pytestmark = pytest.mark.gpu
 
 # the bf16 GEMM paths under test: tensor cores (default) and the CUDA-core cross-check
-BF16_PATHS = {"simt": m.MOE_FLAG_SIMT}
+BF16_PATHS = {"tc": 0, "simt": m.MOE_FLAG_SIMT}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -227,8 +227,7 @@ def test_large_layer(name):
     hottest expert's first tokens and dropped tokens added to the sample."""
     shape = SHAPES[name]
     inp = gpu_inputs(shape)
-    path = "tc" if "tc" in BF16_PATHS else "simt"
-    got = run_forward(shape, inp, BF16_PATHS[path])
+    got = run_forward(shape, inp, BF16_PATHS["tc"])
     counts = got["expert_counts"].cpu()
     hot = int(counts.argmax())
     hot_tokens = (got["topk_idx"].cpu() == hot).any(1).nonzero().flatten()[:4].tolist()
@@ -256,7 +255,7 @@ def test_expert_slice():
     cfg = m.LayerConfig(T=sh.rows, d_model=sh.d_latent, d_latent=sh.d_latent, n_experts=sh.n_local,
                         top_k=1, d_ff=sh.d_ff, n_shared=0, d_ff_shared=0, dtype=sh.dtype,
                         pool_rows=sh.pool_rows,
-                        flags=BF16_PATHS["tc" if "tc" in BF16_PATHS else "simt"])
+                        flags=BF16_PATHS["tc"])
     ws = m.alloc_workspace(cfg, DEV)
     y_perm = torch.full((sh.pool_rows, sh.d_latent), 7.0, dtype=torch.bfloat16, device=DEV)
     m.moe_expert_ffn(cfg, inp["pool"], inp["expert_offsets"], inp["w1"], inp["w3"], inp["w2"],
@@ -270,4 +269,67 @@ def test_expert_slice():
     ref = moe_oracle.slice_rows(inp, pos)
     assert normwise(y_perm[ref["rows"].to(DEV)], ref["y_perm"]) <= 2e-2
     assert normwise(out[pos], ref["out"]) <= 2e-2
+    assert m.moe_get_device_status(ws)["status"] == 0
+
+
+# ------------------------------------------------------- tensor cores vs CUDA cores ----
+
+def test_tc_matches_simt_bitwise_routing_and_close_outputs():
+    """The tcgen05 path and the CUDA-core path of the same layer: identical routing (both
+    are exact), outputs close (both accumulate in fp32, in different orders)."""
+    shape = SHAPES["small_bf16"].with_(T=2048)
+    inp = gpu_inputs(shape)
+    a = run_forward(shape, inp, BF16_PATHS["tc"])
+    b = run_forward(shape, inp, BF16_PATHS["simt"])
+    assert torch.equal(a["topk_idx"], b["topk_idx"])
+    assert torch.equal(a["slot_of"], b["slot_of"])
+    assert normwise(a["y"], b["y"]) <= 1e-2
+
+
+# ----------------------------------------------------------- programmatic dependent launch ----
+
+def test_pdl_changing_groups_stress():
+    """Back-to-back producer -> grouped GEMM launches under programmatic dependent launch with
+    the expert group sizes changing on every launch (the hang of the weekly summary of
+    2026-09-14, hero-run epic, came from warps that read group boundaries before the producer
+    had written them). 50,000 iterations = 100,000 grouped-GEMM launches; the outputs of
+    periodic iterations are compared bitwise with the same routing run without PDL."""
+    T, d, L, E, k, F = 64, 64, 64, 16, 2, 64
+    cfg = m.LayerConfig(T=T, d_model=d, d_latent=L, n_experts=E, top_k=k, d_ff=F, n_shared=0,
+                        d_ff_shared=0, dtype="bf16", flags=m.MOE_FLAG_PDL)
+    cfg0 = m.LayerConfig(**{**cfg.__dict__, "flags": 0})
+    g = torch.Generator().manual_seed(0)
+    n_var = 8
+    idxs = [torch.stack([torch.randperm(E, generator=g)[:k].sort().values for _ in range(T)])
+            .to(torch.int32).to(DEV) for _ in range(n_var)]
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16).to(DEV)
+    wd = (torch.randn(d, L, generator=g) * d ** -0.5).to(torch.bfloat16).to(DEV)
+    gam = torch.ones(L, device=DEV)
+    w1 = (torch.randn(E, L, F, generator=g) * L ** -0.5).to(torch.bfloat16).to(DEV)
+    w3 = (torch.randn(E, L, F, generator=g) * L ** -0.5).to(torch.bfloat16).to(DEV)
+    w2 = (torch.randn(E, F, L, generator=g) * F ** -0.5).to(torch.bfloat16).to(DEV)
+    ws = m.alloc_workspace(cfg, DEV)
+    bufs = dict(counts=torch.empty(E, dtype=torch.int32, device=DEV),
+                offs=torch.empty(E + 1, dtype=torch.int32, device=DEV),
+                perm=torch.empty(T * k, dtype=torch.int32, device=DEV),
+                slot=torch.empty((T, k), dtype=torch.int32, device=DEV),
+                xp=torch.zeros((T * k, L), dtype=torch.bfloat16, device=DEV),
+                yp=torch.zeros((T * k, L), dtype=torch.bfloat16, device=DEV))
+
+    def step(c, i):
+        b = bufs
+        m.moe_permute(c, x, wd, gam, idxs[i % n_var], b["counts"], b["offs"], b["perm"], b["slot"],
+                      None, b["xp"], ws)
+        m.moe_expert_ffn(c, b["xp"], b["offs"], w1, w3, w2, b["yp"], ws=ws)
+
+    ref = []
+    for i in range(n_var):
+        step(cfg0, i)
+        ref.append(bufs["yp"].clone())
+    m.moe_clear_device_status(ws)
+    n_iter = 50000
+    for i in range(n_iter):
+        step(cfg, i)
+        if i % 997 == 0 or i == n_iter - 1:
+            assert torch.equal(bufs["yp"], ref[i % n_var]), i
     assert m.moe_get_device_status(ws)["status"] == 0
