@@ -1,0 +1,363 @@
+"""Benchmark of the routed-MoE forward layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step is one forward of the whole layer (router, top-k, dispatch, grouped expert GEMMs,
+shared experts, combine, up-projection) over one batch of synthetic tokens of the workload
+(default: the 535B-shaped layer, T = 8,192 tokens). Prints one JSON line on rank 0.
+
+For N > 1 (torchrun, one process per GPU) every rank runs its own replica of the layer on its
+own batch (token sharding, no collective on the data path); the barrier and the max over ranks
+are used for timing only ("replicas only" scaling, reported as weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from moe_workloads import SHAPES, make_layer_inputs  # noqa: E402
+
+STAGES = ["prep", "front_gemm", "router_select", "dispatch", "expert_gemm1", "expert_gemm2",
+          "combine", "back_gemm"]
+KERNELS_PER_FORWARD = 15          # launches of this library's kernels in one moe_forward
+METRIC = "MoE-layer tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_burst": p["bf16_tflops"],
+                "bf16_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic(shape, counts):
+    """Algorithmic flops and bytes per stage of one forward (bf16 storage)."""
+    T, d, L, E, k = shape.T, shape.d_model, shape.d_latent, shape.n_experts, shape.top_k
+    F, SF = shape.d_ff, shape.n_shared * shape.d_ff_shared
+    es = 2
+    R = int(min(sum(counts), T * k))
+    active = sum(1 for c in counts if c > 0)
+    fl = shape.flops()
+    fl["expert_up"] = 2.0 * R * L * 2 * F
+    fl["expert_down"] = 2.0 * R * F * L
+    return {
+        "front_gemm": {"flops": fl["router"] + fl["down"] + fl["shared_up"],
+                       "bytes": es * (T * d + d * E + d * L + 2 * d * SF) + 4 * T * E + 4 * T * L
+                       + es * T * SF},
+        "router_select": {"flops": 0.0, "bytes": 4 * T * E + es * T * d + 8 * T * k},
+        "dispatch": {"flops": 0.0, "bytes": es * T * L + es * R * L + 4 * (3 * T * k + R)},
+        "expert_gemm1": {"flops": fl["expert_up"],
+                         "bytes": es * (2 * active * L * F + R * L + R * F)},
+        "expert_gemm2": {"flops": fl["expert_down"],
+                         "bytes": es * (active * F * L + R * F + R * L)},
+        "combine": {"flops": 0.0, "bytes": es * (R * L + T * L) + 8 * T * k},
+        "back_gemm": {"flops": fl["back"],
+                      "bytes": es * (T * L + T * SF + L * d + SF * d + T * d)},
+    }
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = str(index)
+        try:   # nvidia-smi numbers GPUs differently from CUDA when devices are masked
+            uuid = str(torch.cuda.get_device_properties(index).uuid)
+            if uuid:
+                self.index = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except (AttributeError, RuntimeError):
+            pass
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.index], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, shape):
+    """The fp64 CPU oracle timed on the host cores, each step a bounded sample of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import moe_oracle
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = {k: v.cpu() for k, v in make_layer_inputs(shape, gen, T=args.ref_tokens).items()}
+    for _ in range(args.warmup if args.warmup <= 1 else 1):
+        moe_oracle.forward(inp, top_k=shape.top_k, rms_eps=shape.rms_eps,
+                           capacity_factor=shape.capacity)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        moe_oracle.forward(inp, top_k=shape.top_k, rms_eps=shape.rms_eps,
+                           capacity_factor=shape.capacity)
+    dt = time.perf_counter() - t0
+    v = args.ref_tokens * args.steps / dt
+    sample = f"{args.ref_tokens} tokens of {shape.name} per step (full weights)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": shape.name, "T": shape.T, "parallelism": "replicas"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": torch.get_num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def cpu_baseline(shape, n_tokens, inp_gpu):
+    """The oracle as it stands on a bounded token sample, with the workload's weights on the host."""
+    from oracle import moe_oracle
+    host = {k: v.cpu() for k, v in inp_gpu.items()}
+    host["x"] = host["x"][:n_tokens].clone()
+    t0 = time.perf_counter()
+    moe_oracle.forward(host, top_k=shape.top_k, rms_eps=shape.rms_eps,
+                       capacity_factor=shape.capacity)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"the first {n_tokens} tokens of {shape.name} as one batch "
+                      f"(routing, dispatch, every expert MLP, combine, shared, up-projection)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="l535b_t8192", choices=sorted(SHAPES))
+    ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05")
+    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch")
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    shape = SHAPES[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+
+    import sparse_expert_router_gb300 as m
+    m.load()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    flags = (m.MOE_FLAG_SIMT if args.simt else 0) | (m.MOE_FLAG_PDL if args.pdl else 0)
+    cfg = m.LayerConfig.from_shape(shape, flags=flags)
+    inp = make_layer_inputs(shape.with_(seed=shape.seed), dev)
+    if rank > 0:   # each replica processes its own batch
+        inp["x"] = make_layer_inputs(shape.with_(seed=shape.seed + rank, T=shape.T), dev)["x"]
+    ws = m.alloc_workspace(cfg, dev)
+    y = torch.empty((shape.T, shape.d_model), dtype=shape.torch_dtype, device=dev)
+    counts = torch.zeros(shape.n_experts, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
+    stream = torch.cuda.current_stream(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+    for e in evs:
+        e.record(stream)          # creates the CUDA events before their handles are passed on
+    aux = {"stage_events": evs, "expert_counts": counts}
+
+    for _ in range(max(3, args.warmup)):
+        m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
+    torch.cuda.synchronize(dev)
+    rep = m.moe_get_device_status(ws)
+    if rep["status"] != 0:
+        raise RuntimeError(f"device report after warm-up: {rep}")
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    step_ms, stage_ms = [], {s: 0.0 for s in STAGES}
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()                                   # L2 flushed between timed steps
+        m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
+        evs[-1].synchronize()
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+        for i, s in enumerate(STAGES):
+            stage_ms[s] += evs[i].elapsed_time(evs[i + 1])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t)
+    ms_step = total_ms / args.steps
+    value = world * shape.T * args.steps / (total_ms / 1e3)
+
+    rep = m.moe_get_device_status(ws)
+    if rep["status"] != 0:
+        raise RuntimeError(f"device report after the timed steps: {rep}")
+
+    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of y
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp["x"].cpu().pin_memory()
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            x_dev.copy_(x_host, non_blocking=True)
+            m.moe_forward(cfg, inp, x_dev, y, ws, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_ms = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            a.record(stream)
+            x_dev.copy_(x_host, non_blocking=True)
+            m.moe_forward(cfg, inp, x_dev, y, ws, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            e2e_ms += a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t)
+        e2e = {"value": world * shape.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+               "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
+
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    pk = peaks()
+    alg = algorithmic(shape, counts.cpu().tolist())
+    stages = {}
+    for s in STAGES:
+        ms = stage_ms[s] / args.steps
+        st = {"ms": round(ms, 4)}
+        if s in alg:
+            f, by = alg[s]["flops"], alg[s]["bytes"]
+            st["gb_s"] = round(by / (ms * 1e-3) / 1e9, 1)
+            st["hbm_frac"] = round(st["gb_s"] / pk["hbm_gbs"], 3)
+            if f:
+                st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 1)
+                st["bf16_frac"] = round(st["tflop_s"] / pk["bf16_sustained"], 3)
+        stages[s] = st
+    dom = max((s for s in STAGES if s in alg), key=lambda s: stage_ms[s])
+    f, by = alg[dom]["flops"], alg[dom]["bytes"]
+    ms_dom = stage_ms[dom] / args.steps
+    t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), f / (pk["bf16_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = by / (ms_dom * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4)}
+    else:
+        ach = f / (ms_dom * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4)}
+    roof.update({"kernel": dom, "traffic": None, "peak_source": pk["source"]
+                 + (" (bf16 sustained)" if roof["bound"] == "tensor" else " (HBM copy)")})
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, near-uniform "
+                "routing unless the workload is Zipf-skewed)",
+        "config": {"workload": f"{shape.name}: T={shape.T} d={shape.d_model} "
+                               f"latent={shape.d_latent} E={shape.n_experts} k={shape.top_k} "
+                               f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gemm_path": "simt" if args.simt else "tcgen05", "pdl": bool(args.pdl),
+                   "l2": "flushed between timed steps (256 MB write); weights (21.7 GB) exceed L2"},
+        "layer_tflop_s": round(sum(shape.flops().values()) / (ms_step * 1e-3) / 1e12, 1),
+        "stages": stages,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+        "device_report": rep,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, args.cpu_tokens, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

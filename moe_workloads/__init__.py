@@ -127,6 +127,11 @@ SHAPES: Dict[str, LayerShape] = {
     "l535b_t65536": LayerShape("l535b_t65536", T=65536, d_model=6144, d_latent=3072,
                                n_experts=384, top_k=8, d_ff=3072, n_shared=2, d_ff_shared=3072,
                                dtype="bf16"),
+    # Profiling case (a few GB on the device): the 535B layer's widths with 64 of its 384
+    # experts and T=1368, so each expert gets ~171 rows, the same as at T=8192 with all experts.
+    "l535b_e64_t1368": LayerShape("l535b_e64_t1368", T=1368, d_model=6144, d_latent=3072,
+                                  n_experts=64, top_k=8, d_ff=3072, n_shared=2,
+                                  d_ff_shared=3072, dtype="bf16"),
 }
 
 # One GPU of a 64-way expert-parallel domain: 6 local experts, 49,152 arriving

@@ -19,7 +19,6 @@
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing work, frees its tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -68,7 +67,6 @@ struct TcParams {
   int grouped;                 // index of the grouped problem (always the last) or -1
   int glu;                     // any problem has the SwiGLU epilogue (two A tiles per stage)
   int stages;
-  int desc_swap;
   DeviceHeader* hdr;
 };
 
@@ -390,8 +388,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)), b = smem_u32(sB(stage));
-          const uint32_t albo = P.desc_swap ? 1024u : (uint32_t)A_HALF;
-          const uint32_t asbo = P.desc_swap ? (uint32_t)A_HALF : 1024u;
+          // MN-major A: LBO = stride between the two 64-feature atoms, SBO = stride between
+          // 8-row k groups; K-major B: SBO = stride between 8-row groups, LBO unused.
+          const uint32_t albo = (uint32_t)A_HALF, asbo = 1024u;
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
@@ -571,7 +570,6 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     if (g.epi == EPI_SWIGLU) P.glu = 1;
   }
   P.n_probs = n_probs;
-  P.desc_swap = getenv("MOE_TC_DESC_SWAP") ? 1 : 0;
   const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
   P.stages = P.glu ? 3 : 4;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024;

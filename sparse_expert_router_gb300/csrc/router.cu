@@ -161,43 +161,65 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
 }
 
-// x . w + bias with a bound on its error; all lanes return the same values.
+constexpr int MC = 4;   // candidates evaluated together (their loads overlap)
+
+// x . w_j + bias_j for up to MC candidate rows w_j of W_r^T, each with a bound on its error;
+// lane 0 returns the values. Error-free TwoSum accumulation (plus TwoProduct for fp32) per
+// lane, the lanes' (sum, compensation) pairs combined with TwoSum.
 template <typename T>
-__device__ void warp_dot2(const T* x, const T* w, int d, float bias, float g2, int lane,
-                          float& res, float& err_bound) {
+__device__ void warp_dot2_multi(const T* x, const T* wrT, const int* cand, int nc, int d,
+                                const float* bias, float g2, int lane, float* res, float* eb) {
   const bool f32 = sizeof(T) == 4;
-  float s = (lane == 0) ? bias : 0.0f, c = 0.0f, sa = (lane == 0) ? fabsf(bias) : 0.0f;
-  for (int i = lane * 8; i < d; i += 256) {
-    float xv[8], wv[8];
-    load8f(x + i, xv);
-    load8f(w + i, wv);
+  float s[MC], c[MC], sa[MC];
+  const T* wp[MC];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float p = __fmul_rn(xv[j], wv[j]);
-      float ep = f32 ? fmaf(xv[j], wv[j], -p) : 0.0f;   // TwoProduct (exact when bf16)
-      float t, e;
-      two_sum(s, p, t, e);
-      s = t;
-      c = __fadd_rn(c, __fadd_rn(e, ep));
-      sa = __fadd_rn(sa, fabsf(p));
+  for (int j = 0; j < MC; ++j) {
+    const int e = cand[j < nc ? j : nc - 1];
+    const float b = (bias && lane == 0 && j < nc) ? bias[e] : 0.0f;
+    s[j] = b;
+    c[j] = 0.0f;
+    sa[j] = fabsf(b);
+    wp[j] = wrT + (int64_t)e * d;
+  }
+#pragma unroll 2
+  for (int i = lane * 8; i < d; i += 256) {
+    float xv[8];
+    load8f(x + i, xv);
+#pragma unroll
+    for (int j = 0; j < MC; ++j) {
+      float wv[8];
+      load8f(wp[j] + i, wv);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float p = __fmul_rn(xv[q], wv[q]);
+        float ep = f32 ? fmaf(xv[q], wv[q], -p) : 0.0f;   // TwoProduct (exact when bf16)
+        float t, e;
+        two_sum(s[j], p, t, e);
+        s[j] = t;
+        c[j] = __fadd_rn(c[j], __fadd_rn(e, ep));
+        sa[j] = __fadd_rn(sa[j], fabsf(p));
+      }
     }
   }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    float s2 = __shfl_xor_sync(~0u, s, o);
-    float c2 = __shfl_xor_sync(~0u, c, o);
-    float a2 = __shfl_xor_sync(~0u, sa, o);
-    float t, e;
-    two_sum(s, s2, t, e);
-    s = t;
-    c = __fadd_rn(__fadd_rn(c, c2), e);
-    sa = __fadd_rn(sa, a2);
+  for (int j = 0; j < MC; ++j) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      float s2 = __shfl_xor_sync(~0u, s[j], o);
+      float c2 = __shfl_xor_sync(~0u, c[j], o);
+      float a2 = __shfl_xor_sync(~0u, sa[j], o);
+      float t, e;
+      two_sum(s[j], s2, t, e);
+      s[j] = t;
+      c[j] = __fadd_rn(__fadd_rn(c[j], c2), e);
+      sa[j] = __fadd_rn(sa[j], a2);
+    }
+    const float r = __fadd_rn(s[j], c[j]);
+    // sum|p| is computed with relative error <= gamma_n: inflate it, then apply the bound
+    const float sa_ub = __fmul_ru(sa[j], 1.0f + sqrtf(g2) * 2.0f);
+    float b = __fadd_ru(__fmul_ru(2.0f * U32, fabsf(r)), __fmul_ru(2.0f * g2, sa_ub));
+    if (j < nc) { res[j] = r; eb[j] = __fadd_ru(b, 1e-30f); }
   }
-  res = __fadd_rn(s, c);
-  // sum|p| computed with relative error <= gamma_n; inflate it, then apply the bound
-  float sa_ub = __fmul_ru(sa, 1.0f + sqrtf(g2) * 2.0f);
-  err_bound = __fadd_ru(__fmul_ru(2.0f * U32, fabsf(res)), __fmul_ru(2.0f * g2, sa_ub));
-  err_bound = __fadd_ru(err_bound, 1e-30f);
 }
 
 // ---- stage 3: exact logits --------------------------------------------------------------
@@ -224,26 +246,30 @@ __device__ __forceinline__ bool decompose<bf16>(bf16 v, uint32_t& M, int& q, uin
   return true;
 }
 
-__device__ __forceinline__ void bins_add(unsigned long long* bins, uint64_t M, int q,
-                                         uint32_t neg) {
+__device__ __forceinline__ void bins_add(long long (&bins)[NB], uint64_t M, int q, uint32_t neg) {
   if (M == 0) return;
   int p = q + EXP_BIAS;
   int bi = p >> 5, sh = p & 31;
   uint64_t lo = (M & 0xFFFFFFFFull) << sh;
   uint64_t hi = (M >> 32) << sh;
-  uint64_t c0 = lo & 0xFFFFFFFFull, c1 = (lo >> 32) + (hi & 0xFFFFFFFFull), c2 = hi >> 32;
-  if (neg) { c0 = 0ull - c0; c1 = 0ull - c1; c2 = 0ull - c2; }
-  atomicAdd(&bins[bi], (unsigned long long)c0);
-  atomicAdd(&bins[bi + 1], (unsigned long long)c1);
-  if (c2) atomicAdd(&bins[bi + 2], (unsigned long long)c2);
+  long long c0 = (long long)(lo & 0xFFFFFFFFull);
+  long long c1 = (long long)((lo >> 32) + (hi & 0xFFFFFFFFull));
+  long long c2 = (long long)(hi >> 32);
+  if (neg) { c0 = -c0; c1 = -c1; c2 = -c2; }
+  bins[bi] += c0;
+  bins[bi + 1] += c1;
+  bins[bi + 2] += c2;
 }
 
-// Exact x . w + bias into canonical form: limbs 0..NB-2 in [0, 2^32), limb NB-1 signed.
+// Exact x . w + bias into canonical form `out`: limbs 0..NB-2 in [0, 2^32), limb NB-1 signed.
+// Every lane accumulates its products in private limbs (each limb stays below 2^47 in
+// magnitude), the warp adds the limbs, lane 0 propagates the carries.
 template <typename T>
 __device__ bool warp_exact(const T* x, const T* w, int d, float bias, int lane,
-                           unsigned long long* bins) {
-  for (int i = lane; i < NB; i += 32) bins[i] = 0ull;
-  __syncwarp();
+                           unsigned long long* out) {
+  long long bins[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) bins[i] = 0;
   bool ok = true;
   for (int i = lane; i < d; i += 32) {
     uint32_t Mx = 0, Mw = 0, sx = 0, sw = 0;
@@ -260,15 +286,22 @@ __device__ bool warp_exact(const T* x, const T* w, int d, float bias, int lane,
     ok &= fb;
     if (fb) bins_add(bins, (uint64_t)Mb, qb, sb);
   }
-  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    long long v = bins[i];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
+    bins[i] = v;
+  }
   if (lane == 0) {
-    int64_t carry = 0;
+    long long carry = 0;
+#pragma unroll
     for (int i = 0; i < NB - 1; ++i) {
-      int64_t v = (int64_t)bins[i] + carry;
-      bins[i] = (unsigned long long)(v & 0xFFFFFFFFll);
+      long long v = bins[i] + carry;
+      out[i] = (unsigned long long)(v & 0xFFFFFFFFll);
       carry = v >> 32;   // arithmetic shift: floor division
     }
-    bins[NB - 1] = (unsigned long long)((int64_t)bins[NB - 1] + carry);
+    out[NB - 1] = (unsigned long long)(bins[NB - 1] + carry);
   }
   __syncwarp();
   return __all_sync(~0u, ok);
@@ -363,22 +396,33 @@ router_refine_kernel(RouterArgs a) {
     const T* x = static_cast<const T*>(a.x) + t * a.d;
     warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
     warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+    // the undecided experts, in ascending order, into the (now free) work array
+    int* cand = reinterpret_cast<int*>(w.work);
+    int nc = 0;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
       int e = e0 + lane;
-      unsigned amb = __ballot_sync(~0u, e < a.E && w.sel[e] == 2);
-      while (amb) {
-        int l = __ffs(amb) - 1;
-        amb &= amb - 1;
-        int ee = e0 + l;
-        float res, eb;
-        warp_dot2(x, static_cast<const T*>(a.wrT) + (int64_t)ee * a.d, a.d,
-                  a.bias ? a.bias[ee] : 0.0f, a.g2, lane, res, eb);
-        if (lane == 0) {
-          w.lo[ee] = fmaxf(w.lo[ee], __fsub_rd(res, eb));
-          w.hi[ee] = fminf(w.hi[ee], __fadd_ru(res, eb));
+      bool on = e < a.E && w.sel[e] == 2;
+      unsigned b = __ballot_sync(~0u, on);
+      if (on) cand[nc + __popc(b & ((1u << lane) - 1u))] = e;
+      nc += __popc(b);
+    }
+    __syncwarp();
+    for (int c0 = 0; c0 < nc; c0 += MC) {
+      float res[MC], eb[MC];
+      const int n_here = min(MC, nc - c0);
+      warp_dot2_multi(x, static_cast<const T*>(a.wrT), cand + c0, n_here, a.d, a.bias, a.g2,
+                      lane, res, eb);
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < MC; ++j) {
+          if (j < n_here) {
+            const int ee = cand[c0 + j];
+            w.lo[ee] = fmaxf(w.lo[ee], __fsub_rd(res[j], eb[j]));
+            w.hi[ee] = fminf(w.hi[ee], __fadd_ru(res[j], eb[j]));
+          }
         }
-        __syncwarp();
       }
+      __syncwarp();
     }
     int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
     if (n_in == a.k) {

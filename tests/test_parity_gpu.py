@@ -333,3 +333,29 @@ def test_pdl_changing_groups_stress():
         if i % 997 == 0 or i == n_iter - 1:
             assert torch.equal(bufs["yp"], ref[i % n_var]), i
     assert m.moe_get_device_status(ws)["status"] == 0
+
+
+def test_router_logit_error_within_certified_bound():
+    """The stage-1 bound the router certifies with, checked on real tensor-core logits: the
+    fp32 logits of the first router GEMM (at the start of the workspace, after the 256-byte
+    device report) against exact fp64 logits, |l~ - l| <= c gamma_d ||x|| ||w_e|| + 2u|l~|."""
+    from oracle import moe_oracle as O
+    for name, c in (("small_bf16", 2.0), ("l535b_t8192", 2.0)):
+        shape = SHAPES[name].with_(T=1024)
+        inp = gpu_inputs(shape)
+        cfg = m.LayerConfig.from_shape(shape)
+        ws = m.alloc_workspace(cfg, DEV)
+        T, E, d = shape.T, shape.n_experts, shape.d_model
+        idx = torch.empty((T, shape.top_k), dtype=torch.int32, device=DEV)
+        gate = torch.empty((T, shape.top_k), dtype=torch.float32, device=DEV)
+        m.moe_route(cfg, inp["x"], inp["w_router"], inp["b_router"], idx, gate, ws)
+        torch.cuda.synchronize()
+        lt = ws[256:256 + T * E * 4].view(torch.float32).view(T, E).cpu().double()
+        ref, _ = O.router_logits(inp["x"], inp["w_router"], inp["b_router"])
+        x64, w64 = O.to64(inp["x"]), O.to64(inp["w_router"])
+        u = 2.0 ** -24
+        gam = d * u / (1 - d * u)
+        beta = c * gam * x64.norm(dim=1, keepdim=True) * w64.norm(dim=0, keepdim=True) + 2 * u * lt.abs()
+        ratio = float(((lt - ref).abs() / beta).max())
+        print(name, "max |error| / bound =", ratio)
+        assert ratio <= 1.0, ratio
