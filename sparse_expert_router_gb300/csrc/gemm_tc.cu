@@ -27,18 +27,38 @@
 namespace moe {
 namespace {
 
+#ifndef MOE_TC_BN
+#define MOE_TC_BN 256
+#endif
+#ifndef MOE_TC_STAGES_GLU
+#define MOE_TC_STAGES_GLU 3
+#endif
+#ifndef MOE_TC_STAGES
+#define MOE_TC_STAGES 4
+#endif
 constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
-constexpr int BN = 256;        // max token rows per tile (MMA N)
+constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
 constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
-constexpr int NTHREADS = 192;
+#ifndef MOE_TC_EPI_WARPS
+#define MOE_TC_EPI_WARPS 8
+#endif
+constexpr int EPI_WARPS = MOE_TC_EPI_WARPS;           // 4 or 8 (two per tensor-memory lane quadrant)
+constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_STAGE_BYTES = 16 * 32 * 4;           // per-warp transpose tile: 16 tokens x 32 features
 constexpr int MAX_PROBS = 3;
 constexpr int MAX_GROUPS = 1024;
 constexpr int A_HALF = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KB
-constexpr int B_BOX_ROWS = 32;
+#ifndef MOE_TC_BBOX
+#define MOE_TC_BBOX 32
+#endif
+constexpr int B_BOX_ROWS = MOE_TC_BBOX;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;   // 4 KB
 constexpr unsigned long long TIMEOUT_NS = 5000000000ull;
+static_assert(MOE_TC_STAGES <= 8 && MOE_TC_STAGES_GLU <= 8, "at most 8 pipeline stages");
+static_assert(BN % B_BOX_ROWS == 0 && BN % 16 == 0 && BN <= 256, "token tile");
+static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
 
 struct TcSeg {
   CUtensorMap a1, a3, b;
@@ -205,31 +225,29 @@ struct Item {
   int nrows;
 };
 
+// Schedule of the grouped problem, in dynamic shared memory after the stages:
+// clamped group bounds and the exclusive prefix of the groups' work items.
 struct Sched {
-  int32_t glo[MAX_GROUPS];
-  int32_t ghi[MAX_GROUPS];
-  int64_t gitem[MAX_GROUPS + 1];
-  int64_t total;
+  int32_t* glo;     // [G]
+  int32_t* ghi;     // [G]
+  int32_t* gitem;   // [G + 1]
 };
 
 __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_t w) {
   Item it;
   int p = 0;
   while (p + 1 < P.n_probs && w >= P.p[p + 1].item_base) ++p;
-  if (p == P.grouped) {
-    // the grouped problem keeps its item base on the device schedule
-  }
   const TcProblem& q = P.p[p];
-  int64_t local = w - (p == P.grouped ? (S.gitem[0]) : q.item_base);
+  int64_t local = w - (p == P.grouped ? (int64_t)S.gitem[0] : q.item_base);
   it.p = p;
   if (q.group == GROUP_ROWS) {
     int lo = 0, hi = q.G;   // largest g with gitem[g] <= local
     while (hi - lo > 1) {
       int mid = (lo + hi) >> 1;
-      if (S.gitem[mid] - S.gitem[0] <= local) lo = mid; else hi = mid;
+      if ((int64_t)S.gitem[mid] - S.gitem[0] <= local) lo = mid; else hi = mid;
     }
     int g = lo;
-    int64_t within = local - (S.gitem[g] - S.gitem[0]);
+    int64_t within = local - ((int64_t)S.gitem[g] - S.gitem[0]);
     int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
     it.wg = g;
     it.m0 = m_t * BM;
@@ -254,8 +272,8 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
 
 __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ Sched S;
-  __shared__ __align__(8) uint64_t bars[2 * 4 + 2];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
+  __shared__ int64_t s_total;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -268,16 +286,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
   auto sA1 = [&](int s) { return base + s * stage_bytes; };
   auto sA3 = [&](int s) { return base + s * stage_bytes + A_BYTES; };
   auto sB = [&](int s) { return base + s * stage_bytes + (glu ? 2 * A_BYTES : A_BYTES); };
-  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[4]);
-  const uint32_t tmem_full = smem_u32(&bars[8]), tmem_empty = smem_u32(&bars[9]);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
+  // Accumulators in tensor memory: launches without a SwiGLU problem keep two (columns 0 and
+  // BN) so that the epilogue of one tile overlaps the main loop of the next; SwiGLU launches
+  // need both halves (gate and up projections) for one tile.
+  const int nacc = glu ? 1 : 2;
+  auto tmem_full = [&](int b) { return smem_u32(&bars[16 + b]); };
+  auto tmem_empty = [&](int b) { return smem_u32(&bars[18 + b]); };
+  Sched S;
+  unsigned char* epi_stage = base + (size_t)stages * stage_bytes;   // [EPI_WARPS][EPI_STAGE_BYTES]
+  {
+    int32_t* sp = reinterpret_cast<int32_t*>(epi_stage + EPI_WARPS * EPI_STAGE_BYTES);
+    const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
+    S.glo = sp;
+    S.ghi = sp + G;
+    S.gitem = sp + 2 * G;
+  }
   auto full = [&](int s) { return full0 + 8u * s; };
   auto empty = [&](int s) { return empty0 + 8u * s; };
 
   // set-up that reads nothing a preceding kernel writes
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tmem_full(b), 1);
+      mbar_init(tmem_empty(b), 32 * EPI_WARPS);
+    }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int p = 0; p < P.n_probs; ++p)
@@ -324,21 +358,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       for (int i = 0; i < per; ++i) {
         int g = lane * per + i;
         if (g < G) {
-          S.gitem[g] = run;
+          S.gitem[g] = (int32_t)run;
           run += cdiv((int64_t)S.ghi[g] - S.glo[g], BN) * q.m_tiles;
         }
       }
-      if (lane == 31) { S.gitem[G] = run; S.total = run; }
+      if (lane == 31) { S.gitem[G] = (int32_t)run; s_total = run; }
     }
   } else if (threadIdx.x == 0) {
     const TcProblem& q = P.p[P.n_probs - 1];
-    S.total = q.item_base + q.n_items;
+    s_total = q.item_base + q.n_items;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
-  const int64_t total = S.total;
+  const int64_t total = s_total;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -372,15 +406,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    uint32_t phase = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    int li = 0;                                   // this CTA's item counter
+    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++li) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const bool sw = (q.epi == EPI_SWIGLU);
       const int n = ((it.nrows + 15) / 16) * 16;
       const uint32_t idesc = make_idesc(n);
-      if (!mbar_wait(tmem_empty, acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
+      const int buf = li % nacc;
+      const uint32_t acc_phase = (uint32_t)(li / nacc) & 1u;
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      if (!mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
       tc_fence_after();
       uint32_t accumulate = 0;
       for (int s = 0; s < q.n_seg && ok; ++s) {
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-            mma_bf16(tmem_base, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
+            mma_bf16(d_tmem, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
             if (sw)
               mma_bf16(tmem_base + BN, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
                        accumulate);
@@ -404,45 +442,80 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
-      mma_commit(tmem_full);
-      acc_phase ^= 1u;
+      mma_commit(tmem_full(buf));
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
+    // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); with 8 epilogue warps the two
+    // warps of a quadrant take alternate 16-token chunks. Each chunk (32 features x 16 tokens)
+    // is transposed through a per-warp shared-memory tile so that every lane then writes whole
+    // 16-byte pieces of output rows.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;                    // 0, or 1 for the second warp of a quadrant
     const int f_local = quad * 32 + lane;
-    uint32_t acc_phase = 0;
-    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+    float* stg_f = reinterpret_cast<float*>(stg);
+    bf16* stg_h = reinterpret_cast<bf16*>(stg);
+    int li = 0;
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x, ++li) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      if (!mbar_wait(tmem_full, acc_phase, &s_abort, P.hdr, 4)) break;
+      const int buf = li % nacc;
+      const uint32_t acc_phase = (uint32_t)(li / nacc) & 1u;
+      if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
-      const int f = it.m0 + f_local;
-      const bool fok = f < q.M;
-      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
-      const float bias = (q.epi == EPI_F32 && q.bias && fok) ? q.bias[f] : 0.0f;
-      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+      const int f0 = it.m0 + quad * 32;                  // first feature of this warp
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+      const bool f32out = (q.epi == EPI_F32);
+      const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+      for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
         float v[16], v3[16];
         tmem_ld16(lane_addr + c0, v);
         if (q.epi == EPI_SWIGLU) tmem_ld16(lane_addr + BN + c0, v3);
         tmem_wait_ld();
-        if (fok) {
-          const int cmax = min(16, it.nrows - c0);
-          for (int j = 0; j < cmax; ++j) {
-            const int64_t o = (it.row0 + c0 + j) * q.ld_out + q.out_col0 + f;
-            if (q.epi == EPI_F32) {
-              static_cast<float*>(q.out)[o] = __fadd_rn(v[j], bias);
-            } else if (q.epi == EPI_SWIGLU) {
-              static_cast<bf16*>(q.out)[o] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
-            } else {
-              static_cast<bf16*>(q.out)[o] = __float2bfloat16_rn(v[j]);
+        if (f32out) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = __fadd_rn(v[j], bias);
+        } else if (q.epi == EPI_SWIGLU) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+        }
+        __syncwarp();
+        const int rows_here = min(16, it.nrows - c0);
+        if (f32out) {
+          // a row is 32 floats = 8 x 16 bytes: lane -> (row lane/8 + 4r, part lane%8)
+          const int part = lane & 7;
+          const bool ok = f0 + part * 4 < q.M;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = (lane >> 3) + 4 * r;
+            if (ok && row < rows_here) {
+              const float4 val = *reinterpret_cast<const float4*>(stg_f + row * 32 + part * 4);
+              const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 4;
+              *reinterpret_cast<float4*>(static_cast<float*>(q.out) + o) = val;
+            }
+          }
+        } else {
+          // a row is 32 bf16 = 4 x 16 bytes: lane -> (row lane/4 + 8r, part lane%4)
+          const int part = lane & 3;
+          const bool ok = f0 + part * 8 < q.M;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int row = (lane >> 2) + 8 * r;
+            if (ok && row < rows_here) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
+              const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 8;
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(q.out) + o) = val;
             }
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
-      mbar_arrive(tmem_empty);
-      acc_phase ^= 1u;
+      mbar_arrive(tmem_empty(buf));
     }
   }
 
@@ -513,6 +586,8 @@ bool gemm_tc_supported(const GemmProblem& p) {
   for (int s = 0; s < p.n_seg; ++s)
     if (p.seg[s].K < 8 || (p.seg[s].K % 8)) return false;
   if (p.epi != EPI_F32 && p.epi != EPI_STORE && p.epi != EPI_SWIGLU) return false;
+  // the epilogue writes 16-byte pieces of output rows
+  if ((p.M % 8) || (p.ld_out % 8) || (p.out_col0 % 8)) return false;
   return true;
 }
 
@@ -571,8 +646,10 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   }
   P.n_probs = n_probs;
   const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
-  P.stages = P.glu ? 3 : 4;
-  const size_t smem = (size_t)P.stages * stage_bytes + 1024;
+  P.stages = P.glu ? MOE_TC_STAGES_GLU : MOE_TC_STAGES;
+  const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
+  const size_t smem = (size_t)P.stages * stage_bytes + 1024 + (size_t)EPI_WARPS * EPI_STAGE_BYTES +
+                      (size_t)(3 * G + 1) * 4;
   cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int grid = num_sms_tc();
   if (P.grouped < 0) grid = (int)imin64(grid, base);
