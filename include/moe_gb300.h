@@ -214,6 +214,28 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void
 /* Enqueues a reset of the device report (status, detail and counters) to zero. */
 MOE_API moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream);
 
+/* Routing for callers that cannot allocate device memory. Some callers of this library run
+ * where no allocation may happen: inside an allocator-free runtime or plugin that is handed only
+ * its input and output buffers, or code that must not call cudaMalloc (which can synchronise
+ * the device) while other work is in flight. For them this entry point computes exactly what
+ * moe_route computes (same kernels, same results) but takes no workspace: its scratch is a
+ * fixed array of 32 MiB inside the library, present on every GPU that loads the library until
+ * the process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Sizes: the routing scratch (256 B + T*E*4 + E*d*elem + E*4 + 3*T*4 bytes, each region
+ *     rounded up to 256 B) must fit in 32 MiB, else MOE_ERR_WORKSPACE and nothing is enqueued;
+ *     the 535B-shaped router (T = 8192, E = 384, d = 6144, bf16) needs 17.5 MB.
+ *   - Set-up: the first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array and leaves its contents behind; each
+ *     call clears what must start at zero. Calls whose GPU work overlaps (other streams, other
+ *     host threads) race on the array: serialise them.
+ *   - device_report: NULL, or 4 int32 of device memory that receive, stream-ordered, the status,
+ *     detail, refined-token and exact-token counts of moe_device_report_t for this call.
+ * The pages describe no counterpart of this entry point. */
+MOE_API moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router,
+                                       const float* b_router, int32_t* topk_idx, float* topk_gate,
+                                       int32_t* device_report, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,7 @@ import torch
 __all__ = [
     "LayerShape", "SliceShape", "SHAPES", "SLICE_C5B", "get_shape",
     "make_layer_inputs", "make_slice_inputs", "ZIPF_BETA", "zipf_bias",
-    "tensor_seed",
+    "tensor_seed", "make_router_inputs",
 ]
 
 # Scale of the log-popularity bias. 1.0 means the logits are biased by ln(p_e)
@@ -249,3 +249,20 @@ def make_slice_inputs(sh: SliceShape, device="cpu") -> Dict[str, torch.Tensor]:
         "w3": _stacked_normal(E, L, F, L ** -0.5, dt, device, sh.seed, "slice_w3"),
         "w2": _stacked_normal(E, F, L, F ** -0.5, dt, device, sh.seed, "slice_w2"),
     }
+
+
+def make_router_inputs(shape: LayerShape, device="cpu") -> Dict[str, torch.Tensor]:
+    """Only the router's inputs (x, w_router, b_router) of make_layer_inputs(shape, device),
+    drawn identically, without the expert weights."""
+    s = shape
+    dt = s.torch_dtype
+    out = {
+        "x": _normal((s.T, s.d_model), 1.0, dt, device, tensor_seed(s.seed, "x")),
+        "w_router": _normal((s.d_model, s.n_experts), s.d_model ** -0.5, dt, device,
+                            tensor_seed(s.seed, "w_router")),
+    }
+    if s.routing == "zipf":
+        out["b_router"] = zipf_bias(s).to(device)
+    else:
+        out["b_router"] = torch.zeros(s.n_experts, dtype=torch.float32, device=device)
+    return out

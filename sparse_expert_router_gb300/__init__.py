@@ -19,7 +19,8 @@ from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_PDL, MOE_FLAG_SIMT, MOE_FORWARD_S
 
 __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
-           "moe_get_device_status", "moe_clear_device_status", "MOE_FLAG_PDL", "MOE_FLAG_SIMT",
+           "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
+           "MOE_FLAG_PDL", "MOE_FLAG_SIMT",
            "MOE_FORWARD_STAGES", "WEIGHT_NAMES"]
 
 WEIGHT_NAMES = ("w_router", "b_router", "w_down", "rms_gamma", "w1", "w3", "w2", "w1_s", "w3_s",
@@ -159,3 +160,12 @@ def moe_get_device_status(ws, stream=None) -> Dict[str, int]:
 def moe_clear_device_status(ws, stream=None):
     _check("moe_clear_device_status",
            load().moe_clear_device_status(_p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_route_noalloc(cfg, x, w_router, b_router, topk_idx, topk_gate, device_report=None,
+                      stream=None):
+    """moe_route for callers that cannot allocate device memory: no workspace argument; the
+    library's fixed 32 MiB scratch array is used instead (see include/moe_gb300.h)."""
+    _check("moe_route_noalloc", load().moe_route_noalloc(
+        C.byref(cfg.c()), _p(x), _p(w_router), _p(b_router), _p(topk_idx), _p(topk_gate),
+        _p(device_report), _stream(stream)))

@@ -68,6 +68,7 @@ SIGNATURES = {
                               C.POINTER(moe_forward_aux_t)]),
     "moe_get_device_status": (C.c_int, [P, C.c_size_t, P, C.POINTER(moe_device_report_t)]),
     "moe_clear_device_status": (C.c_int, [P, C.c_size_t, P]),
+    "moe_route_noalloc": (C.c_int, [CFG, P, P, P, P, P, P, P]),
 }
 
 _lib = None

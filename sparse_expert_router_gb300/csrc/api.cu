@@ -356,6 +356,62 @@ void record(const moe_forward_aux_t* aux, int i, cudaStream_t st) {
     cudaEventRecord(static_cast<cudaEvent_t>(aux->stage_events[i]), st);
 }
 
+// ---- routing without caller-allocated scratch -------------------------------------------
+// Scratch of moe_route_noalloc: one fixed array per GPU that loads this library, kept until the
+// process exits. Its size caps the routing problems that entry point accepts.
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)32 << 20;
+static __device__ __align__(256) unsigned char g_route_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_route_scratch for the current device (looked up once per device: in host
+// code the array's name is only a host-side stand-in). NULL if the lookup failed.
+void* noalloc_scratch_address() {
+  constexpr int kMaxDev = 64;
+  static void* addr[kMaxDev] = {nullptr};
+  static bool looked_up[kMaxDev] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  if (!looked_up[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+    looked_up[dev] = true;
+  }
+  return addr[dev];
+}
+
+// Layout of the routing scratch inside the fixed array (the same regions moe_route uses).
+struct NoallocLayout {
+  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, total;
+};
+NoallocLayout noalloc_layout(const moe_config_t& c) {
+  NoallocLayout L{};
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    size_t o = off;
+    off = al256(off + (size_t)bytes);
+    return o;
+  };
+  const int64_t es = (c.dtype == MOE_BF16) ? 2 : 4;
+  L.hdr = take(sizeof(DeviceHeader));
+  L.logits = take(c.T * c.n_experts * 4);
+  L.wrT = take((int64_t)c.n_experts * c.d_model * es);
+  L.wnorm = take((int64_t)c.n_experts * 4);
+  L.xnorm = take(c.T * 4);
+  L.rlist = take(c.T * 4);
+  L.elist = take(c.T * 4);
+  L.total = off;
+  return L;
+}
+
+__global__ void noalloc_report_kernel(const DeviceHeader* h, int32_t* out) {
+  if (threadIdx.x == 0) {
+    out[0] = h->status;
+    out[1] = h->detail;
+    out[2] = h->n_refine;
+    out[3] = h->n_exact;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -575,6 +631,47 @@ moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
   return cuda_status(header_reset(static_cast<DeviceHeader*>(ws), true,
                                   static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* b_router, int32_t* topk_idx, float* topk_gate,
+                               int32_t* device_report, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_router_width(cfg)) != MOE_OK) return s;
+  if ((s = check_ptrs({x, w_router, topk_idx, topk_gate}, {b_router, device_report})) != MOE_OK)
+    return s;
+  const NoallocLayout NL = noalloc_layout(*cfg);
+  if (NL.total > NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch_address());
+  if (!scratch) return MOE_ERR_CUDA;
+  // The routing stages index the workspace through a Layout; point the regions they use into
+  // the fixed array (the other regions are not touched by routing).
+  Call k = make_call(cfg, scratch, stream);
+  k.L.hdr = NL.hdr;
+  k.L.logits = NL.logits;
+  k.L.wrT = NL.wrT;
+  k.L.wnorm = NL.wnorm;
+  k.L.xnorm = NL.xnorm;
+  k.L.rlist = NL.rlist;
+  k.L.elist = NL.elist;
+  GemmProblem p = router_problem(k, x, w_router, b_router);
+  if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+  RouterArgs ra = router_args(k, x, w_router, b_router, topk_idx, topk_gate);
+  // the report and the refinement counters start from zero on every call
+  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false));
+  MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
+  MOE_TRY_CUDA(run_gemms(k, &p, 1));
+  MOE_TRY_CUDA(router_select(ra, cfg->dtype, num_sms(), k.st, k.pdl));
+  if (device_report) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(32);
+    lc.stream = k.st;
+    MOE_TRY_CUDA(cudaLaunchKernelEx(&lc, noalloc_report_kernel,
+                                    static_cast<const DeviceHeader*>(k.hdr()), device_report));
+  }
+  return MOE_OK;
 }
 
 }  // extern "C"
