@@ -31,7 +31,7 @@ from moe_workloads import SHAPES, make_layer_inputs  # noqa: E402
 
 STAGES = ["prep", "front_gemm", "router_select", "dispatch", "expert_gemm1", "expert_gemm2",
           "combine", "back_gemm"]
-KERNELS_PER_FORWARD = 15          # launches of this library's kernels in one moe_forward
+KERNELS_PER_FORWARD = 16          # launches of this library's kernels in one moe_forward
 METRIC = "MoE-layer tokens/s"
 
 
@@ -45,6 +45,40 @@ def peaks():
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0,
                 "source": "fallback"}
+
+
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "tc_gemm_grouped_l535b_e64_t1368.md")
+
+
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, or None
+    when there is none or the GEMM source changed since the counters were taken."""
+    import hashlib
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        src = open(os.path.join(ROOT, "sparse_expert_router_gb300", "csrc", "gemm_tc.cu"), "rb").read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    ok_sha = any(ln.split() == ["source_sha256_prefix", "gemm_tc.cu", sha] for ln in text.splitlines())
+    if not ok_sha:
+        return None
+    for ln in text.splitlines():
+        parts = ln.split()
+        if len(parts) == 4 and parts[0] == "traffic_per_launch" and parts[1] == workload \
+                and parts[2] == kernel:
+            return float(parts[3])
+    return None
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank float over the process group (the value itself on one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
 
 
 def algorithmic(shape, counts):
@@ -257,11 +291,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t)
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_step = total_ms / args.steps
     value = world * shape.T * args.steps / (total_ms / 1e3)
 
@@ -291,10 +321,7 @@ def main():
             b.record(stream)
             b.synchronize()
             e2e_ms += a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t)
+        e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": world * shape.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
@@ -329,7 +356,8 @@ def main():
         ach = f / (ms_dom * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4)}
-    roof.update({"kernel": dom, "traffic": None, "peak_source": pk["source"]
+    roof.update({"kernel": dom, "traffic": profiled_traffic(shape.name, dom),
+                 "peak_source": pk["source"]
                  + (" (bf16 sustained)" if roof["bound"] == "tensor" else " (HBM copy)")})
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,

@@ -51,25 +51,56 @@ __global__ void __launch_bounds__(CH) hist_kernel(DispatchArgs a) {
     a.chunk_hist[(int64_t)blockIdx.x * a.E + e] = s_cnt[e];
 }
 
-// One block: per-expert walk over chunks (chunk bases, counts), capacity clamp, scan.
-__global__ void __launch_bounds__(1024) scan_kernel(DispatchArgs a) {
+// One block per expert: exclusive scan of the expert's per-chunk counts (the base of each
+// chunk's ranks) and the expert's total count.
+__global__ void __launch_bounds__(256) scan_chunks_kernel(DispatchArgs a) {
+  pdl_wait();
+  __shared__ int s_warp[8];
+  __shared__ int s_carry;
+  const int e = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int64_t c0 = 0; c0 < a.n_chunks; c0 += 256) {
+    const int64_t c = c0 + threadIdx.x;
+    const int v = (c < a.n_chunks) ? a.chunk_hist[c * a.E + e] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(~0u, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = (lane < 8) ? s_warp[lane] : 0;
+      int iw = w;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        int u = __shfl_up_sync(~0u, iw, o);
+        if (lane >= o) iw += u;
+      }
+      if (lane < 8) s_warp[lane] = iw - w;   // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int carry = s_carry;
+    const int excl = carry + s_warp[warp] + incl - v;
+    if (c < a.n_chunks) a.chunk_base[c * a.E + e] = excl;
+    __syncthreads();
+    if (threadIdx.x == 255) s_carry = excl + v;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.counts[e] = s_carry;
+}
+
+// One block: capacity clamp, exclusive scan of the kept counts into the group offsets, drops.
+__global__ void __launch_bounds__(1024) scan_offsets_kernel(DispatchArgs a) {
   pdl_wait();
   __shared__ int s_warp[32];
   __shared__ int s_drop[32];
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int cnt = 0;
-  if (e < a.E) {
-    for (int c = 0; c < a.n_chunks; ++c) {
-      int64_t o = (int64_t)c * a.E + e;
-      int v = a.chunk_hist[o];
-      a.chunk_base[o] = cnt;
-      cnt += v;
-    }
-    a.counts[e] = cnt;
-  }
+  const int cnt = (e < a.E) ? a.counts[e] : 0;
   int kept = (a.cap >= 0) ? min(cnt, a.cap) : cnt;
   int drop = cnt - kept;
-  // block exclusive scan of kept over experts
   int incl = kept;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -224,7 +255,9 @@ cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool
   const unsigned nch = (unsigned)a.n_chunks;
   err = launch(hist_kernel, dim3(nch), dim3(CH), (size_t)a.E * 4, st, pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(scan_kernel, dim3(1), dim3(1024), 0, st, pdl, a);
+  err = launch(scan_chunks_kernel, dim3(a.E), dim3(256), 0, st, pdl, a);
+  if (err != cudaSuccess) return err;
+  err = launch(scan_offsets_kernel, dim3(1), dim3(1024), 0, st, pdl, a);
   if (err != cudaSuccess) return err;
   err = launch(rank_kernel, dim3(nch), dim3(CH), (size_t)a.E * (CH / 32) * 4, st, pdl, a);
   if (err != cudaSuccess) return err;

@@ -70,6 +70,7 @@ struct TcProblem {
   int n_seg;
   int epi, group, M, Mg, m_tiles;
   int n_fastest;               // dense problems: token tiles vary fastest
+  int dual;                    // item = 256 features as two 128-feature tiles sharing the token tile
   int64_t rows;
   void* out;
   int64_t ld_out;
@@ -85,7 +86,7 @@ struct TcParams {
   TcProblem p[MAX_PROBS];
   int n_probs;
   int grouped;                 // index of the grouped problem (always the last) or -1
-  int glu;                     // any problem has the SwiGLU epilogue (two A tiles per stage)
+  int glu;                     // any problem uses two A tiles per stage (SwiGLU or dual)
   int stages;
   DeviceHeader* hdr;
 };
@@ -250,7 +251,7 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
     int64_t within = local - ((int64_t)S.gitem[g] - S.gitem[0]);
     int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
     it.wg = g;
-    it.m0 = m_t * BM;
+    it.m0 = m_t * BM * (q.dual ? 2 : 1);
     it.m_w = it.m0;
     it.row0 = S.glo[g] + (int64_t)n_t * BN;
     it.nrows = (int)imin64(BN, (int64_t)S.ghi[g] - it.row0);
@@ -259,7 +260,7 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
     int n_t, m_t;
     if (q.n_fastest) { n_t = (int)(local % n_tiles); m_t = (int)(local / n_tiles); }
     else { n_t = (int)(local / q.m_tiles); m_t = (int)(local % q.m_tiles); }
-    it.m0 = m_t * BM;
+    it.m0 = m_t * BM * (q.dual ? 2 : 1);
     if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
     else { it.wg = 0; it.m_w = it.m0; }
     it.row0 = (int64_t)n_t * BN;
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int nb = (it.nrows + B_BOX_ROWS - 1) / B_BOX_ROWS;
-      const uint32_t bytes = (glu && q.epi == EPI_SWIGLU ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
+      const bool two_a = (q.epi == EPI_SWIGLU) || q.dual;
+      const uint32_t bytes = (two_a ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
         for (int kb = 0; kb < sg.kblocks; ++kb) {
@@ -395,6 +397,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           if (q.epi == EPI_SWIGLU) {
             tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
             tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a3, full(stage), it.m_w + 64, k0, it.wg);
+          } else if (q.dual) {
+            tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), it.m_w + BM, k0, it.wg);
+            tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + BM + 64, k0,
+                        it.wg);
           }
           for (int b = 0; b < nb; ++b)
             tma_load_2d(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, full(stage), k0,
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
     for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++li) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      const bool sw = (q.epi == EPI_SWIGLU);
+      const bool sw = (q.epi == EPI_SWIGLU) || q.dual;   // second A tile -> second accumulator
       const int n = ((it.nrows + 15) / 16) * 16;
       const uint32_t idesc = make_idesc(n);
       const int buf = li % nacc;
@@ -464,8 +470,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       const uint32_t acc_phase = (uint32_t)(li / nacc) & 1u;
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
-      const int f0 = it.m0 + quad * 32;                  // first feature of this warp
-      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+      for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
+      const int f0 = it.m0 + sub * BM + quad * 32;       // first feature of this warp
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                 (uint32_t)((buf + sub) * BN);
       const bool f32out = (q.epi == EPI_F32);
       const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
       for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
@@ -513,6 +521,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           }
         }
         __syncwarp();
+      }
       }
       tc_fence_before();
       mbar_arrive(tmem_empty(buf));
@@ -616,6 +625,10 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     q.Mg = g.Mg;
     q.m_tiles = (int)cdiv(g.M, BM);
     q.n_fastest = (g.group != GROUP_ROWS);
+    // two 128-feature tiles per item share one token tile: half the token-tile traffic and
+    // twice the weight bytes in flight per stage
+    q.dual = (g.epi != EPI_SWIGLU && g.group != GROUP_COLS && g.M % (2 * BM) == 0) ? 1 : 0;
+    if (q.dual) q.m_tiles = (int)(g.M / (2 * BM));
     q.rows = g.rows;
     q.out = g.out;
     q.ld_out = g.ld_out;
@@ -642,7 +655,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       q.n_items = q.m_tiles * cdiv(g.rows, BN);
       base += q.n_items;
     }
-    if (g.epi == EPI_SWIGLU) P.glu = 1;
+    if (g.epi == EPI_SWIGLU || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
   const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;

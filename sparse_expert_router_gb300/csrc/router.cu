@@ -346,10 +346,10 @@ __global__ void wr_norm_kernel(const T* __restrict__ wt, float* __restrict__ wno
 
 struct WarpArrays {
   float *lg, *lo, *hi, *work;
-  uint8_t* sel;
+  uint8_t *sel, *refined;
 };
 __device__ __forceinline__ WarpArrays warp_arrays(unsigned char* base, int E, int warp) {
-  size_t per = (size_t)E * 17;
+  size_t per = (size_t)E * 18;
   per = (per + 15) & ~(size_t)15;
   unsigned char* p = base + per * warp;
   WarpArrays a;
@@ -358,6 +358,7 @@ __device__ __forceinline__ WarpArrays warp_arrays(unsigned char* base, int E, in
   a.hi = a.lo + E;
   a.work = a.hi + E;
   a.sel = reinterpret_cast<uint8_t*>(a.work + E);
+  a.refined = a.sel + E;
   return a;
 }
 
@@ -395,36 +396,50 @@ router_refine_kernel(RouterArgs a) {
     const int64_t t = a.refine_list[it];
     const T* x = static_cast<const T*>(a.x) + t * a.d;
     warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
-    warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
-    // the undecided experts, in ascending order, into the (now free) work array
-    int* cand = reinterpret_cast<int*>(w.work);
-    int nc = 0;
-    for (int e0 = 0; e0 < a.E; e0 += 32) {
-      int e = e0 + lane;
-      bool on = e < a.E && w.sel[e] == 2;
-      unsigned b = __ballot_sync(~0u, on);
-      if (on) cand[nc + __popc(b & ((1u << lane) - 1u))] = e;
-      nc += __popc(b);
-    }
+    int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+    // Refine undecided experts MC at a time (highest fp32 logit first among those left) and
+    // re-classify after every batch; stop once the top-k is decided or nothing is left.
+    for (int e = lane; e < a.E; e += 32) w.refined[e] = 0;
     __syncwarp();
-    for (int c0 = 0; c0 < nc; c0 += MC) {
+    while (n_in < a.k) {
+      int cand[MC];
+      int nc = 0;
+      for (int j = 0; j < MC; ++j) {
+        float best = -INFINITY;
+        int bi = INT_MAX;
+        for (int e = lane; e < a.E; e += 32)
+          if (w.sel[e] == 2 && !w.refined[e] && (w.lg[e] > best || (w.lg[e] == best && e < bi))) {
+            best = w.lg[e];
+            bi = e;
+          }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          float ob = __shfl_xor_sync(~0u, best, o);
+          int oi = __shfl_xor_sync(~0u, bi, o);
+          if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+        }
+        if (bi == INT_MAX) break;
+        cand[nc++] = bi;
+        if ((bi & 31) == lane) w.refined[bi] = 1;
+        __syncwarp();
+      }
+      if (nc == 0) break;
       float res[MC], eb[MC];
-      const int n_here = min(MC, nc - c0);
-      warp_dot2_multi(x, static_cast<const T*>(a.wrT), cand + c0, n_here, a.d, a.bias, a.g2,
-                      lane, res, eb);
+      warp_dot2_multi(x, static_cast<const T*>(a.wrT), cand, nc, a.d, a.bias, a.g2, lane, res,
+                      eb);
       if (lane == 0) {
 #pragma unroll
         for (int j = 0; j < MC; ++j) {
-          if (j < n_here) {
-            const int ee = cand[c0 + j];
+          if (j < nc) {
+            const int ee = cand[j];
             w.lo[ee] = fmaxf(w.lo[ee], __fsub_rd(res[j], eb[j]));
             w.hi[ee] = fminf(w.hi[ee], __fadd_ru(res[j], eb[j]));
           }
         }
       }
       __syncwarp();
+      n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
     }
-    int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
     if (n_in == a.k) {
       warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
     } else if (lane == 0) {
@@ -442,7 +457,7 @@ router_exact_kernel(RouterArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpArrays w = warp_arrays(smem, a.E, 0);
-  size_t per = ((size_t)a.E * 17 + 15) & ~(size_t)15;
+  size_t per = ((size_t)a.E * 18 + 15) & ~(size_t)15;
   unsigned long long* forms = reinterpret_cast<unsigned long long*>(smem + per);   // [E][NB]
   int32_t* cand = reinterpret_cast<int32_t*>(forms + (size_t)a.E * NB);          // [E]
   __shared__ int s_ncand, s_nin, s_ok;
@@ -492,7 +507,7 @@ router_exact_kernel(RouterArgs a) {
   }
 }
 
-size_t warp_smem(int E) { return ((size_t)E * 17 + 15) & ~(size_t)15; }
+size_t warp_smem(int E) { return ((size_t)E * 18 + 15) & ~(size_t)15; }
 
 }  // namespace
 
@@ -526,7 +541,7 @@ cudaError_t router_select(const RouterArgs& a, int dtype, int num_sms, cudaStrea
   cudaFuncSetAttribute(ex, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_exact);
   err = launch(sel, dim3((unsigned)cdiv(a.T, RT_WARPS)), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(ref, dim3(num_sms * 2), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
+  err = launch(ref, dim3(num_sms * 4), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
   if (err != cudaSuccess) return err;
   return launch(ex, dim3(num_sms), dim3(RT_WARPS * 32), sm_exact, st, pdl, a);
 }
