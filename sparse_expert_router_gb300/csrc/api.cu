@@ -17,6 +17,10 @@ namespace {
 // FMA and uses 1. Certification needs only a valid bound; a looser bound sends more tokens to
 // the compensated stage. tests/test_parity_gpu.py checks the bound on real logits.
 constexpr float TC_BOUND_FACTOR = 2.0f;
+// The tensor-core router GEMM restarts its accumulator every ROUTER_KCHUNK k-blocks of 64 and
+// sums the chunk results in fp32 (error bound c*gamma_256 per chunk plus gamma_nchunks over the
+// chunk sums, instead of c*gamma_d).
+constexpr int ROUTER_KCHUNK = 4;
 
 int64_t pool_rows_of(const moe_config_t& c) {
   return c.pool_rows > 0 ? c.pool_rows : c.T * (int64_t)c.top_k;
@@ -202,7 +206,16 @@ RouterArgs router_args(const Call& k, const void* x, const void* w_router, const
   const double u = ldexp(1.0, -24);
   const double gd = c.d_model * u / (1.0 - c.d_model * u);
   a.gam_d = round_up_f(gd);
-  a.cgam = round_up_f(gd * (k.tc ? TC_BOUND_FACTOR : 1.0));
+  if (k.tc) {
+    // chunked accumulation: |err| <= (c g_kc + g_nch (1 + c g_kc)) sum|x w| + 2u|l|
+    const double kc = 64.0 * ROUTER_KCHUNK;
+    const double nch = ceil(c.d_model / kc);
+    const double g_kc = kc * u / (1.0 - kc * u), g_n = nch * u / (1.0 - nch * u);
+    const double cf = TC_BOUND_FACTOR;
+    a.cgam = round_up_f(cf * g_kc + g_n * (1.0 + cf * g_kc));
+  } else {
+    a.cgam = round_up_f(gd);
+  }
   const double n2 = (c.dtype == MOE_F32 ? 2.0 : 1.0) * (c.d_model + 1) + 64.0;
   const double gn = n2 * u / (1.0 - n2 * u);
   a.g2 = round_up_f(gn * gn);
@@ -225,6 +238,7 @@ GemmProblem router_problem(const Call& k, const void* x, const void* w_router, c
   p.ld_out = k.c.n_experts;
   p.bias = b;
   p.dtype = k.c.dtype;
+  p.kchunk = k.tc ? ROUTER_KCHUNK : 0;
   return p;
 }
 

@@ -39,6 +39,10 @@ struct GemmProblem {
   int out_col0 = 0;
   const float* bias = nullptr;  // EPI_F32: [M] or NULL
   int dtype = 0;             // DT_BF16 / DT_F32: act, weights and EPI_STORE/EPI_SWIGLU output
+  // tcgen05 only, EPI_F32 dense single-segment problems: the accumulator is restarted every
+  // kchunk k-blocks of 64 and the chunk results are summed in fp32 by the epilogue (a tighter
+  // rounding-error bound for the router's certified top-k). 0 = one accumulation over K.
+  int kchunk = 0;
 };
 
 // CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).

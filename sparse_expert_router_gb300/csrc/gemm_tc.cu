@@ -38,6 +38,7 @@ namespace {
 #endif
 constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
+constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem
 constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
 #ifndef MOE_TC_EPI_WARPS
 #define MOE_TC_EPI_WARPS 8
@@ -71,6 +72,8 @@ struct TcProblem {
   int epi, group, M, Mg, m_tiles;
   int n_fastest;               // dense problems: token tiles vary fastest
   int dual;                    // item = 256 features as two 128-feature tiles sharing the token tile
+  int kchunk;                  // k-blocks per accumulation chunk (0 = whole K)
+  int bn;                      // token rows per tile
   int64_t rows;
   void* out;
   int64_t ld_out;
@@ -256,15 +259,15 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
     it.row0 = S.glo[g] + (int64_t)n_t * BN;
     it.nrows = (int)imin64(BN, (int64_t)S.ghi[g] - it.row0);
   } else {
-    int64_t n_tiles = cdiv(q.rows, BN);
+    int64_t n_tiles = cdiv(q.rows, q.bn);
     int n_t, m_t;
     if (q.n_fastest) { n_t = (int)(local % n_tiles); m_t = (int)(local / n_tiles); }
     else { n_t = (int)(local / q.m_tiles); m_t = (int)(local % q.m_tiles); }
     it.m0 = m_t * BM * (q.dual ? 2 : 1);
     if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
     else { it.wg = 0; it.m_w = it.m0; }
-    it.row0 = (int64_t)n_t * BN;
-    it.nrows = (int)imin64(BN, q.rows - it.row0);
+    it.row0 = (int64_t)n_t * q.bn;
+    it.nrows = (int)imin64(q.bn, q.rows - it.row0);
   }
   return it;
 }
@@ -414,21 +417,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int li = 0;                                   // this CTA's item counter
-    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++li) {
+    int ev = 0;      // accumulator events of this CTA: one per item, or one per k-chunk
+    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const bool sw = (q.epi == EPI_SWIGLU) || q.dual;   // second A tile -> second accumulator
       const int n = ((it.nrows + 15) / 16) * 16;
       const uint32_t idesc = make_idesc(n);
-      const int buf = li % nacc;
-      const uint32_t acc_phase = (uint32_t)(li / nacc) & 1u;
-      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-      if (!mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
-      tc_fence_after();
-      uint32_t accumulate = 0;
-      for (int s = 0; s < q.n_seg && ok; ++s) {
-        for (int kb = 0; kb < q.seg[s].kblocks; ++kb) {
+      int kb_total = 0;
+      for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
+      const int per_ev = q.kchunk ? q.kchunk : kb_total;
+      for (int kb0 = 0; kb0 < kb_total && ok; kb0 += per_ev, ++ev) {
+        const int buf = ev % nacc;
+        const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        if (!mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t accumulate = 0;
+        const int kb_end = min(kb0 + per_ev, kb_total);
+        for (int kk = kb0; kk < kb_end; ++kk) {
           if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)), b = smem_u32(sB(stage));
@@ -447,8 +454,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           mma_commit(empty(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
+        mma_commit(tmem_full(buf));
       }
-      mma_commit(tmem_full(buf));
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
@@ -458,16 +465,105 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
     // 16-byte pieces of output rows.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;                    // 0, or 1 for the second warp of a quadrant
-    const int f_local = quad * 32 + lane;
     unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
     float* stg_f = reinterpret_cast<float*>(stg);
     bf16* stg_h = reinterpret_cast<bf16*>(stg);
-    int li = 0;
-    for (int64_t w = blockIdx.x; w < total; w += gridDim.x, ++li) {
+    // Writes one 16-token x 32-feature chunk of this warp (values already final) through the
+    // transpose tile; f32 rows are 8 x 16 bytes, bf16 rows 4 x 16 bytes.
+    auto store_chunk = [&](const TcProblem& q, const Item& it, int c0, int f0, const float* v,
+                           const float* v3) {
+      const bool f32out = (q.epi == EPI_F32);
+      if (f32out) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = v[j];
+      } else if (q.epi == EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+      }
+      __syncwarp();
+      const int rows_here = min(16, it.nrows - c0);
+      if (f32out) {
+        const int part = lane & 7;
+        const bool ok = f0 + part * 4 < q.M;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = (lane >> 3) + 4 * r;
+          if (ok && row < rows_here) {
+            const float4 val = *reinterpret_cast<const float4*>(stg_f + row * 32 + part * 4);
+            const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 4;
+            *reinterpret_cast<float4*>(static_cast<float*>(q.out) + o) = val;
+          }
+        }
+      } else {
+        const int part = lane & 3;
+        const bool ok = f0 + part * 8 < q.M;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int row = (lane >> 2) + 8 * r;
+          if (ok && row < rows_here) {
+            const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
+            const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 8;
+            *reinterpret_cast<uint4*>(static_cast<bf16*>(q.out) + o) = val;
+          }
+        }
+      }
+      __syncwarp();
+    };
+    int ev = 0;
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      const int buf = li % nacc;
-      const uint32_t acc_phase = (uint32_t)(li / nacc) & 1u;
+      if (q.kchunk) {
+        // k-chunked fp32 problem: sum the chunk accumulators in registers, in chunk order.
+        // This warp owns columns half*16 + 32*i (i < 4) of the <= 128-token tile.
+        int kb_total = q.seg[0].kblocks;
+        const int f0 = it.m0 + quad * 32;
+        float acc[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+        bool ok = true;
+        for (int kb0 = 0; kb0 < kb_total; kb0 += q.kchunk, ++ev) {
+          const int buf = ev % nacc;
+          const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
+          if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c0 = half * 16 + 32 * i;
+            if (c0 < it.nrows) {
+              float v[16];
+              tmem_ld16(lane_addr + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[i][j] = __fadd_rn(acc[i][j], v[j]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(tmem_empty(buf));
+        }
+        if (!ok) break;
+        const float bias = (q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c0 = half * 16 + 32 * i;
+          if (c0 < it.nrows) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(acc[i][j], bias);
+            store_chunk(q, it, c0, f0, v, v);
+          }
+        }
+        continue;
+      }
+      const int buf = ev % nacc;
+      const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
+      ++ev;
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
       for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
@@ -483,44 +579,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
         tmem_wait_ld();
         if (f32out) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = __fadd_rn(v[j], bias);
-        } else if (q.epi == EPI_SWIGLU) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
         }
-        __syncwarp();
-        const int rows_here = min(16, it.nrows - c0);
-        if (f32out) {
-          // a row is 32 floats = 8 x 16 bytes: lane -> (row lane/8 + 4r, part lane%8)
-          const int part = lane & 7;
-          const bool ok = f0 + part * 4 < q.M;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int row = (lane >> 3) + 4 * r;
-            if (ok && row < rows_here) {
-              const float4 val = *reinterpret_cast<const float4*>(stg_f + row * 32 + part * 4);
-              const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 4;
-              *reinterpret_cast<float4*>(static_cast<float*>(q.out) + o) = val;
-            }
-          }
-        } else {
-          // a row is 32 bf16 = 4 x 16 bytes: lane -> (row lane/4 + 8r, part lane%4)
-          const int part = lane & 3;
-          const bool ok = f0 + part * 8 < q.M;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int row = (lane >> 2) + 8 * r;
-            if (ok && row < rows_here) {
-              const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
-              const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 8;
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(q.out) + o) = val;
-            }
-          }
-        }
-        __syncwarp();
+        store_chunk(q, it, c0, f0, v, v3);
       }
       }
       tc_fence_before();
@@ -597,6 +658,9 @@ bool gemm_tc_supported(const GemmProblem& p) {
   if (p.epi != EPI_F32 && p.epi != EPI_STORE && p.epi != EPI_SWIGLU) return false;
   // the epilogue writes 16-byte pieces of output rows
   if ((p.M % 8) || (p.ld_out % 8) || (p.out_col0 % 8)) return false;
+  if (p.kchunk < 0) return false;
+  if (p.kchunk > 0 && (p.epi != EPI_F32 || p.group != GROUP_NONE || p.n_seg != 1 || EPI_WARPS != 8))
+    return false;
   return true;
 }
 
@@ -627,7 +691,10 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     q.n_fastest = (g.group != GROUP_ROWS);
     // two 128-feature tiles per item share one token tile: half the token-tile traffic and
     // twice the weight bytes in flight per stage
-    q.dual = (g.epi != EPI_SWIGLU && g.group != GROUP_COLS && g.M % (2 * BM) == 0) ? 1 : 0;
+    q.kchunk = g.kchunk;
+    q.bn = g.kchunk ? BN_CHUNKED : BN;
+    q.dual = (!g.kchunk && g.epi != EPI_SWIGLU && g.group != GROUP_COLS && g.M % (2 * BM) == 0)
+                 ? 1 : 0;
     if (q.dual) q.m_tiles = (int)(g.M / (2 * BM));
     q.rows = g.rows;
     q.out = g.out;
@@ -652,7 +719,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       P.grouped = j;
       q.n_items = 0;
     } else {
-      q.n_items = q.m_tiles * cdiv(g.rows, BN);
+      q.n_items = q.m_tiles * cdiv(g.rows, q.bn);
       base += q.n_items;
     }
     if (g.epi == EPI_SWIGLU || q.dual) P.glu = 1;

@@ -246,65 +246,70 @@ __device__ __forceinline__ bool decompose<bf16>(bf16 v, uint32_t& M, int& q, uin
   return true;
 }
 
-__device__ __forceinline__ void bins_add(long long (&bins)[NB], uint64_t M, int q, uint32_t neg) {
-  if (M == 0) return;
-  int p = q + EXP_BIAS;
-  int bi = p >> 5, sh = p & 31;
-  uint64_t lo = (M & 0xFFFFFFFFull) << sh;
-  uint64_t hi = (M >> 32) << sh;
-  long long c0 = (long long)(lo & 0xFFFFFFFFull);
-  long long c1 = (long long)((lo >> 32) + (hi & 0xFFFFFFFFull));
-  long long c2 = (long long)(hi >> 32);
-  if (neg) { c0 = -c0; c1 = -c1; c2 = -c2; }
-  bins[bi] += c0;
-  bins[bi + 1] += c1;
-  bins[bi + 2] += c2;
-}
-
-// Exact x . w + bias into canonical form `out`: limbs 0..NB-2 in [0, 2^32), limb NB-1 signed.
-// Every lane accumulates its products in private limbs (each limb stays below 2^47 in
-// magnitude), the warp adds the limbs, lane 0 propagates the carries.
+// Block-wide exact x . w + bias (blockDim = RT_WARPS * 32) into canonical form `out`. Every
+// thread accumulates its products in 20 register limbs (updated with predicated adds, so the
+// limbs stay in registers); warps add their limbs with shuffles, thread 0 adds the warps' limbs
+// (from `red`, RT_WARPS * NB int64 of shared memory) and propagates the carries.
 template <typename T>
-__device__ bool warp_exact(const T* x, const T* w, int d, float bias, int lane,
-                           unsigned long long* out) {
+__device__ bool block_exact(const T* x, const T* w, int d, float bias,
+                            long long* red, unsigned long long* out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   long long bins[NB];
 #pragma unroll
   for (int i = 0; i < NB; ++i) bins[i] = 0;
   bool ok = true;
-  for (int i = lane; i < d; i += 32) {
+  auto add = [&](uint64_t M, int q, uint32_t neg) {
+    if (M == 0) return;
+    const int p = q + EXP_BIAS;
+    const int bi = p >> 5, sh = p & 31;
+    const uint64_t lo = (M & 0xFFFFFFFFull) << sh;
+    const uint64_t hi = (M >> 32) << sh;
+    long long c0 = (long long)(lo & 0xFFFFFFFFull);
+    long long c1 = (long long)((lo >> 32) + (hi & 0xFFFFFFFFull));
+    long long c2 = (long long)(hi >> 32);
+    if (neg) { c0 = -c0; c1 = -c1; c2 = -c2; }
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+      bins[i] += (i == bi) ? c0 : (i == bi + 1) ? c1 : (i == bi + 2) ? c2 : 0ll;
+  };
+  for (int i = tid; i < d; i += RT_WARPS * 32) {
     uint32_t Mx = 0, Mw = 0, sx = 0, sw = 0;
     int qx = 0, qw = 0;
     bool fx = decompose<T>(x[i], Mx, qx, sx);
     bool fw = decompose<T>(w[i], Mw, qw, sw);
     ok &= fx && fw;
-    if (fx && fw) bins_add(bins, (uint64_t)Mx * (uint64_t)Mw, qx + qw, sx ^ sw);
+    if (fx && fw) add((uint64_t)Mx * (uint64_t)Mw, qx + qw, sx ^ sw);
   }
-  if (lane == 0) {
+  if (tid == 0) {
     uint32_t Mb = 0, sb = 0;
     int qb = 0;
     bool fb = decompose<float>(bias, Mb, qb, sb);   // the bias is Mb 2^qb, qb >= -149
     ok &= fb;
-    if (fb) bins_add(bins, (uint64_t)Mb, qb, sb);
+    if (fb) add((uint64_t)Mb, qb, sb);
   }
 #pragma unroll
   for (int i = 0; i < NB; ++i) {
     long long v = bins[i];
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
-    bins[i] = v;
+    if (lane == 0) red[warp * NB + i] = v;
   }
-  if (lane == 0) {
+  ok = __syncthreads_and(ok);
+  if (tid == 0) {
     long long carry = 0;
-#pragma unroll
-    for (int i = 0; i < NB - 1; ++i) {
-      long long v = bins[i] + carry;
-      out[i] = (unsigned long long)(v & 0xFFFFFFFFll);
-      carry = v >> 32;   // arithmetic shift: floor division
+    for (int i = 0; i < NB; ++i) {
+      long long v = carry;
+      for (int wv = 0; wv < RT_WARPS; ++wv) v += red[wv * NB + i];
+      if (i < NB - 1) {
+        out[i] = (unsigned long long)(v & 0xFFFFFFFFll);
+        carry = v >> 32;   // arithmetic shift: floor division
+      } else {
+        out[i] = (unsigned long long)v;
+      }
     }
-    out[NB - 1] = (unsigned long long)(bins[NB - 1] + carry);
   }
-  __syncwarp();
-  return __all_sync(~0u, ok);
+  __syncthreads();
+  return ok;
 }
 
 // -1, 0, +1 as a < b, a == b, a > b for canonical exact values.
@@ -449,7 +454,10 @@ router_refine_kernel(RouterArgs a) {
   }
 }
 
-// One block per token still undecided: exact logits of every stage-1 candidate.
+// One block per token still undecided after stage 2. Warp 0 re-derives the stage-1
+// candidates; the 8 warps re-run their compensated dot products in parallel; only experts still
+// undecided then get exact logits, each computed by the whole block; the remaining top-k slots
+// go to the largest exact values, ties to the lower index.
 template <typename T>
 __global__ void __launch_bounds__(RT_WARPS * 32)
 router_exact_kernel(RouterArgs a) {
@@ -459,7 +467,10 @@ router_exact_kernel(RouterArgs a) {
   WarpArrays w = warp_arrays(smem, a.E, 0);
   size_t per = ((size_t)a.E * 18 + 15) & ~(size_t)15;
   unsigned long long* forms = reinterpret_cast<unsigned long long*>(smem + per);   // [E][NB]
-  int32_t* cand = reinterpret_cast<int32_t*>(forms + (size_t)a.E * NB);          // [E]
+  long long* red = reinterpret_cast<long long*>(forms + (size_t)a.E * NB);      // [RT_WARPS][NB]
+  int32_t* cand = reinterpret_cast<int32_t*>(red + RT_WARPS * NB);             // [E]
+  float* cres = reinterpret_cast<float*>(cand + a.E);                           // [E]
+  float* ceb = cres + a.E;                                                      // [E]
   __shared__ int s_ncand, s_nin, s_ok;
   const int n = min(a.hdr->n_exact, (int)a.T);
   for (int it = blockIdx.x; it < n; it += gridDim.x) {
@@ -467,6 +478,34 @@ router_exact_kernel(RouterArgs a) {
     const T* x = static_cast<const T*>(a.x) + t * a.d;
     if (warp == 0) {
       warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
+      warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+      int base = 0;
+      for (int e0 = 0; e0 < a.E; e0 += 32) {
+        int e = e0 + lane;
+        bool on = e < a.E && w.sel[e] == 2;
+        unsigned b = __ballot_sync(~0u, on);
+        if (on) cand[base + __popc(b & ((1u << lane) - 1u))] = e;
+        base += __popc(b);
+      }
+      if (lane == 0) { s_ncand = base; s_ok = 1; }
+    }
+    __syncthreads();
+    // stage 2 for every candidate, one warp per candidate
+    const int nc = s_ncand;
+    for (int ci = warp; ci < nc; ci += RT_WARPS) {
+      float res[MC], eb[MC];
+      warp_dot2_multi(x, static_cast<const T*>(a.wrT), cand + ci, 1, a.d, a.bias, a.g2, lane, res,
+                      eb);
+      if (lane == 0) { cres[ci] = res[0]; ceb[ci] = eb[0]; }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      for (int ci = lane; ci < nc; ci += 32) {
+        const int e = cand[ci];
+        w.lo[e] = fmaxf(w.lo[e], __fsub_rd(cres[ci], ceb[ci]));
+        w.hi[e] = fminf(w.hi[e], __fadd_ru(cres[ci], ceb[ci]));
+      }
+      __syncwarp();
       int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
       int base = 0;
       for (int e0 = 0; e0 < a.E; e0 += 32) {
@@ -476,23 +515,23 @@ router_exact_kernel(RouterArgs a) {
         if (on) cand[base + __popc(b & ((1u << lane) - 1u))] = e;
         base += __popc(b);
       }
-      if (lane == 0) { s_ncand = base; s_nin = n_in; s_ok = 1; }
+      if (lane == 0) { s_ncand = base; s_nin = n_in; }
     }
     __syncthreads();
-    const int nc = s_ncand;
-    for (int ci = warp; ci < nc; ci += RT_WARPS) {
-      int e = cand[ci];
-      bool ok = warp_exact(x, static_cast<const T*>(a.wrT) + (int64_t)e * a.d, a.d,
-                           a.bias ? a.bias[e] : 0.0f, lane, forms + (size_t)ci * NB);
-      if (!ok && lane == 0) s_ok = 0;
+    // stage 3: exact values of the experts still undecided, one block-wide sum each
+    const int nc2 = s_ncand;
+    for (int ci = 0; ci < nc2; ++ci) {
+      const int e = cand[ci];
+      bool ok = block_exact(x, static_cast<const T*>(a.wrT) + (int64_t)e * a.d, a.d,
+                            a.bias ? a.bias[e] : 0.0f, red, forms + (size_t)ci * NB);
+      if (!ok && threadIdx.x == 0) s_ok = 0;
     }
-    __syncthreads();
     if (warp == 0) {
       const int need = a.k - s_nin;
       // rank each candidate among the candidates: larger exact value first, then lower index
-      for (int ci = lane; ci < nc; ci += 32) {
+      for (int ci = lane; ci < nc2; ci += 32) {
         int r = 0;
-        for (int cj = 0; cj < nc; ++cj) {
+        for (int cj = 0; cj < nc2; ++cj) {
           if (cj == ci) continue;
           int c = exact_cmp(forms + (size_t)cj * NB, forms + (size_t)ci * NB);
           if (c > 0 || (c == 0 && cand[cj] < cand[ci])) ++r;
@@ -531,7 +570,8 @@ cudaError_t router_prepare(const RouterArgs& a, int dtype, cudaStream_t st, bool
 
 cudaError_t router_select(const RouterArgs& a, int dtype, int num_sms, cudaStream_t st, bool pdl) {
   size_t sm_sel = warp_smem(a.E) * RT_WARPS;
-  size_t sm_exact = warp_smem(a.E) + (size_t)a.E * NB * 8 + (size_t)a.E * 4;
+  size_t sm_exact = warp_smem(a.E) + (size_t)a.E * NB * 8 + (size_t)RT_WARPS * NB * 8 +
+                    (size_t)a.E * 12;
   cudaError_t err;
   auto sel = (dtype == DT_BF16) ? router_select_kernel<bf16> : router_select_kernel<float>;
   auto ref = (dtype == DT_BF16) ? router_refine_kernel<bf16> : router_refine_kernel<float>;
