@@ -229,7 +229,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="l535b_t8192", choices=sorted(SHAPES))
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05")
-    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -249,7 +249,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
 
-    flags = (m.MOE_FLAG_SIMT if args.simt else 0) | (m.MOE_FLAG_PDL if args.pdl else 0)
+    flags = (m.MOE_FLAG_SIMT if args.simt else 0) | (0 if args.no_pdl else m.MOE_FLAG_PDL)
     cfg = m.LayerConfig.from_shape(shape, flags=flags)
     inp = make_layer_inputs(shape.with_(seed=shape.seed), dev)
     if rank > 0:   # each replica processes its own batch
@@ -369,7 +369,7 @@ def main():
                                f"latent={shape.d_latent} E={shape.n_experts} k={shape.top_k} "
                                f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "gemm_path": "simt" if args.simt else "tcgen05", "pdl": bool(args.pdl),
+                   "gemm_path": "simt" if args.simt else "tcgen05", "pdl": not args.no_pdl,
                    "l2": "flushed between timed steps (256 MB write); weights (21.7 GB) exceed L2"},
         "layer_tflop_s": round(sum(shape.flops().values()) / (ms_step * 1e-3) / 1e12, 1),
         "stages": stages,

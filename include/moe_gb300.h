@@ -214,6 +214,14 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void
 /* Enqueues a reset of the device report (status, detail and counters) to zero. */
 MOE_API moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream);
 
+/* Self-test of failure detection: enqueues a kernel whose single thread waits, with the bounded
+ * mbarrier wait every tensor-core kernel of this library uses, on a barrier that nothing ever
+ * arrives at. After limit_ms (1..10000) the wait gives up and records MOE_ERR_DEVICE_TIMEOUT
+ * (detail 99) in the workspace's device report; the kernel then returns normally and the CUDA
+ * context stays usable. Read the result with moe_get_device_status. */
+MOE_API moe_status_t moe_selftest_device_timeout(void* ws, size_t ws_bytes, uint32_t limit_ms,
+                                                 void* stream);
+
 /* Routing for callers that cannot allocate device memory. Some callers of this library run
  * where no allocation may happen: inside an allocator-free runtime or plugin that is handed only
  * its input and output buffers, or code that must not call cudaMalloc (which can synchronise

@@ -20,6 +20,7 @@ from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_PDL, MOE_FLAG_SIMT, MOE_FORWARD_S
 __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
            "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
+           "moe_selftest_device_timeout",
            "MOE_FLAG_PDL", "MOE_FLAG_SIMT",
            "MOE_FORWARD_STAGES", "WEIGHT_NAMES"]
 
@@ -155,6 +156,12 @@ def moe_get_device_status(ws, stream=None) -> Dict[str, int]:
            load().moe_get_device_status(_p(ws), ws.numel(), _stream(stream), C.byref(r)))
     return {"status": r.status, "detail": r.detail, "n_refined": r.n_refined,
             "n_exact": r.n_exact}
+
+
+def moe_selftest_device_timeout(ws, limit_ms=200, stream=None):
+    """Enqueue a bounded wait that nothing satisfies; it records MOE_ERR_DEVICE_TIMEOUT."""
+    _check("moe_selftest_device_timeout",
+           load().moe_selftest_device_timeout(_p(ws), ws.numel(), int(limit_ms), _stream(stream)))
 
 
 def moe_clear_device_status(ws, stream=None):

@@ -69,6 +69,7 @@ SIGNATURES = {
     "moe_get_device_status": (C.c_int, [P, C.c_size_t, P, C.POINTER(moe_device_report_t)]),
     "moe_clear_device_status": (C.c_int, [P, C.c_size_t, P]),
     "moe_route_noalloc": (C.c_int, [CFG, P, P, P, P, P, P, P]),
+    "moe_selftest_device_timeout": (C.c_int, [P, C.c_size_t, C.c_uint32, P]),
 }
 
 _lib = None

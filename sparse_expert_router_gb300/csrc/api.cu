@@ -641,6 +641,15 @@ moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream
   return MOE_OK;
 }
 
+moe_status_t moe_selftest_device_timeout(void* ws, size_t ws_bytes, uint32_t limit_ms,
+                                         void* stream) {
+  if (!ws || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
+  if ((uintptr_t)ws & 255u) return MOE_ERR_ALIGNMENT;
+  if (limit_ms < 1 || limit_ms > 10000) return MOE_ERR_INVALID_ARG;
+  return cuda_status(bounded_wait_selftest(ws, (uint64_t)limit_ms * 1000000ull,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_clear_device_status(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
   return cuda_status(header_reset(static_cast<DeviceHeader*>(ws), true,

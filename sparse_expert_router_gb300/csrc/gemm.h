@@ -54,4 +54,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
                     bool pdl);
 bool gemm_tc_supported(const GemmProblem& p);
 
+// Self-test of the kernels' bounded mbarrier wait (a barrier nothing arrives at).
+cudaError_t bounded_wait_selftest(void* dev_header, uint64_t limit_ns, cudaStream_t stream);
+
 }  // namespace moe

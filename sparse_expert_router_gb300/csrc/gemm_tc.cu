@@ -128,7 +128,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait: false when the kernel is aborting (timeout here or elsewhere in the CTA).
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                          DeviceHeader* hdr, int where) {
+                          DeviceHeader* hdr, int where, uint64_t limit_ns = TIMEOUT_NS) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -137,7 +137,7 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
       uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > TIMEOUT_NS) {
+      } else if (now - t0 > limit_ns) {
         report_error(hdr, MOE_ERR_DEVICE_TIMEOUT, where);
         *abort_flag = 1;
         return false;
@@ -598,6 +598,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing arrives at, with
+// the same routine the GEMM's roles use; it gives up after limit_ns and records
+// MOE_ERR_DEVICE_TIMEOUT (detail 99) in the device report.
+__global__ void bounded_wait_selftest_kernel(DeviceHeader* hdr, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int s_abort;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(smem_u32(&bar), 0, &s_abort, hdr, 99, limit_ns);
+  }
+}
+
 // ---- host side ----------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -735,6 +749,11 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   if (P.grouped < 0) grid = (int)imin64(grid, base);
   if (grid < 1) return cudaSuccess;
   return launch(tc_gemm_kernel, dim3(grid), dim3(NTHREADS), smem, stream, pdl, P);
+}
+
+cudaError_t bounded_wait_selftest(void* dev_header, uint64_t limit_ns, cudaStream_t stream) {
+  return launch(bounded_wait_selftest_kernel, dim3(1), dim3(32), 0, stream, false,
+                static_cast<DeviceHeader*>(dev_header), limit_ns);
 }
 
 }  // namespace moe

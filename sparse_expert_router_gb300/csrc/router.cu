@@ -142,6 +142,7 @@ __device__ __forceinline__ void load8f(const T* p, float v[8]) { ld8(p, v); }
 template <typename T>
 __device__ float warp_norm_ub(const T* x, int d, float gam_d, int lane) {
   float s = 0.0f;
+#pragma unroll 4
   for (int i = lane * 8; i < d; i += 256) {
     float v[8];
     load8f(x + i, v);

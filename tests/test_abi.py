@@ -107,6 +107,8 @@ def test_argument_errors_before_any_launch(lib):
     assert lib.moe_forward(C.byref(cfg2.c()), C.byref(w), good, good, ws, n, None, None) == \
         L.MOE_ERR_INVALID_ARG
     assert lib.moe_get_device_status(None, 256, None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_device_timeout(ws, 256, 0, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_device_timeout(ws, 256, 20000, None) == L.MOE_ERR_INVALID_ARG
     # a bf16 router needs a 16-byte row pitch of W_r (E a multiple of 8); the expert calls do not
     c12 = _cfg(dtype="bf16", n_experts=12)
     n12 = _ws(lib, c12)

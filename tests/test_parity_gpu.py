@@ -215,6 +215,27 @@ def test_bad_routing_is_reported_not_faulted():
     torch.cuda.synchronize()
 
 
+def test_bounded_wait_times_out_and_context_survives():
+    """Failure detection without a fault: a bounded device wait that nothing satisfies gives up
+    after its limit, the host reads MOE_ERR_DEVICE_TIMEOUT, and the GPU keeps working."""
+    import time
+    shape = SHAPES["tiny_f32"]
+    cfg = m.LayerConfig.from_shape(shape)
+    ws = m.alloc_workspace(cfg, DEV)
+    t0 = time.perf_counter()
+    m.moe_selftest_device_timeout(ws, 200)
+    rep = m.moe_get_device_status(ws)
+    dt = time.perf_counter() - t0
+    assert rep["status"] == 7 and rep["detail"] == 99, rep      # MOE_ERR_DEVICE_TIMEOUT
+    assert 0.15 < dt < 5.0, dt
+    # the context is intact: a forward right after runs and matches the oracle's routing
+    inp = gpu_inputs(shape)
+    got = run_forward(shape, inp)
+    ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()})
+    check_routing(got, ref, shape)
+    assert got["report"]["status"] == 0
+
+
 # ------------------------------------------------------------------- 535B-shaped ----
 
 LARGE = ["l535b_t8192", "l535b_zipf_t16384", "l535b_zipf_t16384_cf110", "l535b_t65536"]
