@@ -167,9 +167,10 @@ constexpr int MC = 4;   // candidates evaluated together (their loads overlap)
 // x . w_j + bias_j for up to MC candidate rows w_j of W_r^T, each with a bound on its error;
 // lane 0 returns the values. Error-free TwoSum accumulation (plus TwoProduct for fp32) per
 // lane, the lanes' (sum, compensation) pairs combined with TwoSum.
-template <typename T>
+template <typename T, int NMC = MC>
 __device__ void warp_dot2_multi(const T* x, const T* wrT, const int* cand, int nc, int d,
                                 const float* bias, float g2, int lane, float* res, float* eb) {
+  constexpr int MC = NMC;
   const bool f32 = sizeof(T) == 4;
   float s[MC], c[MC], sa[MC];
   const T* wp[MC];
@@ -368,6 +369,10 @@ __device__ __forceinline__ WarpArrays warp_arrays(unsigned char* base, int E, in
   return a;
 }
 
+// Stage 1 for every token. Every expert's logit gets the same, token-wide error bound beta
+// (the largest of the per-expert bounds), so one extraction of the k+1 largest fp32 logits
+// decides: an expert is surely in when l_e - beta > l_(k+1) + beta, surely out when
+// l_e + beta < l_(k) - beta. Tokens with an undecided expert go to the refine list.
 template <typename T>
 __global__ void __launch_bounds__(RT_WARPS * 32)
 router_select_kernel(RouterArgs a) {
@@ -378,10 +383,59 @@ router_select_kernel(RouterArgs a) {
   if (t >= a.T) return;
   WarpArrays w = warp_arrays(smem, a.E, warp);
   const T* x = static_cast<const T*>(a.x) + t * a.d;
-  float xn = warp_norm_ub(x, a.d, a.gam_d, lane);
+  const float xn = warp_norm_ub(x, a.d, a.gam_d, lane);
   if (lane == 0) a.xnorm[t] = xn;
-  warp_stage1(a.logits + t * a.E, a.wnorm, xn, a.cgam, a.E, lane, w.lg, w.lo, w.hi);
-  int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+  const float* lt = a.logits + t * a.E;
+  float wmax = 0.0f, amax = 0.0f;
+  for (int e = lane; e < a.E; e += 32) {
+    const float l = lt[e];
+    w.lg[e] = l;
+    w.work[e] = l;
+    wmax = fmaxf(wmax, a.wnorm[e]);
+    amax = fmaxf(amax, fabsf(l));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    wmax = fmaxf(wmax, __shfl_xor_sync(~0u, wmax, o));
+    amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+  }
+  float beta = __fadd_ru(__fmul_ru(__fmul_ru(a.cgam, xn), wmax), __fmul_ru(2.0f * U32, amax));
+  beta = __fadd_ru(beta, 1e-30f);
+  __syncwarp();
+  // the k-th and (k+1)-th largest fp32 logits (with multiplicity)
+  float lk = -INFINITY, lk1 = -INFINITY;
+  const int kk = min(a.k + 1, a.E);
+  for (int it = 0; it < kk; ++it) {
+    float best = -INFINITY;
+    int bi = INT_MAX;
+    for (int e = lane; e < a.E; e += 32) {
+      const float v = w.work[e];
+      if (v > best) { best = v; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ob = __shfl_xor_sync(~0u, best, o);
+      const int oi = __shfl_xor_sync(~0u, bi, o);
+      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    }
+    if (it == a.k - 1) lk = best;
+    if (it == a.k) lk1 = best;
+    if (bi != INT_MAX && (bi & 31) == lane) w.work[bi] = -INFINITY;
+    __syncwarp();
+  }
+  const float in_thr = __fadd_ru(__fadd_ru(lk1, beta), beta);    // l_e - beta > l_(k+1) + beta
+  const float out_thr = __fsub_rd(__fsub_rd(lk, beta), beta);    // l_e + beta < l_(k) - beta
+  int n_in = 0, n_amb = 0;
+  for (int e = lane; e < a.E; e += 32) {
+    const float l = w.lg[e];
+    uint8_t sl = 2;
+    if (l > in_thr) { sl = 1; ++n_in; }
+    else if (l < out_thr) sl = 0;
+    n_amb += (sl == 2);
+    w.sel[e] = sl;
+  }
+  __syncwarp();
+  n_in = warp_sum_i(n_in);
   if (n_in == a.k) {
     warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
   } else if (lane == 0) {
@@ -494,9 +548,9 @@ router_exact_kernel(RouterArgs a) {
     // stage 2 for every candidate, one warp per candidate
     const int nc = s_ncand;
     for (int ci = warp; ci < nc; ci += RT_WARPS) {
-      float res[MC], eb[MC];
-      warp_dot2_multi(x, static_cast<const T*>(a.wrT), cand + ci, 1, a.d, a.bias, a.g2, lane, res,
-                      eb);
+      float res[1], eb[1];
+      warp_dot2_multi<T, 1>(x, static_cast<const T*>(a.wrT), cand + ci, 1, a.d, a.bias, a.g2, lane,
+                            res, eb);
       if (lane == 0) { cres[ci] = res[0]; ceb[ci] = eb[0]; }
     }
     __syncthreads();
