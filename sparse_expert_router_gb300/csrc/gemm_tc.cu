@@ -30,11 +30,8 @@ namespace {
 #ifndef MOE_TC_BN
 #define MOE_TC_BN 256
 #endif
-#ifndef MOE_TC_STAGES_GLU
-#define MOE_TC_STAGES_GLU 3
-#endif
-#ifndef MOE_TC_STAGES
-#define MOE_TC_STAGES 4
+#ifndef MOE_TC_SMEM_BUDGET
+#define MOE_TC_SMEM_BUDGET (220 * 1024)   // dynamic shared memory per CTA, bytes
 #endif
 constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
@@ -50,14 +47,12 @@ constexpr int MAX_PROBS = 3;
 constexpr int MAX_GROUPS = 1024;
 constexpr int A_HALF = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 #ifndef MOE_TC_BBOX
 #define MOE_TC_BBOX 32
 #endif
 constexpr int B_BOX_ROWS = MOE_TC_BBOX;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;   // 4 KB
 constexpr unsigned long long TIMEOUT_NS = 5000000000ull;
-static_assert(MOE_TC_STAGES <= 8 && MOE_TC_STAGES_GLU <= 8, "at most 8 pipeline stages");
 static_assert(BN % B_BOX_ROWS == 0 && BN % 16 == 0 && BN <= 256, "token tile");
 static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
 
@@ -91,6 +86,9 @@ struct TcParams {
   int grouped;                 // index of the grouped problem (always the last) or -1
   int glu;                     // any problem uses two A tiles per stage (SwiGLU or dual)
   int stages;
+  int nacc;                    // accumulator buffers in tensor memory (1 or 2)
+  int acc2_off;                // column offset of the second accumulator of a two-A item
+  int b_bytes;                 // bytes of the token tile slot of a stage
   DeviceHeader* hdr;
 };
 
@@ -252,12 +250,12 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
     }
     int g = lo;
     int64_t within = local - ((int64_t)S.gitem[g] - S.gitem[0]);
-    int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
+    const int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
     it.wg = g;
     it.m0 = m_t * BM * (q.dual ? 2 : 1);
     it.m_w = it.m0;
-    it.row0 = S.glo[g] + (int64_t)n_t * BN;
-    it.nrows = (int)imin64(BN, (int64_t)S.ghi[g] - it.row0);
+    it.row0 = S.glo[g] + (int64_t)n_t * q.bn;
+    it.nrows = (int)imin64(q.bn, (int64_t)S.ghi[g] - it.row0);
   } else {
     int64_t n_tiles = cdiv(q.rows, q.bn);
     int n_t, m_t;
@@ -286,15 +284,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
   const bool glu = P.glu != 0;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int stage_bytes = (glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
+  const int stage_bytes = (glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
   auto sA1 = [&](int s) { return base + s * stage_bytes; };
   auto sA3 = [&](int s) { return base + s * stage_bytes + A_BYTES; };
   auto sB = [&](int s) { return base + s * stage_bytes + (glu ? 2 * A_BYTES : A_BYTES); };
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
-  // Accumulators in tensor memory: launches without a SwiGLU problem keep two (columns 0 and
-  // BN) so that the epilogue of one tile overlaps the main loop of the next; SwiGLU launches
-  // need both halves (gate and up projections) for one tile.
-  const int nacc = glu ? 1 : 2;
+  // Accumulators in tensor memory (512 columns): buffer b starts at column b*BN. A launch keeps
+  // two buffers, so that the epilogue of one tile overlaps the main loop of the next, unless a
+  // two-A item (SwiGLU gate+up or a dual 256-feature item) with more than 128 token columns needs
+  // both halves; two-A items of at most 128 token columns put their second accumulator at
+  // column +128 of their buffer.
+  const int nacc = P.nacc;
+  const uint32_t acc2 = (uint32_t)P.acc2_off;
   auto tmem_full = [&](int b) { return smem_u32(&bars[16 + b]); };
   auto tmem_empty = [&](int b) { return smem_u32(&bars[18 + b]); };
   Sched S;
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           int64_t hi = imin64(imax64(q.offsets[g + 1], lo), q.rows);
           S.glo[g] = (int32_t)lo;
           S.ghi[g] = (int32_t)hi;
-          sum += cdiv(hi - lo, BN) * q.m_tiles;
+          sum += cdiv(hi - lo, q.bn) * q.m_tiles;
         }
       }
       int64_t incl = sum;
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
         int g = lane * per + i;
         if (g < G) {
           S.gitem[g] = (int32_t)run;
-          run += cdiv((int64_t)S.ghi[g] - S.glo[g], BN) * q.m_tiles;
+          run += cdiv((int64_t)S.ghi[g] - S.glo[g], q.bn) * q.m_tiles;
         }
       }
       if (lane == 31) { S.gitem[G] = (int32_t)run; s_total = run; }
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
             const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
             mma_bf16(d_tmem, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
             if (sw)
-              mma_bf16(tmem_base + BN, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
+              mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
                        accumulate);
             accumulate = 1;
           }
@@ -569,13 +570,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
       const int f0 = it.m0 + sub * BM + quad * 32;       // first feature of this warp
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
-                                 (uint32_t)((buf + sub) * BN);
+                                 (uint32_t)(buf * BN) + (uint32_t)sub * acc2;
       const bool f32out = (q.epi == EPI_F32);
       const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
       for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
         float v[16], v3[16];
         tmem_ld16(lane_addr + c0, v);
-        if (q.epi == EPI_SWIGLU) tmem_ld16(lane_addr + BN + c0, v3);
+        if (q.epi == EPI_SWIGLU) tmem_ld16(lane_addr + acc2 + c0, v3);
         tmem_wait_ld();
         if (f32out) {
 #pragma unroll
@@ -739,8 +740,23 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     if (g.epi == EPI_SWIGLU || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
-  const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + B_BYTES;
-  P.stages = P.glu ? MOE_TC_STAGES_GLU : MOE_TC_STAGES;
+  int max_bn = 0, max_two_a_bn = 0;
+  for (int j = 0; j < n_probs; ++j) {
+    max_bn = max(max_bn, P.p[j].bn);
+    if (P.p[j].epi == EPI_SWIGLU || P.p[j].dual) max_two_a_bn = max(max_two_a_bn, P.p[j].bn);
+  }
+  P.nacc = (max_two_a_bn > 128) ? 1 : 2;
+  P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
+  P.b_bytes = max_bn * BK * 2;
+  const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
+  // as many stages as fit next to the epilogue tiles and the schedule (at most 8)
+  {
+    const size_t fixed = 1024 + (size_t)EPI_WARPS * EPI_STAGE_BYTES +
+                         (size_t)(3 * ((P.grouped >= 0) ? P.p[P.grouped].G : 0) + 1) * 4;
+    const size_t budget = (size_t)MOE_TC_SMEM_BUDGET;
+    int st = (int)((budget - fixed) / (size_t)stage_bytes);
+    P.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
+  }
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024 + (size_t)EPI_WARPS * EPI_STAGE_BYTES +
                       (size_t)(3 * G + 1) * 4;
