@@ -67,6 +67,12 @@ class LayerShape:
     zipf_s: float = 1.1
     seed: int = 0
     rms_eps: float = 1e-6
+    expert_dtype: str = "bf16"   # routed expert banks: "bf16", or "fp8" (E4M3 + per-column scales)
+    # fp8 experts: per-tensor quantization multipliers of the grouped rows and of the SwiGLU
+    # hidden (the delayed-scaling state). Powers of two that keep the largest expected values
+    # (|rows| <= ~7 after the RMSNorm, |hidden| <= ~30) below the E4M3 maximum of 448.
+    fp8_x_scale: float = 32.0
+    fp8_h_scale: float = 8.0
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -134,6 +140,11 @@ SHAPES: Dict[str, LayerShape] = {
                                   d_ff_shared=3072, dtype="bf16"),
 }
 
+# fp8 expert weights (E4M3 with a power-of-two scale per expert output column), everything
+# else as the bf16 shapes above.
+SHAPES["small_fp8"] = SHAPES["small_bf16"].with_(name="small_fp8", expert_dtype="fp8")
+SHAPES["l535b_t8192_fp8"] = SHAPES["l535b_t8192"].with_(name="l535b_t8192_fp8", expert_dtype="fp8")
+
 # One GPU of a 64-way expert-parallel domain: 6 local experts, 49,152 arriving
 # latent rows, receive pool sized with the receiver capacity factor 1.15 and
 # rounded up to a multiple of 128 rows.
@@ -176,6 +187,25 @@ def _stacked_normal(n: int, rows: int, cols: int, std: float, dtype, device, see
     return out
 
 
+FP8_MAX = 448.0   # largest finite E4M3 value
+
+
+def _stacked_fp8(n: int, rows: int, cols: int, std: float, device, seed: int, tensor: str):
+    """[n, rows, cols] E4M3 weights and [n, cols] fp32 scales: slice i is drawn like
+    _stacked_normal (fp32), each column is divided by the power of two that brings its largest
+    magnitude to at most 448, and rounded to E4M3 (nearest even). The layer's weight is the
+    E4M3 value times its column's scale."""
+    q = torch.empty((n, rows, cols), dtype=torch.float8_e4m3fn, device=device)
+    sc = torch.empty((n, cols), dtype=torch.float32, device=device)
+    for i in range(n):
+        w = _normal((rows, cols), std, torch.float32, device, tensor_seed(seed, tensor, i))
+        amax = w.abs().amax(dim=0).clamp_min(1e-30)
+        scale = torch.exp2(torch.ceil(torch.log2(amax / FP8_MAX)))
+        q[i].copy_((w / scale).to(torch.float8_e4m3fn))
+        sc[i].copy_(scale)
+    return q, sc
+
+
 def zipf_bias(shape: LayerShape, beta: float = ZIPF_BETA) -> torch.Tensor:
     """Router bias giving a Zipf(s) expert popularity: b[e] = -beta * s * ln(rank(e))."""
     g = torch.Generator(device="cpu")
@@ -189,7 +219,9 @@ def make_layer_inputs(shape: LayerShape, device="cpu", *, T: Optional[int] = Non
     """All inputs of one layer forward: activations x and every weight.
 
     Layouts (row-major): x [T, d]; w_router [d, E]; b_router [E] fp32;
-    w_down [d, L]; rms_gamma [L] fp32; w1, w3 [E, L, F]; w2 [E, F, L];
+    w_down [d, L]; rms_gamma [L] fp32; w1, w3 [E, L, F]; w2 [E, F, L] (with
+    expert_dtype "fp8": E4M3, plus w1_scale, w3_scale [E, F] and w2_scale [E, L] fp32, and the
+    activation quantization multipliers x_scale, h_scale [1] fp32);
     w1_s, w3_s [S, d, F_s]; w2_s [S, F_s, d]; w_up [L, d].
     Expert banks are stacked [experts, d_in, d_out] as the teardown's
     section "A sphere for every matrix" describes.
@@ -203,14 +235,21 @@ def make_layer_inputs(shape: LayerShape, device="cpu", *, T: Optional[int] = Non
         "w_router": _normal((d, E), d ** -0.5, dt, device, tensor_seed(s.seed, "w_router")),
         "w_down": _normal((d, L), d ** -0.5, dt, device, tensor_seed(s.seed, "w_down")),
         "rms_gamma": torch.ones(L, dtype=torch.float32, device=device),
-        "w1": _stacked_normal(E, L, F, L ** -0.5, dt, device, s.seed, "w1"),
-        "w3": _stacked_normal(E, L, F, L ** -0.5, dt, device, s.seed, "w3"),
-        "w2": _stacked_normal(E, F, L, F ** -0.5, dt, device, s.seed, "w2"),
         "w1_s": _stacked_normal(S, d, Fs, d ** -0.5, dt, device, s.seed, "w1_s"),
         "w3_s": _stacked_normal(S, d, Fs, d ** -0.5, dt, device, s.seed, "w3_s"),
         "w2_s": _stacked_normal(S, Fs, d, Fs ** -0.5, dt, device, s.seed, "w2_s"),
         "w_up": _normal((L, d), L ** -0.5, dt, device, tensor_seed(s.seed, "w_up")),
     }
+    if s.expert_dtype == "fp8":
+        out["x_scale"] = torch.tensor([s.fp8_x_scale], dtype=torch.float32, device=device)
+        out["h_scale"] = torch.tensor([s.fp8_h_scale], dtype=torch.float32, device=device)
+        out["w1"], out["w1_scale"] = _stacked_fp8(E, L, F, L ** -0.5, device, s.seed, "w1")
+        out["w3"], out["w3_scale"] = _stacked_fp8(E, L, F, L ** -0.5, device, s.seed, "w3")
+        out["w2"], out["w2_scale"] = _stacked_fp8(E, F, L, F ** -0.5, device, s.seed, "w2")
+    else:
+        out["w1"] = _stacked_normal(E, L, F, L ** -0.5, dt, device, s.seed, "w1")
+        out["w3"] = _stacked_normal(E, L, F, L ** -0.5, dt, device, s.seed, "w3")
+        out["w2"] = _stacked_normal(E, F, L, F ** -0.5, dt, device, s.seed, "w2")
     if s.routing == "zipf":
         out["b_router"] = zipf_bias(s, zipf_beta).to(device)
     else:

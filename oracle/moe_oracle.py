@@ -43,7 +43,10 @@ Readings taken where the pages are silent (each is listed in the design doc):
 
 All arithmetic is fp64 on exactly promoted inputs (bf16 and fp32 values are
 exact in fp64, and so is every product of two of them). Nothing is rounded
-to a lower precision anywhere in this module.
+to a lower precision anywhere in this module, except where the layer itself
+quantizes: the fp8 expert MLP (section "fp8 expert MLP" below) rounds its
+activations to E4M3, taking each rounding decision from the fp32 value the
+layer quantizes (readings R12-R14).
 """
 from __future__ import annotations
 
@@ -51,6 +54,7 @@ import math
 from fractions import Fraction
 from typing import Dict, List, Optional, Sequence, Tuple
 
+import numpy as np
 import torch
 
 F64 = torch.float64
@@ -60,6 +64,16 @@ U64 = 2.0 ** -53          # unit roundoff of fp64
 def to64(t: torch.Tensor) -> torch.Tensor:
     """Exact promotion of a stored bf16/fp32 tensor to fp64 on the CPU."""
     return t.detach().to(device="cpu").to(F64)
+
+
+def expert_weight(inp: Dict[str, torch.Tensor], name: str, e: int) -> torch.Tensor:
+    """Expert e's weight matrix in fp64: the stored values, times the per-output-column scale
+    when the bank is stored as E4M3 with a `<name>_scale` [E, d_out] tensor (exact in fp64)."""
+    w = to64(inp[name][e])
+    sc = inp.get(name + "_scale")
+    if sc is not None:
+        w = w * to64(sc[e]).unsqueeze(0)
+    return w
 
 
 # ---------------------------------------------------------------- router ----
@@ -253,25 +267,101 @@ def shared_hidden(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor) -> to
 
 
 def grouped_experts(rows: torch.Tensor, offsets: Sequence[int], w1: torch.Tensor,
-                    w3: torch.Tensor, w2: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+                    w3: torch.Tensor, w2: torch.Tensor,
+                    fp8: Optional[Dict[str, object]] = None
+                    ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Expert MLPs over expert-grouped rows: rows offsets[e]:offsets[e+1] go through expert e.
 
     Returns (hidden a [R, F], output o [R, L]) in fp64 for the active rows
     only; rows past offsets[-1] (pool padding) are never computed, matching
     the "mask-free" ragged expert MLP of the teardown's section
     "21% to 27% MFU without stopping the run".
+    With ``fp8`` (keys w1_scale, w3_scale, w2_scale, x_scale, h_scale) the rows are E4M3
+    codes and every expert runs fp8_expert; a is then the hidden before its quantization.
     """
     r64 = to64(rows)
     n_act = int(offsets[-1])
     F = w1.shape[2]
+    bank = {"w1": w1, "w3": w3, "w2": w2}
+    if fp8:
+        bank.update({k: v for k, v in fp8.items() if k.endswith("_scale")})
     a = torch.zeros((n_act, F), dtype=F64)
     o = torch.zeros((n_act, w2.shape[2]), dtype=F64)
     for e in range(len(offsets) - 1):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
-            a[lo:hi] = swiglu_hidden(r64[lo:hi], to64(w1[e]), to64(w3[e]))
-            o[lo:hi] = a[lo:hi] @ to64(w2[e])
+            W1, W3, W2 = (expert_weight(bank, n, e) for n in ("w1", "w3", "w2"))
+            if fp8:
+                o[lo:hi], a[lo:hi], _ = fp8_expert(r64[lo:hi], float(fp8["x_scale"]),
+                                                   float(fp8["h_scale"]), W1, W3, W2)
+            else:
+                a[lo:hi] = swiglu_hidden(r64[lo:hi], W1, W3)
+                o[lo:hi] = a[lo:hi] @ W2
     return a, o
+
+
+# ------------------------------------------------------------ fp8 expert MLP ----
+#
+# The July summary (section on the B200 training MFU epic, #6880 and #7079) describes an fp8
+# ragged dot for the expert MLP: E4M3 in the forward pass, with delayed scaling (the scale of a
+# tensor comes from the amax recorded at earlier steps). Readings taken here:
+#   R12 both operands of each expert GEMM are E4M3: the grouped rows x_perm, quantized with the
+#       per-tensor multiplier S_x, and the SwiGLU hidden a, quantized with S_h; the expert
+#       weights are E4M3 with one scale per output column (weight ~ code * scale);
+#   R13 quantization is q = e4m3(fp32(v * S)) (round to nearest even, saturating at 448) and
+#       dequantization multiplies by fp32(1 / S); S_x and S_h are inputs (the delayed-scaling
+#       state), and the layer reports this step's amax of each quantized tensor;
+#   R14 router, latent projection, shared experts, combine and up-projection stay 16-bit.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v: torch.Tensor) -> torch.Tensor:
+    """Nearest E4M3 value of each element (fp64 in, fp64 out), ties to the even code;
+    magnitudes above the largest finite value, 448, saturate to it.
+
+    E4M3 has a sign, 4 exponent bits (bias 7) and 3 fraction bits: normal values
+    1.f x 2^e for e in [-6, 8] (the all-ones code of e = 8 is NaN, so 1.75 x 2^8 = 448 is the
+    largest finite value) and subnormal values 0.f x 2^-6. Within [2^e, 2^(e+1)) consecutive
+    values are 2^(e-3) apart; below 2^-6 they are 2^-9 apart. Rounding to the nearest multiple
+    of that step, ties to the even multiple, is round-to-nearest-even on the code."""
+    v = to64(v)
+    a = v.abs()
+    _, ex = torch.frexp(a)                      # a = m * 2^ex with m in [0.5, 1)
+    e = torch.clamp(ex - 1, min=-6)             # binade of a; the subnormal range uses e = -6
+    step = torch.exp2((e - 3).to(F64))
+    r = torch.clamp(torch.round(a / step) * step, max=E4M3_MAX)   # torch.round: half to even
+    return torch.sign(v) * r
+
+
+def to_fp32(v: torch.Tensor) -> torch.Tensor:
+    """Round to the nearest fp32 value (as fp64)."""
+    return to64(v).to(torch.float32).to(F64)
+
+
+def quantize_e4m3(v: torch.Tensor, scale: float) -> torch.Tensor:
+    """E4M3 codes (as their values) of v under the quantization multiplier `scale` (R13):
+    e4m3(fp32(v * scale)). The product is rounded to fp32 first, the precision in which the
+    layer holds the activations it quantizes, so that both roundings decide as the layer does."""
+    return e4m3_round(to_fp32(to64(v) * float(scale)))
+
+
+def dequant_multiplier(scale: float) -> float:
+    """fp32(1 / scale), correctly rounded (numpy's fp32 division is IEEE)."""
+    return float(np.float32(1.0) / np.float32(scale))
+
+
+def fp8_expert(codes: torch.Tensor, x_scale: float, h_scale: float, w1: torch.Tensor,
+               w3: torch.Tensor, w2: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor,
+                                                          torch.Tensor]:
+    """One expert's fp8 forward on rows already quantized to E4M3 codes (R12, R13):
+    xq = codes * fp32(1/S_x); a = silu(xq W1) * (xq W3); aq = e4m3(fp32(a S_h)) * fp32(1/S_h);
+    o = aq W2, with W* the dequantized weights. Returns (o, a, the codes of a)."""
+    xq = to64(codes) * dequant_multiplier(x_scale)
+    a = swiglu_hidden(xq, w1, w3)
+    a_codes = quantize_e4m3(a, h_scale)
+    o = (a_codes * dequant_multiplier(h_scale)) @ w2
+    return o, a, a_codes
 
 
 def combine(y_perm: torch.Tensor, slot_of: torch.Tensor, gate: torch.Tensor) -> torch.Tensor:
@@ -328,10 +418,19 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
         for j in range(top_k):
             if int(slot[i, j]) >= 0:
                 by_expert.setdefault(int(idx[i, j]), []).append((i, j))
+    fp8 = "x_scale" in inp
+    amax_x = amax_h = 0.0
     for e in sorted(by_expert):
         pairs = by_expert[e]
         rows = torch.stack([h[i] for i, _ in pairs])
-        out_e = swiglu_mlp(rows, to64(w1[e]), to64(w3[e]), to64(w2[e]))
+        W1, W3, W2 = (expert_weight(inp, n, e) for n in ("w1", "w3", "w2"))
+        if fp8:
+            sx, sh = float(inp["x_scale"].reshape(-1)[0]), float(inp["h_scale"].reshape(-1)[0])
+            out_e, a_e, _ = fp8_expert(quantize_e4m3(rows, sx), sx, sh, W1, W3, W2)
+            amax_x = max(amax_x, float(rows.abs().max()))
+            amax_h = max(amax_h, float(a_e.abs().max()))
+        else:
+            out_e = swiglu_mlp(rows, W1, W3, W2)
         for n, (i, j) in enumerate(pairs):
             o[i, j] = out_e[n]
     c = torch.zeros((len(toks), L), dtype=F64)
@@ -345,6 +444,9 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
     out.update(dsp)
     out.update({"tokens": torch.tensor(toks, dtype=torch.int64), "z": z, "h": h, "o": o,
                 "c": c, "a_s": a_s, "y": y, "capacity": torch.tensor(-1 if cap is None else cap)})
+    if fp8:   # amax of the tensors the layer quantized, over the computed tokens' kept rows
+        out.update({"x_amax": torch.tensor(amax_x, dtype=F64),
+                    "h_amax": torch.tensor(amax_h, dtype=F64)})
     return out
 
 
@@ -373,6 +475,7 @@ def slice_rows(inp: Dict[str, torch.Tensor], positions: Sequence[int]) -> Dict[s
     o = torch.zeros((len(pos), L), dtype=F64)
     for e, ns in groups.items():
         v = to64(inp["pool"][[rows[n] for n in ns]])
-        o[ns] = swiglu_mlp(v, to64(inp["w1"][e]), to64(inp["w3"][e]), to64(inp["w2"][e]))
+        o[ns] = swiglu_mlp(v, expert_weight(inp, "w1", e), expert_weight(inp, "w3", e),
+                           expert_weight(inp, "w2", e))
     g = to64(inp["gate"][pos]).unsqueeze(1)
     return {"rows": torch.tensor(rows), "y_perm": o, "out": g * o}

@@ -278,7 +278,113 @@ def pin_forward_drop_skips_expert():
         assert torch.allclose(diff, exp, atol=1e-12, rtol=0), t
 
 
-ALL_PINS = [pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
+def pin_fp8_expert_golden():
+    """fp8 expert MLP (E4M3 weights with column scales, E4M3 rows and hidden under per-tensor
+    multipliers), hand-derived from the E4M3 value grid."""
+    gd = _load("fp8_expert_scales.json")
+    lay = {kk: torch.tensor(gd[kk], dtype=torch.float32) for kk in
+           ("x", "w_router", "b_router", "w_down", "rms_gamma", "w1_s", "w3_s", "w2_s", "w_up")}
+    for n in ("w1", "w3", "w2"):
+        lay[n] = torch.tensor(gd[n + "_fp8"], dtype=torch.float32).to(torch.float8_e4m3fn)
+        lay[n + "_scale"] = torch.tensor(gd[n + "_scale"], dtype=torch.float32)
+    lay["x_scale"] = torch.tensor([gd["x_scale"]], dtype=torch.float32)
+    lay["h_scale"] = torch.tensor([gd["h_scale"]], dtype=torch.float32)
+    out = O.forward(lay, top_k=gd["top_k"], rms_eps=gd["rms_eps"])
+    assert torch.equal(out["y"], torch.tensor(gd["expected_y"], dtype=F64)), out["y"]
+    env = {"sig": lambda v: 1.0 / (1.0 + math.exp(-v)), "sqrt": math.sqrt}
+    for key in ("x_amax", "h_amax"):
+        want = eval(gd["expected_" + key], {"__builtins__": {}}, env)
+        assert abs(float(out[key]) - want) <= 1e-15 * want, (key, float(out[key]), want)
+
+
+def _e4m3_table():
+    """Every finite E4M3 value with its code, decoded by torch's float8_e4m3fn type."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(F64)
+    fin = ~torch.isnan(vals)
+    return codes[fin].long(), vals[fin]
+
+
+def _nearest_even_bruteforce(v: torch.Tensor) -> torch.Tensor:
+    """Nearest finite E4M3 value by search over the whole decoded table; at equal distance the
+    value whose code is even; beyond 448 the largest magnitude of the sign (saturation)."""
+    codes, vals = _e4m3_table()
+    out = torch.empty_like(v)
+    for i, x in enumerate(v.tolist()):
+        if abs(x) >= 448.0:
+            out[i] = math.copysign(448.0, x)
+            continue
+        d = (vals - x).abs()
+        best = d.min()
+        cand = (d == best).nonzero().flatten()
+        if len(cand) > 1:
+            even = [c for c in cand.tolist() if int(codes[c]) % 2 == 0]
+            cand = torch.tensor(even or cand.tolist())
+        out[i] = vals[int(cand[0])]
+    return out
+
+
+def pin_e4m3_rounding():
+    """E4M3 rounding against a brute-force search of the value table, and against torch's own
+    float8 conversion of fp32 values in range: exact ties, both sides of every tie, every value,
+    subnormals and saturation."""
+    _, vals = _e4m3_table()
+    pos = torch.unique(vals[vals > 0])
+    mids = (pos[1:] + pos[:-1]) / 2                               # exact ties
+    g = torch.Generator().manual_seed(11)
+    rnd = torch.randn(400, generator=g, dtype=F64) * torch.exp2(
+        torch.randint(-12, 9, (400,), generator=g).to(F64))
+    probe = torch.cat([pos, mids, mids * (1 + 2.0 ** -30), mids * (1 - 2.0 ** -30), rnd,
+                       torch.tensor([0.0, 2.0 ** -10, 3 * 2.0 ** -11, 449.0, 464.0, 479.9,
+                                     480.0, 1e6])])
+    probe = torch.cat([probe, -probe])
+    got = O.e4m3_round(probe)
+    assert torch.equal(got, _nearest_even_bruteforce(probe))
+    # torch converts through fp32 (then to nearest even): compare on fp32 values
+    p32 = O.to_fp32(probe[probe.abs() <= 448.0])
+    lib = p32.to(torch.float32).to(torch.float8_e4m3fn).to(F64)
+    assert torch.equal(O.e4m3_round(p32), lib)
+    assert float(O.e4m3_round(torch.tensor([464.0]))) == 448.0
+    assert float(O.e4m3_round(torch.tensor([1.0625]))) == 1.0      # tie to even code
+    assert float(O.e4m3_round(torch.tensor([1.1875]))) == 1.25     # tie to even code
+
+
+def pin_fp8_quantize_in_fp32():
+    """The rounding decision is taken on the fp32 product: 1.0625 + 2^-40 is an E4M3 tie once
+    rounded to fp32 (to even: 1.0), though nearer to 1.125 in exact arithmetic."""
+    v = torch.tensor([1.0625 + 2.0 ** -40], dtype=F64)
+    assert float(O.quantize_e4m3(v, 1.0)) == 1.0
+    assert float(O.quantize_e4m3(v * 2, 0.5)) == 1.0
+    assert O.dequant_multiplier(3.0) == float(torch.tensor(1 / 3, dtype=torch.float32))
+
+
+def pin_fp8_layer_grid():
+    """On a small random fp8 layer every quantized row and hidden value the oracle produces is
+    the brute-force nearest E4M3 value of its fp32-rounded scaled input."""
+    from moe_workloads import SHAPES, make_layer_inputs
+    s = SHAPES["small_fp8"].with_(T=24, d_model=64, n_experts=8, d_latent=32, d_ff=32,
+                                  n_shared=1, d_ff_shared=32)
+    inp = make_layer_inputs(s, "cpu")
+    out = O.forward(inp, top_k=s.top_k, rms_eps=s.rms_eps)
+    sx, sh = float(inp["x_scale"][0]), float(inp["h_scale"][0])
+    e = int(out["idx"][0, 0])
+    rows = out["h"][(out["idx"] == e).any(1)]
+    codes = O.quantize_e4m3(rows, sx)
+    flat = O.to_fp32(rows * sx).flatten()
+    assert torch.equal(codes.flatten(), _nearest_even_bruteforce(flat))
+    W = [O.expert_weight(inp, n, e) for n in ("w1", "w3", "w2")]
+    o, a, a_codes = O.fp8_expert(codes, sx, sh, *W)
+    assert torch.equal(a_codes.flatten(), _nearest_even_bruteforce(O.to_fp32(a * sh).flatten()))
+    assert float((codes * O.dequant_multiplier(sx) - rows).abs().max()) <= \
+        float(rows.abs().max()) * 2.0 ** -4 + 2.0 ** -10 / sx
+    # the layer's own output for those tokens uses the same quantized rows
+    toks = (out["idx"] == e).any(1).nonzero().flatten()
+    j = (out["idx"][toks] == e).long().argmax(1)
+    assert torch.allclose(out["o"][toks, j], o, rtol=1e-12, atol=1e-12)
+
+
+ALL_PINS = [pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
+            pin_fp8_layer_grid, pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
             pin_capacity, pin_dispatch_golden, pin_dispatch_invariants, pin_forced_single_expert,
             pin_identical_experts, pin_two_token_golden, pin_rmsnorm,
             pin_combine_drop_not_renormalised, pin_slice_rowwise]
@@ -346,6 +452,32 @@ def _mut_forward_renorm(monkeypatch):
     monkeypatch.setattr(O, "softmax_gates", bad)
 
 
+def _mut_fp8_scale_ignored(monkeypatch):
+    monkeypatch.setattr(O, "expert_weight", lambda inp, name, e: O.to64(inp[name][e]))
+
+
+def _mut_e4m3_ties_away(monkeypatch):
+    def bad(v):
+        v = O.to64(v)
+        a = v.abs()
+        _, ex = torch.frexp(a)
+        step = torch.exp2((torch.clamp(ex - 1, min=-6) - 3).to(F64))
+        return torch.sign(v) * torch.clamp(torch.floor(a / step + 0.5) * step, max=448.0)
+    monkeypatch.setattr(O, "e4m3_round", bad)
+
+
+def _mut_fp8_no_activation_rounding(monkeypatch):
+    monkeypatch.setattr(O, "quantize_e4m3", lambda v, scale: O.to64(v) * float(scale))
+
+
+def _mut_fp8_dequant_by_scale(monkeypatch):
+    monkeypatch.setattr(O, "dequant_multiplier", lambda scale: float(scale))
+
+
+def _mut_fp8_quantize_in_fp64(monkeypatch):
+    monkeypatch.setattr(O, "quantize_e4m3", lambda v, scale: O.e4m3_round(O.to64(v) * float(scale)))
+
+
 def _mut_unstable_perm(monkeypatch):
     orig = O.dispatch
 
@@ -371,7 +503,9 @@ def _mut_transposed_up(monkeypatch):
 
 
 MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mut_no_shared,
-             _mut_rms_sum, _mut_full_softmax, _mut_renorm_after_drop, _mut_forward_renorm, _mut_unstable_perm,
+             _mut_rms_sum, _mut_full_softmax, _mut_renorm_after_drop, _mut_forward_renorm, _mut_fp8_scale_ignored, _mut_e4m3_ties_away,
+             _mut_fp8_no_activation_rounding, _mut_fp8_dequant_by_scale,
+             _mut_fp8_quantize_in_fp64, _mut_unstable_perm,
              _mut_transposed_up]
 
 

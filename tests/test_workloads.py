@@ -43,3 +43,17 @@ def test_slice_inputs():
     assert sorted(d["slot_of"].tolist()) == list(range(1000))
     assert float(d["gate"].min()) > 0.0 and float(d["gate"].max()) <= 1.0
     assert d["pool"][1000:].abs().sum() == 0
+
+
+def test_fp8_expert_weights():
+    s = SHAPES["small_fp8"].with_(T=32, n_experts=8, d_latent=64, d_ff=32)
+    a = make_layer_inputs(s)
+    assert a["w1"].dtype == torch.float8_e4m3fn and a["w1_scale"].shape == (8, 32)
+    assert a["w2_scale"].shape == (8, 64)
+    sc = a["w1_scale"]
+    assert torch.equal(torch.exp2(torch.log2(sc).round()), sc)          # powers of two
+    deq = a["w1"].float() * sc.unsqueeze(1)
+    assert float(deq.abs().amax(dim=1).div(sc).max()) <= 448.0
+    # the dequantized weights stay close to the bf16 draw of the same generator
+    ref = make_layer_inputs(s.with_(expert_dtype="bf16"))["w1"].float()
+    assert float((deq - ref).norm() / ref.norm()) < 0.05
