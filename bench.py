@@ -82,10 +82,16 @@ def max_over_ranks(x: float, device) -> float:
 
 
 def algorithmic(shape, counts):
-    """Algorithmic flops and bytes per stage of one forward (bf16 storage)."""
+    """Algorithmic flops and bytes per stage of one forward: bf16 storage, except that an
+    fp8-expert layer keeps its expert banks (plus one fp32 scale per output column), grouped
+    rows and hidden in E4M3 (one byte). "tc_peak" names the tensor-core rate a stage runs at."""
     T, d, L, E, k = shape.T, shape.d_model, shape.d_latent, shape.n_experts, shape.top_k
     F, SF = shape.d_ff, shape.n_shared * shape.d_ff_shared
     es = 2
+    fp8 = getattr(shape, "expert_dtype", "bf16") == "fp8"
+    wb = 1 if fp8 else es                              # bytes per expert-bank weight
+    ab = 1 if fp8 else es                              # bytes per grouped-row / hidden value
+    xp = "fp8" if fp8 else "bf16"
     R = int(min(sum(counts), T * k))
     active = sum(1 for c in counts if c > 0)
     fl = shape.flops()
@@ -96,15 +102,32 @@ def algorithmic(shape, counts):
                        "bytes": es * (T * d + d * E + d * L + 2 * d * SF) + 4 * T * E + 4 * T * L
                        + es * T * SF},
         "router_select": {"flops": 0.0, "bytes": 4 * T * E + es * T * d + 8 * T * k},
-        "dispatch": {"flops": 0.0, "bytes": es * T * L + es * R * L + 4 * (3 * T * k + R)},
-        "expert_gemm1": {"flops": fl["expert_up"],
-                         "bytes": es * (2 * active * L * F + R * L + R * F)},
-        "expert_gemm2": {"flops": fl["expert_down"],
-                         "bytes": es * (active * F * L + R * F + R * L)},
+        "dispatch": {"flops": 0.0, "bytes": 4 * T * L + ab * R * L + 4 * (3 * T * k + R)},
+        "expert_gemm1": {"flops": fl["expert_up"], "tc_peak": xp,
+                         "bytes": wb * 2 * active * L * F + ab * (R * L + R * F)
+                         + (8 * active * F if fp8 else 0)},
+        "expert_gemm2": {"flops": fl["expert_down"], "tc_peak": xp,
+                         "bytes": wb * active * F * L + ab * R * F + es * R * L
+                         + (4 * active * L if fp8 else 0)},
         "combine": {"flops": 0.0, "bytes": es * (R * L + T * L) + 8 * T * k},
         "back_gemm": {"flops": fl["back"],
                       "bytes": es * (T * L + T * SF + L * d + SF * d + T * d)},
     }
+
+
+def weight_bytes(shape) -> int:
+    """Bytes of every weight of the layer as stored."""
+    d, L, E, F = shape.d_model, shape.d_latent, shape.n_experts, shape.d_ff
+    SF = shape.n_shared * shape.d_ff_shared
+    bank = 3 * E * L * F * (1 if shape.expert_dtype == "fp8" else 2)
+    scales = 4 * E * (2 * F + L) if shape.expert_dtype == "fp8" else 0
+    return bank + scales + 2 * (d * E + 2 * d * L + 3 * d * SF) + 4 * (E + L)
+
+
+def tc_peak(pk, stage) -> float:
+    """Tensor-core peak (TFLOP/s) of a stage: the measured sustained bf16 rate, doubled for E4M3
+    operands (the nominal dense ratio 4.5 / 2.25 PFLOP/s)."""
+    return pk["bf16_sustained"] * (2.0 if stage.get("tc_peak") == "fp8" else 1.0)
 
 
 class ClockSampler:
@@ -341,28 +364,33 @@ def main():
             st["gb_s"] = round(by / (ms * 1e-3) / 1e9, 1)
             st["hbm_frac"] = round(st["gb_s"] / pk["hbm_gbs"], 3)
             if f:
+                tp = tc_peak(pk, alg[s])
                 st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 1)
-                st["bf16_frac"] = round(st["tflop_s"] / pk["bf16_sustained"], 3)
+                st[alg[s].get("tc_peak", "bf16") + "_frac"] = round(st["tflop_s"] / tp, 3)
         stages[s] = st
     dom = max((s for s in STAGES if s in alg), key=lambda s: stage_ms[s])
     f, by = alg[dom]["flops"], alg[dom]["bytes"]
     ms_dom = stage_ms[dom] / args.steps
-    t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), f / (pk["bf16_sustained"] * 1e12)
+    tp = tc_peak(pk, alg[dom])
+    t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), f / (tp * 1e12)
     if t_hbm >= t_tc:
         ach = by / (ms_dom * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4)}
     else:
         ach = f / (ms_dom * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4)}
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(tp, 1),
+                "unit": "TFLOP/s", "frac": round(ach / tp, 4)}
     roof.update({"kernel": dom, "traffic": profiled_traffic(shape.name, dom),
                  "peak_source": pk["source"]
-                 + (" (bf16 sustained)" if roof["bound"] == "tensor" else " (HBM copy)")})
+                 + ((" (bf16 sustained" + (" x 2, the nominal E4M3/bf16 ratio)"
+                                           if alg[dom].get("tc_peak") == "fp8" else ")"))
+                    if roof["bound"] == "tensor" else " (HBM copy)")})
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.expert_dtype == "bf16" else "bf16; expert MLP e4m3 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, near-uniform "
                 "routing unless the workload is Zipf-skewed)",
         "config": {"workload": f"{shape.name}: T={shape.T} d={shape.d_model} "
@@ -370,7 +398,9 @@ def main():
                                f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gemm_path": "simt" if args.simt else "tcgen05", "pdl": not args.no_pdl,
-                   "l2": "flushed between timed steps (256 MB write); weights (21.7 GB) exceed L2"},
+                   "expert_weights": shape.expert_dtype,
+                   "l2": "flushed between timed steps (256 MB write); weights "
+                         f"({weight_bytes(shape) / 1e9:.1f} GB) exceed L2"},
         "layer_tflop_s": round(sum(shape.flops().values()) / (ms_step * 1e-3) / 1e12, 1),
         "stages": stages,
         "roofline": roof,

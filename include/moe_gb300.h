@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -76,6 +76,31 @@ typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype_t;
 /* cfg->flags */
 #define MOE_FLAG_PDL  (1u << 0)  /* launch dependent kernels with programmatic dependent launch */
 #define MOE_FLAG_SIMT (1u << 1)  /* bf16: run every GEMM on CUDA cores (fp32 FMA) instead of tcgen05 */
+/* bf16 layers on the tensor-core path: the routed expert MLP runs as fp8 ragged dots (the Marin
+ * summary of the week of 2026-07-06, B200 training MFU epic, #6880 / #7079: E4M3 in the forward
+ * pass, delayed scaling). Both operands of both expert GEMMs are FP8 E4M3 (OCP: 1 sign, 4
+ * exponent bits with bias 7, 3 fraction bits, largest finite 448): the banks w1, w3, w2 with
+ * one fp32 scale per expert output column, the grouped rows x_perm and the SwiGLU hidden with
+ * one fp32 quantization multiplier each (moe_fp8_t). Router, latent projection, shared experts,
+ * combine and up-projection stay bf16. Requires d_latent and d_ff to be multiples of 128. */
+#define MOE_FLAG_FP8_EXPERTS (1u << 2)
+
+/* Operands and state of the fp8 expert MLP (MOE_FLAG_FP8_EXPERTS). All pointers are device
+ * memory owned by the caller.
+ * A tensor v is quantized with its multiplier S to codes q = e4m3(fp32(v * S)), round to nearest
+ * even, magnitudes beyond 448 saturated; it is dequantized as q * fp32(1 / S). x_scale and
+ * h_scale are the delayed-scaling state (set from the amax of earlier steps by the caller);
+ * x_amax and h_amax receive this call's max |v| of the tensors quantized (before
+ * quantization), for the caller's next scales. */
+typedef struct {
+  const float* w1_scale;  /* [E, F] expert weight = E4M3 value * its column's scale */
+  const float* w3_scale;  /* [E, F] */
+  const float* w2_scale;  /* [E, L] */
+  const float* x_scale;   /* [1] S_x: multiplier of the grouped rows h (x_perm) */
+  const float* h_scale;   /* [1] S_h: multiplier of the hidden silu(x W1) * (x W3) */
+  float*       x_amax;    /* [1] or NULL: max |h| over the rows written to x_perm */
+  float*       h_amax;    /* [1] or NULL: max |hidden| over the active rows */
+} moe_fp8_t;
 
 /* Limits: 1 <= top_k <= 32, top_k <= n_experts <= 1024, T * top_k < 2^31. */
 
@@ -120,6 +145,7 @@ typedef struct {
   const void*  w3_s;       /* [S, d, F_s] */
   const void*  w2_s;       /* [S, F_s, d] */
   const void*  w_up;       /* [L, d] */
+  const moe_fp8_t* fp8;    /* MOE_FLAG_FP8_EXPERTS: required (w1, w3, w2 are E4M3); else ignored */
 } moe_weights_t;
 
 /* Optional extras of moe_forward; every pointer may be NULL. Device buffers receive copies of
@@ -149,6 +175,10 @@ typedef struct {
 MOE_API int32_t     moe_abi_version(void);
 MOE_API const char* moe_status_string(moe_status_t status);
 
+/* The cudaError_t behind the calling thread's most recent MOE_ERR_CUDA (cudaSuccess if none), and
+ * its name in *name (static storage) when name is not NULL. */
+MOE_API int32_t moe_last_cuda_error(const char** name);
+
 /* Bytes of workspace every call below needs for this configuration (one size fits all calls).
  * The workspace must be 256-byte aligned device memory owned by the caller. */
 MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
@@ -171,12 +201,14 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const voi
  * as the ragged transport delivers them), -1 if dropped; perm [T*k] = t*k + j at each used
  * row (entries past expert_offsets[E] are left untouched); n_dropped [1];
  * x_perm [pool_rows, L] receives h at every used row. topk_idx must hold ascending, distinct
- * expert ids (as moe_route writes them). */
+ * expert ids (as moe_route writes them). Under MOE_FLAG_FP8_EXPERTS x_perm receives the E4M3
+ * codes of h (one byte each) under fp8->x_scale, and fp8->x_amax (if not NULL) max |h| over the
+ * rows written; fp8 is ignored (may be NULL) otherwise. */
 MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
                          const float* rms_gamma, const int32_t* topk_idx,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
                          int32_t* slot_of, int32_t* n_dropped, void* x_perm,
-                         void* ws, size_t ws_bytes, void* stream);
+                         const moe_fp8_t* fp8, void* ws, size_t ws_bytes, void* stream);
 
 /* Experts: for every expert e and every row r in [expert_offsets[e], expert_offsets[e+1]):
  * y_perm[r] = (silu(x_perm[r] W1_e) * (x_perm[r] W3_e)) W2_e. Rows past expert_offsets[E]
@@ -184,13 +216,17 @@ MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const v
  * The grouped GEMM reads expert_offsets only after the kernel that wrote them has completed
  * (the hang of the weekly summary of 2026-09-14, hero-run epic, came from warps that read
  * the group boundaries early under programmatic dependent launch).
+ * Under MOE_FLAG_FP8_EXPERTS, x_perm and w1/w3/w2 are E4M3 codes (x_perm as moe_permute
+ * writes it), fp8 supplies their scales, the hidden is quantized with fp8->h_scale before the
+ * second GEMM, fp8->h_amax (if not NULL) receives max |hidden|; y_perm is bf16 either way.
+ * fp8 is ignored (may be NULL) without the flag.
  * When x is not NULL, also the shared experts' hidden activations
  * a_shared [T, S*F_s] = concat_s silu(x W1_s[s]) * (x W3_s[s]). */
 MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
-                            const int32_t* expert_offsets, const void* w1, const void* w3,
-                            const void* w2, void* y_perm, const void* x, const void* w1_s,
-                            const void* w3_s, void* a_shared, void* ws, size_t ws_bytes,
-                            void* stream);
+                                    const int32_t* expert_offsets, const void* w1, const void* w3,
+                                    const void* w2, const moe_fp8_t* fp8, void* y_perm,
+                                    const void* x, const void* w1_s, const void* w3_s,
+                                    void* a_shared, void* ws, size_t ws_bytes, void* stream);
 
 /* Combine: c[t] = sum over j with slot_of[t, j] >= 0, in order j = 0..k-1, of
  * topk_gate[t, j] * y_perm[slot_of[t, j]] (fp32 accumulation). When w_up is NULL, out [T, L]

@@ -144,6 +144,8 @@ SHAPES: Dict[str, LayerShape] = {
 # else as the bf16 shapes above.
 SHAPES["small_fp8"] = SHAPES["small_bf16"].with_(name="small_fp8", expert_dtype="fp8")
 SHAPES["l535b_t8192_fp8"] = SHAPES["l535b_t8192"].with_(name="l535b_t8192_fp8", expert_dtype="fp8")
+SHAPES["l535b_e64_t1368_fp8"] = SHAPES["l535b_e64_t1368"].with_(name="l535b_e64_t1368_fp8",
+                                                                expert_dtype="fp8")
 
 # One GPU of a 64-way expert-parallel domain: 6 local experts, 49,152 arriving
 # latent rows, receive pool sized with the receiver capacity factor 1.15 and

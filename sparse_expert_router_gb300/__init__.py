@@ -14,24 +14,32 @@ from typing import Dict, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_PDL, MOE_FLAG_SIMT, MOE_FORWARD_STAGES,
-                   moe_config_t, moe_device_report_t, moe_forward_aux_t, moe_weights_t)
+from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_FP8_EXPERTS, MOE_FLAG_PDL, MOE_FLAG_SIMT,
+                   MOE_FORWARD_STAGES,
+                   moe_config_t, moe_device_report_t, moe_forward_aux_t, moe_fp8_t, moe_weights_t)
 
 __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
            "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
            "moe_selftest_device_timeout",
-           "MOE_FLAG_PDL", "MOE_FLAG_SIMT",
-           "MOE_FORWARD_STAGES", "WEIGHT_NAMES"]
+           "MOE_FLAG_PDL", "MOE_FLAG_SIMT", "MOE_FLAG_FP8_EXPERTS",
+           "MOE_FORWARD_STAGES", "WEIGHT_NAMES", "FP8_NAMES"]
 
 WEIGHT_NAMES = ("w_router", "b_router", "w_down", "rms_gamma", "w1", "w3", "w2", "w1_s", "w3_s",
                 "w2_s", "w_up")
+# moe_fp8_t: weight column scales, activation multipliers (inputs) and amax (outputs)
+FP8_NAMES = ("w1_scale", "w3_scale", "w2_scale", "x_scale", "h_scale", "x_amax", "h_amax")
 
 
 class MoEError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} returned {_lib.STATUS_NAMES.get(status, status)}")
+        msg = f"{fn} returned {_lib.STATUS_NAMES.get(status, status)}"
+        if status == 5:   # MOE_ERR_CUDA: name the CUDA error behind it
+            name = C.c_char_p()
+            code = load().moe_last_cuda_error(C.byref(name))
+            msg += f" ({name.value.decode() if name.value else '?'}, {code})"
+        super().__init__(msg)
 
 
 @dataclass
@@ -52,6 +60,8 @@ class LayerConfig:
 
     @classmethod
     def from_shape(cls, shape, **kw) -> "LayerConfig":
+        if getattr(shape, "expert_dtype", "bf16") == "fp8":
+            kw["flags"] = kw.get("flags", 0) | MOE_FLAG_FP8_EXPERTS
         return cls(T=shape.T, d_model=shape.d_model, d_latent=shape.d_latent,
                    n_experts=shape.n_experts, top_k=shape.top_k, d_ff=shape.d_ff,
                    n_shared=shape.n_shared, d_ff_shared=shape.d_ff_shared, dtype=shape.dtype,
@@ -81,6 +91,14 @@ def _stream(stream) -> C.c_void_p:
     return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _fp8(fp8: Optional[Dict[str, torch.Tensor]]):
+    """A moe_fp8_t from a dict of device tensors named as its fields (missing ones NULL)."""
+    if fp8 is None:
+        return None
+    return C.pointer(moe_fp8_t(**{n: (fp8[n].data_ptr() if fp8.get(n) is not None else None)
+                                  for n in FP8_NAMES}))
+
+
 def _check(fn: str, status: int):
     if status != 0:
         raise MoEError(fn, status)
@@ -105,18 +123,21 @@ def moe_route(cfg, x, w_router, b_router, topk_idx, topk_gate, ws, stream=None):
 
 
 def moe_permute(cfg, x, w_down, rms_gamma, topk_idx, expert_counts, expert_offsets, perm,
-                slot_of, n_dropped, x_perm, ws, stream=None):
+                slot_of, n_dropped, x_perm, ws, stream=None, fp8=None):
+    """``fp8``: dict of moe_fp8_t fields (x_scale, optional x_amax) for an fp8-expert layer."""
     _check("moe_permute", load().moe_permute(
         C.byref(cfg.c()), _p(x), _p(w_down), _p(rms_gamma), _p(topk_idx), _p(expert_counts),
-        _p(expert_offsets), _p(perm), _p(slot_of), _p(n_dropped), _p(x_perm), _p(ws),
+        _p(expert_offsets), _p(perm), _p(slot_of), _p(n_dropped), _p(x_perm), _fp8(fp8), _p(ws),
         ws.numel(), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, x_perm, expert_offsets, w1, w3, w2, y_perm, x=None, w1_s=None,
-                   w3_s=None, a_shared=None, ws=None, stream=None):
+                   w3_s=None, a_shared=None, ws=None, stream=None, fp8=None):
+    """``fp8``: dict of moe_fp8_t fields for an fp8-expert layer (scales, optional h_amax)."""
     _check("moe_expert_ffn", load().moe_expert_ffn(
-        C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _p(y_perm),
-        _p(x), _p(w1_s), _p(w3_s), _p(a_shared), _p(ws), ws.numel(), _stream(stream)))
+        C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _fp8(fp8),
+        _p(y_perm), _p(x), _p(w1_s), _p(w3_s), _p(a_shared), _p(ws), ws.numel(),
+        _stream(stream)))
 
 
 def moe_combine(cfg, y_perm, slot_of, topk_gate, out, ws, a_shared=None, w_up=None, w2_s=None,
@@ -130,9 +151,16 @@ def moe_forward(cfg, weights: Dict[str, torch.Tensor], x, y, ws, stream=None,
                 aux: Optional[Dict[str, object]] = None):
     """y = layer(x). ``aux`` may map topk_idx / topk_gate / expert_counts / expert_offsets /
     slot_of / n_dropped to device tensors, and stage_events to MOE_FORWARD_STAGES + 1
-    torch.cuda.Event objects (created with enable_timing=True)."""
+    torch.cuda.Event objects (created with enable_timing=True). For an fp8-expert layer
+    ``weights`` also holds w1_scale, w3_scale, w2_scale, x_scale and h_scale, and ``aux`` may
+    map x_amax / h_amax to [1] fp32 device tensors."""
     w = moe_weights_t(**{n: (weights[n].data_ptr() if weights.get(n) is not None else None)
                          for n in WEIGHT_NAMES})
+    if cfg.flags & MOE_FLAG_FP8_EXPERTS:
+        f8 = {n: weights.get(n) for n in FP8_NAMES[:5]}
+        f8.update({n: (aux or {}).get(n) for n in FP8_NAMES[5:]})
+        fp8_ref = _fp8(f8)
+        w.fp8 = fp8_ref
     a = None
     keep = None
     if aux:

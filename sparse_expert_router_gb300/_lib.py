@@ -20,6 +20,7 @@ MOE_BF16 = 0
 MOE_F32 = 1
 MOE_FLAG_PDL = 1 << 0
 MOE_FLAG_SIMT = 1 << 1
+MOE_FLAG_FP8_EXPERTS = 1 << 2
 MOE_FORWARD_STAGES = 8
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -36,9 +37,15 @@ class moe_config_t(C.Structure):
                 ("pool_rows", C.c_int64)]
 
 
+class moe_fp8_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("w1_scale", "w3_scale", "w2_scale", "x_scale",
+                                          "h_scale", "x_amax", "h_amax")]
+
+
 class moe_weights_t(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("w_router", "b_router", "w_down", "rms_gamma", "w1", "w3",
-                                          "w2", "w1_s", "w3_s", "w2_s", "w_up")]
+                                          "w2", "w1_s", "w3_s", "w2_s", "w_up")] + \
+               [("fp8", C.POINTER(moe_fp8_t))]
 
 
 class moe_forward_aux_t(C.Structure):
@@ -59,10 +66,13 @@ CFG = C.POINTER(moe_config_t)
 SIGNATURES = {
     "moe_abi_version": (C.c_int32, []),
     "moe_status_string": (C.c_char_p, [C.c_int]),
+    "moe_last_cuda_error": (C.c_int32, [C.POINTER(C.c_char_p)]),
     "moe_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
     "moe_route": (C.c_int, [CFG, P, P, P, P, P, P, C.c_size_t, P]),
-    "moe_permute": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
-    "moe_expert_ffn": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
+    "moe_permute": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, C.POINTER(moe_fp8_t), P,
+                              C.c_size_t, P]),
+    "moe_expert_ffn": (C.c_int, [CFG, P, P, P, P, P, C.POINTER(moe_fp8_t), P, P, P, P, P, P,
+                                 C.c_size_t, P]),
     "moe_combine": (C.c_int, [CFG, P, P, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_forward": (C.c_int, [CFG, C.POINTER(moe_weights_t), P, P, P, C.c_size_t, P,
                               C.POINTER(moe_forward_aux_t)]),

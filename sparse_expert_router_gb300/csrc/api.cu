@@ -89,6 +89,22 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if ((c->d_model % 8) || (c->d_latent % 8) || (c->d_ff % 8) ||
       (c->n_shared > 0 && (c->d_ff_shared % 8)))
     return MOE_ERR_ALIGNMENT;
+  if (c->flags & MOE_FLAG_FP8_EXPERTS) {
+    if (c->dtype != MOE_BF16 || (c->flags & MOE_FLAG_SIMT)) return MOE_ERR_UNSUPPORTED;
+    if ((c->d_latent % 128) || (c->d_ff % 128)) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+bool fp8_experts(const moe_config_t& c) { return (c.flags & MOE_FLAG_FP8_EXPERTS) != 0; }
+
+// The fp8 operands a call reads must be present (and 16-byte aligned where they are arrays).
+moe_status_t check_fp8(const moe_config_t& c, const moe_fp8_t* f, bool rows, bool mlp) {
+  if (!fp8_experts(c)) return MOE_OK;
+  if (!f) return MOE_ERR_INVALID_ARG;
+  if (rows && !f->x_scale) return MOE_ERR_INVALID_ARG;
+  if (mlp && (!f->w1_scale || !f->w3_scale || !f->w2_scale || !f->x_scale || !f->h_scale))
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -163,12 +179,19 @@ Call make_call(const moe_config_t* cfg, void* ws, void* stream) {
   return k;
 }
 
-moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+// The CUDA error behind the calling thread's last MOE_ERR_CUDA (moe_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = e;
+  return MOE_ERR_CUDA;
+}
 
 #define MOE_TRY_CUDA(expr)                         \
   do {                                             \
     cudaError_t e_ = (expr);                       \
-    if (e_ != cudaSuccess) return MOE_ERR_CUDA;    \
+    if (e_ != cudaSuccess) return cuda_status(e_); \
   } while (0)
 
 cudaError_t run_gemms(const Call& k, GemmProblem* probs, int n) {
@@ -271,8 +294,17 @@ GemmProblem shared_problem(const Call& k, const void* x, const void* w1_s, const
 }
 
 GemmProblem expert_up_problem(const Call& k, const void* x_perm, const int32_t* offsets,
-                              const void* w1, const void* w3) {
+                              const void* w1, const void* w3, const moe_fp8_t* f8) {
   GemmProblem p;
+  if (fp8_experts(k.c)) {        // E4M3 rows and weights in, E4M3 hidden out
+    p.w_fp8 = 1;
+    p.w_scale = f8->w1_scale;
+    p.w3_scale = f8->w3_scale;
+    p.act_scale = f8->x_scale;
+    p.out_fp8 = 1;
+    p.out_scale = f8->h_scale;
+    p.amax = &k.hdr()->amax_h;
+  }
   p.epi = EPI_SWIGLU;
   p.group = GROUP_ROWS;
   p.M = k.c.d_ff;
@@ -287,8 +319,13 @@ GemmProblem expert_up_problem(const Call& k, const void* x_perm, const int32_t* 
 }
 
 GemmProblem expert_down_problem(const Call& k, const int32_t* offsets, const void* w2,
-                                void* y_perm) {
+                                void* y_perm, const moe_fp8_t* f8) {
   GemmProblem p;
+  if (fp8_experts(k.c)) {        // E4M3 hidden and weights in, bf16 out
+    p.w_fp8 = 1;
+    p.w_scale = f8->w2_scale;
+    p.act_scale = f8->h_scale;
+  }
   p.epi = EPI_STORE;
   p.group = GROUP_ROWS;
   p.M = k.c.d_latent;
@@ -323,7 +360,7 @@ GemmProblem back_problem(const Call& k, const void* c_buf, const void* w_up, con
 
 DispatchArgs dispatch_args(const Call& k, const int32_t* idx, const float* gamma,
                            int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
-                           int32_t* n_dropped, void* x_perm) {
+                           int32_t* n_dropped, void* x_perm, const moe_fp8_t* f8) {
   const moe_config_t& c = k.c;
   DispatchArgs a{};
   a.idx = idx;
@@ -345,6 +382,8 @@ DispatchArgs dispatch_args(const Call& k, const int32_t* idx, const float* gamma
   a.gamma = gamma;
   a.eps = c.rms_eps;
   a.x_perm = x_perm;
+  a.xperm_fp8 = fp8_experts(c) ? 1 : 0;
+  a.x_scale = a.xperm_fp8 ? f8->x_scale : nullptr;
   a.hdr = k.hdr();
   return a;
 }
@@ -446,6 +485,11 @@ const char* moe_status_string(moe_status_t s) {
   return "unknown status";
 }
 
+int32_t moe_last_cuda_error(const char** name) {
+  if (name) *name = cudaGetErrorName(g_last_cuda_error);
+  return (int32_t)g_last_cuda_error;
+}
+
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
@@ -473,52 +517,73 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   return MOE_OK;
 }
 
+// Copies an amax the kernels max-reduced into the workspace header to the caller's buffer.
+cudaError_t copy_amax(float* dst, const uint32_t* src, cudaStream_t st) {
+  if (!dst) return cudaSuccess;
+  return cudaMemcpyAsync(dst, src, sizeof(float), cudaMemcpyDeviceToDevice, st);
+}
+
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
                          const float* rms_gamma, const int32_t* topk_idx, int32_t* expert_counts,
                          int32_t* expert_offsets, int32_t* perm, int32_t* slot_of,
-                         int32_t* n_dropped, void* x_perm, void* ws, size_t ws_bytes,
-                         void* stream) {
+                         int32_t* n_dropped, void* x_perm, const moe_fp8_t* fp8, void* ws,
+                         size_t ws_bytes, void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if ((s = check_ptrs({x, w_down, rms_gamma, topk_idx, expert_counts, expert_offsets, perm,
                        slot_of, x_perm},
                       {n_dropped})) != MOE_OK)
     return s;
+  if ((s = check_fp8(*cfg, fp8, true, false)) != MOE_OK) return s;
   if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
   Call k = make_call(cfg, ws, stream);
+  const bool f8 = fp8_experts(*cfg);
   GemmProblem p = down_problem(k, x, w_down);
   if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+  if (f8) MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false, 1));
   MOE_TRY_CUDA(run_gemms(k, &p, 1));
   DispatchArgs da = dispatch_args(k, topk_idx, rms_gamma, expert_counts, expert_offsets, perm,
-                                  slot_of, n_dropped, x_perm);
+                                  slot_of, n_dropped, x_perm, fp8);
   MOE_TRY_CUDA(dispatch_run(da, cfg->dtype, k.st, k.pdl));
+  if (f8) MOE_TRY_CUDA(copy_amax(fp8->x_amax, &k.hdr()->amax_x, k.st));
   return MOE_OK;
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
                             const int32_t* expert_offsets, const void* w1, const void* w3,
-                            const void* w2, void* y_perm, const void* x, const void* w1_s,
-                            const void* w3_s, void* a_shared, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            const void* w2, const moe_fp8_t* fp8, void* y_perm, const void* x,
+                            const void* w1_s, const void* w3_s, void* a_shared, void* ws,
+                            size_t ws_bytes, void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
-  if ((s = check_ptrs({x_perm, expert_offsets, w1, w3, w2, y_perm}, {x, w1_s, w3_s, a_shared})) !=
-      MOE_OK)
+  if ((s = check_ptrs({x_perm, expert_offsets, w1, w3, w2, y_perm},
+                      {x, w1_s, w3_s, a_shared})) != MOE_OK)
     return s;
+  if ((s = check_fp8(*cfg, fp8, true, true)) != MOE_OK) return s;
   const bool shared = x && cfg->n_shared > 0;
   if (shared && (!w1_s || !w3_s || !a_shared)) return MOE_ERR_INVALID_ARG;
   if ((s = check_ws(*cfg, ws, ws_bytes)) != MOE_OK) return s;
   Call k = make_call(cfg, ws, stream);
-  GemmProblem up[2] = {expert_up_problem(k, x_perm, expert_offsets, w1, w3)};
-  int n_up = 1;
-  if (shared) up[n_up++] = shared_problem(k, x, w1_s, w3_s, a_shared);
-  GemmProblem down = expert_down_problem(k, expert_offsets, w2, y_perm);
-  if ((s = check_tc(k, up, n_up)) != MOE_OK) return s;
+  const bool f8 = fp8_experts(*cfg);
+  GemmProblem up = expert_up_problem(k, x_perm, expert_offsets, w1, w3, fp8);
+  GemmProblem sh;
+  if (shared) sh = shared_problem(k, x, w1_s, w3_s, a_shared);
+  GemmProblem down = expert_down_problem(k, expert_offsets, w2, y_perm, fp8);
+  if ((s = check_tc(k, &up, 1)) != MOE_OK) return s;
+  if (shared && (s = check_tc(k, &sh, 1)) != MOE_OK) return s;
   if ((s = check_tc(k, &down, 1)) != MOE_OK) return s;
+  if (f8) MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false, 2));
   MOE_TRY_CUDA(validate_offsets(expert_offsets, cfg->n_experts, pool_rows_of(*cfg), k.hdr(), k.st,
                                 false));
-  MOE_TRY_CUDA(run_gemms(k, up, n_up));
+  if (shared && !f8) {
+    GemmProblem both[2] = {up, sh};          // one launch: the grouped and the shared GEMM
+    MOE_TRY_CUDA(run_gemms(k, both, 2));
+  } else {                                   // an fp8 launch holds fp8 problems only
+    MOE_TRY_CUDA(run_gemms(k, &up, 1));
+    if (shared) MOE_TRY_CUDA(run_gemms(k, &sh, 1));
+  }
   MOE_TRY_CUDA(run_gemms(k, &down, 1));
+  if (f8) MOE_TRY_CUDA(copy_amax(fp8->h_amax, &k.hdr()->amax_h, k.st));
   return MOE_OK;
 }
 
@@ -554,6 +619,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   if ((s = check_ptrs({x, y, w->w_router, w->w_down, w->rms_gamma, w->w1, w->w3, w->w2, w->w_up},
                       {w->b_router})) != MOE_OK)
     return s;
+  if ((s = check_fp8(*cfg, w->fp8, true, true)) != MOE_OK) return s;
   if (cfg->n_shared > 0 && (s = check_ptrs({w->w1_s, w->w3_s, w->w2_s}, {})) != MOE_OK) return s;
   if (cfg->pool_rows != 0 && cfg->pool_rows < cfg->T * (int64_t)cfg->top_k)
     return MOE_ERR_INVALID_ARG;
@@ -576,8 +642,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
                           down_problem(k, x, w->w_down)};
   int n_front = 2;
   if (shared) front[n_front++] = shared_problem(k, x, w->w1_s, w->w3_s, a_s);
-  GemmProblem up = expert_up_problem(k, k.at<void>(L.x_perm), offsets, w->w1, w->w3);
-  GemmProblem down = expert_down_problem(k, offsets, w->w2, k.at<void>(L.y_perm));
+  GemmProblem up = expert_up_problem(k, k.at<void>(L.x_perm), offsets, w->w1, w->w3, w->fp8);
+  GemmProblem down = expert_down_problem(k, offsets, w->w2, k.at<void>(L.y_perm), w->fp8);
   GemmProblem back = back_problem(k, k.at<void>(L.c), w->w_up, shared ? a_s : nullptr,
                                   shared ? w->w2_s : nullptr, y);
   if ((s = check_tc(k, front, n_front)) != MOE_OK) return s;
@@ -588,11 +654,12 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   RouterArgs ra = router_args(k, x, w->w_router, w->b_router, idx, gate);
   DispatchArgs da = dispatch_args(k, idx, w->rms_gamma, k.at<int32_t>(L.counts), offsets,
                                   k.at<int32_t>(L.perm), slot_of, k.at<int32_t>(L.ndrop),
-                                  k.at<void>(L.x_perm));
+                                  k.at<void>(L.x_perm), w->fp8);
   CombineArgs ca = combine_args(k, k.at<void>(L.y_perm), slot_of, gate, k.at<void>(L.c));
 
   record(aux, 0, k.st);
-  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false));
+  const bool f8 = fp8_experts(*cfg);
+  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false, f8 ? 3 : 0));
   MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
   record(aux, 1, k.st);
   MOE_TRY_CUDA(run_gemms(k, front, n_front));
@@ -623,6 +690,10 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
     MOE_TRY_CUDA(cp(aux->slot_of, L.slot_of, Tk * 4));
     MOE_TRY_CUDA(cp(aux->n_dropped, L.ndrop, 4));
   }
+  if (f8) {
+    MOE_TRY_CUDA(copy_amax(w->fp8->x_amax, &k.hdr()->amax_x, k.st));
+    MOE_TRY_CUDA(copy_amax(w->fp8->h_amax, &k.hdr()->amax_h, k.st));
+  }
   return MOE_OK;
 }
 
@@ -631,9 +702,8 @@ moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream
   if (!ws || !out || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;
   DeviceHeader h;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY_CUDA(cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st));
+  MOE_TRY_CUDA(cudaStreamSynchronize(st));
   out->status = h.status;
   out->detail = h.detail;
   out->n_refined = h.n_refine;

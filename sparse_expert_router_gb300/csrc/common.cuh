@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "moe_gb300.h"
@@ -17,7 +18,9 @@ struct DeviceHeader {
   int32_t detail;
   int32_t n_refine;    // ambiguous-token list length (router stage 2)
   int32_t n_exact;     // exact-token list length (router stage 3)
-  int32_t reserved[60];
+  uint32_t amax_x;     // fp8 experts: bits of max |row| quantized by the gather (fp32, >= 0)
+  uint32_t amax_h;     // fp8 experts: bits of max |hidden| quantized by expert GEMM 1
+  int32_t reserved[58];
 };
 static_assert(sizeof(DeviceHeader) == 256, "header is 256 bytes");
 
@@ -54,6 +57,28 @@ __device__ __forceinline__ void st8(bf16* p, const float v[8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) b[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
   *reinterpret_cast<uint4*>(p) = u;
+}
+// An FP8 E4M3 code (sign, 4 exponent bits with bias 7, 3 fraction bits; largest finite 448).
+struct e4m3 {
+  uint8_t bits;
+};
+// Two fp32 values to two E4M3 codes, round to nearest even, saturating at +-448; `hi` goes to
+// the upper byte.
+__device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight values (already multiplied by their quantization scale) to eight codes, one 8-byte store.
+__device__ __forceinline__ void st8(e4m3* p, const float v[8]) {
+  uint2 u;
+  u.x = e4m3x2(v[1], v[0]) | (e4m3x2(v[3], v[2]) << 16);
+  u.y = e4m3x2(v[5], v[4]) | (e4m3x2(v[7], v[6]) << 16);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+// Running maximum of non-negative fp32 values kept as their bit patterns (monotone for >= 0).
+__device__ __forceinline__ void amax_update(uint32_t* dst, float m) {
+  atomicMax(dst, __float_as_uint(m));
 }
 __device__ __forceinline__ void st8(float* p, const float v[8]) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);

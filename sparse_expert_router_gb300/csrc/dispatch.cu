@@ -11,6 +11,8 @@
 // ordered gather rather than an atomic scatter-add, so repeated runs are bitwise identical
 // (weekly summary of 2026-09-14, post-training epic, #9144).
 #include "common.cuh"
+#include <type_traits>
+
 #include "dispatch.h"
 
 namespace moe {
@@ -18,12 +20,14 @@ namespace {
 
 constexpr int CH = 128;   // tokens per dispatch chunk (one thread per token)
 
-__global__ void header_reset_kernel(DeviceHeader* h, int clear_status) {
+__global__ void header_reset_kernel(DeviceHeader* h, int clear_status, int amax_mask) {
   pdl_wait();
   if (threadIdx.x == 0) {
     if (clear_status) { h->status = 0; h->detail = 0; }
     h->n_refine = 0;
     h->n_exact = 0;
+    if (amax_mask & 1) h->amax_x = 0;
+    if (amax_mask & 2) h->amax_h = 0;
   }
 }
 
@@ -166,9 +170,12 @@ __global__ void __launch_bounds__(CH) rank_kernel(DispatchArgs a) {
   }
 }
 
-// h = z * rsqrt(mean(z^2) + eps) * gamma written to every kept slot of the token.
+// h = z * rsqrt(mean(z^2) + eps) * gamma written to every kept slot of the token. With E4M3
+// output the rows hold the codes of h * x_scale (round to nearest even, saturating) and the
+// block's max |h| joins the layer's amax when the token has a kept slot.
 template <typename T>
 __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
+  constexpr bool kFp8 = std::is_same<T, e4m3>::value;
   pdl_wait();
   __shared__ float s_red[4];
   const int64_t t = blockIdx.x;
@@ -193,13 +200,27 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
     if (s >= 0 && s < a.pool_rows) slots[ns++] = s;
   }
   T* xp = static_cast<T*>(a.x_perm);
+  const float qs = kFp8 ? *a.x_scale : 1.0f;
+  float amax = 0.0f;
   for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
     float v[8], g[8];
     ld8(z + i, v);
     ld8(a.gamma + i, g);
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = v[q] * rstd * g[q];
+    if (kFp8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        amax = fmaxf(amax, fabsf(v[q]));
+        v[q] = v[q] * qs;
+      }
+    }
     for (int j = 0; j < ns; ++j) st8(xp + (int64_t)slots[j] * a.L + i, v);
+  }
+  if (kFp8 && ns > 0) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+    if ((threadIdx.x & 31) == 0) amax_update(&a.hdr->amax_x, amax);
   }
 }
 
@@ -244,8 +265,10 @@ __global__ void validate_offsets_kernel(const int32_t* off, int G, int64_t rows,
 
 }  // namespace
 
-cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl) {
-  return launch(header_reset_kernel, dim3(1), dim3(32), 0, st, pdl, h, clear_status ? 1 : 0);
+cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl,
+                         int amax_mask) {
+  return launch(header_reset_kernel, dim3(1), dim3(32), 0, st, pdl, h, clear_status ? 1 : 0,
+                amax_mask);
 }
 
 int64_t dispatch_chunks(int64_t T) { return cdiv(T, CH); }
@@ -262,6 +285,8 @@ cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool
   err = launch(rank_kernel, dim3(nch), dim3(CH), (size_t)a.E * (CH / 32) * 4, st, pdl, a);
   if (err != cudaSuccess) return err;
   if (a.x_perm == nullptr) return cudaSuccess;
+  if (a.xperm_fp8)
+    return launch(gather_kernel<e4m3>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
   if (dtype == DT_BF16) return launch(gather_kernel<bf16>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
   return launch(gather_kernel<float>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
 }

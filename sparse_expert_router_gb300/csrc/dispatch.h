@@ -23,6 +23,10 @@ struct DispatchArgs {
   const float* gamma;     // [L]
   float eps;
   void* x_perm;           // [pool_rows, L] or NULL (no scatter)
+  // fp8 experts: x_perm holds E4M3 codes of h * x_scale[0]; max |h| over the quantized rows
+  // goes to hdr->amax_x
+  int xperm_fp8;
+  const float* x_scale;
   DeviceHeader* hdr;
 };
 
@@ -38,7 +42,10 @@ struct CombineArgs {
   DeviceHeader* hdr;
 };
 
-cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl);
+// Zeroes the router counters, and the status (clear_status) and the amax fields named by
+// amax_mask (bit 0: amax_x, bit 1: amax_h).
+cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl,
+                         int amax_mask = 0);
 int64_t dispatch_chunks(int64_t T);
 cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool pdl);
 cudaError_t combine_run(const CombineArgs& a, int dtype, cudaStream_t st, bool pdl);

@@ -43,6 +43,19 @@ struct GemmProblem {
   // kchunk k-blocks of 64 and the chunk results are summed in fp32 by the epilogue (a tighter
   // rounding-error bound for the router's certified top-k). 0 = one accumulation over K.
   int kchunk = 0;
+  // tcgen05 only: weights (w, w3) and activations are E4M3 codes (MMA kind::f8f6f4). The
+  // epilogue multiplies each output feature's accumulator by fp32(1 / act_scale[0]) times the
+  // feature's weight scale ([G, M] fp32: w_scale for w, w3_scale for w3) before the epilogue
+  // function.
+  int w_fp8 = 0;
+  const float* w_scale = nullptr;
+  const float* w3_scale = nullptr;
+  const float* act_scale = nullptr;
+  // EPI_SWIGLU with E4M3 output: out receives the codes of value * out_scale[0]; the largest
+  // |value| is max-reduced into *amax (fp32 bits).
+  int out_fp8 = 0;
+  const float* out_scale = nullptr;
+  uint32_t* amax = nullptr;
 };
 
 // CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).

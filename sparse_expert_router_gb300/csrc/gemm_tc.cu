@@ -11,15 +11,21 @@
 // of the week of 2026-09-14 (hero-run epic, #9183) traces a hang to MMA and epilogue warps
 // that decoded their tiles from group boundaries before the producing kernel had written them.
 //
-// Roles of the 6 warps of a CTA (one CTA per SM, persistent over work items):
+// Roles of the warps of a CTA (one CTA per SM, persistent over work items):
 //   warp 0: TMA producer (one thread) filling a ring of shared-memory stages;
 //   warp 1: TMEM allocator and MMA issuer (one thread issues tcgen05.mma, commits to barriers);
-//   warps 2-5: epilogue, tcgen05.ld from tensor memory, fused epilogue, global stores.
+//   warps 2..: epilogue, tcgen05.ld from tensor memory, fused epilogue, global stores.
+// fp8 problems (the fp8 ragged dot of the expert MLP in the Marin summary of the week of
+// 2026-07-06, #6880 / #7079) take E4M3 weights and E4M3 activations straight into
+// tcgen05.mma kind::f8f6f4: a stage then carries 128 k per 128-byte swizzle row instead of 64,
+// and the epilogue applies the per-tensor activation scale and the per-feature weight scales.
 // Every wait on an mbarrier is bounded: after a few seconds the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing work, frees its tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -37,12 +43,19 @@ constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
 constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem
 constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
+constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte row of E4M3)
 #ifndef MOE_TC_EPI_WARPS
-#define MOE_TC_EPI_WARPS 8
+#define MOE_TC_EPI_WARPS 12
 #endif
-constexpr int EPI_WARPS = MOE_TC_EPI_WARPS;           // 4 or 8 (two per tensor-memory lane quadrant)
-constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
-constexpr int EPI_STAGE_BYTES = 16 * 32 * 4;           // per-warp transpose tile: 16 tokens x 32 features
+// Kernel instances: KC runs k-chunked fp32 problems (the router) with 8 epilogue warps; the
+// others (bf16 or FP8 operands) take MOE_TC_EPI_WARPS. The warps of one tensor-memory lane
+// quadrant take alternate 16-token chunks. Keeping the instances apart keeps each one's
+// registers within what its warp count allows (three or four warps share one sub-partition's
+// 16K registers).
+template <bool FP8, bool KC> struct Inst {
+  static constexpr int EW = KC ? 8 : MOE_TC_EPI_WARPS;
+};
+constexpr int EPI_TILE_MAX = 16 * 32 * 4;   // transpose tile of one warp: 16 tokens x 32 fp32
 constexpr int MAX_PROBS = 3;
 constexpr int MAX_GROUPS = 1024;
 constexpr int A_HALF = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
@@ -54,7 +67,7 @@ constexpr int B_BOX_ROWS = MOE_TC_BBOX;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;   // 4 KB
 constexpr unsigned long long TIMEOUT_NS = 5000000000ull;
 static_assert(BN % B_BOX_ROWS == 0 && BN % 16 == 0 && BN <= 256, "token tile");
-static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+static_assert(MOE_TC_EPI_WARPS % 4 == 0 && MOE_TC_EPI_WARPS <= 12, "epilogue warps");
 
 struct TcSeg {
   CUtensorMap a1, a3, b;
@@ -69,6 +82,12 @@ struct TcProblem {
   int dual;                    // item = 256 features as two 128-feature tiles sharing the token tile
   int kchunk;                  // k-blocks per accumulation chunk (0 = whole K)
   int bn;                      // token rows per tile
+  const float* w_scale;        // fp8: per-feature weight scales [G, M] of w (and of w3)
+  const float* w3_scale;
+  const float* act_scale;      // fp8: quantization multiplier of the activations ([1])
+  int out_fp8;                 // fp8 SwiGLU output: E4M3 codes of value * out_scale[0]
+  const float* out_scale;
+  uint32_t* amax;              // fp8 output: running max |value| (fp32 bits)
   int64_t rows;
   void* out;
   int64_t ld_out;
@@ -86,9 +105,12 @@ struct TcParams {
   int grouped;                 // index of the grouped problem (always the last) or -1
   int glu;                     // any problem uses two A tiles per stage (SwiGLU or dual)
   int stages;
+  int fp8;                     // E4M3 weights and activations (kind::f8f6f4)
+  uint32_t* amax;              // running max |value| of the launch's fp8 output, or NULL
   int nacc;                    // accumulator buffers in tensor memory (1 or 2)
   int acc2_off;                // column offset of the second accumulator of a two-A item
   int b_bytes;                 // bytes of the token tile slot of a stage
+  int epi_tile;                // bytes of each epilogue warp's transpose tile (widest output)
   DeviceHeader* hdr;
 };
 
@@ -178,10 +200,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A MN-major
-// (transposed), B K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-__device__ __forceinline__ uint32_t make_idesc(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor: fp32 accumulator (bits 4..5 = 1), A and B formats at bits 7..9 and
+// 10..12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3), A MN-major (transposed, bit 15),
+// B K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
+__device__ __forceinline__ uint32_t make_idesc(int n, bool fp8) {
+  const uint32_t ab = fp8 ? 0u : 1u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -191,6 +215,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -272,7 +305,14 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
 
 // ---- the kernel ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
+// Two instances: FP8 = false (bf16 operands, k-chunked fp32 problems) and FP8 = true (E4M3
+// operands, scales and the E4M3 SwiGLU output), so that neither carries the other's registers:
+// with 10 warps per CTA three warps share one sub-partition's 16K registers, 168 per thread.
+template <bool FP8, bool KC>
+__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams P) {
+  constexpr int EPI_WARPS = Inst<FP8, KC>::EW;
+  const int EPI_STAGE_BYTES = P.epi_tile;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
   __shared__ int64_t s_total;
@@ -288,6 +328,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
   auto sA1 = [&](int s) { return base + s * stage_bytes; };
   auto sA3 = [&](int s) { return base + s * stage_bytes + A_BYTES; };
   auto sB = [&](int s) { return base + s * stage_bytes + (glu ? 2 * A_BYTES : A_BYTES); };
+  constexpr bool fp8 = FP8;
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
   // Accumulators in tensor memory (512 columns): buffer b starts at column b*BN. A launch keeps
   // two buffers, so that the epilogue of one tile overlaps the main loop of the next, unless a
@@ -312,7 +353,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
 
   // set-up that reads nothing a preceding kernel writes
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tmem_full(b), 1);
       mbar_init(tmem_empty(b), 32 * EPI_WARPS);
@@ -384,6 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    const int bk = fp8 ? BK8 : BK;
     for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
@@ -393,18 +438,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
         for (int kb = 0; kb < sg.kblocks; ++kb) {
+          const int k0 = kb * bk;
           if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
           mbar_expect_tx(full(stage), bytes);
-          const int k0 = kb * BK;
-          tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
-          tma_load_3d(smem_u32(sA1(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + 64, k0, it.wg);
-          if (q.epi == EPI_SWIGLU) {
-            tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
-            tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a3, full(stage), it.m_w + 64, k0, it.wg);
-          } else if (q.dual) {
-            tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), it.m_w + BM, k0, it.wg);
-            tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + BM + 64, k0,
-                        it.wg);
+          if constexpr (FP8) {
+            // one [128 k][128 features] box of E4M3 per A tile
+            tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
+            if (q.epi == EPI_SWIGLU)
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
+            else if (q.dual)
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), it.m_w + BM, k0, it.wg);
+          } else {
+            tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
+            tma_load_3d(smem_u32(sA1(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + 64, k0, it.wg);
+            if (q.epi == EPI_SWIGLU) {
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
+              tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a3, full(stage), it.m_w + 64, k0, it.wg);
+            } else if (q.dual) {
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), it.m_w + BM, k0, it.wg);
+              tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + BM + 64, k0,
+                          it.wg);
+            }
           }
           for (int b = 0; b < nb; ++b)
             tma_load_2d(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, full(stage), k0,
@@ -424,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       const TcProblem& q = P.p[it.p];
       const bool sw = (q.epi == EPI_SWIGLU) || q.dual;   // second A tile -> second accumulator
       const int n = ((it.nrows + 15) / 16) * 16;
-      const uint32_t idesc = make_idesc(n);
+      const uint32_t idesc = make_idesc(n, fp8);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
       const int per_ev = q.kchunk ? q.kchunk : kb_total;
@@ -440,17 +494,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
           if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)), b = smem_u32(sB(stage));
-          // MN-major A: LBO = stride between the two 64-feature atoms, SBO = stride between
-          // 8-row k groups; K-major B: SBO = stride between 8-row groups, LBO unused.
+          // MN-major A: LBO = stride between 128-byte feature atoms (two 64-feature halves for
+          // bf16; one atom holds all 128 E4M3 features), SBO = stride between 8-row k groups;
+          // K-major B: SBO = stride between 8-row groups, LBO unused. Every MMA consumes 32
+          // bytes of each 128-byte row: 16 k of bf16 or 32 k of E4M3.
           const uint32_t albo = (uint32_t)A_HALF, asbo = 1024u;
+          if constexpr (FP8) {
 #pragma unroll
-          for (int k16 = 0; k16 < BK / 16; ++k16) {
-            const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-            mma_bf16(d_tmem, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
-            if (sw)
-              mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
-                       accumulate);
-            accumulate = 1;
+            for (int k32 = 0; k32 < BK8 / 32; ++k32) {
+              const uint64_t bd = smem_desc(b + k32 * 32, 16, 1024);
+              mma_e4m3(d_tmem, smem_desc(a1 + k32 * 4096, albo, asbo), bd, idesc, accumulate);
+              if (sw)
+                mma_e4m3(d_tmem + acc2, smem_desc(a3 + k32 * 4096, albo, asbo), bd, idesc,
+                         accumulate);
+              accumulate = 1;
+            }
+          } else {
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
+              mma_bf16(d_tmem, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
+              if (sw)
+                mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
+                         accumulate);
+              accumulate = 1;
+            }
           }
           mma_commit(empty(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -477,6 +545,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       if (f32out) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = v[j];
+      } else if (FP8 && q.out_fp8) {
+        // v holds the scaled SwiGLU values; pairs of tokens share one conversion
+        uint8_t* stg_b = reinterpret_cast<uint8_t*>(stg);
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const uint32_t c = e4m3x2(v[j + 1], v[j]);
+          stg_b[j * 32 + lane] = (uint8_t)(c & 0xFFu);
+          stg_b[(j + 1) * 32 + lane] = (uint8_t)(c >> 8);
+        }
       } else if (q.epi == EPI_SWIGLU) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
@@ -486,7 +563,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       }
       __syncwarp();
       const int rows_here = min(16, it.nrows - c0);
-      if (f32out) {
+      if (FP8 && q.out_fp8) {
+        // 16 token rows x 32 bytes: lane -> (row lane / 2, 16-byte half lane % 2)
+        const int row = lane >> 1, part = lane & 1;
+        if (f0 + part * 16 < q.M && row < rows_here) {
+          const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 32 + part * 16);
+          const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 16;
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(q.out) + o) = val;
+        }
+      } else if (f32out) {
         const int part = lane & 7;
         const bool ok = f0 + part * 4 < q.M;
 #pragma unroll
@@ -514,10 +599,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       __syncwarp();
     };
     int ev = 0;
+    float amax = 0.0f;                                   // fp8 output: this thread's max |value|
     for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      if (q.kchunk) {
+      if (KC && q.kchunk) {
         // k-chunked fp32 problem: sum the chunk accumulators in registers, in chunk order.
         // This warp owns columns half*16 + 32*i (i < 4) of the <= 128-token tile.
         int kb_total = q.seg[0].kblocks;
@@ -572,7 +658,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                  (uint32_t)(buf * BN) + (uint32_t)sub * acc2;
       const bool f32out = (q.epi == EPI_F32);
-      const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+      const bool fok = f0 + lane < q.M;
+      const float bias = (f32out && q.bias && fok) ? q.bias[f0 + lane] : 0.0f;
+      // fp8: dequantization factor of each accumulator, fp32(1 / activation scale) times the
+      // feature's weight scale in this expert (w, and w3 for the up projection)
+      const int64_t fs = (int64_t)it.wg * q.M + f0 + lane;
+      float sc1 = 1.0f, sc3 = 1.0f, osc = 1.0f;
+      if constexpr (FP8) {
+        const float da = __fdiv_rn(1.0f, *q.act_scale);
+        sc1 = fok ? __fmul_rn(da, q.w_scale[fs]) : 0.0f;
+        sc3 = (fok && q.w3_scale) ? __fmul_rn(da, q.w3_scale[fs]) : 0.0f;
+        if (q.out_fp8) osc = *q.out_scale;
+      }
       for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
         float v[16], v3[16];
         tmem_ld16(lane_addr + c0, v);
@@ -582,11 +679,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
         }
+        if constexpr (FP8) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) { v[j] = __fmul_rn(v[j], sc1); v3[j] = __fmul_rn(v3[j], sc3); }
+        }
+        if (FP8 && q.out_fp8) {
+          // SwiGLU in fp32, running max of |hidden| over this thread's stored values, then the
+          // quantization multiplier; store_chunk rounds to E4M3
+          const int valid = min(16, it.nrows - c0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h = swiglu(v[j], v3[j]);
+            if (fok && j < valid) amax = fmaxf(amax, fabsf(h));
+            v[j] = __fmul_rn(h, osc);
+          }
+        }
         store_chunk(q, it, c0, f0, v, v3);
       }
       }
       tc_fence_before();
       mbar_arrive(tmem_empty(buf));
+    }
+    if (FP8 && P.amax) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+      if (lane == 0 && amax > 0.0f) amax_update(P.amax, amax);
     }
   }
 
@@ -640,13 +757,29 @@ bool map_weights(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, int64_t
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Activations [rows, K] (K contiguous): 2-D map with a 64 x 32 box, 128-byte swizzle.
-bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows) {
+// E4M3 weights [G, K, Mw] (Mw contiguous bytes): 3-D map with a 128 x 128 x 1 box (one 128-byte
+// swizzle row of 128 features per k), 128-byte swizzle.
+bool map_weights_fp8(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, int64_t G) {
+  cuuint64_t dims[3] = {(cuuint64_t)Mw, (cuuint64_t)K, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)Mw, (cuuint64_t)(Mw * K)};
+  cuuint32_t box[3] = {128, BK8, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Activations [rows, K] (K contiguous): 2-D map with a box of one 128-byte swizzle row (64 bf16
+// or 128 E4M3) by 32 rows, 128-byte swizzle.
+bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, bool fp8) {
+  const int64_t es_bytes = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
-  cuuint32_t box[2] = {BK, B_BOX_ROWS};
+  cuuint64_t strides[1] = {(cuuint64_t)(K * es_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)(fp8 ? BK8 : BK), B_BOX_ROWS};
   cuuint32_t es[2] = {1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  return encode_fn()(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void*>(ptr), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -674,7 +807,16 @@ bool gemm_tc_supported(const GemmProblem& p) {
   // the epilogue writes 16-byte pieces of output rows
   if ((p.M % 8) || (p.ld_out % 8) || (p.out_col0 % 8)) return false;
   if (p.kchunk < 0) return false;
-  if (p.kchunk > 0 && (p.epi != EPI_F32 || p.group != GROUP_NONE || p.n_seg != 1 || EPI_WARPS != 8))
+  if (p.kchunk > 0 && (p.epi != EPI_F32 || p.group != GROUP_NONE || p.n_seg != 1))
+    return false;
+  if (p.w_fp8) {
+    const int Mw8 = (p.group == GROUP_COLS) ? p.Mg : p.M;
+    if (Mw8 % BM || p.n_seg != 1 || p.kchunk || p.epi == EPI_F32 || !p.w_scale ||
+        !p.act_scale || (p.epi == EPI_SWIGLU && !p.w3_scale) || (p.seg[0].K % 16))
+      return false;
+  }
+  if (p.out_fp8 && (!p.w_fp8 || p.epi != EPI_SWIGLU || !p.out_scale || (p.M % 16) ||
+                    (p.ld_out % 16) || (p.out_col0 % 16)))
     return false;
   return true;
 }
@@ -720,14 +862,27 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     q.G = g.G;
     const int64_t Mw = (g.group == GROUP_COLS) ? g.Mg : g.M;
     const int64_t Gw = (g.group == GROUP_ROWS) ? g.G : (g.group == GROUP_COLS ? g.M / g.Mg : 1);
+    q.w_scale = g.w_scale;
+    q.w3_scale = g.w3_scale;
+    q.act_scale = g.act_scale;
+    q.out_fp8 = g.out_fp8;
+    q.out_scale = g.out_scale;
+    if (g.out_fp8) {
+      if (P.amax && P.amax != g.amax) return cudaErrorNotSupported;   // one amax per launch
+      P.amax = g.amax;
+    }
+    if (j == 0) P.fp8 = g.w_fp8 ? 1 : 0;
+    if ((g.w_fp8 ? 1 : 0) != P.fp8) return cudaErrorNotSupported;   // all or none per launch
     for (int s = 0; s < g.n_seg; ++s) {
       const GemmSeg& sg = g.seg[s];
       TcSeg& ts = q.seg[s];
-      ts.kblocks = (int)cdiv(sg.K, BK);
-      if (!map_weights(&ts.a1, sg.w, Mw, sg.K, Gw)) return cudaErrorInvalidValue;
-      if (g.epi == EPI_SWIGLU && !map_weights(&ts.a3, sg.w3, Mw, sg.K, Gw))
-        return cudaErrorInvalidValue;
-      if (!map_act(&ts.b, sg.act, sg.K, g.rows)) return cudaErrorInvalidValue;
+      ts.kblocks = (int)cdiv(sg.K, g.w_fp8 ? BK8 : BK);
+      auto mapw = [&](CUtensorMap* m, const void* w) {
+        return g.w_fp8 ? map_weights_fp8(m, w, Mw, sg.K, Gw) : map_weights(m, w, Mw, sg.K, Gw);
+      };
+      if (!mapw(&ts.a1, sg.w)) return cudaErrorInvalidValue;
+      if (g.epi == EPI_SWIGLU && !mapw(&ts.a3, sg.w3)) return cudaErrorInvalidValue;
+      if (!map_act(&ts.b, sg.act, sg.K, g.rows, g.w_fp8 != 0)) return cudaErrorInvalidValue;
     }
     q.item_base = base;
     if (g.group == GROUP_ROWS) {
@@ -749,22 +904,33 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
   P.b_bytes = max_bn * BK * 2;
   const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
+  // transpose tiles sized for the widest output of the launch
+  P.epi_tile = 16 * 32 * 2;
+  for (int j = 0; j < n_probs; ++j)
+    if (P.p[j].epi == EPI_F32) P.epi_tile = EPI_TILE_MAX;
+  bool kc = false;
+  for (int j = 0; j < n_probs; ++j) kc = kc || P.p[j].kchunk > 0;
+  const int ew = P.fp8 ? Inst<true, false>::EW : (kc ? Inst<false, true>::EW : Inst<false, false>::EW);
+  const size_t epi_bytes = (size_t)ew * P.epi_tile;
   // as many stages as fit next to the epilogue tiles and the schedule (at most 8)
   {
-    const size_t fixed = 1024 + (size_t)EPI_WARPS * EPI_STAGE_BYTES +
+    const size_t fixed = 1024 + epi_bytes +
                          (size_t)(3 * ((P.grouped >= 0) ? P.p[P.grouped].G : 0) + 1) * 4;
     const size_t budget = (size_t)MOE_TC_SMEM_BUDGET;
     int st = (int)((budget - fixed) / (size_t)stage_bytes);
     P.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
   }
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
-  const size_t smem = (size_t)P.stages * stage_bytes + 1024 + (size_t)EPI_WARPS * EPI_STAGE_BYTES +
-                      (size_t)(3 * G + 1) * 4;
-  cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = (size_t)P.stages * stage_bytes + 1024 +
+                      epi_bytes + (size_t)(3 * G + 1) * 4;
+  auto kern = P.fp8 ? tc_gemm_kernel<true, false>
+                    : (kc ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   int grid = num_sms_tc();
   if (P.grouped < 0) grid = (int)imin64(grid, base);
   if (grid < 1) return cudaSuccess;
-  return launch(tc_gemm_kernel, dim3(grid), dim3(NTHREADS), smem, stream, pdl, P);
+  return launch(kern, dim3(grid), dim3(64 + 32 * ew), smem, stream, pdl, P);
 }
 
 cudaError_t bounded_wait_selftest(void* dev_header, uint64_t limit_ns, cudaStream_t stream) {

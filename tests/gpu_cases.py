@@ -35,6 +35,9 @@ def run_forward(shape, inp, flags=0):
         "slot_of": torch.zeros((T, k), dtype=torch.int32, device=DEV),
         "n_dropped": torch.zeros(1, dtype=torch.int32, device=DEV),
     }
+    if shape.expert_dtype == "fp8":
+        out["x_amax"] = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
+        out["h_amax"] = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
     ws = m.alloc_workspace(cfg, DEV)
     m.moe_forward(cfg, inp, inp["x"], out["y"], ws, aux={n: out[n] for n in out if n != "y"})
     out["report"] = m.moe_get_device_status(ws)
@@ -64,3 +67,30 @@ def check_routing(got, ref, shape):
     assert torch.equal(got["slot_of"].cpu().long(), ref["slot_of"])
     assert int(got["n_dropped"].cpu()) == int(ref["n_dropped"])
     return gerr
+
+
+def e4m3_codes_match(got_vals: torch.Tensor, exact: torch.Tensor, atol: float):
+    """E4M3 codes written by the device against the oracle's quantization of the same tensor.
+
+    ``exact`` holds the oracle's unrounded scaled values v = fp64(x) * S; the device rounded its
+    own fp32 value of v, which differs from v by up to ``atol`` (the device's fp32 error in x,
+    times S). Both round to nearest even, so the codes may differ only where v lies within atol
+    of a rounding midpoint, and there the two codes must be neighbours. Returns the number of
+    such elements."""
+    got = got_vals.double().cpu().flatten()
+    want = moe_oracle.e4m3_round(moe_oracle.to_fp32(exact)).flatten()
+    bad = (got != want).nonzero().flatten()
+    v = exact.double().cpu().flatten()[bad]
+    mid = (got[bad] + want[bad]) / 2
+    dist = (v - mid).abs()
+    step = (got[bad] - want[bad]).abs()
+    lo = torch.minimum(got[bad].abs(), want[bad].abs())
+    # neighbours: the gap is one E4M3 step at the smaller magnitude (2^(e-3), or 2^-9 below 2^-6)
+    _, ex = torch.frexp(lo.clamp_min(2.0 ** -9))
+    one_step = step <= torch.exp2((ex - 1 - 3).clamp_min(-9).double()) * 1.0000001
+    far = dist > atol
+    assert not bool(far.any()), (f"{int(far.sum())} of {bad.numel()} differing codes lie away "
+                                 f"from a rounding tie (largest distance {float(dist.max()):.3e}, "
+                                 f"atol {atol:.1e})")
+    assert bool(one_step.all()), "codes differ by more than one step"
+    return int(bad.numel())

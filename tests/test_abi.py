@@ -90,13 +90,35 @@ def test_argument_errors_before_any_launch(lib):
     # workspace too small / misaligned
     assert lib.moe_route(c, good, good, None, good, good, ws, n - 256, None) == L.MOE_ERR_WORKSPACE
     assert lib.moe_route(c, good, good, None, good, good, P(0x100080), n, None) == L.MOE_ERR_ALIGNMENT
-    assert lib.moe_permute(c, good, good, good, good, good, good, good, good, None, None, ws, n,
-                           None) == L.MOE_ERR_INVALID_ARG
-    assert lib.moe_expert_ffn(c, good, good, good, good, None, good, None, None, None, None, ws, n,
-                              None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(c, good, good, good, good, good, good, good, good, None, None, None,
+                           ws, n, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_ffn(c, good, good, good, good, None, None, good, None, None, None, None,
+                              ws, n, None) == L.MOE_ERR_INVALID_ARG
     # shared experts requested without their weights
-    assert lib.moe_expert_ffn(c, good, good, good, good, good, good, good, None, None, good, ws,
-                              n, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_ffn(c, good, good, good, good, good, None, good, good, None, None, good,
+                              ws, n, None) == L.MOE_ERR_INVALID_ARG
+    # an fp8-expert layer needs its moe_fp8_t, with every scale the call reads
+    c8 = _cfg(dtype="bf16", flags=L.MOE_FLAG_FP8_EXPERTS)
+    cc8 = C.byref(c8.c())
+    n8 = _ws(lib, c8)
+    assert lib.moe_expert_ffn(cc8, good, good, good, good, good, None, good, None, None, None,
+                              None, ws, n8, None) == L.MOE_ERR_INVALID_ARG
+    part = L.moe_fp8_t(w1_scale=0x10000, w3_scale=0x10000, w2_scale=0x10000, x_scale=0x10000)
+    assert lib.moe_expert_ffn(cc8, good, good, good, good, good, C.byref(part), good, None, None,
+                              None, None, ws, n8, None) == L.MOE_ERR_INVALID_ARG   # no h_scale
+    assert lib.moe_permute(cc8, good, good, good, good, good, good, good, good, None, good,
+                           C.byref(L.moe_fp8_t()), ws, n8, None) == L.MOE_ERR_INVALID_ARG
+    w8 = L.moe_weights_t(w_router=0x10000, w_down=0x10000, rms_gamma=0x10000, w1=0x10000,
+                         w3=0x10000, w2=0x10000, w1_s=0x10000, w3_s=0x10000, w2_s=0x10000,
+                         w_up=0x10000)
+    assert lib.moe_forward(cc8, C.byref(w8), good, good, ws, n8, None, None) == \
+        L.MOE_ERR_INVALID_ARG
+    cf8 = _cfg(flags=L.MOE_FLAG_FP8_EXPERTS)          # fp32 layer
+    assert lib.moe_workspace_size(C.byref(cf8.c()), C.byref(C.c_size_t())) == L.MOE_ERR_UNSUPPORTED
+    cs8 = _cfg(dtype="bf16", flags=L.MOE_FLAG_FP8_EXPERTS | L.MOE_FLAG_SIMT)
+    assert lib.moe_workspace_size(C.byref(cs8.c()), C.byref(C.c_size_t())) == L.MOE_ERR_UNSUPPORTED
+    c8w = _cfg(dtype="bf16", d_latent=64, flags=L.MOE_FLAG_FP8_EXPERTS)   # widths not /128
+    assert lib.moe_workspace_size(C.byref(c8w.c()), C.byref(C.c_size_t())) == L.MOE_ERR_ALIGNMENT
     assert lib.moe_combine(c, good, good, None, None, None, None, good, ws, n, None) == \
         L.MOE_ERR_INVALID_ARG
     w = L.moe_weights_t(w_router=0x10000, w_down=0x10000, rms_gamma=0x10000, w1=0x10000,
@@ -125,3 +147,10 @@ def test_binding_refuses_missing_library(tmp_path):
             _lib.load(str(tmp_path / "nope.so"))
     finally:
         _lib._lib = saved
+
+
+def test_last_cuda_error_starts_clear(lib):
+    name = C.c_char_p()
+    assert lib.moe_last_cuda_error(C.byref(name)) == 0
+    assert name.value == b"cudaSuccess"
+    assert lib.moe_last_cuda_error(None) == 0

@@ -11,7 +11,8 @@ import sparse_expert_router_gb300 as m
 from moe_workloads import SHAPES, SLICE_C5B, make_layer_inputs, make_slice_inputs
 from oracle import moe_oracle
 
-from gpu_cases import (DEV, check_routing, gpu_inputs, normwise, oracle_forward, run_forward,
+from gpu_cases import (DEV, check_routing, e4m3_codes_match, gpu_inputs, normwise, oracle_forward,
+                       run_forward,
                        sample_tokens)
 
 pytestmark = pytest.mark.gpu
@@ -238,7 +239,8 @@ def test_bounded_wait_times_out_and_context_survives():
 
 # ------------------------------------------------------------------- 535B-shaped ----
 
-LARGE = ["l535b_t8192", "l535b_zipf_t16384", "l535b_zipf_t16384_cf110", "l535b_t65536"]
+LARGE = ["l535b_t8192", "l535b_zipf_t16384", "l535b_zipf_t16384_cf110", "l535b_t65536",
+         "l535b_t8192_fp8"]
 
 
 @pytest.mark.parametrize("name", LARGE)
@@ -383,3 +385,107 @@ def test_router_logit_error_within_certified_bound():
         ratio = float(((lt - ref).abs() / beta).max())
         print(name, "max |error| / bound =", ratio)
         assert ratio <= 1.0, ratio
+
+
+# -------------------------------------------------------------- fp8 expert MLP ----
+
+def _fp8_args(inp, **extra):
+    d = {n: inp[n] for n in ("w1_scale", "w3_scale", "w2_scale", "x_scale", "h_scale")}
+    d.update(extra)
+    return d
+
+
+def test_small_fp8_forward():
+    """fp8 expert MLP (E4M3 rows, hidden and weights): routing bit-exact, outputs against the
+    oracle's fp8 layer, the amax outputs bracket the sampled tokens' values."""
+    shape = SHAPES["small_fp8"]
+    inp = gpu_inputs(shape)
+    got = run_forward(shape, inp)
+    toks = sample_tokens(shape.T, 256)
+    ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()}, tokens=toks)
+    check_routing(got, ref, shape)
+    err = normwise(got["y"][toks], ref["y"])
+    assert err <= 2e-2, err
+    assert got["report"]["status"] == 0
+    # the device's amax runs over every token; the oracle's over the sampled ones
+    assert float(got["x_amax"]) >= float(ref["x_amax"]) * (1 - 1e-5)
+    assert float(got["h_amax"]) >= float(ref["h_amax"]) * (1 - 1e-4)
+    assert float(got["x_amax"]) < 448.0 / float(inp["x_scale"][0])      # no saturation here
+    assert float(got["h_amax"]) < 448.0 / float(inp["h_scale"][0])
+
+
+def test_fp8_split_calls():
+    """moe_permute's E4M3 rows and amax against the oracle's quantization; moe_expert_ffn on the
+    oracle's codes (with the shared experts in the same call) and its hidden amax."""
+    shape = SHAPES["small_fp8"].with_(T=512)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    cfg = m.LayerConfig.from_shape(shape)
+    assert cfg.flags & m.MOE_FLAG_FP8_EXPERTS
+    T, k, E, L = shape.T, shape.top_k, shape.n_experts, shape.d_latent
+    ref = oracle_forward(shape, cpu)
+    sx, sh = float(cpu["x_scale"][0]), float(cpu["h_scale"][0])
+    ws = m.alloc_workspace(cfg, DEV)
+
+    oidx = ref["idx"].to(torch.int32).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    slot = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ndrop = torch.empty(1, dtype=torch.int32, device=DEV)
+    x_perm = torch.zeros((T * k, L), dtype=torch.uint8, device=DEV)
+    x_amax = torch.full((1,), -1.0, device=DEV)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], oidx, counts, offs, perm, slot,
+                  ndrop, x_perm, ws, fp8={"x_scale": inp["x_scale"], "x_amax": x_amax})
+    R = int(ref["offsets"][-1])
+    assert torch.equal(perm.cpu().long()[:R], ref["perm"])
+    tok = ref["perm"] // k
+    rows = ref["h"][tok]
+    # the device's latent carries fp32 GEMM and norm rounding, well below 1e-3 absolute here
+    n_ties = e4m3_codes_match(x_perm[:R].view(torch.float8_e4m3fn).to(torch.float64), rows * sx,
+                              atol=1e-3 * sx)
+    assert n_ties <= R * L * 1e-3, n_ties
+    assert abs(float(x_amax) - float(rows.abs().max())) <= 1e-5 * float(rows.abs().max())
+
+    # the oracle's codes as the grouped rows; 64 rows past the pool are never touched
+    codes = moe_oracle.quantize_e4m3(rows, sx)
+    xp = torch.zeros((T * k + 64, L), dtype=torch.uint8, device=DEV)
+    xp[:R] = codes.to(torch.float8_e4m3fn).view(torch.uint8).to(DEV)
+    y_perm = torch.zeros((T * k + 64, L), dtype=torch.bfloat16, device=DEV)
+    a_s = torch.empty((T, shape.n_shared * shape.d_ff_shared), dtype=torch.bfloat16, device=DEV)
+    h_amax = torch.full((1,), -1.0, device=DEV)
+    m.moe_expert_ffn(cfg, xp, ref["offsets"].to(torch.int32).to(DEV), inp["w1"], inp["w3"],
+                     inp["w2"], y_perm, inp["x"], inp["w1_s"], inp["w3_s"], a_s, ws,
+                     fp8=_fp8_args(inp, h_amax=h_amax))
+    a_ref, o_ref = moe_oracle.grouped_experts(
+        codes, ref["offsets"].tolist(), cpu["w1"], cpu["w3"], cpu["w2"],
+        fp8={n: cpu[n] for n in ("w1_scale", "w3_scale", "w2_scale", "x_scale", "h_scale")})
+    assert normwise(y_perm[:R], o_ref) <= 1e-2
+    assert float(y_perm[R:].float().abs().max()) == 0.0
+    assert normwise(a_s, ref["a_s"]) <= 1e-2
+    hmax = float(a_ref.abs().max())
+    assert abs(float(h_amax) - hmax) <= 1e-4 * hmax, (float(h_amax), hmax)
+    # an fp8 layer without its moe_fp8_t is an argument error, not a fault
+    with pytest.raises(m.MoEError):
+        m.moe_expert_ffn(cfg, xp, offs, inp["w1"], inp["w3"], inp["w2"], y_perm, ws=ws)
+    with pytest.raises(m.MoEError):
+        m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], oidx, counts, offs, perm,
+                      slot, ndrop, x_perm, ws)
+    assert m.moe_get_device_status(ws)["status"] == 0
+
+
+def test_fp8_close_to_bf16_layer():
+    """The fp8 layer and the bf16 layer with the same weights (dequantized, exact in bf16):
+    identical routing, outputs apart by no more than E4M3 activation rounding allows (each
+    quantized value is within 2^-4 of its input, relatively), and not identical."""
+    shape = SHAPES["small_fp8"].with_(T=2048)
+    inp = gpu_inputs(shape)
+    a = run_forward(shape, inp)
+    deq = dict(inp)
+    for n in ("w1", "w3", "w2"):
+        deq[n] = (inp[n].float() * inp[n + "_scale"].unsqueeze(1)).to(torch.bfloat16)
+    b = run_forward(shape.with_(expert_dtype="bf16"), deq)
+    assert torch.equal(a["topk_idx"], b["topk_idx"])
+    assert torch.equal(a["expert_offsets"], b["expert_offsets"])
+    err = normwise(a["y"], b["y"])
+    assert 1e-3 < err <= 0.1, err
