@@ -39,7 +39,11 @@ Readings taken where the pages are silent (each is listed in the design doc):
      computed exactly (the July summary records a ~2.6% mismatch caused by an
      approximate fused SwiGLU epilogue);
   R7 shared experts read x and are summed unweighted;
-  R8 y = c W_up + sum_s SwiGLU_s(x).
+  R8 y = c W_up + sum_s SwiGLU_s(x);
+  R15 an optional token mask marks attention-mask padding, which is excluded from dispatch
+     (September 14 weekly summary, hero-run epic, #9159; the teardown's run counts padding
+     tokens skipped by routing): a padding token is routed but sends no row to any expert,
+     takes no capacity, is not a drop, and keeps only its shared-expert output.
 
 All arithmetic is fp64 on exactly promoted inputs (bf16 and fp32 values are
 exact in fp64, and so is every product of two of them). Nothing is rounded
@@ -178,7 +182,8 @@ def capacity(T: int, k: int, E: int, cf: Optional[Tuple[int, int]]) -> Optional[
     return -(-(num * T * k) // (den * E))
 
 
-def dispatch(idx: torch.Tensor, E: int, cap: Optional[int]) -> Dict[str, torch.Tensor]:
+def dispatch(idx: torch.Tensor, E: int, cap: Optional[int],
+             mask: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
     """Expert counts, capacity clamp, group offsets and the stable permutation.
 
     counts[e] = number of assignments to e; kept[e] = min(counts[e], C);
@@ -187,11 +192,18 @@ def dispatch(idx: torch.Tensor, E: int, cap: Optional[int]) -> Dict[str, torch.T
     r < C, else slot -1 (dropped). perm[slot] = t * k + j. Rows of one expert
     therefore sit together in ascending token order, as the ragged transport
     delivers them (teardown, section "21% to 27% MFU without stopping the run").
+
+    mask[t] == 0 marks attention-mask padding (reading R15): the token's assignments are not
+    dispatched at all. They are not counted, take no rank and no capacity, are not drops,
+    and get slot -1.
     """
     T, k = idx.shape
     il = idx.tolist()
+    real = [True] * T if mask is None else [bool(v) for v in mask.tolist()]
     counts = [0] * E
-    for row in il:
+    for t, row in enumerate(il):
+        if not real[t]:
+            continue
         for e in row:
             counts[e] += 1
     kept = [c if cap is None else min(c, cap) for c in counts]
@@ -202,6 +214,8 @@ def dispatch(idx: torch.Tensor, E: int, cap: Optional[int]) -> Dict[str, torch.T
     slot_of = [[-1] * k for _ in range(T)]
     perm = [-1] * offsets[E]
     for t in range(T):
+        if not real[t]:
+            continue
         for j in range(k):
             e = il[t][j]
             r = seen[e]
@@ -391,6 +405,10 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
             tokens: Optional[Sequence[int]] = None) -> Dict[str, torch.Tensor]:
     """The whole layer: route, dispatch, latent, experts, combine, up-projection + shared.
 
+    An optional ``inp["token_mask"]`` [T] marks padding tokens with 0 (reading R15): they are
+    routed like every token but not dispatched, so their routed part c[t] is zero and
+    y[t] is the shared experts' output alone.
+
     Routing and dispatch are always computed for every token (capacity drops
     depend on all earlier tokens). The expert, combine and output stages are
     computed for ``tokens`` only when given (each token's output depends only
@@ -402,7 +420,7 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
     E = inp["w_router"].shape[1]
     r = route(x, inp["w_router"], inp.get("b_router"), top_k)
     cap = capacity(T, top_k, E, capacity_factor)
-    dsp = dispatch(r["idx"], E, cap)
+    dsp = dispatch(r["idx"], E, cap, inp.get("token_mask"))
     toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
     xt = x[toks]
     z, h = latent(xt, inp["w_down"], inp["rms_gamma"], rms_eps)

@@ -383,7 +383,55 @@ def pin_fp8_layer_grid():
     assert torch.allclose(out["o"][toks, j], o, rtol=1e-12, atol=1e-12)
 
 
-ALL_PINS = [pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
+def pin_mask_all_ones_is_no_mask():
+    """An all-ones token mask changes nothing, bit for bit."""
+    from moe_workloads import SHAPES, make_layer_inputs
+    s = SHAPES["tiny_f32"].with_(T=48, capacity=(1, 2))
+    inp = make_layer_inputs(s, "cpu")
+    a = O.forward(inp, top_k=s.top_k, rms_eps=s.rms_eps, capacity_factor=s.capacity)
+    inp1 = dict(inp, token_mask=torch.ones(s.T, dtype=torch.uint8))
+    b = O.forward(inp1, top_k=s.top_k, rms_eps=s.rms_eps, capacity_factor=s.capacity)
+    for key in ("counts", "offsets", "slot_of", "perm", "n_dropped", "y"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def pin_mask_padding_keeps_shared_only():
+    """Without capacity, a padding token's output is the shared path alone (the same layer with
+    every routed W2 zero), and every other token's output is unchanged by the mask."""
+    from moe_workloads import SHAPES, make_layer_inputs
+    s = SHAPES["tiny_f32"].with_(T=40)
+    inp = make_layer_inputs(s, "cpu")
+    mask = torch.ones(s.T, dtype=torch.uint8)
+    pad = [0, 7, 8, 39]
+    mask[pad] = 0
+    kw = dict(top_k=s.top_k, rms_eps=s.rms_eps)
+    full = O.forward(inp, **kw)
+    masked = O.forward(dict(inp, token_mask=mask), **kw)
+    no_routed = O.forward(dict(inp, w2=torch.zeros_like(inp["w2"])), **kw)
+    real = mask.bool()
+    assert torch.allclose(masked["y"][~real], no_routed["y"][~real], rtol=0, atol=1e-14)
+    assert torch.equal(masked["y"][real], full["y"][real])
+    assert int(masked["counts"].sum()) == s.top_k * (s.T - len(pad))
+    assert bool((masked["slot_of"][~real] == -1).all()) and int(masked["n_dropped"]) == 0
+
+
+def pin_mask_frees_capacity():
+    """Hand-derived: 4 tokens all choose expert 0 of 2 (k = 1) with capacity 2. Unmasked, tokens
+    0 and 1 are kept and 2 and 3 dropped. With token 0 padding, tokens 1 and 2 take the two slots,
+    token 3 is the only drop, and the padding token is neither counted nor dropped."""
+    idx = torch.zeros((4, 1), dtype=torch.int64)
+    d0 = O.dispatch(idx, 2, 2)
+    assert d0["slot_of"].flatten().tolist() == [0, 1, -1, -1] and int(d0["n_dropped"]) == 2
+    d = O.dispatch(idx, 2, 2, torch.tensor([0, 1, 1, 1]))
+    assert d["counts"].tolist() == [3, 0]
+    assert d["offsets"].tolist() == [0, 2, 2]
+    assert d["slot_of"].flatten().tolist() == [-1, 0, 1, -1]
+    assert d["perm"].tolist() == [1, 2]
+    assert int(d["n_dropped"]) == 1
+
+
+ALL_PINS = [pin_mask_all_ones_is_no_mask, pin_mask_padding_keeps_shared_only,
+            pin_mask_frees_capacity, pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
             pin_fp8_layer_grid, pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
             pin_capacity, pin_dispatch_golden, pin_dispatch_invariants, pin_forced_single_expert,
             pin_identical_experts, pin_two_token_golden, pin_rmsnorm,
@@ -478,11 +526,28 @@ def _mut_fp8_quantize_in_fp64(monkeypatch):
     monkeypatch.setattr(O, "quantize_e4m3", lambda v, scale: O.e4m3_round(O.to64(v) * float(scale)))
 
 
+def _mut_mask_ignored(monkeypatch):
+    orig = O.dispatch
+    monkeypatch.setattr(O, "dispatch", lambda idx, E, cap, mask=None: orig(idx, E, cap))
+
+
+def _mut_mask_counts_padding(monkeypatch):
+    orig = O.dispatch
+
+    def bad(idx, E, cap, mask=None):
+        d = orig(idx, E, cap, mask)
+        if mask is not None:   # padding assignments still counted before the clamp
+            full = orig(idx, E, cap)
+            d["counts"] = full["counts"]
+        return d
+    monkeypatch.setattr(O, "dispatch", bad)
+
+
 def _mut_unstable_perm(monkeypatch):
     orig = O.dispatch
 
-    def bad(idx, E, cap):
-        d = orig(idx.flip(0), E, cap)          # ranks taken in reverse token order
+    def bad(idx, E, cap, mask=None):
+        d = orig(idx.flip(0), E, cap, None if mask is None else mask.flip(0))   # reverse order
         d["slot_of"] = d["slot_of"].flip(0)
         T, k = idx.shape
         d["perm"] = torch.where(d["perm"] >= 0, (T - 1 - d["perm"] // k) * k + d["perm"] % k,
@@ -505,7 +570,8 @@ def _mut_transposed_up(monkeypatch):
 MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mut_no_shared,
              _mut_rms_sum, _mut_full_softmax, _mut_renorm_after_drop, _mut_forward_renorm, _mut_fp8_scale_ignored, _mut_e4m3_ties_away,
              _mut_fp8_no_activation_rounding, _mut_fp8_dequant_by_scale,
-             _mut_fp8_quantize_in_fp64, _mut_unstable_perm,
+             _mut_fp8_quantize_in_fp64, _mut_mask_ignored, _mut_mask_counts_padding,
+             _mut_unstable_perm,
              _mut_transposed_up]
 
 
