@@ -162,6 +162,12 @@ typedef struct {
   int32_t* slot_of;         /* [T, k] */
   int32_t* n_dropped;       /* [1] */
   void* const* stage_events;
+  /* Input, [T] bytes or NULL (every token real): 0 marks attention-mask padding, which is
+   * routed but not dispatched (the weekly summary of 2026-09-14, hero-run epic, #9159, excludes
+   * attention-mask padding from MoE dispatch). A padding token's assignments are not counted,
+   * take no capacity, are not drops and get slot -1; its routed output is zero, so y[t] is the
+   * shared experts' output alone. */
+  const uint8_t* token_mask;
 } moe_forward_aux_t;
 
 /* Diagnostics recorded on the device by the last calls (see moe_get_device_status). */
@@ -203,9 +209,11 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const voi
  * x_perm [pool_rows, L] receives h at every used row. topk_idx must hold ascending, distinct
  * expert ids (as moe_route writes them). Under MOE_FLAG_FP8_EXPERTS x_perm receives the E4M3
  * codes of h (one byte each) under fp8->x_scale, and fp8->x_amax (if not NULL) max |h| over the
- * rows written; fp8 is ignored (may be NULL) otherwise. */
+ * rows written; fp8 is ignored (may be NULL) otherwise. token_mask ([T] bytes or NULL) marks
+ * attention-mask padding with 0: those tokens are not dispatched (see moe_forward_aux_t). */
 MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
                          const float* rms_gamma, const int32_t* topk_idx,
+                         const uint8_t* token_mask,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
                          int32_t* slot_of, int32_t* n_dropped, void* x_perm,
                          const moe_fp8_t* fp8, void* ws, size_t ws_bytes, void* stream);

@@ -157,7 +157,7 @@ SLICE_C5B = SliceShape("l535b_ep_slice", rows=49152, pool_rows=56576, d_latent=3
 _TENSOR_IDS = {
     "x": 1, "w_router": 2, "w_down": 3, "w1": 4, "w3": 5, "w2": 6, "w1_s": 7, "w3_s": 8,
     "w2_s": 9, "w_up": 10, "zipf_perm": 11, "slice_x": 12, "slice_w1": 13, "slice_w3": 14,
-    "slice_w2": 15, "slice_draws": 16,
+    "slice_w2": 15, "slice_draws": 16, "padding_mask": 17,
 }
 
 
@@ -307,3 +307,18 @@ def make_router_inputs(shape: LayerShape, device="cpu") -> Dict[str, torch.Tenso
     else:
         out["b_router"] = torch.zeros(s.n_experts, dtype=torch.float32, device=device)
     return out
+
+
+def padding_mask(T: int, seq_len: int = 64, max_pad_frac: float = 0.5, seed: int = 0,
+                 device="cpu") -> torch.Tensor:
+    """[T] uint8 attention mask of packed sequences: the tokens are cut into sequences of
+    `seq_len`, and each sequence ends with a seeded run of padding (0) of up to
+    `max_pad_frac` of its length; real tokens are 1."""
+    g = torch.Generator().manual_seed(tensor_seed(seed, "padding_mask"))
+    mask = torch.ones(T, dtype=torch.uint8)
+    for s0 in range(0, T, seq_len):
+        n = min(seq_len, T - s0)
+        pad = int(torch.randint(0, int(n * max_pad_frac) + 1, (1,), generator=g))
+        if pad:
+            mask[s0 + n - pad:s0 + n] = 0
+    return mask.to(device)

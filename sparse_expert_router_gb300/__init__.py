@@ -123,10 +123,12 @@ def moe_route(cfg, x, w_router, b_router, topk_idx, topk_gate, ws, stream=None):
 
 
 def moe_permute(cfg, x, w_down, rms_gamma, topk_idx, expert_counts, expert_offsets, perm,
-                slot_of, n_dropped, x_perm, ws, stream=None, fp8=None):
-    """``fp8``: dict of moe_fp8_t fields (x_scale, optional x_amax) for an fp8-expert layer."""
+                slot_of, n_dropped, x_perm, ws, stream=None, fp8=None, token_mask=None):
+    """``fp8``: dict of moe_fp8_t fields (x_scale, optional x_amax) for an fp8-expert layer.
+    ``token_mask``: [T] uint8, 0 for attention-mask padding (not dispatched), or None."""
     _check("moe_permute", load().moe_permute(
-        C.byref(cfg.c()), _p(x), _p(w_down), _p(rms_gamma), _p(topk_idx), _p(expert_counts),
+        C.byref(cfg.c()), _p(x), _p(w_down), _p(rms_gamma), _p(topk_idx), _p(token_mask),
+        _p(expert_counts),
         _p(expert_offsets), _p(perm), _p(slot_of), _p(n_dropped), _p(x_perm), _fp8(fp8), _p(ws),
         ws.numel(), _stream(stream)))
 
@@ -150,7 +152,8 @@ def moe_combine(cfg, y_perm, slot_of, topk_gate, out, ws, a_shared=None, w_up=No
 def moe_forward(cfg, weights: Dict[str, torch.Tensor], x, y, ws, stream=None,
                 aux: Optional[Dict[str, object]] = None):
     """y = layer(x). ``aux`` may map topk_idx / topk_gate / expert_counts / expert_offsets /
-    slot_of / n_dropped to device tensors, and stage_events to MOE_FORWARD_STAGES + 1
+    slot_of / n_dropped to device tensors, token_mask to a [T] uint8 input (0 = padding, not
+    dispatched), and stage_events to MOE_FORWARD_STAGES + 1
     torch.cuda.Event objects (created with enable_timing=True). For an fp8-expert layer
     ``weights`` also holds w1_scale, w3_scale, w2_scale, x_scale and h_scale, and ``aux`` may
     map x_amax / h_amax to [1] fp32 device tensors."""
@@ -166,7 +169,7 @@ def moe_forward(cfg, weights: Dict[str, torch.Tensor], x, y, ws, stream=None,
     if aux:
         fields = {n: (aux[n].data_ptr() if aux.get(n) is not None else None)
                   for n in ("topk_idx", "topk_gate", "expert_counts", "expert_offsets",
-                            "slot_of", "n_dropped")}
+                            "slot_of", "n_dropped", "token_mask")}
         if aux.get("stage_events") is not None:
             evs = aux["stage_events"]
             keep = (C.c_void_p * len(evs))(*[e.cuda_event for e in evs])

@@ -51,7 +51,7 @@ class moe_weights_t(C.Structure):
 class moe_forward_aux_t(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("topk_idx", "topk_gate", "expert_counts",
                                           "expert_offsets", "slot_of", "n_dropped",
-                                          "stage_events")]
+                                          "stage_events", "token_mask")]
 
 
 class moe_device_report_t(C.Structure):
@@ -69,7 +69,7 @@ SIGNATURES = {
     "moe_last_cuda_error": (C.c_int32, [C.POINTER(C.c_char_p)]),
     "moe_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
     "moe_route": (C.c_int, [CFG, P, P, P, P, P, P, C.c_size_t, P]),
-    "moe_permute": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, C.POINTER(moe_fp8_t), P,
+    "moe_permute": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.POINTER(moe_fp8_t), P,
                               C.c_size_t, P]),
     "moe_expert_ffn": (C.c_int, [CFG, P, P, P, P, P, C.POINTER(moe_fp8_t), P, P, P, P, P, P,
                                  C.c_size_t, P]),

@@ -358,12 +358,14 @@ GemmProblem back_problem(const Call& k, const void* c_buf, const void* w_up, con
   return p;
 }
 
-DispatchArgs dispatch_args(const Call& k, const int32_t* idx, const float* gamma,
+DispatchArgs dispatch_args(const Call& k, const int32_t* idx, const uint8_t* mask,
+                           const float* gamma,
                            int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* slot_of,
                            int32_t* n_dropped, void* x_perm, const moe_fp8_t* f8) {
   const moe_config_t& c = k.c;
   DispatchArgs a{};
   a.idx = idx;
+  a.mask = mask;
   a.T = c.T;
   a.k = c.top_k;
   a.E = c.n_experts;
@@ -524,7 +526,8 @@ cudaError_t copy_amax(float* dst, const uint32_t* src, cudaStream_t st) {
 }
 
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_down,
-                         const float* rms_gamma, const int32_t* topk_idx, int32_t* expert_counts,
+                         const float* rms_gamma, const int32_t* topk_idx,
+                         const uint8_t* token_mask, int32_t* expert_counts,
                          int32_t* expert_offsets, int32_t* perm, int32_t* slot_of,
                          int32_t* n_dropped, void* x_perm, const moe_fp8_t* fp8, void* ws,
                          size_t ws_bytes, void* stream) {
@@ -542,8 +545,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const void* w_d
   if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
   if (f8) MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false, 1));
   MOE_TRY_CUDA(run_gemms(k, &p, 1));
-  DispatchArgs da = dispatch_args(k, topk_idx, rms_gamma, expert_counts, expert_offsets, perm,
-                                  slot_of, n_dropped, x_perm, fp8);
+  DispatchArgs da = dispatch_args(k, topk_idx, token_mask, rms_gamma, expert_counts,
+                                  expert_offsets, perm, slot_of, n_dropped, x_perm, fp8);
   MOE_TRY_CUDA(dispatch_run(da, cfg->dtype, k.st, k.pdl));
   if (f8) MOE_TRY_CUDA(copy_amax(fp8->x_amax, &k.hdr()->amax_x, k.st));
   return MOE_OK;
@@ -652,7 +655,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   if ((s = check_tc(k, &back, 1)) != MOE_OK) return s;
 
   RouterArgs ra = router_args(k, x, w->w_router, w->b_router, idx, gate);
-  DispatchArgs da = dispatch_args(k, idx, w->rms_gamma, k.at<int32_t>(L.counts), offsets,
+  DispatchArgs da = dispatch_args(k, idx, aux ? aux->token_mask : nullptr, w->rms_gamma,
+                                  k.at<int32_t>(L.counts), offsets,
                                   k.at<int32_t>(L.perm), slot_of, k.at<int32_t>(L.ndrop),
                                   k.at<void>(L.x_perm), w->fp8);
   CombineArgs ca = combine_args(k, k.at<void>(L.y_perm), slot_of, gate, k.at<void>(L.c));

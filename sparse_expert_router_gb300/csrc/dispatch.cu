@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(CH) hist_kernel(DispatchArgs a) {
   for (int e = threadIdx.x; e < a.E; e += CH) s_cnt[e] = 0;
   __syncthreads();
   int64_t t = (int64_t)blockIdx.x * CH + threadIdx.x;
-  if (t < a.T) {
+  if (t < a.T && (!a.mask || a.mask[t])) {   // padding tokens are not dispatched
     const int32_t* row = a.idx + t * a.k;
     for (int j = 0; j < a.k; ++j) {
       if (valid_assignment(row, j, a.E)) atomicAdd(&s_cnt[row[j]], 1);
@@ -148,14 +148,15 @@ __global__ void __launch_bounds__(CH) rank_kernel(DispatchArgs a) {
   const int tl = threadIdx.x;
   const int64_t t = (int64_t)blockIdx.x * CH + tl;
   const int32_t* row = a.idx + t * a.k;
-  if (t < a.T)
+  const bool real = t < a.T && (!a.mask || a.mask[t]);
+  if (real)
     for (int j = 0; j < a.k; ++j)
       if (valid_assignment(row, j, a.E)) atomicOr(&s_mask[row[j] * W + (tl >> 5)], 1u << (tl & 31));
   __syncthreads();
   if (t >= a.T) return;
   for (int j = 0; j < a.k; ++j) {
     int32_t slot = -1;
-    if (valid_assignment(row, j, a.E)) {
+    if (real && valid_assignment(row, j, a.E)) {
       const int e = row[j];
       int r = __popc(s_mask[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u));
       for (int w = 0; w < (tl >> 5); ++w) r += __popc(s_mask[e * W + w]);

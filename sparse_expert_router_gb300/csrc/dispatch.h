@@ -7,6 +7,7 @@ namespace moe {
 
 struct DispatchArgs {
   const int32_t* idx;     // [T, k] ascending expert ids
+  const uint8_t* mask;    // [T] or NULL: 0 = attention-mask padding, not dispatched
   int64_t T;
   int k, E, L;
   int cap;                // capacity, -1 = none

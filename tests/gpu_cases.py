@@ -23,7 +23,7 @@ def gpu_inputs(shape):
     return {k: v.to(DEV) for k, v in make_layer_inputs(shape, "cpu").items()}
 
 
-def run_forward(shape, inp, flags=0):
+def run_forward(shape, inp, flags=0, token_mask=None):
     cfg = m.LayerConfig.from_shape(shape, flags=flags)
     T, k, E = shape.T, shape.top_k, shape.n_experts
     out = {
@@ -39,7 +39,10 @@ def run_forward(shape, inp, flags=0):
         out["x_amax"] = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
         out["h_amax"] = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)
     ws = m.alloc_workspace(cfg, DEV)
-    m.moe_forward(cfg, inp, inp["x"], out["y"], ws, aux={n: out[n] for n in out if n != "y"})
+    aux = {n: out[n] for n in out if n != "y"}
+    if token_mask is not None:
+        aux["token_mask"] = token_mask.to(DEV)
+    m.moe_forward(cfg, inp, inp["x"], out["y"], ws, aux=aux)
     out["report"] = m.moe_get_device_status(ws)
     out["ws"] = ws
     return out

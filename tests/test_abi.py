@@ -90,8 +90,8 @@ def test_argument_errors_before_any_launch(lib):
     # workspace too small / misaligned
     assert lib.moe_route(c, good, good, None, good, good, ws, n - 256, None) == L.MOE_ERR_WORKSPACE
     assert lib.moe_route(c, good, good, None, good, good, P(0x100080), n, None) == L.MOE_ERR_ALIGNMENT
-    assert lib.moe_permute(c, good, good, good, good, good, good, good, good, None, None, None,
-                           ws, n, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(c, good, good, good, good, None, good, good, good, None, None, None,
+                           None, ws, n, None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_expert_ffn(c, good, good, good, good, None, None, good, None, None, None, None,
                               ws, n, None) == L.MOE_ERR_INVALID_ARG
     # shared experts requested without their weights
@@ -106,7 +106,7 @@ def test_argument_errors_before_any_launch(lib):
     part = L.moe_fp8_t(w1_scale=0x10000, w3_scale=0x10000, w2_scale=0x10000, x_scale=0x10000)
     assert lib.moe_expert_ffn(cc8, good, good, good, good, good, C.byref(part), good, None, None,
                               None, None, ws, n8, None) == L.MOE_ERR_INVALID_ARG   # no h_scale
-    assert lib.moe_permute(cc8, good, good, good, good, good, good, good, good, None, good,
+    assert lib.moe_permute(cc8, good, good, good, good, None, good, good, good, good, None, good,
                            C.byref(L.moe_fp8_t()), ws, n8, None) == L.MOE_ERR_INVALID_ARG
     w8 = L.moe_weights_t(w_router=0x10000, w_down=0x10000, rms_gamma=0x10000, w1=0x10000,
                          w3=0x10000, w2=0x10000, w1_s=0x10000, w3_s=0x10000, w2_s=0x10000,

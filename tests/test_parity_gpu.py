@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import sparse_expert_router_gb300 as m
-from moe_workloads import SHAPES, SLICE_C5B, make_layer_inputs, make_slice_inputs
+from moe_workloads import SHAPES, SLICE_C5B, make_layer_inputs, make_slice_inputs, padding_mask
 from oracle import moe_oracle
 
 from gpu_cases import (DEV, check_routing, e4m3_codes_match, gpu_inputs, normwise, oracle_forward,
@@ -489,3 +489,54 @@ def test_fp8_close_to_bf16_layer():
     assert torch.equal(a["expert_offsets"], b["expert_offsets"])
     err = normwise(a["y"], b["y"])
     assert 1e-3 < err <= 0.1, err
+
+
+# --------------------------------------------------------- attention-mask padding ----
+
+@pytest.mark.parametrize("cap", [None, (1, 2)], ids=["nocap", "cf050"])
+def test_token_mask_tiny_f32(cap):
+    """Padding tokens excluded from dispatch: every output against the oracle, and moe_permute
+    with the same mask writes the same slots."""
+    shape = SHAPES["tiny_f32"].with_(capacity=cap)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    mask = padding_mask(shape.T, seq_len=32, seed=1)
+    assert 0 < int(mask.sum()) < shape.T
+    got = run_forward(shape, inp, token_mask=mask)
+    ref = oracle_forward(shape, dict(cpu, token_mask=mask))
+    check_routing(got, ref, shape)
+    assert bool((got["slot_of"].cpu()[mask == 0] == -1).all())
+    err = normwise(got["y"], ref["y"])
+    assert err <= 1e-5, err
+    assert got["report"]["status"] == 0
+    # the split call with the mask
+    T, k, E, L = shape.T, shape.top_k, shape.n_experts, shape.d_latent
+    cfg = m.LayerConfig.from_shape(shape)
+    ws = m.alloc_workspace(cfg, DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    slot = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ndrop = torch.empty(1, dtype=torch.int32, device=DEV)
+    x_perm = torch.zeros((T * k, L), dtype=torch.float32, device=DEV)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"],
+                  ref["idx"].to(torch.int32).to(DEV), counts, offs, perm, slot, ndrop, x_perm, ws,
+                  token_mask=mask.to(DEV))
+    assert torch.equal(slot.cpu().long(), ref["slot_of"])
+    assert torch.equal(counts.cpu().long(), ref["counts"])
+    assert int(ndrop.cpu()) == int(ref["n_dropped"])
+
+
+def test_token_mask_small_bf16():
+    shape = SHAPES["small_bf16"].with_(T=2048, capacity=(11, 10))
+    inp = gpu_inputs(shape)
+    mask = padding_mask(shape.T, seq_len=256, seed=2)
+    got = run_forward(shape, inp, token_mask=mask)
+    pads = (mask == 0).nonzero().flatten()[:6].tolist()
+    toks = sample_tokens(shape.T, 96, extra=pads)
+    ref = oracle_forward(shape, dict({k: v.cpu() for k, v in inp.items()}, token_mask=mask),
+                         tokens=toks)
+    check_routing(got, ref, shape)
+    err = normwise(got["y"][toks], ref["y"])
+    assert err <= 2e-2, err
+    assert got["report"]["status"] == 0
