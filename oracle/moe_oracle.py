@@ -398,6 +398,60 @@ def combine(y_perm: torch.Tensor, slot_of: torch.Tensor, gate: torch.Tensor) -> 
     return c
 
 
+# -------------------------------------------------------- expert MLP backward ----
+#
+# The July summary (#5330, the Grug MoE microbenchmark) moves the backward of the ragged dot to a
+# custom VJP: the input gradient is a grouped GEMM against the transposed expert weights, and the
+# weight gradient a GEMM that contracts over each expert's ragged rows. Written out for the
+# SwiGLU expert MLP y = (silu(x W1) * (x W3)) W2 by the chain rule.
+
+def silu_grad(v: torch.Tensor) -> torch.Tensor:
+    """d silu(v) / dv = s (1 + v (1 - s)) with s = 1 / (1 + e^-v), fp64."""
+    s = 1.0 / (1.0 + torch.exp(-v))
+    return s * (1.0 + v * (1.0 - s))
+
+
+def grouped_experts_backward(rows: torch.Tensor, offsets: Sequence[int], w1: torch.Tensor,
+                             w3: torch.Tensor, w2: torch.Tensor, dy: torch.Tensor
+                             ) -> Dict[str, torch.Tensor]:
+    """Gradients of the grouped expert MLP (grouped_experts) given dy = dL/dy_perm.
+
+    For expert e with rows X = rows[offsets[e]:offsets[e+1]], G = X W1_e, U = X W3_e,
+    A = silu(G) * U (the forward's hidden) and Y = A W2_e:
+      dA = dY W2_e^T,  dG = dA * U * silu'(G),  dU = dA * silu(G),
+      dX = dG W1_e^T + dU W3_e^T,
+      dW1_e = X^T dG,  dW3_e = X^T dU,  dW2_e = A^T dY.
+    Experts without rows get zero weight gradients; rows past offsets[-1] get no dX. All fp64.
+    Returns dx [n_active, L], dw1, dw3 [E, L, F], dw2 [E, F, L] and the intermediates
+    g, u, a, da, dg, du [n_active, F]."""
+    x64, dy64 = to64(rows), to64(dy)
+    n_act = int(offsets[-1])
+    E, L, F = w1.shape
+    out = {"dx": torch.zeros((n_act, L), dtype=F64),
+           "dw1": torch.zeros((E, L, F), dtype=F64), "dw3": torch.zeros((E, L, F), dtype=F64),
+           "dw2": torch.zeros((E, F, w2.shape[2]), dtype=F64)}
+    for n in ("g", "u", "a", "da", "dg", "du"):
+        out[n] = torch.zeros((n_act, F), dtype=F64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi <= lo:
+            continue
+        X, dY = x64[lo:hi], dy64[lo:hi]
+        W1, W3, W2 = to64(w1[e]), to64(w3[e]), to64(w2[e])
+        G, U = X @ W1, X @ W3
+        A = silu(G) * U
+        dA = dY @ W2.T
+        dG = dA * U * silu_grad(G)
+        dU = dA * silu(G)
+        out["dx"][lo:hi] = dG @ W1.T + dU @ W3.T
+        out["dw1"][e] = X.T @ dG
+        out["dw3"][e] = X.T @ dU
+        out["dw2"][e] = A.T @ dY
+        for n, v in (("g", G), ("u", U), ("a", A), ("da", dA), ("dg", dG), ("du", dU)):
+            out[n][lo:hi] = v
+    return out
+
+
 # --------------------------------------------------------------- forward ----
 
 def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,

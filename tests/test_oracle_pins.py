@@ -430,7 +430,71 @@ def pin_mask_frees_capacity():
     assert int(d["n_dropped"]) == 1
 
 
-ALL_PINS = [pin_mask_all_ones_is_no_mask, pin_mask_padding_keeps_shared_only,
+def _tiny_grouped(seed=5, E=3, L=6, F=5, counts=(3, 0, 4)):
+    g = torch.Generator().manual_seed(seed)
+    R = sum(counts)
+    rows = torch.randn(R, L, generator=g, dtype=F64)
+    w1 = torch.randn(E, L, F, generator=g, dtype=F64) * 0.5
+    w3 = torch.randn(E, L, F, generator=g, dtype=F64) * 0.5
+    w2 = torch.randn(E, F, L, generator=g, dtype=F64) * 0.5
+    dy = torch.randn(R, L, generator=g, dtype=F64)
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    return rows, offs, w1, w3, w2, dy
+
+
+def pin_expert_backward_autograd():
+    """The hand-written chain rule against torch.autograd of the SwiGLU expert definition
+    y = (silu(x W1) * (x W3)) W2 per group: input and every weight gradient, an expert with no
+    rows included. (The oracle's forward promotes without autograd; the finite-difference pin
+    uses it as a black box.)"""
+    rows, offs, w1, w3, w2, dy = _tiny_grouped()
+    leaves = [t.clone().requires_grad_(True) for t in (rows, w1, w3, w2)]
+    parts = []
+    for e in range(len(offs) - 1):
+        X = leaves[0][offs[e]:offs[e + 1]]
+        parts.append((torch.nn.functional.silu(X @ leaves[1][e]) * (X @ leaves[2][e])) @ leaves[3][e])
+    (torch.cat(parts) * dy).sum().backward()
+    got = O.grouped_experts_backward(rows, offs, w1, w3, w2, dy)
+    for name, leaf in zip(("dx", "dw1", "dw3", "dw2"), leaves):
+        assert torch.allclose(got[name], leaf.grad, rtol=1e-12, atol=1e-12), name
+    assert float(got["dw1"][1].abs().max()) == 0.0 and float(got["dw2"][1].abs().max()) == 0.0
+
+
+def pin_expert_backward_finite_differences():
+    """Central differences of <dy, y_perm> in fp64 for sampled entries of every gradient."""
+    rows, offs, w1, w3, w2, dy = _tiny_grouped(seed=9, counts=(2, 5, 1))
+    got = O.grouped_experts_backward(rows, offs, w1, w3, w2, dy)
+
+    def loss(r, a, b, c):
+        return float((O.grouped_experts(r, offs, a, b, c)[1] * dy).sum())
+    h = 1e-6
+    args = [rows, w1, w3, w2]
+    for ai, name, index in ((0, "dx", (4, 2)), (1, "dw1", (1, 3, 2)), (2, "dw3", (2, 0, 4)),
+                            (3, "dw2", (0, 1, 5)), (3, "dw2", (2, 4, 0))):
+        plus = [t.clone() for t in args]
+        minus = [t.clone() for t in args]
+        plus[ai][index] += h
+        minus[ai][index] -= h
+        fd = (loss(*plus) - loss(*minus)) / (2 * h)
+        assert abs(fd - float(got[name][index])) <= 1e-6 * (1 + abs(fd)), (name, fd)
+
+
+def pin_silu_grad_closed_form():
+    """silu'(0) = 1/2; silu'(v) -> 1 for large v and -> 0 for very negative v; against the
+    derivative of v / (1 + e^-v) by central differences."""
+    v = torch.tensor([0.0, 30.0, -40.0, 1.3, -2.7], dtype=F64)
+    d = O.silu_grad(v)
+    assert float(d[0]) == 0.5
+    assert abs(float(d[1]) - 1.0) < 1e-11 and abs(float(d[2])) < 1e-15
+    h = 1e-6
+    fd = (O.silu(v[3:] + h) - O.silu(v[3:] - h)) / (2 * h)
+    assert torch.allclose(d[3:], fd, rtol=0, atol=1e-9)
+
+
+ALL_PINS = [pin_expert_backward_autograd, pin_expert_backward_finite_differences,
+            pin_silu_grad_closed_form, pin_mask_all_ones_is_no_mask, pin_mask_padding_keeps_shared_only,
             pin_mask_frees_capacity, pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
             pin_fp8_layer_grid, pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
             pin_capacity, pin_dispatch_golden, pin_dispatch_invariants, pin_forced_single_expert,
@@ -543,6 +607,36 @@ def _mut_mask_counts_padding(monkeypatch):
     monkeypatch.setattr(O, "dispatch", bad)
 
 
+def _mut_silu_grad_no_inner(monkeypatch):
+    monkeypatch.setattr(O, "silu_grad", lambda v: 1.0 / (1.0 + torch.exp(-v)))
+
+
+def _mut_backward_dw2_from_g(monkeypatch):
+    orig = O.grouped_experts_backward
+
+    def bad(rows, offsets, w1, w3, w2, dy):
+        out = orig(rows, offsets, w1, w3, w2, dy)
+        for e in range(len(offsets) - 1):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                out["dw2"][e] = out["g"][lo:hi].T @ O.to64(dy)[lo:hi]
+        return out
+    monkeypatch.setattr(O, "grouped_experts_backward", bad)
+
+
+def _mut_backward_dx_no_w3(monkeypatch):
+    orig = O.grouped_experts_backward
+
+    def bad(rows, offsets, w1, w3, w2, dy):
+        out = orig(rows, offsets, w1, w3, w2, dy)
+        for e in range(len(offsets) - 1):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                out["dx"][lo:hi] = out["dg"][lo:hi] @ O.to64(w1[e]).T
+        return out
+    monkeypatch.setattr(O, "grouped_experts_backward", bad)
+
+
 def _mut_unstable_perm(monkeypatch):
     orig = O.dispatch
 
@@ -571,6 +665,7 @@ MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mu
              _mut_rms_sum, _mut_full_softmax, _mut_renorm_after_drop, _mut_forward_renorm, _mut_fp8_scale_ignored, _mut_e4m3_ties_away,
              _mut_fp8_no_activation_rounding, _mut_fp8_dequant_by_scale,
              _mut_fp8_quantize_in_fp64, _mut_mask_ignored, _mut_mask_counts_padding,
+             _mut_silu_grad_no_inner, _mut_backward_dw2_from_g, _mut_backward_dx_no_w3,
              _mut_unstable_perm,
              _mut_transposed_up]
 
