@@ -236,6 +236,27 @@ MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
                                     const void* x, const void* w1_s, const void* w3_s,
                                     void* a_shared, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of workspace moe_expert_ffn_backward needs (256-byte aligned device memory owned by the
+ * caller, zero-filled before its first use like the forward's; it starts with the same device
+ * report, read with moe_get_device_status). */
+MOE_API moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Backward of moe_expert_ffn's routed experts, given dy_perm = dL/dy_perm [pool_rows, L]: with
+ * G = x W1_e, U = x W3_e and A = silu(G) * U for the rows of expert e (recomputed here),
+ *   dA = dy W2_e^T, dG = dA * U * silu'(G), dU = dA * silu(G),
+ *   dx_perm = dG W1_e^T + dU W3_e^T            [pool_rows, L] (rows past expert_offsets[E] untouched),
+ *   dw1[e] = x^T dG, dw3[e] = x^T dU            [E, L, F], dw2[e] = A^T dy  [E, F, L]
+ * (experts with no rows get zero gradients). This is the custom VJP of the ragged dot in the
+ * Marin summary of the week of 2026-07-06 (#5330): the input gradient is a grouped GEMM against
+ * the transposed expert weights, the weight gradients contract over each expert's ragged rows.
+ * bf16 layers on the tensor-core path only (else MOE_ERR_UNSUPPORTED); d_latent and d_ff must
+ * be multiples of 128 (else MOE_ERR_ALIGNMENT). All outputs bf16 with fp32 accumulation. */
+MOE_API moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm,
+                                             const int32_t* expert_offsets, const void* w1,
+                                             const void* w3, const void* w2, const void* dy_perm,
+                                             void* dx_perm, void* dw1, void* dw3, void* dw2,
+                                             void* ws, size_t ws_bytes, void* stream);
+
 /* Combine: c[t] = sum over j with slot_of[t, j] >= 0, in order j = 0..k-1, of
  * topk_gate[t, j] * y_perm[slot_of[t, j]] (fp32 accumulation). When w_up is NULL, out [T, L]
  * receives c (the gate-weighted un-permute back to arrival order, e.g. of one expert-parallel

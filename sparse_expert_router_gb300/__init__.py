@@ -20,6 +20,7 @@ from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_FP8_EXPERTS, MOE_FLAG_PDL, MOE_FL
 
 __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+           "backward_workspace_size", "alloc_backward_workspace", "moe_expert_ffn_backward",
            "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
            "moe_selftest_device_timeout",
            "MOE_FLAG_PDL", "MOE_FLAG_SIMT", "MOE_FLAG_FP8_EXPERTS",
@@ -140,6 +141,25 @@ def moe_expert_ffn(cfg, x_perm, expert_offsets, w1, w3, w2, y_perm, x=None, w1_s
         C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _fp8(fp8),
         _p(y_perm), _p(x), _p(w1_s), _p(w3_s), _p(a_shared), _p(ws), ws.numel(),
         _stream(stream)))
+
+
+def backward_workspace_size(cfg: LayerConfig) -> int:
+    n = C.c_size_t(0)
+    _check("moe_backward_workspace_size",
+           load().moe_backward_workspace_size(C.byref(cfg.c()), C.byref(n)))
+    return n.value
+
+
+def alloc_backward_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of moe_expert_ffn_backward."""
+    return torch.zeros(backward_workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def moe_expert_ffn_backward(cfg, x_perm, expert_offsets, w1, w3, w2, dy_perm, dx_perm, dw1, dw3,
+                            dw2, ws, stream=None):
+    _check("moe_expert_ffn_backward", load().moe_expert_ffn_backward(
+        C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _p(dy_perm),
+        _p(dx_perm), _p(dw1), _p(dw3), _p(dw2), _p(ws), ws.numel(), _stream(stream)))
 
 
 def moe_combine(cfg, y_perm, slot_of, topk_gate, out, ws, a_shared=None, w_up=None, w2_s=None,

@@ -74,6 +74,8 @@ SIGNATURES = {
     "moe_expert_ffn": (C.c_int, [CFG, P, P, P, P, P, C.POINTER(moe_fp8_t), P, P, P, P, P, P,
                                  C.c_size_t, P]),
     "moe_combine": (C.c_int, [CFG, P, P, P, P, P, P, P, P, C.c_size_t, P]),
+    "moe_backward_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
+    "moe_expert_ffn_backward": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_forward": (C.c_int, [CFG, C.POINTER(moe_weights_t), P, P, P, C.c_size_t, P,
                               C.POINTER(moe_forward_aux_t)]),
     "moe_get_device_status": (C.c_int, [P, C.c_size_t, P, C.POINTER(moe_device_report_t)]),

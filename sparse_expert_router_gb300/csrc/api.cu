@@ -6,6 +6,7 @@
 #include "dispatch.h"
 #include "gemm.h"
 #include "router.h"
+#include "wgrad.h"
 
 using namespace moe;
 
@@ -67,6 +68,31 @@ Layout make_layout(const moe_config_t& c) {
   L.y_perm = take(P * Lt * es);
   L.a_s = take(T * (SF > 0 ? SF : 1) * es);
   L.c = take(T * Lt * es);
+  L.total = off;
+  return L;
+}
+
+// Workspace of moe_expert_ffn_backward: the device report, then the recomputed G = X W1,
+// U = X W3 and A = silu(G) U and the gradients dG, dU, each [pool_rows, F] bf16.
+struct BwdLayout {
+  size_t hdr, g, u, a, dg, du, total;
+};
+
+BwdLayout make_bwd_layout(const moe_config_t& c) {
+  BwdLayout L{};
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    size_t o = off;
+    off = al256(off + (size_t)bytes);
+    return o;
+  };
+  const int64_t PF = pool_rows_of(c) * (int64_t)c.d_ff * 2;
+  L.hdr = take(sizeof(DeviceHeader));
+  L.g = take(PF);
+  L.u = take(PF);
+  L.a = take(PF);
+  L.dg = take(PF);
+  L.du = take(PF);
   L.total = off;
   return L;
 }
@@ -587,6 +613,120 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
   }
   MOE_TRY_CUDA(run_gemms(k, &down, 1));
   if (f8) MOE_TRY_CUDA(copy_amax(fp8->h_amax, &k.hdr()->amax_h, k.st));
+  return MOE_OK;
+}
+
+moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm,
+                                     const int32_t* expert_offsets, const void* w1,
+                                     const void* w3, const void* w2, const void* dy_perm,
+                                     void* dx_perm, void* dw1, void* dw3, void* dw2, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptrs({x_perm, expert_offsets, w1, w3, w2, dy_perm, dx_perm, dw1, dw3, dw2},
+                      {})) != MOE_OK)
+    return s;
+  // tensor cores, bf16 and 128-multiple widths (the weight-gradient tiles are 128 x 64 aligned)
+  if (cfg->dtype != MOE_BF16 || (cfg->flags & (MOE_FLAG_SIMT | MOE_FLAG_FP8_EXPERTS)))
+    return MOE_ERR_UNSUPPORTED;
+  if ((cfg->d_latent % 128) || (cfg->d_ff % 128)) return MOE_ERR_ALIGNMENT;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((uintptr_t)ws & 255u) return MOE_ERR_ALIGNMENT;
+  const BwdLayout B = make_bwd_layout(*cfg);
+  if (ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+  Call k = make_call(cfg, ws, stream);
+  k.L.hdr = B.hdr;                                   // the report sits at the same place
+  auto at = [&](size_t off) { return static_cast<void*>(k.ws + off); };
+  const int64_t P = pool_rows_of(*cfg);
+  const int E = cfg->n_experts, L = cfg->d_latent, F = cfg->d_ff;
+
+  // 1. recompute G, U and A = silu(G) U over the grouped rows
+  GemmProblem rec;
+  rec.epi = EPI_SWIGLU_SAVE;
+  rec.group = GROUP_ROWS;
+  rec.M = F;
+  rec.seg[0] = {x_perm, w1, w3, L};
+  rec.offsets = expert_offsets;
+  rec.G = E;
+  rec.rows = P;
+  rec.out = at(B.a);
+  rec.out2 = at(B.g);
+  rec.out3 = at(B.u);
+  rec.ld_out = F;
+  rec.dtype = DT_BF16;
+  // 2. dA = dY W2^T, then dG = dA U silu'(G), dU = dA silu(G) in the epilogue
+  GemmProblem da;
+  da.epi = EPI_SWIGLU_BWD;
+  da.group = GROUP_ROWS;
+  da.M = F;
+  da.seg[0] = {dy_perm, w2, nullptr, L};
+  da.a_kmajor = 1;
+  da.offsets = expert_offsets;
+  da.G = E;
+  da.rows = P;
+  da.out = at(B.dg);
+  da.out2 = at(B.du);
+  da.ld_out = F;
+  da.aux_g = at(B.g);
+  da.aux_u = at(B.u);
+  da.ld_aux = F;
+  da.dtype = DT_BF16;
+  // 3. dX = dG W1^T + dU W3^T
+  GemmProblem dx;
+  dx.epi = EPI_STORE;
+  dx.group = GROUP_ROWS;
+  dx.M = L;
+  dx.n_seg = 2;
+  dx.seg[0] = {at(B.dg), w1, nullptr, F};
+  dx.seg[1] = {at(B.du), w3, nullptr, F};
+  dx.a_kmajor = 1;
+  dx.offsets = expert_offsets;
+  dx.G = E;
+  dx.rows = P;
+  dx.out = dx_perm;
+  dx.ld_out = L;
+  dx.dtype = DT_BF16;
+  // 4. dW2 = A^T dY; dW1 = X^T dG, dW3 = X^T dU, contracting over each expert's rows
+  WgradProblem w2g;
+  w2g.a = at(B.a);
+  w2g.b = dy_perm;
+  w2g.offsets = expert_offsets;
+  w2g.G = E;
+  w2g.M = F;
+  w2g.N = L;
+  w2g.rows = P;
+  w2g.out = dw2;
+  WgradProblem w13[2];
+  w13[0].a = x_perm;
+  w13[0].b = at(B.dg);
+  w13[0].offsets = expert_offsets;
+  w13[0].G = E;
+  w13[0].M = L;
+  w13[0].N = F;
+  w13[0].rows = P;
+  w13[0].out = dw1;
+  w13[1] = w13[0];
+  w13[1].b = at(B.du);
+  w13[1].out = dw3;
+  if (!gemm_tc_supported(rec) || !gemm_tc_supported(da) || !gemm_tc_supported(dx) ||
+      !gemm_wgrad_supported(w2g) || !gemm_wgrad_supported(w13[0]))
+    return MOE_ERR_UNSUPPORTED;
+
+  MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false));
+  MOE_TRY_CUDA(validate_offsets(expert_offsets, E, P, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&rec, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&da, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&dx, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(&w2g, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(w13, 2, k.hdr(), k.st, k.pdl));
   return MOE_OK;
 }
 

@@ -14,12 +14,17 @@
 
 namespace moe {
 
-enum Epi { EPI_F32 = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
+// EPI_SWIGLU_SAVE: as EPI_SWIGLU, and also stores both pre-activations (out2 = x W, out3 = x W3).
+// EPI_SWIGLU_BWD: acc = dA (the hidden's gradient); with G, U of the same rows read from aux_g,
+// aux_u: out = dA * U * silu'(G), out2 = dA * silu(G).
+enum Epi { EPI_F32 = 0, EPI_STORE = 1, EPI_SWIGLU = 2, EPI_SWIGLU_SAVE = 3, EPI_SWIGLU_BWD = 4 };
 enum GroupMode { GROUP_NONE = 0, GROUP_ROWS = 1, GROUP_COLS = 2 };
 
 struct GemmSeg {
   const void* act;   // [rows, K] row-major (leading dimension K)
-  const void* w;     // NONE: [K, M]; ROWS: [G, K, M]; COLS: [M / Mg, K, Mg]
+  // NONE: [K, M]; ROWS: [G, K, M]; COLS: [M / Mg, K, Mg]. With a_kmajor the bank holds the
+  // transposed matrices, [M, K] per weight group (a stored [d_in, d_out] weight used as W^T).
+  const void* w;
   const void* w3;    // EPI_SWIGLU: the up-projection weights, same layout as w
   int K;
 };
@@ -56,6 +61,15 @@ struct GemmProblem {
   int out_fp8 = 0;
   const float* out_scale = nullptr;
   uint32_t* amax = nullptr;
+  // tcgen05 only, bf16: the weight operand is K-major ([M, K] per group, see GemmSeg::w)
+  int a_kmajor = 0;
+  // EPI_SWIGLU_SAVE / EPI_SWIGLU_BWD extra outputs and inputs ([rows, M] bf16, leading
+  // dimension ld_out for outputs and ld_aux for inputs)
+  void* out2 = nullptr;
+  void* out3 = nullptr;
+  const void* aux_g = nullptr;
+  const void* aux_u = nullptr;
+  int64_t ld_aux = 0;
 };
 
 // CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).

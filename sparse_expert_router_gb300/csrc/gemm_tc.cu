@@ -29,9 +29,12 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 #ifndef MOE_TC_BN
 #define MOE_TC_BN 256
@@ -48,11 +51,12 @@ constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte ro
 #define MOE_TC_EPI_WARPS 12
 #endif
 // Kernel instances: KC runs k-chunked fp32 problems (the router) with 8 epilogue warps; the
-// others (bf16 or FP8 operands) take MOE_TC_EPI_WARPS. The warps of one tensor-memory lane
+// others (bf16 or FP8 operands, and BWD: the backward's transposed weights and its SwiGLU
+// epilogues) take MOE_TC_EPI_WARPS. The warps of one tensor-memory lane
 // quadrant take alternate 16-token chunks. Keeping the instances apart keeps each one's
 // registers within what its warp count allows (three or four warps share one sub-partition's
 // 16K registers).
-template <bool FP8, bool KC> struct Inst {
+template <bool FP8, bool KC, bool BWD> struct Inst {
   static constexpr int EW = KC ? 8 : MOE_TC_EPI_WARPS;
 };
 constexpr int EPI_TILE_MAX = 16 * 32 * 4;   // transpose tile of one warp: 16 tokens x 32 fp32
@@ -65,7 +69,6 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 #endif
 constexpr int B_BOX_ROWS = MOE_TC_BBOX;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;   // 4 KB
-constexpr unsigned long long TIMEOUT_NS = 5000000000ull;
 static_assert(BN % B_BOX_ROWS == 0 && BN % 16 == 0 && BN <= 256, "token tile");
 static_assert(MOE_TC_EPI_WARPS % 4 == 0 && MOE_TC_EPI_WARPS <= 12, "epilogue warps");
 
@@ -88,6 +91,12 @@ struct TcProblem {
   int out_fp8;                 // fp8 SwiGLU output: E4M3 codes of value * out_scale[0]
   const float* out_scale;
   uint32_t* amax;              // fp8 output: running max |value| (fp32 bits)
+  int a_kmajor;                // weight tiles K-major ([M, K] per group)
+  void* out2;                  // EPI_SWIGLU_SAVE / EPI_SWIGLU_BWD second and third outputs
+  void* out3;
+  const void* aux_g;           // EPI_SWIGLU_BWD: G and U of the same rows, [rows, M] bf16
+  const void* aux_u;
+  int64_t ld_aux;
   int64_t rows;
   void* out;
   int64_t ld_out;
@@ -114,139 +123,19 @@ struct TcParams {
   DeviceHeader* hdr;
 };
 
-// ---- PTX wrappers -------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: false when the kernel is aborting (timeout here or elsewhere in the CTA).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                          DeviceHeader* hdr, int where, uint64_t limit_ns = TIMEOUT_NS) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u) {
-      if (*abort_flag) return false;
-      uint64_t now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > limit_ns) {
-        report_error(hdr, MOE_ERR_DEVICE_TIMEOUT, where);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte offsets,
-// the fixed version bits 0b001 at 46..48, 128-byte swizzle (2) at 61..63.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
 // Instruction descriptor: fp32 accumulator (bits 4..5 = 1), A and B formats at bits 7..9 and
 // 10..12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3), A MN-major (transposed, bit 15),
 // B K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-__device__ __forceinline__ uint32_t make_idesc(int n, bool fp8) {
+__device__ __forceinline__ uint32_t make_idesc(int n, bool fp8, bool a_kmajor = false) {
   const uint32_t ab = fp8 ? 0u : 1u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+  const uint32_t ta = a_kmajor ? 0u : 1u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | (ta << 15) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Problems whose items carry two weight tiles (gate and up) and two accumulators.
+__host__ __device__ __forceinline__ bool is_glu(int epi) {
+  return epi == EPI_SWIGLU || epi == EPI_SWIGLU_SAVE;
 }
 
 // ---- work decomposition -----------------------------------------------------------------
@@ -308,10 +197,10 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
 // Two instances: FP8 = false (bf16 operands, k-chunked fp32 problems) and FP8 = true (E4M3
 // operands, scales and the E4M3 SwiGLU output), so that neither carries the other's registers:
 // with 10 warps per CTA three warps share one sub-partition's 16K registers, 168 per thread.
-template <bool FP8, bool KC>
-__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
+template <bool FP8, bool KC, bool BWD>
+__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams P) {
-  constexpr int EPI_WARPS = Inst<FP8, KC>::EW;
+  constexpr int EPI_WARPS = Inst<FP8, KC, BWD>::EW;
   const int EPI_STAGE_BYTES = P.epi_tile;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
@@ -433,7 +322,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int nb = (it.nrows + B_BOX_ROWS - 1) / B_BOX_ROWS;
-      const bool two_a = (q.epi == EPI_SWIGLU) || q.dual;
+      const bool two_a = is_glu(q.epi) || q.dual;
       const uint32_t bytes = (two_a ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
@@ -444,14 +333,21 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
           if constexpr (FP8) {
             // one [128 k][128 features] box of E4M3 per A tile
             tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
-            if (q.epi == EPI_SWIGLU)
+            if (is_glu(q.epi))
               tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
             else if (q.dual)
               tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), it.m_w + BM, k0, it.wg);
+          } else if (BWD && q.a_kmajor) {
+            // one [128 features][64 k] box per A tile (K-major)
+            tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), k0, it.m_w, it.wg);
+            if (is_glu(q.epi))
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), k0, it.m_w, it.wg);
+            else if (q.dual)
+              tma_load_3d(smem_u32(sA3(stage)), &sg.a1, full(stage), k0, it.m_w + BM, it.wg);
           } else {
             tma_load_3d(smem_u32(sA1(stage)), &sg.a1, full(stage), it.m_w, k0, it.wg);
             tma_load_3d(smem_u32(sA1(stage)) + A_HALF, &sg.a1, full(stage), it.m_w + 64, k0, it.wg);
-            if (q.epi == EPI_SWIGLU) {
+            if (is_glu(q.epi)) {
               tma_load_3d(smem_u32(sA3(stage)), &sg.a3, full(stage), it.m_w, k0, it.wg);
               tma_load_3d(smem_u32(sA3(stage)) + A_HALF, &sg.a3, full(stage), it.m_w + 64, k0, it.wg);
             } else if (q.dual) {
@@ -476,9 +372,10 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
     for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      const bool sw = (q.epi == EPI_SWIGLU) || q.dual;   // second A tile -> second accumulator
+      const bool sw = is_glu(q.epi) || q.dual;   // second A tile -> second accumulator
       const int n = ((it.nrows + 15) / 16) * 16;
-      const uint32_t idesc = make_idesc(n, fp8);
+      const bool akm = BWD && q.a_kmajor;
+      const uint32_t idesc = make_idesc(n, fp8, akm);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
       const int per_ev = q.kchunk ? q.kchunk : kb_total;
@@ -510,12 +407,15 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
               accumulate = 1;
             }
           } else {
+            // K-major A tiles advance 32 bytes per k16 like B; MN-major ones 16 rows (2 KB)
+            const uint32_t astep = akm ? 32u : 2048u;
+            const uint32_t alb = akm ? 16u : albo;
 #pragma unroll
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-              mma_bf16(d_tmem, smem_desc(a1 + k16 * 2048, albo, asbo), bd, idesc, accumulate);
+              mma_bf16(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc, accumulate);
               if (sw)
-                mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * 2048, albo, asbo), bd, idesc,
+                mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * astep, alb, asbo), bd, idesc,
                          accumulate);
               accumulate = 1;
             }
@@ -537,16 +437,17 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
     unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
     float* stg_f = reinterpret_cast<float*>(stg);
     bf16* stg_h = reinterpret_cast<bf16*>(stg);
-    // Writes one 16-token x 32-feature chunk of this warp (values already final) through the
-    // transpose tile; f32 rows are 8 x 16 bytes, bf16 rows 4 x 16 bytes.
-    auto store_chunk = [&](const TcProblem& q, const Item& it, int c0, int f0, const float* v,
-                           const float* v3) {
-      const bool f32out = (q.epi == EPI_F32);
-      if (f32out) {
+    // Writes one 16-token x 32-feature chunk of this warp (values final: lane = feature,
+    // v[j] = token c0 + j) to out[row][col0 + feature] through the transpose tile, so that every
+    // lane stores whole 16-byte pieces of output rows. kind: 0 fp32, 1 bf16, 2 E4M3 (v already
+    // multiplied by its quantization scale).
+    auto store_rows = [&](void* out, int64_t ld, int col0, int kind, const Item& it, int c0,
+                          int f0, int M, const float* v) {
+      if (kind == 0) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = v[j];
-      } else if (FP8 && q.out_fp8) {
-        // v holds the scaled SwiGLU values; pairs of tokens share one conversion
+      } else if (FP8 && kind == 2) {
+        // pairs of tokens share one conversion
         uint8_t* stg_b = reinterpret_cast<uint8_t*>(stg);
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
@@ -554,45 +455,42 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
           stg_b[j * 32 + lane] = (uint8_t)(c & 0xFFu);
           stg_b[(j + 1) * 32 + lane] = (uint8_t)(c >> 8);
         }
-      } else if (q.epi == EPI_SWIGLU) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(swiglu(v[j], v3[j]));
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
       }
       __syncwarp();
       const int rows_here = min(16, it.nrows - c0);
-      if (FP8 && q.out_fp8) {
+      if (FP8 && kind == 2) {
         // 16 token rows x 32 bytes: lane -> (row lane / 2, 16-byte half lane % 2)
         const int row = lane >> 1, part = lane & 1;
-        if (f0 + part * 16 < q.M && row < rows_here) {
+        if (f0 + part * 16 < M && row < rows_here) {
           const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 32 + part * 16);
-          const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 16;
-          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(q.out) + o) = val;
+          const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 16;
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + o) = val;
         }
-      } else if (f32out) {
+      } else if (kind == 0) {
         const int part = lane & 7;
-        const bool ok = f0 + part * 4 < q.M;
+        const bool ok = f0 + part * 4 < M;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int row = (lane >> 3) + 4 * r;
           if (ok && row < rows_here) {
             const float4 val = *reinterpret_cast<const float4*>(stg_f + row * 32 + part * 4);
-            const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 4;
-            *reinterpret_cast<float4*>(static_cast<float*>(q.out) + o) = val;
+            const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 4;
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = val;
           }
         }
       } else {
         const int part = lane & 3;
-        const bool ok = f0 + part * 8 < q.M;
+        const bool ok = f0 + part * 8 < M;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int row = (lane >> 2) + 8 * r;
           if (ok && row < rows_here) {
             const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
-            const int64_t o = (it.row0 + c0 + row) * q.ld_out + q.out_col0 + f0 + part * 8;
-            *reinterpret_cast<uint4*>(static_cast<bf16*>(q.out) + o) = val;
+            const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 8;
+            *reinterpret_cast<uint4*>(static_cast<bf16*>(out) + o) = val;
           }
         }
       }
@@ -643,7 +541,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(acc[i][j], bias);
-            store_chunk(q, it, c0, f0, v, v);
+            store_rows(q.out, q.ld_out, q.out_col0, 0, it, c0, f0, q.M, v);
           }
         }
         continue;
@@ -673,7 +571,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
       for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
         float v[16], v3[16];
         tmem_ld16(lane_addr + c0, v);
-        if (q.epi == EPI_SWIGLU) tmem_ld16(lane_addr + acc2 + c0, v3);
+        if (is_glu(q.epi)) tmem_ld16(lane_addr + acc2 + c0, v3);
         tmem_wait_ld();
         if (f32out) {
 #pragma unroll
@@ -685,7 +583,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
         }
         if (FP8 && q.out_fp8) {
           // SwiGLU in fp32, running max of |hidden| over this thread's stored values, then the
-          // quantization multiplier; store_chunk rounds to E4M3
+          // quantization multiplier; store_rows rounds to E4M3
           const int valid = min(16, it.nrows - c0);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -693,8 +591,41 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC>::EW, 1)
             if (fok && j < valid) amax = fmaxf(amax, fabsf(h));
             v[j] = __fmul_rn(h, osc);
           }
+          store_rows(q.out, q.ld_out, q.out_col0, 2, it, c0, f0, q.M, v);
+          continue;
         }
-        store_chunk(q, it, c0, f0, v, v3);
+        if constexpr (BWD) {
+          if (q.epi == EPI_SWIGLU_SAVE) {
+            // the pre-activations of the backward's recompute, then the hidden below
+            store_rows(q.out2, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
+            store_rows(q.out3, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v3);
+          } else if (q.epi == EPI_SWIGLU_BWD) {
+            // v = dA; G and U of the same (row, feature): dG = dA U silu'(G), dU = dA silu(G)
+            const bf16* gp = static_cast<const bf16*>(q.aux_g);
+            const bf16* up = static_cast<const bf16*>(q.aux_u);
+            const int valid = min(16, it.nrows - c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float g = 0.0f, u = 0.0f;
+              if (fok && j < valid) {
+                const int64_t o = (it.row0 + c0 + j) * q.ld_aux + f0 + lane;
+                g = __bfloat162float(gp[o]);
+                u = __bfloat162float(up[o]);
+              }
+              const float sg = __fdiv_rn(1.0f, 1.0f + expf(-g));   // sigmoid(G)
+              v3[j] = v[j] * u * (sg * (1.0f + g * (1.0f - sg)));
+              v[j] = v[j] * (g * sg);
+            }
+            store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v3);
+            store_rows(q.out2, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
+            continue;
+          }
+        }
+        if (is_glu(q.epi)) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
+        }
+        store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
       }
       }
       tc_fence_before();
@@ -770,6 +701,19 @@ bool map_weights_fp8(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, int
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Transposed weights [G, Mw, K] (K contiguous): 3-D map with a 64 x 128 x 1 box, 128-byte swizzle
+// (one K-major tile of 128 features by 64 k).
+bool map_weights_kmajor(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, int64_t G) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Mw, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)(K * 2), (cuuint64_t)(Mw * K * 2)};
+  cuuint32_t box[3] = {BK, BM, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Activations [rows, K] (K contiguous): 2-D map with a box of one 128-byte swizzle row (64 bf16
 // or 128 E4M3) by 32 rows, 128-byte swizzle.
 bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, bool fp8) {
@@ -803,7 +747,12 @@ bool gemm_tc_supported(const GemmProblem& p) {
   if (p.n_seg < 1 || p.n_seg > 2) return false;
   for (int s = 0; s < p.n_seg; ++s)
     if (p.seg[s].K < 8 || (p.seg[s].K % 8)) return false;
-  if (p.epi != EPI_F32 && p.epi != EPI_STORE && p.epi != EPI_SWIGLU) return false;
+  if (p.epi < EPI_F32 || p.epi > EPI_SWIGLU_BWD) return false;
+  if (p.epi == EPI_SWIGLU_SAVE || p.epi == EPI_SWIGLU_BWD) {
+    if (p.w_fp8 || p.kchunk || !p.out2 || (p.epi == EPI_SWIGLU_SAVE && !p.out3)) return false;
+    if (p.epi == EPI_SWIGLU_BWD && (!p.aux_g || !p.aux_u || p.ld_aux < p.M)) return false;
+  }
+  if (p.a_kmajor && (p.w_fp8 || p.kchunk || p.group == GROUP_COLS)) return false;
   // the epilogue writes 16-byte pieces of output rows
   if ((p.M % 8) || (p.ld_out % 8) || (p.out_col0 % 8)) return false;
   if (p.kchunk < 0) return false;
@@ -850,7 +799,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     // twice the weight bytes in flight per stage
     q.kchunk = g.kchunk;
     q.bn = g.kchunk ? BN_CHUNKED : BN;
-    q.dual = (!g.kchunk && g.epi != EPI_SWIGLU && g.group != GROUP_COLS && g.M % (2 * BM) == 0)
+    q.dual = (!g.kchunk && !is_glu(g.epi) && g.group != GROUP_COLS && g.M % (2 * BM) == 0)
                  ? 1 : 0;
     if (q.dual) q.m_tiles = (int)(g.M / (2 * BM));
     q.rows = g.rows;
@@ -865,6 +814,12 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     q.w_scale = g.w_scale;
     q.w3_scale = g.w3_scale;
     q.act_scale = g.act_scale;
+    q.a_kmajor = g.a_kmajor;
+    q.out2 = g.out2;
+    q.out3 = g.out3;
+    q.aux_g = g.aux_g;
+    q.aux_u = g.aux_u;
+    q.ld_aux = g.ld_aux;
     q.out_fp8 = g.out_fp8;
     q.out_scale = g.out_scale;
     if (g.out_fp8) {
@@ -878,10 +833,11 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       TcSeg& ts = q.seg[s];
       ts.kblocks = (int)cdiv(sg.K, g.w_fp8 ? BK8 : BK);
       auto mapw = [&](CUtensorMap* m, const void* w) {
-        return g.w_fp8 ? map_weights_fp8(m, w, Mw, sg.K, Gw) : map_weights(m, w, Mw, sg.K, Gw);
+        if (g.w_fp8) return map_weights_fp8(m, w, Mw, sg.K, Gw);
+        return g.a_kmajor ? map_weights_kmajor(m, w, Mw, sg.K, Gw) : map_weights(m, w, Mw, sg.K, Gw);
       };
       if (!mapw(&ts.a1, sg.w)) return cudaErrorInvalidValue;
-      if (g.epi == EPI_SWIGLU && !mapw(&ts.a3, sg.w3)) return cudaErrorInvalidValue;
+      if (is_glu(g.epi) && !mapw(&ts.a3, sg.w3)) return cudaErrorInvalidValue;
       if (!map_act(&ts.b, sg.act, sg.K, g.rows, g.w_fp8 != 0)) return cudaErrorInvalidValue;
     }
     q.item_base = base;
@@ -892,13 +848,13 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       q.n_items = q.m_tiles * cdiv(g.rows, q.bn);
       base += q.n_items;
     }
-    if (g.epi == EPI_SWIGLU || q.dual) P.glu = 1;
+    if (is_glu(g.epi) || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
   int max_bn = 0, max_two_a_bn = 0;
   for (int j = 0; j < n_probs; ++j) {
     max_bn = max(max_bn, P.p[j].bn);
-    if (P.p[j].epi == EPI_SWIGLU || P.p[j].dual) max_two_a_bn = max(max_two_a_bn, P.p[j].bn);
+    if (is_glu(P.p[j].epi) || P.p[j].dual) max_two_a_bn = max(max_two_a_bn, P.p[j].bn);
   }
   P.nacc = (max_two_a_bn > 128) ? 1 : 2;
   P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
@@ -908,9 +864,15 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   P.epi_tile = 16 * 32 * 2;
   for (int j = 0; j < n_probs; ++j)
     if (P.p[j].epi == EPI_F32) P.epi_tile = EPI_TILE_MAX;
-  bool kc = false;
-  for (int j = 0; j < n_probs; ++j) kc = kc || P.p[j].kchunk > 0;
-  const int ew = P.fp8 ? Inst<true, false>::EW : (kc ? Inst<false, true>::EW : Inst<false, false>::EW);
+  bool kc = false, bwd = false;
+  for (int j = 0; j < n_probs; ++j) {
+    kc = kc || P.p[j].kchunk > 0;
+    bwd = bwd || P.p[j].a_kmajor || P.p[j].epi == EPI_SWIGLU_SAVE || P.p[j].epi == EPI_SWIGLU_BWD;
+  }
+  if (kc && bwd) return cudaErrorNotSupported;
+  const int ew = P.fp8 ? Inst<true, false, false>::EW
+                       : (kc ? Inst<false, true, false>::EW
+                             : (bwd ? Inst<false, false, true>::EW : Inst<false, false, false>::EW));
   const size_t epi_bytes = (size_t)ew * P.epi_tile;
   // as many stages as fit next to the epilogue tiles and the schedule (at most 8)
   {
@@ -923,8 +885,10 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024 +
                       epi_bytes + (size_t)(3 * G + 1) * 4;
-  auto kern = P.fp8 ? tc_gemm_kernel<true, false>
-                    : (kc ? tc_gemm_kernel<false, true> : tc_gemm_kernel<false, false>);
+  auto kern = P.fp8 ? tc_gemm_kernel<true, false, false>
+                    : (kc ? tc_gemm_kernel<false, true, false>
+                          : (bwd ? tc_gemm_kernel<false, false, true>
+                                 : tc_gemm_kernel<false, false, false>));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms_tc();

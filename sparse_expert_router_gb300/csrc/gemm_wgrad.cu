@@ -1,0 +1,333 @@
+// tcgen05 weight-gradient GEMM over ragged row groups, for the backward of the grouped expert
+// MLP: dW_e = X_e^T dY_e, where the contraction runs over the rows of expert e. The Marin
+// summary of the week of 2026-07-06 (#5330) describes this as the ragged-contracting-dimension
+// kernel of the ragged dot's custom VJP.
+//
+// Both operands are MN-major in shared memory: the contraction index is their row index, so a
+// stage holds 64 rows of a (two 64-feature boxes, 128 features) and of b (four 64-column boxes,
+// 256 columns). A group's rows start anywhere; its last stage may run past the group's end, so
+// the MMA warp zeroes the rows past the end in both tiles before it issues that stage's MMAs.
+//
+// Roles of the warps of a CTA (one CTA per SM, persistent over (problem, group, m tile, n tile)
+// items, n tiles fastest so the items of one group run together and share its rows in L2):
+//   warp 0: TMA producer (one thread); warp 1: TMEM allocator and MMA issuer (the whole warp
+//   zeroes tail rows, one thread issues MMAs); warps 2..9: epilogue, each thread storing 16
+//   consecutive columns of its output row as 32 contiguous bytes. Accumulators are
+//   double-buffered (2 x 256 tensor-memory columns). Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "wgrad.h"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int WM = 128;              // output rows (features of a) per item: MMA M, TMEM lanes
+constexpr int WN = 256;              // output columns per item: MMA N
+constexpr int WK = 64;               // contraction rows per stage
+constexpr int W_EPI = 8;             // epilogue warps
+constexpr int W_THREADS = 64 + 32 * W_EPI;
+constexpr int WA_HALF = 64 * WK * 2; // one [64 rows][64 features] box: 8 KB
+constexpr int WA_BYTES = 2 * WA_HALF;
+constexpr int WB_ATOM = 64 * WK * 2; // one [64 rows][64 columns] box: 8 KB
+constexpr int WB_BYTES = 4 * WB_ATOM;
+constexpr int W_STAGE = WA_BYTES + WB_BYTES;   // 48 KB
+constexpr int W_STAGES = 4;
+constexpr int W_MAX_PROBS = 2;
+
+struct WgProb {
+  CUtensorMap a, b;
+  const int32_t* offsets;
+  int G, M, N, m_tiles, n_tiles;
+  int64_t rows;
+  bf16* out;
+  int64_t item_base;
+};
+
+struct WgParams {
+  WgProb p[W_MAX_PROBS];
+  int n_probs;
+  int64_t total;
+  DeviceHeader* hdr;
+};
+
+struct WItem {
+  int p, g, m0, n0;
+  int64_t lo, hi;   // the group's rows
+};
+
+__device__ __forceinline__ WItem wdecode(const WgParams& P, int64_t w) {
+  WItem it;
+  int p = 0;
+  while (p + 1 < P.n_probs && w >= P.p[p + 1].item_base) ++p;
+  const WgProb& q = P.p[p];
+  const int64_t local = w - q.item_base;
+  const int per_group = q.m_tiles * q.n_tiles;
+  it.p = p;
+  it.g = (int)(local / per_group);
+  const int rem = (int)(local % per_group);
+  it.m0 = (rem / q.n_tiles) * WM;
+  it.n0 = (rem % q.n_tiles) * WN;
+  const int64_t lo = imin64(imax64(q.offsets[it.g], 0), q.rows);
+  it.lo = lo;
+  it.hi = imin64(imax64(q.offsets[it.g + 1], lo), q.rows);
+  return it;
+}
+
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both MN-major (transposed), N, M=128.
+__device__ __forceinline__ uint32_t wg_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
+         ((uint32_t)(WN >> 3) << 17) | ((uint32_t)(WM >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_constant__ WgParams P) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * W_STAGES + 4];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  auto sA = [&](int s) { return base + s * W_STAGE; };
+  auto sB = [&](int s) { return base + s * W_STAGE + WA_BYTES; };
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[W_STAGES + s]); };
+  auto tmem_full = [&](int b) { return smem_u32(&bars[2 * W_STAGES + b]); };
+  auto tmem_empty = [&](int b) { return smem_u32(&bars[2 * W_STAGES + 2 + b]); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < W_STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(tmem_full(b), 1); mbar_init(tmem_empty(b), 32 * W_EPI); }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int p = 0; p < P.n_probs; ++p) { prefetch_map(&P.p[p].a); prefetch_map(&P.p[p].b); }
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // every thread waits for the kernel that wrote the group offsets and the operands
+  pdl_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
+      const WItem it = wdecode(P, w);
+      const WgProb& q = P.p[it.p];
+      for (int64_t r0 = it.lo; r0 < it.hi; r0 += WK) {
+        if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 11)) { ok = false; break; }
+        mbar_expect_tx(full(stage), (uint32_t)W_STAGE);
+        const uint32_t a = smem_u32(sA(stage)), b = smem_u32(sB(stage));
+        tma_load_2d(a, &q.a, full(stage), it.m0, (int)r0);
+        tma_load_2d(a + WA_HALF, &q.a, full(stage), it.m0 + 64, (int)r0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          tma_load_2d(b + i * WB_ATOM, &q.b, full(stage), it.n0 + 64 * i, (int)r0);
+        if (++stage == W_STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp: tail zeroing) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int ev = 0;
+    bool ok = true;
+    const uint32_t idesc = wg_idesc();
+    for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
+      const WItem it = wdecode(P, w);
+      if (it.hi <= it.lo) continue;                       // empty group: the epilogue writes zeros
+      const int buf = ev & 1;
+      const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
+      ++ev;
+      ok = mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 12);
+      if (!__all_sync(~0u, ok)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * WN);
+      uint32_t accumulate = 0;
+      for (int64_t r0 = it.lo; r0 < it.hi; r0 += WK) {
+        ok = mbar_wait(full(stage), phase, &s_abort, P.hdr, 13);
+        if (!__all_sync(~0u, ok)) { ok = false; break; }
+        tc_fence_after();
+        const int valid = (int)imin64(WK, it.hi - r0);
+        if (valid < WK) {
+          // rows past the group's end belong to the next group (or are padding): zero them in
+          // both tiles. A row is one 128-byte line per 64-wide box (swizzling permutes 16-byte
+          // pieces within the line only).
+          const int nz = WK - valid;
+          uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int i = lane; i < nz * 6 * 8; i += 32) {
+            const int row = valid + i / 48, box = (i / 8) % 6, piece = i % 8;
+            unsigned char* line = (box < 2 ? sA(stage) + box * WA_HALF
+                                           : sB(stage) + (box - 2) * WB_ATOM) + row * 128;
+            *reinterpret_cast<uint4*>(line + piece * 16) = z;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t a = smem_u32(sA(stage)), b = smem_u32(sB(stage));
+#pragma unroll
+          for (int k16 = 0; k16 < WK / 16; ++k16) {
+            mma_bf16(d_tmem, smem_desc(a + k16 * 2048, WA_HALF, 1024),
+                     smem_desc(b + k16 * 2048, WB_ATOM, 1024), idesc, accumulate);
+            accumulate = 1;
+          }
+          mma_commit(empty(stage));
+        }
+        __syncwarp();
+        if (++stage == W_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(tmem_full(buf));
+      __syncwarp();
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); the two warps of a quadrant
+    // take alternate 16-column chunks.
+    const int quad = warp & 3, half = (warp - 2) >> 2;
+    int ev = 0;
+    for (int64_t w = blockIdx.x; w < P.total; w += gridDim.x) {
+      const WItem it = wdecode(P, w);
+      const WgProb& q = P.p[it.p];
+      const int m = it.m0 + quad * 32 + lane;
+      bf16* orow = q.out + ((int64_t)it.g * q.M + m) * q.N;
+      const bool mok = m < q.M;
+      if (it.hi <= it.lo) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        for (int c0 = half * 16; c0 < WN; c0 += 32) {
+          const int n = it.n0 + c0;
+          if (mok && n < q.N) {
+            *reinterpret_cast<uint4*>(orow + n) = z;
+            *reinterpret_cast<uint4*>(orow + n + 8) = z;
+          }
+        }
+        continue;
+      }
+      const int buf = ev & 1;
+      const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
+      ++ev;
+      if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 14)) break;
+      tc_fence_after();
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * WN);
+      for (int c0 = half * 16; c0 < WN; c0 += 32) {
+        float v[16];
+        tmem_ld16(lane_addr + c0, v);
+        tmem_wait_ld();
+        const int n = it.n0 + c0;
+        if (mok && n < q.N) {
+          uint4 u0, u1;
+          __nv_bfloat162* h0 = reinterpret_cast<__nv_bfloat162*>(&u0);
+          __nv_bfloat162* h1 = reinterpret_cast<__nv_bfloat162*>(&u1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            h0[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            h1[i] = __floats2bfloat162_rn(v[8 + 2 * i], v[8 + 2 * i + 1]);
+          }
+          *reinterpret_cast<uint4*>(orow + n) = u0;
+          *reinterpret_cast<uint4*>(orow + n + 8) = u1;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 wg_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult qr;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [rows, cols] bf16 row-major as an MN-major operand: 64 columns (one 128-byte swizzle row) by
+// 64 rows per box.
+bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint32_t box[2] = {64, WK};
+  cuuint32_t es[2] = {1, 1};
+  return wg_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_wgrad_supported(const WgradProblem& p) {
+  return p.a && p.b && p.offsets && p.out && p.G >= 1 && p.M >= WM && p.M % WM == 0 &&
+         p.N >= 64 && p.N % 64 == 0 && p.rows >= 0 && p.rows < (1ll << 31);
+}
+
+cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
+                       cudaStream_t stream, bool pdl) {
+  if (n_probs < 1 || n_probs > W_MAX_PROBS) return cudaErrorInvalidValue;
+  if (!wg_encode_fn()) return cudaErrorNotSupported;
+  static WgParams P;
+  memset(&P, 0, sizeof(P));
+  P.hdr = static_cast<DeviceHeader*>(dev_header);
+  int64_t base = 0;
+  for (int j = 0; j < n_probs; ++j) {
+    const WgradProblem& g = probs[j];
+    if (!gemm_wgrad_supported(g)) return cudaErrorNotSupported;
+    WgProb& q = P.p[j];
+    const int64_t rows = g.rows > 0 ? g.rows : 1;
+    if (!map_mn(&q.a, g.a, g.M, rows) || !map_mn(&q.b, g.b, g.N, rows))
+      return cudaErrorInvalidValue;
+    q.offsets = g.offsets;
+    q.G = g.G;
+    q.M = g.M;
+    q.N = g.N;
+    q.m_tiles = g.M / WM;
+    q.n_tiles = (int)cdiv(g.N, WN);
+    q.rows = g.rows;
+    q.out = static_cast<bf16*>(g.out);
+    q.item_base = base;
+    base += (int64_t)g.G * q.m_tiles * q.n_tiles;
+  }
+  P.n_probs = n_probs;
+  P.total = base;
+  const size_t smem = (size_t)W_STAGES * W_STAGE + 1024;
+  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = (int)imin64(sms > 0 ? sms : 148, base);
+  if (grid < 1) return cudaSuccess;
+  return launch(wgrad_kernel, dim3(grid), dim3(W_THREADS), smem, stream, pdl, P);
+}
+
+}  // namespace moe

@@ -154,3 +154,23 @@ def test_last_cuda_error_starts_clear(lib):
     assert lib.moe_last_cuda_error(C.byref(name)) == 0
     assert name.value == b"cudaSuccess"
     assert lib.moe_last_cuda_error(None) == 0
+
+
+def test_backward_argument_errors(lib):
+    from sparse_expert_router_gb300 import _lib as L
+    P = lambda v: C.c_void_p(v)
+    good, ws = P(0x10000), P(0x100000)
+    cfg = _cfg(dtype="bf16", d_latent=128, d_ff=128)
+    c = C.byref(cfg.c())
+    n = C.c_size_t()
+    assert lib.moe_backward_workspace_size(c, C.byref(n)) == L.MOE_OK and n.value > 0
+    args = [good] * 10
+    assert lib.moe_expert_ffn_backward(c, *args[:9], None, ws, n.value, None) == \
+        L.MOE_ERR_INVALID_ARG                                          # dw2 missing
+    assert lib.moe_expert_ffn_backward(c, *args, ws, n.value - 256, None) == L.MOE_ERR_WORKSPACE
+    f32 = _cfg(d_latent=128, d_ff=128)                                 # fp32 layer
+    assert lib.moe_expert_ffn_backward(C.byref(f32.c()), *args, ws, n.value, None) == \
+        L.MOE_ERR_UNSUPPORTED
+    odd = _cfg(dtype="bf16", d_latent=128, d_ff=64)                    # width not /128
+    assert lib.moe_expert_ffn_backward(C.byref(odd.c()), *args, ws, n.value, None) == \
+        L.MOE_ERR_ALIGNMENT

@@ -540,3 +540,79 @@ def test_token_mask_small_bf16():
     err = normwise(got["y"][toks], ref["y"])
     assert err <= 2e-2, err
     assert got["report"]["status"] == 0
+
+
+# ---------------------------------------------------------- expert MLP backward ----
+
+def _backward_case(E, L, F, counts, seed=21, pad=64):
+    """bf16 grouped rows (expert-major, ragged groups with empty experts and tails that are not
+    multiples of 64 rows), weights and an output gradient; the pool's padding rows hold NaN so
+    that anything read past the groups shows."""
+    g = torch.Generator().manual_seed(seed)
+    R = sum(counts)
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    P = R + pad
+    x = torch.full((P, L), float("nan"))
+    x[:R] = torch.randn(R, L, generator=g)
+    dy = torch.full((P, L), float("nan"))
+    dy[:R] = torch.randn(R, L, generator=g)
+    w1 = torch.randn(E, L, F, generator=g) * L ** -0.5
+    w3 = torch.randn(E, L, F, generator=g) * L ** -0.5
+    w2 = torch.randn(E, F, L, generator=g) * F ** -0.5
+    bf = lambda t: t.to(torch.bfloat16)
+    return {"x": bf(x), "dy": bf(dy), "w1": bf(w1), "w3": bf(w3), "w2": bf(w2), "offs": offs,
+            "P": P, "R": R}
+
+
+def _run_backward(c, E, L, F):
+    cfg = m.LayerConfig(T=c["P"], d_model=L, d_latent=L, n_experts=E, top_k=1, d_ff=F,
+                        n_shared=0, d_ff_shared=0, dtype="bf16", pool_rows=c["P"])
+    ws = m.alloc_backward_workspace(cfg, DEV)
+    d = {n: c[n].to(DEV) for n in ("x", "dy", "w1", "w3", "w2")}
+    offs = torch.tensor(c["offs"], dtype=torch.int32, device=DEV)
+    out = {"dx": torch.full((c["P"], L), 3.0, dtype=torch.bfloat16, device=DEV),
+           "dw1": torch.full((E, L, F), 5.0, dtype=torch.bfloat16, device=DEV),
+           "dw3": torch.full((E, L, F), 5.0, dtype=torch.bfloat16, device=DEV),
+           "dw2": torch.full((E, F, L), 5.0, dtype=torch.bfloat16, device=DEV)}
+    m.moe_expert_ffn_backward(cfg, d["x"], offs, d["w1"], d["w3"], d["w2"], d["dy"], out["dx"],
+                              out["dw1"], out["dw3"], out["dw2"], ws)
+    torch.cuda.synchronize()
+    out["report"] = m.moe_get_device_status(ws)
+    return out
+
+
+@pytest.mark.parametrize("E,L,F,counts", [
+    (6, 256, 384, (70, 0, 129, 1, 64, 200)),
+    (8, 1024, 1024, (171, 333, 0, 17, 256, 97, 0, 512)),
+], ids=["ragged_small", "ragged_1024"])
+def test_expert_backward(E, L, F, counts):
+    """dx_perm and every weight gradient against the oracle's chain rule; rows past the groups
+    untouched; experts without rows get exact zeros."""
+    c = _backward_case(E, L, F, counts)
+    got = _run_backward(c, E, L, F)
+    ref = moe_oracle.grouped_experts_backward(c["x"][:c["R"]], c["offs"], c["w1"], c["w3"],
+                                              c["w2"], c["dy"][:c["R"]])
+    R = c["R"]
+    assert got["report"]["status"] == 0
+    assert normwise(got["dx"][:R], ref["dx"]) <= 2e-2
+    assert bool((got["dx"][R:].float() == 3.0).all())
+    for n in ("dw1", "dw3", "dw2"):
+        g = got[n].float()
+        assert not bool(torch.isnan(g).any()), n
+        err = normwise(g, ref[n])
+        assert err <= 2e-2, (n, err)
+        for e, cnt in enumerate(counts):
+            if cnt == 0:
+                assert float(g[e].abs().max()) == 0.0, (n, e)
+
+
+def test_expert_backward_deterministic():
+    """Two runs give bitwise equal gradients (fixed accumulation order, no atomics)."""
+    E, L, F, counts = 4, 256, 256, (100, 37, 0, 300)
+    c = _backward_case(E, L, F, counts, seed=5)
+    a = _run_backward(c, E, L, F)
+    b = _run_backward(c, E, L, F)
+    for n in ("dx", "dw1", "dw3", "dw2"):
+        assert torch.equal(a[n].view(torch.int16), b[n].view(torch.int16)), n
