@@ -799,7 +799,10 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     // twice the weight bytes in flight per stage
     q.kchunk = g.kchunk;
     q.bn = g.kchunk ? BN_CHUNKED : BN;
-    q.dual = (!g.kchunk && !is_glu(g.epi) && g.group != GROUP_COLS && g.M % (2 * BM) == 0)
+    // (not for the backward's SwiGLU epilogue: its global loads of G and U are better hidden
+    // behind the next item's main loop, which double-buffered accumulators allow)
+    q.dual = (!g.kchunk && !is_glu(g.epi) && g.epi != EPI_SWIGLU_BWD && g.group != GROUP_COLS &&
+              g.M % (2 * BM) == 0)
                  ? 1 : 0;
     if (q.dual) q.m_tiles = (int)(g.M / (2 * BM));
     q.rows = g.rows;

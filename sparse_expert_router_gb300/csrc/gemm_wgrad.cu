@@ -11,8 +11,10 @@
 // Roles of the warps of a CTA (one CTA per SM, persistent over (problem, group, m tile, n tile)
 // items, n tiles fastest so the items of one group run together and share its rows in L2):
 //   warp 0: TMA producer (one thread); warp 1: TMEM allocator and MMA issuer (the whole warp
-//   zeroes tail rows, one thread issues MMAs); warps 2..9: epilogue, each thread storing 16
-//   consecutive columns of its output row as 32 contiguous bytes. Accumulators are
+//   zeroes tail rows, one thread issues MMAs); warps 2..9: epilogue, the two warps of a lane
+//   quadrant each taking half of the 256 columns, 64 per tensor-memory load, and each thread
+//   writing its row's 64 values into a 128-byte-swizzled shared tile that one TMA bulk tensor
+//   store then copies out (whole 128-byte lines, no scattered stores). Accumulators are
 //   double-buffered (2 x 256 tensor-memory columns). Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,9 +41,10 @@ constexpr int WB_BYTES = 4 * WB_ATOM;
 constexpr int W_STAGE = WA_BYTES + WB_BYTES;   // 48 KB
 constexpr int W_STAGES = 4;
 constexpr int W_MAX_PROBS = 2;
+constexpr int W_OUT_TILE = 32 * 64 * 2;   // one warp's store tile: 32 rows x 64 bf16 columns
 
 struct WgProb {
-  CUtensorMap a, b;
+  CUtensorMap a, b, o;
   const int32_t* offsets;
   int G, M, N, m_tiles, n_tiles;
   int64_t rows;
@@ -80,6 +83,21 @@ __device__ __forceinline__ WItem wdecode(const WgParams& P, int64_t w) {
 }
 
 // Instruction descriptor: fp32 accumulator, bf16 A and B, both MN-major (transposed), N, M=128.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t wg_idesc() {
   return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
          ((uint32_t)(WN >> 3) << 17) | ((uint32_t)(WM >> 4) << 24);
@@ -199,8 +217,9 @@ __global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_consta
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); the two warps of a quadrant
-    // take alternate 16-column chunks.
+    // take the two halves of the columns.
     const int quad = warp & 3, half = (warp - 2) >> 2;
+    unsigned char* otile = base + W_STAGES * W_STAGE + (warp - 2) * W_OUT_TILE;
     int ev = 0;
     for (int64_t w = blockIdx.x; w < P.total; w += gridDim.x) {
       const WItem it = wdecode(P, w);
@@ -210,11 +229,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_consta
       const bool mok = m < q.M;
       if (it.hi <= it.lo) {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        for (int c0 = half * 16; c0 < WN; c0 += 32) {
+        for (int c0 = half * (WN / 2); c0 < (half + 1) * (WN / 2); c0 += 64) {
           const int n = it.n0 + c0;
           if (mok && n < q.N) {
-            *reinterpret_cast<uint4*>(orow + n) = z;
-            *reinterpret_cast<uint4*>(orow + n + 8) = z;
+#pragma unroll
+            for (int p8 = 0; p8 < 8; ++p8) *reinterpret_cast<uint4*>(orow + n + 8 * p8) = z;
           }
         }
         continue;
@@ -225,27 +244,37 @@ __global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_consta
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 14)) break;
       tc_fence_after();
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * WN);
-      for (int c0 = half * 16; c0 < WN; c0 += 32) {
-        float v[16];
-        tmem_ld16(lane_addr + c0, v);
+      // this warp's half of the columns, 64 at a time: one tensor-memory load and one wait per
+      // 64 columns; each thread puts its row's 128 bytes into the shared tile in the 128-byte
+      // swizzle (16-byte piece p of row r at piece p ^ (r % 8)), then one bulk tensor store
+      for (int c0 = half * (WN / 2); c0 < (half + 1) * (WN / 2); c0 += 64) {
+        float v[64];
+        tmem_ld64(lane_addr + c0, v);
         tmem_wait_ld();
         const int n = it.n0 + c0;
-        if (mok && n < q.N) {
-          uint4 u0, u1;
-          __nv_bfloat162* h0 = reinterpret_cast<__nv_bfloat162*>(&u0);
-          __nv_bfloat162* h1 = reinterpret_cast<__nv_bfloat162*>(&u1);
+        if (n < q.N) {
+          if (lane == 0) bulk_wait_read0();       // the tile's previous store has read it
+          __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            h0[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            h1[i] = __floats2bfloat162_rn(v[8 + 2 * i], v[8 + 2 * i + 1]);
+          for (int p8 = 0; p8 < 8; ++p8) {
+            uint4 u;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              h[i] = __floats2bfloat162_rn(v[8 * p8 + 2 * i], v[8 * p8 + 2 * i + 1]);
+            *reinterpret_cast<uint4*>(otile + lane * 128 + ((p8 ^ (lane & 7)) << 4)) = u;
           }
-          *reinterpret_cast<uint4*>(orow + n) = u0;
-          *reinterpret_cast<uint4*>(orow + n + 8) = u1;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0)
+            tma_store_2d(&q.o, smem_u32(otile), n, it.g * q.M + it.m0 + quad * 32);
         }
       }
       tc_fence_before();
       mbar_arrive(tmem_empty(buf));
     }
+    if (lane == 0) bulk_wait0();                 // every store of this warp has completed
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -283,6 +312,19 @@ bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The output [G * M rows, N] bf16 for bulk tensor stores: 64 columns by 32 rows per box,
+// 128-byte swizzle (the layout the epilogue writes its shared tile in).
+bool map_out(CUtensorMap* m, void* ptr, int64_t cols, int64_t rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  return wg_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool gemm_wgrad_supported(const WgradProblem& p) {
@@ -303,7 +345,8 @@ cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
     if (!gemm_wgrad_supported(g)) return cudaErrorNotSupported;
     WgProb& q = P.p[j];
     const int64_t rows = g.rows > 0 ? g.rows : 1;
-    if (!map_mn(&q.a, g.a, g.M, rows) || !map_mn(&q.b, g.b, g.N, rows))
+    if (!map_mn(&q.a, g.a, g.M, rows) || !map_mn(&q.b, g.b, g.N, rows) ||
+        !map_out(&q.o, g.out, g.N, (int64_t)g.G * g.M))
       return cudaErrorInvalidValue;
     q.offsets = g.offsets;
     q.G = g.G;
@@ -318,7 +361,7 @@ cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
   }
   P.n_probs = n_probs;
   P.total = base;
-  const size_t smem = (size_t)W_STAGES * W_STAGE + 1024;
+  const size_t smem = (size_t)W_STAGES * W_STAGE + (size_t)W_EPI * W_OUT_TILE + 1024;
   cudaError_t e = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
