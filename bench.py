@@ -244,6 +244,88 @@ def cpu_baseline(shape, n_tokens, inp_gpu):
                       f"(routing, dispatch, every expert MLP, combine, shared, up-projection)"}
 
 
+def run_expert_backward(args, shape):
+    """Backward of the routed expert MLP on the workload's own routing: moe_route and
+    moe_permute give the grouped rows and offsets, dy_perm is seeded N(0, 1) bf16, and each step
+    is one moe_expert_ffn_backward call (recompute, dA, dX, dW2, dW1 and dW3). One GPU."""
+    import sparse_expert_router_gb300 as m
+    m.load()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    flags = 0 if args.no_pdl else m.MOE_FLAG_PDL
+    cfg = m.LayerConfig.from_shape(shape, flags=flags)
+    T, k, E, L, F = shape.T, shape.top_k, shape.n_experts, shape.d_latent, shape.d_ff
+    inp = make_layer_inputs(shape, dev)
+    ws = m.alloc_workspace(cfg, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    m.moe_route(cfg, inp["x"], inp["w_router"], inp["b_router"], idx, gate, ws)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, k), dtype=torch.int32, device=dev)
+    ndrop = torch.empty(1, dtype=torch.int32, device=dev)
+    xp = torch.empty((T * k, L), dtype=torch.bfloat16, device=dev)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], idx, counts, offs, perm, slot,
+                  ndrop, xp, ws)
+    g = torch.Generator(device=dev).manual_seed(7)
+    dy = torch.randn((T * k, L), generator=g, device=dev).to(torch.bfloat16)
+    dx = torch.empty_like(xp)
+    dw1, dw3, dw2 = (torch.empty_like(inp[n]) for n in ("w1", "w3", "w2"))
+    bws = m.alloc_backward_workspace(cfg, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        m.moe_expert_ffn_backward(cfg, xp, offs, inp["w1"], inp["w3"], inp["w2"], dy, dx, dw1,
+                                  dw3, dw2, bws, stream=st)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(0)
+    clk.start()
+    ms = 0.0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.zero_()
+        a.record(st)
+        step()
+        b.record(st)
+        b.synchronize()
+        ms += a.elapsed_time(b)
+    clocks = clk.stop()
+    ms /= args.steps
+    rep = m.moe_get_device_status(bws)
+    R = int(offs[-1].item())
+    active = int((counts > 0).sum().item())
+    flops = 16.0 * R * L * F          # recompute 4RLF, dA 2RFL, dX 4RFL, dW2 2RFL, dW1+dW3 4RLF
+    # bf16 bytes of this design's passes: W1 and W3 read twice and W2 once, the three weight
+    # gradients written; rows: x read 3x, dy 2x, dx written; G, U, A and dG, dU written (5x),
+    # then read (G, U by dA; A by dW2; dG, dU by dX and by dW1 / dW3: 7x)
+    by = 2 * 5 * active * L * F + 2 * 3 * active * L * F + 2 * R * 6 * L + 2 * R * 12 * F
+    pk = peaks()
+    if by / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_sustained"] * 1e12):
+        ach = by / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (HBM copy)"}
+    else:
+        ach = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
+                "peak_source": pk["source"] + " (bf16 sustained)"}
+    roof["traffic"] = None
+    print(json.dumps({
+        "metric": "routed-expert MLP backward tokens/s", "value": round(T / (ms * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (the workload's routing of seeded inputs; dy_perm seeded N(0,1))",
+        "config": {"workload": f"{shape.name}: T={T} E={E} k={k} L={L} F={F}", "rows": R,
+                   "pdl": not args.no_pdl, "l2": "flushed between timed steps (256 MB write)"},
+        "tflop_s": round(flops / (ms * 1e-3) / 1e12, 1),
+        "roofline": roof, "gpu_launches": 7 * args.steps, "clocks": clocks, "device_report": rep}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -257,10 +339,15 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--expert-backward", action="store_true",
+                    help="time the routed experts' backward (moe_expert_ffn_backward) instead")
     args = ap.parse_args()
     shape = SHAPES[args.workload]
     if args.impl == "reference":
         run_reference(args, shape)
+        return
+    if args.expert_backward:
+        run_expert_backward(args, shape)
         return
 
     import sparse_expert_router_gb300 as m
