@@ -522,6 +522,104 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
     return out
 
 
+# --------------------------------------------------------------- layer backward ----
+
+def backward(inp: Dict[str, torch.Tensor], fwd: Dict[str, torch.Tensor], dy: torch.Tensor, *,
+             rms_eps: float) -> Dict[str, torch.Tensor]:
+    """Gradients of <dy, y> for the whole layer (16-bit or fp32 expert banks), by the chain
+    rule through the forward's definition, given ``fwd`` = forward(inp, ...) over all tokens.
+
+    Top-k selection is piecewise constant, so no gradient flows through the choice of experts;
+    it flows through the selected logits' softmax gates. With G = the selected gates and dG the
+    gradient of the gates, the selected logits get G_j (dG_j - sum_i G_i dG_i).
+      y = c W_up + a_s W2s                  -> dc = dy W_up^T, dW_up = c^T dy, da_s = dy W2s^T,
+                                               dW2s = a_s^T dy
+      c[t] = sum_j g[t,j] o[t,j] (kept j)   -> do[t,j] = g[t,j] dc[t], dg[t,j] = <dc[t], o[t,j]>
+      o = expert MLP of h (per expert)      -> grouped_experts_backward
+      h = z rstd gamma, rstd = (mean(z^2) + eps)^-1/2
+                                            -> dgamma = sum_t dh z rstd,
+                                               dz = rstd (dh gamma - zhat mean(dh gamma zhat))
+      z = x W_down                          -> dW_down = x^T dz, dx += dz W_down^T
+      logits = x W_r + b                    -> dW_r = x^T dl, db = sum_t dl, dx += dl W_r^T
+      shared: a_s = silu(x W1_s) (x W3_s)   -> as the expert MLP, dx += ...
+    Returns every gradient in fp64 (names d<weight>, dx)."""
+    x64, dy64 = to64(inp["x"]), to64(dy)
+    T, d = x64.shape
+    E = inp["w_router"].shape[1]
+    k = fwd["idx"].shape[1]
+    L = inp["w_up"].shape[0]
+    idx, gate, slot = fwd["idx"], fwd["gate"], fwd["slot_of"]
+    w_up = to64(inp["w_up"])
+    w2s = to64(inp["w2_s"])
+    S, Fs = w2s.shape[0], w2s.shape[1]
+    out: Dict[str, torch.Tensor] = {}
+    # up-projection and the shared experts' down projection
+    dc = dy64 @ w_up.T
+    out["dw_up"] = fwd["c"].T @ dy64
+    da_s = dy64 @ w2s.reshape(S * Fs, d).T
+    out["dw2_s"] = (fwd["a_s"].T @ dy64).reshape(S, Fs, d)
+    # shared experts (read x)
+    dx = torch.zeros((T, d), dtype=F64)
+    out["dw1_s"] = torch.zeros_like(to64(inp["w1_s"]))
+    out["dw3_s"] = torch.zeros_like(to64(inp["w3_s"]))
+    for s in range(S):
+        W1, W3 = to64(inp["w1_s"][s]), to64(inp["w3_s"][s])
+        G, U = x64 @ W1, x64 @ W3
+        dA = da_s[:, s * Fs:(s + 1) * Fs]
+        dG = dA * U * silu_grad(G)
+        dU = dA * silu(G)
+        out["dw1_s"][s] = x64.T @ dG
+        out["dw3_s"][s] = x64.T @ dU
+        dx += dG @ W1.T + dU @ W3.T
+    # combine: per kept assignment
+    o = fwd["o"]
+    dgate = torch.zeros((T, k), dtype=F64)
+    kept = slot >= 0
+    dgate[kept] = (dc.unsqueeze(1) * o).sum(-1)[kept]
+    # expert MLPs over the kept assignments in dispatch order (rows of expert e by token)
+    E_rows: Dict[int, List[Tuple[int, int]]] = {}
+    for t in range(T):
+        for j in range(k):
+            if int(slot[t, j]) >= 0:
+                E_rows.setdefault(int(idx[t, j]), []).append((t, j))
+    h = fwd["h"]
+    order = [(e, t, j) for e in sorted(E_rows) for (t, j) in E_rows[e]]
+    offsets = [0] * (E + 1)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + len(E_rows.get(e, []))
+    rows = torch.stack([h[t] for _, t, _ in order]) if order else torch.zeros((0, L), dtype=F64)
+    dys = (torch.stack([gate[t, j] * dc[t] for _, t, j in order]) if order
+           else torch.zeros((0, L), dtype=F64))
+    eb = grouped_experts_backward(rows, offsets, inp["w1"], inp["w3"], inp["w2"], dys)
+    out["dw1"], out["dw3"], out["dw2"] = eb["dw1"], eb["dw3"], eb["dw2"]
+    dh = torch.zeros((T, L), dtype=F64)
+    for n, (_, t, _) in enumerate(order):
+        dh[t] += eb["dx"][n]
+    # RMSNorm and the down-projection
+    z = fwd["z"]
+    rstd = 1.0 / torch.sqrt((z * z).mean(dim=1, keepdim=True) + rms_eps)
+    zhat = z * rstd
+    gamma = to64(inp["rms_gamma"])
+    out["drms_gamma"] = (dh * zhat).sum(0)
+    dhg = dh * gamma
+    dz = rstd * (dhg - zhat * (dhg * zhat).mean(dim=1, keepdim=True))
+    out["dw_down"] = x64.T @ dz
+    dx += dz @ to64(inp["w_down"]).T
+    # router: softmax over the selected logits
+    dl = torch.zeros((T, E), dtype=F64)
+    s_t = (gate * dgate).sum(1, keepdim=True)
+    dsel = gate * (dgate - s_t)
+    for j in range(k):
+        dl[torch.arange(T), idx[:, j]] += dsel[:, j]
+    out["dw_router"] = x64.T @ dl
+    out["db_router"] = dl.sum(0)
+    dx += dl @ to64(inp["w_router"]).T
+    out["dx"] = dx
+    out["dgate"] = dgate
+    out["dh"] = dh
+    return out
+
+
 def slice_forward(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
     """One expert-parallel rank's slice: grouped SwiGLU experts over the pool, then the
     gate-weighted un-permute back to arrival order: out[i] = gate[i] * o[slot_of[i]]."""

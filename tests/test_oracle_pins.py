@@ -493,7 +493,52 @@ def pin_silu_grad_closed_form():
     assert torch.allclose(d[3:], fd, rtol=0, atol=1e-9)
 
 
-ALL_PINS = [pin_expert_backward_autograd, pin_expert_backward_finite_differences,
+def _tiny_layer(seed=13, cap=None):
+    """A random fp64 layer small enough for finite differences over every weight."""
+    g = torch.Generator().manual_seed(seed)
+    T, d, L, E, k, F, S, Fs = 6, 8, 6, 4, 2, 5, 1, 4
+    r = lambda *sh: torch.randn(*sh, generator=g, dtype=F64)
+    inp = {"x": r(T, d), "w_router": r(d, E), "b_router": r(E) * 0.3, "w_down": r(d, L) * 0.4,
+           "rms_gamma": 1.0 + 0.2 * r(L), "w1": r(E, L, F) * 0.5, "w3": r(E, L, F) * 0.5,
+           "w2": r(E, F, L) * 0.5, "w1_s": r(S, d, Fs) * 0.4, "w3_s": r(S, d, Fs) * 0.4,
+           "w2_s": r(S, Fs, d) * 0.4, "w_up": r(L, d) * 0.4}
+    return inp, r(T, d), dict(top_k=k, rms_eps=1e-6, capacity_factor=cap)
+
+
+def pin_layer_backward_finite_differences():
+    """Central differences of <dy, y> through the oracle's forward, for sampled entries of every
+    gradient, with and without a capacity that drops assignments (routing is unchanged by the
+    1e-6 perturbations of these random inputs)."""
+    for cap in (None, (1, 2)):
+        inp, dy, kw = _tiny_layer(cap=cap)
+        fwd = O.forward(inp, **kw)
+        if cap:
+            assert int(fwd["n_dropped"]) > 0
+        got = O.backward(inp, fwd, dy, rms_eps=kw["rms_eps"])
+
+        def loss(mod):
+            return float((O.forward(mod, **kw)["y"] * dy).sum())
+        h = 1e-6
+        checks = [("x", "dx", (2, 3)), ("x", "dx", (5, 0)), ("w_router", "dw_router", (1, 2)),
+                  ("w_router", "dw_router", (7, 0)), ("b_router", "db_router", (3,)),
+                  ("w_down", "dw_down", (4, 1)), ("rms_gamma", "drms_gamma", (2,)),
+                  ("w1", "dw1", (int(fwd["idx"][0, 0]), 1, 2)),
+                  ("w3", "dw3", (int(fwd["idx"][1, 1]), 0, 4)),
+                  ("w2", "dw2", (int(fwd["idx"][2, 0]), 3, 5)),
+                  ("w1_s", "dw1_s", (0, 6, 1)), ("w3_s", "dw3_s", (0, 2, 3)),
+                  ("w2_s", "dw2_s", (0, 1, 7)), ("w_up", "dw_up", (5, 6))]
+        for wname, gname, index in checks:
+            plus, minus = dict(inp), dict(inp)
+            plus[wname] = inp[wname].clone()
+            minus[wname] = inp[wname].clone()
+            plus[wname][index] += h
+            minus[wname][index] -= h
+            fd = (loss(plus) - loss(minus)) / (2 * h)
+            an = float(got[gname][index])
+            assert abs(fd - an) <= 1e-6 * (1 + abs(fd)), (cap, gname, index, fd, an)
+
+
+ALL_PINS = [pin_layer_backward_finite_differences, pin_expert_backward_autograd, pin_expert_backward_finite_differences,
             pin_silu_grad_closed_form, pin_mask_all_ones_is_no_mask, pin_mask_padding_keeps_shared_only,
             pin_mask_frees_capacity, pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
             pin_fp8_layer_grid, pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
@@ -637,6 +682,33 @@ def _mut_backward_dx_no_w3(monkeypatch):
     monkeypatch.setattr(O, "grouped_experts_backward", bad)
 
 
+def _mut_router_grad_full_softmax(monkeypatch):
+    orig = O.backward
+
+    def bad(inp, fwd, dy, *, rms_eps):
+        out = orig(inp, fwd, dy, rms_eps=rms_eps)
+        # forget the normalisation over the selected experts: dl_j = g_j dg_j
+        dl = torch.zeros((fwd["idx"].shape[0], inp["w_router"].shape[1]), dtype=F64)
+        for j in range(fwd["idx"].shape[1]):
+            dl[torch.arange(dl.shape[0]), fwd["idx"][:, j]] += fwd["gate"][:, j] * out["dgate"][:, j]
+        out["dw_router"] = O.to64(inp["x"]).T @ dl
+        return out
+    monkeypatch.setattr(O, "backward", bad)
+
+
+def _mut_rmsnorm_grad_no_projection(monkeypatch):
+    orig = O.backward
+
+    def bad(inp, fwd, dy, *, rms_eps):
+        out = orig(inp, fwd, dy, rms_eps=rms_eps)
+        z = fwd["z"]
+        rstd = 1.0 / torch.sqrt((z * z).mean(dim=1, keepdim=True) + rms_eps)
+        dz = rstd * out["dh"] * O.to64(inp["rms_gamma"])         # drops the mean term
+        out["dw_down"] = O.to64(inp["x"]).T @ dz
+        return out
+    monkeypatch.setattr(O, "backward", bad)
+
+
 def _mut_unstable_perm(monkeypatch):
     orig = O.dispatch
 
@@ -666,6 +738,7 @@ MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mu
              _mut_fp8_no_activation_rounding, _mut_fp8_dequant_by_scale,
              _mut_fp8_quantize_in_fp64, _mut_mask_ignored, _mut_mask_counts_padding,
              _mut_silu_grad_no_inner, _mut_backward_dw2_from_g, _mut_backward_dx_no_w3,
+             _mut_router_grad_full_softmax, _mut_rmsnorm_grad_no_projection,
              _mut_unstable_perm,
              _mut_transposed_up]
 
