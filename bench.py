@@ -326,6 +326,75 @@ def run_expert_backward(args, shape):
         "roofline": roof, "gpu_launches": 7 * args.steps, "clocks": clocks, "device_report": rep}))
 
 
+def run_layer_backward(args, shape):
+    """The whole layer's backward (moe_backward) after one moe_forward on the workload; each
+    step is one backward call with a seeded bf16 dy. One GPU."""
+    import sparse_expert_router_gb300 as m
+    m.load()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    cfg = m.LayerConfig.from_shape(shape, flags=0 if args.no_pdl else m.MOE_FLAG_PDL)
+    T, d, L, E, F = shape.T, shape.d_model, shape.d_latent, shape.n_experts, shape.d_ff
+    S, Fs = shape.n_shared, shape.d_ff_shared
+    inp = make_layer_inputs(shape, dev)
+    fws = m.alloc_workspace(cfg, dev)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    counts = torch.zeros(E, dtype=torch.int32, device=dev)
+    m.moe_forward(cfg, inp, inp["x"], y, fws, aux={"expert_counts": counts})
+    g = torch.Generator(device=dev).manual_seed(7)
+    dy = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
+    dx = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    grads = {n: torch.empty_like(inp[n[1:]]) for n in m.GRAD_NAMES
+             if n not in ("db_router", "drms_gamma")}
+    grads["db_router"] = torch.empty(E, dtype=torch.float32, device=dev)
+    grads["drms_gamma"] = torch.empty(L, dtype=torch.float32, device=dev)
+    bws = m.alloc_layer_backward_workspace(cfg, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        m.moe_backward(cfg, inp, inp["x"], dy, dx, grads, fws, bws, stream=st)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(0)
+    clk.start()
+    ms = 0.0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.zero_()
+        a.record(st)
+        step()
+        b.record(st)
+        b.synchronize()
+        ms += a.elapsed_time(b)
+    clocks = clk.stop()
+    ms /= args.steps
+    R = int(min(int(counts.sum()), T * shape.top_k))
+    SF = S * Fs
+    # flops: the experts' backward (16 R L F), the dense gradients: dc and dW_up (2 x 2TLd),
+    # shared recompute (4 T d SF), shared dA and dW2s (2 x 2 T SF d), dx and dW for the
+    # down-projection (2 x 2 T d L), for the shared gate/up (2 x 4 T d SF), router (2 x 2 T d E)
+    flops = 16.0 * R * L * F + 2.0 * T * (2 * L * d + 4 * d * SF + 2 * SF * d + 2 * d * L
+                                          + 4 * d * SF + 2 * d * E)
+    pk = peaks()
+    ach = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "MoE-layer backward tokens/s", "value": round(T / (ms * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded layer inputs, the forward's routing, dy seeded N(0,1))",
+        "config": {"workload": f"{shape.name}: T={T} d={d} latent={L} E={E} "
+                               f"k={shape.top_k} F={F} shared={S}x{Fs}",
+                   "pdl": not args.no_pdl, "l2": "flushed between timed steps (256 MB write)"},
+        "tflop_s": round(ach, 1),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
+                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
+                     "traffic": None, "peak_source": pk["source"] + " (bf16 sustained)"},
+        "clocks": clocks, "device_report": m.moe_get_device_status(bws)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -341,6 +410,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--expert-backward", action="store_true",
                     help="time the routed experts' backward (moe_expert_ffn_backward) instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the whole layer's backward (moe_backward) instead")
     args = ap.parse_args()
     shape = SHAPES[args.workload]
     if args.impl == "reference":
@@ -348,6 +419,9 @@ def main():
         return
     if args.expert_backward:
         run_expert_backward(args, shape)
+        return
+    if args.backward:
+        run_layer_backward(args, shape)
         return
 
     import sparse_expert_router_gb300 as m

@@ -257,6 +257,42 @@ MOE_API moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void
                                              void* dx_perm, void* dw1, void* dw3, void* dw2,
                                              void* ws, size_t ws_bytes, void* stream);
 
+/* Gradients of one layer's weights (device memory owned by the caller; layouts as in
+ * moe_weights_t, bf16 unless stated). */
+typedef struct {
+  void*  dw_router;   /* [d, E] */
+  float* db_router;   /* [E] fp32, or NULL (not computed) */
+  void*  dw_down;     /* [d, L] */
+  float* drms_gamma;  /* [L] fp32, or NULL (not computed) */
+  void*  dw1;         /* [E, L, F] */
+  void*  dw3;         /* [E, L, F] */
+  void*  dw2;         /* [E, F, L] */
+  void*  dw1_s;       /* [S, d, F_s] (NULL when S = 0) */
+  void*  dw3_s;       /* [S, d, F_s] */
+  void*  dw2_s;       /* [S, F_s, d] */
+  void*  dw_up;       /* [L, d] */
+} moe_grads_t;
+
+/* Bytes of workspace moe_backward needs (256-byte aligned, zero-filled before first use). */
+MOE_API moe_status_t moe_layer_backward_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Backward of moe_forward: given dy = dL/dy [T, d], writes dx = dL/dx [T, d] and every weight
+ * gradient into g. fwd_ws is the workspace of a moe_forward call with the same cfg, weights and
+ * x, left untouched since: the backward reads the routing, gates, slots, group offsets, the
+ * latent z, the grouped rows, the experts' outputs, the combine c and the shared hidden from
+ * it. Top-k selection has no gradient; the router's logits get the softmax-over-selection
+ * gradient G_j (dG_j - sum_i G_i dG_i) of their gates. The routed experts run
+ * moe_expert_ffn_backward's kernels; everything else is bf16 GEMMs on tensor cores (K-major
+ * weight tiles for the input gradients, row-contracting kernels for the weight gradients) and
+ * per-token kernels for the combine, RMSNorm and router backward. Padding tokens (token_mask)
+ * and dropped assignments contribute nothing to the routed part. bf16 layers on the
+ * tensor-core path only, without fp8 experts (else MOE_ERR_UNSUPPORTED); d, d_latent, d_ff and
+ * n_shared * d_ff_shared multiples of 128, n_experts and d_ff_shared of 64, n_shared <= 2. */
+MOE_API moe_status_t moe_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                                  const void* dy, void* dx, const moe_grads_t* g,
+                                  const void* fwd_ws, size_t fwd_ws_bytes, void* ws,
+                                  size_t ws_bytes, void* stream);
+
 /* Combine: c[t] = sum over j with slot_of[t, j] >= 0, in order j = 0..k-1, of
  * topk_gate[t, j] * y_perm[slot_of[t, j]] (fp32 accumulation). When w_up is NULL, out [T, L]
  * receives c (the gate-weighted un-permute back to arrival order, e.g. of one expert-parallel

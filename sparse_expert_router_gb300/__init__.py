@@ -14,13 +14,15 @@ from typing import Dict, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import (MOE_BF16, MOE_F32, MOE_FLAG_FP8_EXPERTS, MOE_FLAG_PDL, MOE_FLAG_SIMT,
-                   MOE_FORWARD_STAGES,
-                   moe_config_t, moe_device_report_t, moe_forward_aux_t, moe_fp8_t, moe_weights_t)
+from ._lib import (GRAD_NAMES, MOE_BF16, MOE_F32, MOE_FLAG_FP8_EXPERTS, MOE_FLAG_PDL,
+                   MOE_FLAG_SIMT, MOE_FORWARD_STAGES, moe_config_t, moe_device_report_t,
+                   moe_forward_aux_t, moe_fp8_t, moe_grads_t, moe_weights_t)
 
 __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
            "backward_workspace_size", "alloc_backward_workspace", "moe_expert_ffn_backward",
+           "layer_backward_workspace_size", "alloc_layer_backward_workspace", "moe_backward",
+           "GRAD_NAMES",
            "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
            "moe_selftest_device_timeout",
            "MOE_FLAG_PDL", "MOE_FLAG_SIMT", "MOE_FLAG_FP8_EXPERTS",
@@ -160,6 +162,31 @@ def moe_expert_ffn_backward(cfg, x_perm, expert_offsets, w1, w3, w2, dy_perm, dx
     _check("moe_expert_ffn_backward", load().moe_expert_ffn_backward(
         C.byref(cfg.c()), _p(x_perm), _p(expert_offsets), _p(w1), _p(w3), _p(w2), _p(dy_perm),
         _p(dx_perm), _p(dw1), _p(dw3), _p(dw2), _p(ws), ws.numel(), _stream(stream)))
+
+
+def layer_backward_workspace_size(cfg: LayerConfig) -> int:
+    n = C.c_size_t(0)
+    _check("moe_layer_backward_workspace_size",
+           load().moe_layer_backward_workspace_size(C.byref(cfg.c()), C.byref(n)))
+    return n.value
+
+
+def alloc_layer_backward_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of moe_backward."""
+    return torch.zeros(layer_backward_workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def moe_backward(cfg, weights: Dict[str, torch.Tensor], x, dy, dx, grads: Dict[str, torch.Tensor],
+                 fwd_ws, ws, stream=None):
+    """dx and the weight gradients (``grads`` maps GRAD_NAMES to device tensors; db_router and
+    drms_gamma may be missing) of the layer whose moe_forward used ``fwd_ws`` on x."""
+    w = moe_weights_t(**{n: (weights[n].data_ptr() if weights.get(n) is not None else None)
+                         for n in WEIGHT_NAMES})
+    g = moe_grads_t(**{n: (grads[n].data_ptr() if grads.get(n) is not None else None)
+                       for n in GRAD_NAMES})
+    _check("moe_backward", load().moe_backward(
+        C.byref(cfg.c()), C.byref(w), _p(x), _p(dy), _p(dx), C.byref(g), _p(fwd_ws),
+        fwd_ws.numel(), _p(ws), ws.numel(), _stream(stream)))
 
 
 def moe_combine(cfg, y_perm, slot_of, topk_gate, out, ws, a_shared=None, w_up=None, w2_s=None,

@@ -48,6 +48,14 @@ class moe_weights_t(C.Structure):
                [("fp8", C.POINTER(moe_fp8_t))]
 
 
+GRAD_NAMES = ("dw_router", "db_router", "dw_down", "drms_gamma", "dw1", "dw3", "dw2", "dw1_s",
+              "dw3_s", "dw2_s", "dw_up")
+
+
+class moe_grads_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in GRAD_NAMES]
+
+
 class moe_forward_aux_t(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("topk_idx", "topk_gate", "expert_counts",
                                           "expert_offsets", "slot_of", "n_dropped",
@@ -75,6 +83,9 @@ SIGNATURES = {
                                  C.c_size_t, P]),
     "moe_combine": (C.c_int, [CFG, P, P, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_backward_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
+    "moe_layer_backward_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
+    "moe_backward": (C.c_int, [CFG, C.POINTER(moe_weights_t), P, P, P, C.POINTER(moe_grads_t), P,
+                               C.c_size_t, P, C.c_size_t, P]),
     "moe_expert_ffn_backward": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_forward": (C.c_int, [CFG, C.POINTER(moe_weights_t), P, P, P, C.c_size_t, P,
                               C.POINTER(moe_forward_aux_t)]),

@@ -2,6 +2,7 @@
 #include <math.h>
 #include <string.h>
 
+#include "backward.h"
 #include "common.cuh"
 #include "dispatch.h"
 #include "gemm.h"
@@ -624,6 +625,107 @@ moe_status_t moe_backward_workspace_size(const moe_config_t* cfg, size_t* bytes)
   return MOE_OK;
 }
 
+// The routed experts' backward on the grouped rows: recompute G, U, A; dA with the SwiGLU
+// backward; dX; the weight gradients. Scratch buffers G, U, A, dG, dU ([pool_rows, F] bf16).
+struct ExpertBwdScratch {
+  void *g, *u, *a, *dg, *du;
+};
+
+moe_status_t expert_backward_launches(const Call& k, const void* x_perm, const int32_t* offsets,
+                                      const void* w1, const void* w3, const void* w2,
+                                      const void* dy_perm, void* dx_perm, void* dw1, void* dw3,
+                                      void* dw2, const ExpertBwdScratch& B) {
+  const moe_config_t& c = k.c;
+  const int64_t P = pool_rows_of(c);
+  const int E = c.n_experts, L = c.d_latent, F = c.d_ff;
+  // 1. recompute G, U and A = silu(G) U over the grouped rows
+  GemmProblem rec;
+  rec.epi = EPI_SWIGLU_SAVE;
+  rec.group = GROUP_ROWS;
+  rec.M = F;
+  rec.seg[0] = {x_perm, w1, w3, L};
+  rec.offsets = offsets;
+  rec.G = E;
+  rec.rows = P;
+  rec.out = B.a;
+  rec.out2 = B.g;
+  rec.out3 = B.u;
+  rec.ld_out = F;
+  rec.dtype = DT_BF16;
+  // 2. dA = dY W2^T, then dG = dA U silu'(G), dU = dA silu(G) in the epilogue
+  GemmProblem da;
+  da.epi = EPI_SWIGLU_BWD;
+  da.group = GROUP_ROWS;
+  da.M = F;
+  da.seg[0] = {dy_perm, w2, nullptr, L};
+  da.a_kmajor = 1;
+  da.offsets = offsets;
+  da.G = E;
+  da.rows = P;
+  da.out = B.dg;
+  da.out2 = B.du;
+  da.ld_out = F;
+  da.aux_g = B.g;
+  da.aux_u = B.u;
+  da.ld_aux = F;
+  da.dtype = DT_BF16;
+  // 3. dX = dG W1^T + dU W3^T
+  GemmProblem dx;
+  dx.epi = EPI_STORE;
+  dx.group = GROUP_ROWS;
+  dx.M = L;
+  dx.n_seg = 2;
+  dx.seg[0] = {B.dg, w1, nullptr, F};
+  dx.seg[1] = {B.du, w3, nullptr, F};
+  dx.a_kmajor = 1;
+  dx.offsets = offsets;
+  dx.G = E;
+  dx.rows = P;
+  dx.out = dx_perm;
+  dx.ld_out = L;
+  dx.dtype = DT_BF16;
+  // 4. dW2 = A^T dY; dW1 = X^T dG, dW3 = X^T dU, contracting over each expert's rows
+  WgradProblem w2g;
+  w2g.a = B.a;
+  w2g.b = dy_perm;
+  w2g.offsets = offsets;
+  w2g.G = E;
+  w2g.M = F;
+  w2g.N = L;
+  w2g.rows = P;
+  w2g.out = dw2;
+  WgradProblem w13[2];
+  w13[0].a = x_perm;
+  w13[0].b = B.dg;
+  w13[0].offsets = offsets;
+  w13[0].G = E;
+  w13[0].M = L;
+  w13[0].N = F;
+  w13[0].rows = P;
+  w13[0].out = dw1;
+  w13[1] = w13[0];
+  w13[1].b = B.du;
+  w13[1].out = dw3;
+  if (!gemm_tc_supported(rec) || !gemm_tc_supported(da) || !gemm_tc_supported(dx) ||
+      !gemm_wgrad_supported(w2g) || !gemm_wgrad_supported(w13[0]))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_TRY_CUDA(validate_offsets(offsets, E, P, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&rec, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&da, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&dx, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(&w2g, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(w13, 2, k.hdr(), k.st, k.pdl));
+  return MOE_OK;
+}
+
+// Conditions of the tensor-core backward: bf16, no fp8 experts, widths the tiles divide.
+moe_status_t check_backward_cfg(const moe_config_t& c) {
+  if (c.dtype != MOE_BF16 || (c.flags & (MOE_FLAG_SIMT | MOE_FLAG_FP8_EXPERTS)))
+    return MOE_ERR_UNSUPPORTED;
+  if ((c.d_latent % 128) || (c.d_ff % 128)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
 moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm,
                                      const int32_t* expert_offsets, const void* w1,
                                      const void* w3, const void* w2, const void* dy_perm,
@@ -634,10 +736,7 @@ moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm
   if ((s = check_ptrs({x_perm, expert_offsets, w1, w3, w2, dy_perm, dx_perm, dw1, dw3, dw2},
                       {})) != MOE_OK)
     return s;
-  // tensor cores, bf16 and 128-multiple widths (the weight-gradient tiles are 128 x 64 aligned)
-  if (cfg->dtype != MOE_BF16 || (cfg->flags & (MOE_FLAG_SIMT | MOE_FLAG_FP8_EXPERTS)))
-    return MOE_ERR_UNSUPPORTED;
-  if ((cfg->d_latent % 128) || (cfg->d_ff % 128)) return MOE_ERR_ALIGNMENT;
+  if ((s = check_backward_cfg(*cfg)) != MOE_OK) return s;
   if (!ws) return MOE_ERR_INVALID_ARG;
   if ((uintptr_t)ws & 255u) return MOE_ERR_ALIGNMENT;
   const BwdLayout B = make_bwd_layout(*cfg);
@@ -645,88 +744,229 @@ moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm
   Call k = make_call(cfg, ws, stream);
   k.L.hdr = B.hdr;                                   // the report sits at the same place
   auto at = [&](size_t off) { return static_cast<void*>(k.ws + off); };
-  const int64_t P = pool_rows_of(*cfg);
-  const int E = cfg->n_experts, L = cfg->d_latent, F = cfg->d_ff;
+  MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false));
+  return expert_backward_launches(k, x_perm, expert_offsets, w1, w3, w2, dy_perm, dx_perm, dw1,
+                                  dw3, dw2, {at(B.g), at(B.u), at(B.a), at(B.dg), at(B.du)});
+}
 
-  // 1. recompute G, U and A = silu(G) U over the grouped rows
-  GemmProblem rec;
-  rec.epi = EPI_SWIGLU_SAVE;
-  rec.group = GROUP_ROWS;
-  rec.M = F;
-  rec.seg[0] = {x_perm, w1, w3, L};
-  rec.offsets = expert_offsets;
-  rec.G = E;
-  rec.rows = P;
-  rec.out = at(B.a);
-  rec.out2 = at(B.g);
-  rec.out3 = at(B.u);
-  rec.ld_out = F;
-  rec.dtype = DT_BF16;
-  // 2. dA = dY W2^T, then dG = dA U silu'(G), dU = dA silu(G) in the epilogue
-  GemmProblem da;
-  da.epi = EPI_SWIGLU_BWD;
-  da.group = GROUP_ROWS;
-  da.M = F;
-  da.seg[0] = {dy_perm, w2, nullptr, L};
-  da.a_kmajor = 1;
-  da.offsets = expert_offsets;
-  da.G = E;
-  da.rows = P;
-  da.out = at(B.dg);
-  da.out2 = at(B.du);
-  da.ld_out = F;
-  da.aux_g = at(B.g);
-  da.aux_u = at(B.u);
-  da.ld_aux = F;
-  da.dtype = DT_BF16;
-  // 3. dX = dG W1^T + dU W3^T
-  GemmProblem dx;
-  dx.epi = EPI_STORE;
-  dx.group = GROUP_ROWS;
-  dx.M = L;
-  dx.n_seg = 2;
-  dx.seg[0] = {at(B.dg), w1, nullptr, F};
-  dx.seg[1] = {at(B.du), w3, nullptr, F};
-  dx.a_kmajor = 1;
-  dx.offsets = expert_offsets;
-  dx.G = E;
-  dx.rows = P;
-  dx.out = dx_perm;
-  dx.ld_out = L;
-  dx.dtype = DT_BF16;
-  // 4. dW2 = A^T dY; dW1 = X^T dG, dW3 = X^T dU, contracting over each expert's rows
-  WgradProblem w2g;
-  w2g.a = at(B.a);
-  w2g.b = dy_perm;
-  w2g.offsets = expert_offsets;
-  w2g.G = E;
-  w2g.M = F;
-  w2g.N = L;
-  w2g.rows = P;
-  w2g.out = dw2;
-  WgradProblem w13[2];
-  w13[0].a = x_perm;
-  w13[0].b = at(B.dg);
-  w13[0].offsets = expert_offsets;
-  w13[0].G = E;
-  w13[0].M = L;
-  w13[0].N = F;
-  w13[0].rows = P;
-  w13[0].out = dw1;
-  w13[1] = w13[0];
-  w13[1].b = at(B.du);
-  w13[1].out = dw3;
-  if (!gemm_tc_supported(rec) || !gemm_tc_supported(da) || !gemm_tc_supported(dx) ||
-      !gemm_wgrad_supported(w2g) || !gemm_wgrad_supported(w13[0]))
+// Workspace of moe_backward: the experts' backward scratch, then the rest of the layer's
+// intermediates (sizes from the configuration).
+struct LayerBwdLayout {
+  BwdLayout e;
+  size_t dc, gs, us, as2, dgs, dus, dy_perm, dgate, dx_perm, dz, dhz, dx32, dl32, dlbf, off01,
+      total;
+};
+
+LayerBwdLayout make_layer_bwd_layout(const moe_config_t& c) {
+  LayerBwdLayout L{};
+  L.e = make_bwd_layout(c);
+  size_t off = L.e.total;
+  auto take = [&](int64_t bytes) {
+    size_t o = off;
+    off = al256(off + (size_t)bytes);
+    return o;
+  };
+  const int64_t T = c.T, k = c.top_k, d = c.d_model, Lt = c.d_latent, E = c.n_experts,
+                SF = (int64_t)c.n_shared * c.d_ff_shared, P = pool_rows_of(c);
+  const int64_t sf = SF > 0 ? SF : 1;
+  L.dc = take(T * Lt * 2);
+  L.gs = take(T * sf * 2);
+  L.us = take(T * sf * 2);
+  L.as2 = take(T * sf * 2);
+  L.dgs = take(T * sf * 2);
+  L.dus = take(T * sf * 2);
+  L.dy_perm = take(P * Lt * 2);
+  L.dgate = take(T * k * 4);
+  L.dx_perm = take(P * Lt * 2);
+  L.dz = take(T * Lt * 2);
+  L.dhz = take(T * Lt * 4);
+  L.dx32 = take(T * d * 4);
+  L.dl32 = take(T * E * 4);
+  L.dlbf = take(T * E * 2);
+  L.off01 = take(2 * 4);
+  L.total = off;
+  return L;
+}
+
+moe_status_t moe_layer_backward_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layer_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                          const void* dy, void* dx, const moe_grads_t* g, const void* fwd_ws,
+                          size_t fwd_ws_bytes, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!w || !g) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ptrs({x, dy, dx, w->w_router, w->w_down, w->rms_gamma, w->w1, w->w3, w->w2,
+                       w->w_up, g->dw_router, g->dw_down, g->dw1, g->dw3, g->dw2, g->dw_up},
+                      {g->db_router, g->drms_gamma})) != MOE_OK)
+    return s;
+  const int S = cfg->n_shared, Fs = cfg->d_ff_shared;
+  if (S > 0 && (s = check_ptrs({w->w1_s, w->w3_s, w->w2_s, g->dw1_s, g->dw3_s, g->dw2_s}, {})) !=
+                   MOE_OK)
+    return s;
+  if ((s = check_backward_cfg(*cfg)) != MOE_OK) return s;
+  const int64_t T = cfg->T, P = pool_rows_of(*cfg), SF = (int64_t)S * Fs;
+  const int d = cfg->d_model, L = cfg->d_latent, E = cfg->n_experts, kk = cfg->top_k;
+  // tile divisibility of the dense gradients (output rows of 128, columns of 64) and at most
+  // two shared experts (the input gradient's GEMM sums at most six K segments)
+  if ((d % 128) || (E % 64) || (S > 0 && ((SF % 128) || (Fs % 64))) || S > 2)
     return MOE_ERR_UNSUPPORTED;
+  if (!fwd_ws || fwd_ws_bytes < make_layout(*cfg).total) return MOE_ERR_WORKSPACE;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 255u) || ((uintptr_t)fwd_ws & 255u)) return MOE_ERR_ALIGNMENT;
+  const LayerBwdLayout B = make_layer_bwd_layout(*cfg);
+  if (ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+  Call k = make_call(cfg, ws, stream);
+  k.L.hdr = B.e.hdr;
+  auto at = [&](size_t off) { return static_cast<void*>(k.ws + off); };
+  const Layout FL = make_layout(*cfg);
+  const unsigned char* fw = static_cast<const unsigned char*>(fwd_ws);
+  auto fat = [&](size_t off) { return static_cast<const void*>(fw + off); };
+  const int32_t* idx = static_cast<const int32_t*>(fat(FL.idx));
+  const float* gate = static_cast<const float*>(fat(FL.gate));
+  const int32_t* slot_of = static_cast<const int32_t*>(fat(FL.slot_of));
+  const int32_t* offsets = static_cast<const int32_t*>(fat(FL.offsets));
+  int32_t* off01 = static_cast<int32_t*>(at(B.off01));
+
+  // 1. the shared experts' pre-activations (recomputed)
+  GemmProblem shr;
+  if (S > 0) {
+    shr = shared_problem(k, x, w->w1_s, w->w3_s, at(B.as2));
+    shr.epi = EPI_SWIGLU_SAVE;
+    shr.out2 = at(B.gs);
+    shr.out3 = at(B.us);
+  }
+  // 2. dc = dy W_up^T and the shared experts' dA = dy W2s^T with their SwiGLU backward
+  GemmProblem d1[2];
+  d1[0].epi = EPI_STORE;
+  d1[0].M = L;
+  d1[0].seg[0] = {dy, w->w_up, nullptr, d};
+  d1[0].a_kmajor = 1;
+  d1[0].rows = T;
+  d1[0].out = at(B.dc);
+  d1[0].ld_out = L;
+  d1[0].dtype = DT_BF16;
+  if (S > 0) {
+    d1[1].epi = EPI_SWIGLU_BWD;
+    d1[1].M = (int)SF;
+    d1[1].seg[0] = {dy, w->w2_s, nullptr, d};
+    d1[1].a_kmajor = 1;
+    d1[1].rows = T;
+    d1[1].out = at(B.dgs);
+    d1[1].out2 = at(B.dus);
+    d1[1].ld_out = SF;
+    d1[1].aux_g = at(B.gs);
+    d1[1].aux_u = at(B.us);
+    d1[1].ld_aux = SF;
+    d1[1].dtype = DT_BF16;
+  }
+  // 3. dW_up = c^T dy and dW2s = a_s^T dy (one group of T rows)
+  WgradProblem w1g[2];
+  w1g[0].a = fat(FL.c);
+  w1g[0].b = dy;
+  w1g[0].offsets = off01;
+  w1g[0].M = L;
+  w1g[0].N = d;
+  w1g[0].rows = T;
+  w1g[0].out = g->dw_up;
+  if (S > 0) {
+    w1g[1] = w1g[0];
+    w1g[1].a = fat(FL.a_s);
+    w1g[1].M = (int)SF;
+    w1g[1].out = g->dw2_s;
+  }
+  // 8. dx32 = dz W_down^T + sum_s dG_s W1_s[s]^T + dU_s W3_s[s]^T
+  GemmProblem dxp;
+  dxp.epi = EPI_F32;
+  dxp.M = d;
+  dxp.seg[0] = {at(B.dz), w->w_down, nullptr, L};
+  dxp.n_seg = 1;
+  for (int e = 0; e < S; ++e) {
+    const int64_t wo = (int64_t)e * d * Fs * 2;      // bytes to shared expert e's [d, F_s]
+    GemmSeg g1, g3;
+    g1.act = static_cast<const unsigned char*>(at(B.dgs)) + (int64_t)e * Fs * 2;
+    g1.w = static_cast<const unsigned char*>(w->w1_s) + wo;
+    g1.w3 = nullptr;
+    g1.K = Fs;
+    g1.ld = SF;
+    g3 = g1;
+    g3.act = static_cast<const unsigned char*>(at(B.dus)) + (int64_t)e * Fs * 2;
+    g3.w = static_cast<const unsigned char*>(w->w3_s) + wo;
+    dxp.seg[dxp.n_seg++] = g1;
+    dxp.seg[dxp.n_seg++] = g3;
+  }
+  dxp.a_kmajor = 1;
+  dxp.rows = T;
+  dxp.out = at(B.dx32);
+  dxp.ld_out = d;
+  dxp.dtype = DT_BF16;
+  // 11. dW_down = x^T dz; dW1_s[s] = x^T dG_s, dW3_s[s] = x^T dU_s; dW_r = x^T dl
+  WgradProblem w2g[6];
+  int n_w2 = 0;
+  WgradProblem base;
+  base.a = x;
+  base.offsets = off01;
+  base.M = d;
+  base.rows = T;
+  w2g[n_w2] = base;
+  w2g[n_w2].b = at(B.dz);
+  w2g[n_w2].N = L;
+  w2g[n_w2++].out = g->dw_down;
+  for (int e = 0; e < S; ++e) {
+    const int64_t wo = (int64_t)e * d * Fs * 2;
+    w2g[n_w2] = base;
+    w2g[n_w2].b = static_cast<const unsigned char*>(at(B.dgs)) + (int64_t)e * Fs * 2;
+    w2g[n_w2].ldb = SF;
+    w2g[n_w2].N = Fs;
+    w2g[n_w2++].out = static_cast<unsigned char*>(g->dw1_s) + wo;
+    w2g[n_w2] = w2g[n_w2 - 1];
+    w2g[n_w2].b = static_cast<const unsigned char*>(at(B.dus)) + (int64_t)e * Fs * 2;
+    w2g[n_w2++].out = static_cast<unsigned char*>(g->dw3_s) + wo;
+  }
+  w2g[n_w2] = base;
+  w2g[n_w2].b = at(B.dlbf);
+  w2g[n_w2].N = E;
+  w2g[n_w2++].out = g->dw_router;
+
+  if ((S > 0 && !gemm_tc_supported(shr)) || !gemm_tc_supported(d1[0]) ||
+      (S > 0 && !gemm_tc_supported(d1[1])) || !gemm_tc_supported(dxp))
+    return MOE_ERR_UNSUPPORTED;
+  for (int i = 0; i < (S > 0 ? 2 : 1); ++i)
+    if (!gemm_wgrad_supported(w1g[i])) return MOE_ERR_UNSUPPORTED;
+  for (int i = 0; i < n_w2; ++i)
+    if (!gemm_wgrad_supported(w2g[i])) return MOE_ERR_UNSUPPORTED;
 
   MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false));
-  MOE_TRY_CUDA(validate_offsets(expert_offsets, E, P, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_tc(&rec, 1, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_tc(&da, 1, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_tc(&dx, 1, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_wgrad(&w2g, 1, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_wgrad(w13, 2, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(write_int2(off01, 0, (int32_t)T, k.st, k.pdl));
+  if (S > 0) MOE_TRY_CUDA(gemm_tc(&shr, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(d1, S > 0 ? 2 : 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(w1g, S > 0 ? 2 : 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(combine_backward(at(B.dc), fat(FL.y_perm), slot_of, gate, T, kk, L, P,
+                                at(B.dy_perm), static_cast<float*>(at(B.dgate)), k.st, k.pdl));
+  moe_status_t es = expert_backward_launches(
+      k, fat(FL.x_perm), offsets, w->w1, w->w3, w->w2, at(B.dy_perm), at(B.dx_perm), g->dw1,
+      g->dw3, g->dw2, {at(B.e.g), at(B.e.u), at(B.e.a), at(B.e.dg), at(B.e.du)});
+  if (es != MOE_OK) return es;
+  MOE_TRY_CUDA(rms_backward(at(B.dx_perm), slot_of, static_cast<const float*>(fat(FL.z)),
+                            w->rms_gamma, cfg->rms_eps, T, kk, L, P, at(B.dz),
+                            static_cast<float*>(at(B.dhz)), k.st, k.pdl));
+  if (g->drms_gamma)
+    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dhz)), T, L, g->drms_gamma, k.st,
+                            k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&dxp, 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(router_backward(idx, gate, static_cast<const float*>(at(B.dgate)), fat(FL.wrT),
+                               static_cast<const float*>(at(B.dx32)), T, kk, E, d, dx,
+                               static_cast<float*>(at(B.dl32)), at(B.dlbf), k.st, k.pdl));
+  if (g->db_router)
+    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dl32)), T, E, g->db_router, k.st,
+                            k.pdl));
+  MOE_TRY_CUDA(gemm_wgrad(w2g, n_w2, k.hdr(), k.st, k.pdl));
   return MOE_OK;
 }
 

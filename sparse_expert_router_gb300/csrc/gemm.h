@@ -20,13 +20,16 @@ namespace moe {
 enum Epi { EPI_F32 = 0, EPI_STORE = 1, EPI_SWIGLU = 2, EPI_SWIGLU_SAVE = 3, EPI_SWIGLU_BWD = 4 };
 enum GroupMode { GROUP_NONE = 0, GROUP_ROWS = 1, GROUP_COLS = 2 };
 
+constexpr int GEMM_MAX_SEG = 6;
+
 struct GemmSeg {
-  const void* act;   // [rows, K] row-major (leading dimension K)
+  const void* act;   // [rows, K] row-major (leading dimension ld, or K when ld is 0)
   // NONE: [K, M]; ROWS: [G, K, M]; COLS: [M / Mg, K, Mg]. With a_kmajor the bank holds the
   // transposed matrices, [M, K] per weight group (a stored [d_in, d_out] weight used as W^T).
   const void* w;
   const void* w3;    // EPI_SWIGLU: the up-projection weights, same layout as w
   int K;
+  int64_t ld = 0;    // tcgen05 only: elements between rows of act (0: K)
 };
 
 struct GemmProblem {
@@ -35,7 +38,7 @@ struct GemmProblem {
   int M = 0;                 // output columns
   int Mg = 0;                // GROUP_COLS: columns per weight matrix
   int n_seg = 1;
-  GemmSeg seg[2] = {};
+  GemmSeg seg[GEMM_MAX_SEG] = {};
   const int32_t* offsets = nullptr;  // GROUP_ROWS: [G + 1], device
   int G = 1;
   int64_t rows = 0;          // rows of act and out (GROUP_ROWS: physical rows; offsets clamp to it)

@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
 cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl) {
   // fp8, transposed weights and the backward epilogues run on tensor cores only
   if (p.w_fp8 || p.out_fp8 || p.a_kmajor || p.epi > EPI_SWIGLU) return cudaErrorNotSupported;
+  for (int s = 0; s < p.n_seg; ++s)
+    if (p.seg[s].ld && p.seg[s].ld != p.seg[s].K) return cudaErrorNotSupported;
   if (p.rows <= 0 || p.M <= 0) return cudaSuccess;
   int64_t tiles = cdiv(p.rows, BM) + (p.group == GROUP_ROWS ? p.G : 0);
   dim3 grid((unsigned)tiles, (unsigned)cdiv(p.M, BN));

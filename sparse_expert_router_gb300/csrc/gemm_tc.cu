@@ -78,7 +78,7 @@ struct TcSeg {
 };
 
 struct TcProblem {
-  TcSeg seg[2];
+  TcSeg seg[GEMM_MAX_SEG];
   int n_seg;
   int epi, group, M, Mg, m_tiles;
   int n_fastest;               // dense problems: token tiles vary fastest
@@ -716,10 +716,10 @@ bool map_weights_kmajor(CUtensorMap* m, const void* ptr, int64_t Mw, int64_t K, 
 
 // Activations [rows, K] (K contiguous): 2-D map with a box of one 128-byte swizzle row (64 bf16
 // or 128 E4M3) by 32 rows, 128-byte swizzle.
-bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, bool fp8) {
+bool map_act(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, bool fp8, int64_t ld = 0) {
   const int64_t es_bytes = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(K * es_bytes)};
+  cuuint64_t strides[1] = {(cuuint64_t)((ld ? ld : K) * es_bytes)};
   cuuint32_t box[2] = {(cuuint32_t)(fp8 ? BK8 : BK), B_BOX_ROWS};
   cuuint32_t es[2] = {1, 1};
   return encode_fn()(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -744,7 +744,9 @@ bool gemm_tc_supported(const GemmProblem& p) {
   if (Mw < 64 || (Mw % 8)) return false;
   if (p.group == GROUP_COLS && (p.Mg % BM || p.M % p.Mg)) return false;
   if (p.group == GROUP_ROWS && (p.G < 1 || p.G > MAX_GROUPS)) return false;
-  if (p.n_seg < 1 || p.n_seg > 2) return false;
+  if (p.n_seg < 1 || p.n_seg > GEMM_MAX_SEG) return false;
+  for (int s = 0; s < p.n_seg; ++s)   // an activation row stride: 16-byte aligned, >= K
+    if (p.seg[s].ld && (p.seg[s].ld < p.seg[s].K || (p.seg[s].ld % 8) || p.w_fp8)) return false;
   for (int s = 0; s < p.n_seg; ++s)
     if (p.seg[s].K < 8 || (p.seg[s].K % 8)) return false;
   if (p.epi < EPI_F32 || p.epi > EPI_SWIGLU_BWD) return false;
@@ -841,7 +843,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       };
       if (!mapw(&ts.a1, sg.w)) return cudaErrorInvalidValue;
       if (is_glu(g.epi) && !mapw(&ts.a3, sg.w3)) return cudaErrorInvalidValue;
-      if (!map_act(&ts.b, sg.act, sg.K, g.rows, g.w_fp8 != 0)) return cudaErrorInvalidValue;
+      if (!map_act(&ts.b, sg.act, sg.K, g.rows, g.w_fp8 != 0, sg.ld)) return cudaErrorInvalidValue;
     }
     q.item_base = base;
     if (g.group == GROUP_ROWS) {

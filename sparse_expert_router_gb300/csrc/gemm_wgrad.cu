@@ -40,7 +40,7 @@ constexpr int WB_ATOM = 64 * WK * 2; // one [64 rows][64 columns] box: 8 KB
 constexpr int WB_BYTES = 4 * WB_ATOM;
 constexpr int W_STAGE = WA_BYTES + WB_BYTES;   // 48 KB
 constexpr int W_STAGES = 4;
-constexpr int W_MAX_PROBS = 2;
+constexpr int W_MAX_PROBS = 6;
 constexpr int W_OUT_TILE = 32 * 64 * 2;   // one warp's store tile: 32 rows x 64 bf16 columns
 
 struct WgProb {
@@ -301,9 +301,9 @@ PFN_cuTensorMapEncodeTiled_v12000 wg_encode_fn() {
 
 // [rows, cols] bf16 row-major as an MN-major operand: 64 columns (one 128-byte swizzle row) by
 // 64 rows per box.
-bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
+bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t ld) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint64_t strides[1] = {(cuuint64_t)((ld ? ld : cols) * 2)};
   cuuint32_t box[2] = {64, WK};
   cuuint32_t es[2] = {1, 1};
   return wg_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
@@ -329,7 +329,9 @@ bool map_out(CUtensorMap* m, void* ptr, int64_t cols, int64_t rows) {
 
 bool gemm_wgrad_supported(const WgradProblem& p) {
   return p.a && p.b && p.offsets && p.out && p.G >= 1 && p.M >= WM && p.M % WM == 0 &&
-         p.N >= 64 && p.N % 64 == 0 && p.rows >= 0 && p.rows < (1ll << 31);
+         p.N >= 64 && p.N % 64 == 0 && p.rows >= 0 && p.rows < (1ll << 31) &&
+         (p.lda == 0 || (p.lda >= p.M && p.lda % 8 == 0)) &&
+         (p.ldb == 0 || (p.ldb >= p.N && p.ldb % 8 == 0));
 }
 
 cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
@@ -345,7 +347,7 @@ cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
     if (!gemm_wgrad_supported(g)) return cudaErrorNotSupported;
     WgProb& q = P.p[j];
     const int64_t rows = g.rows > 0 ? g.rows : 1;
-    if (!map_mn(&q.a, g.a, g.M, rows) || !map_mn(&q.b, g.b, g.N, rows) ||
+    if (!map_mn(&q.a, g.a, g.M, rows, g.lda) || !map_mn(&q.b, g.b, g.N, rows, g.ldb) ||
         !map_out(&q.o, g.out, g.N, (int64_t)g.G * g.M))
       return cudaErrorInvalidValue;
     q.offsets = g.offsets;

@@ -13,6 +13,7 @@ namespace moe {
 struct WgradProblem {
   const void* a;
   const void* b;
+  int64_t lda = 0, ldb = 0;   // elements between rows of a and b (0: M and N)
   const int32_t* offsets;   // [G + 1], device
   int G = 1;
   int M = 0, N = 0;

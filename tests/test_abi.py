@@ -174,3 +174,30 @@ def test_backward_argument_errors(lib):
     odd = _cfg(dtype="bf16", d_latent=128, d_ff=64)                    # width not /128
     assert lib.moe_expert_ffn_backward(C.byref(odd.c()), *args, ws, n.value, None) == \
         L.MOE_ERR_ALIGNMENT
+
+
+def test_layer_backward_argument_errors(lib):
+    from sparse_expert_router_gb300 import _lib as L
+    P = lambda v: C.c_void_p(v)
+    good, ws = P(0x10000), P(0x100000)
+    cfg = _cfg(dtype="bf16", d_model=256, d_latent=128, d_ff=128, n_experts=64, n_shared=1,
+               d_ff_shared=128)
+    c = C.byref(cfg.c())
+    n = C.c_size_t()
+    assert lib.moe_layer_backward_workspace_size(c, C.byref(n)) == L.MOE_OK
+    fw = _ws(lib, cfg)
+    w = L.moe_weights_t(**{f: 0x10000 for f in ("w_router", "w_down", "rms_gamma", "w1", "w3",
+                                                "w2", "w1_s", "w3_s", "w2_s", "w_up")})
+    grads = L.moe_grads_t(**{f: 0x10000 for f in L.GRAD_NAMES})
+    ok_args = (C.byref(w), good, good, good, C.byref(grads), P(0x200000), fw, ws, n.value, None)
+    none_g = L.moe_grads_t(**{f: 0x10000 for f in L.GRAD_NAMES if f != "dw_up"})
+    assert lib.moe_backward(c, C.byref(w), good, good, good, C.byref(none_g), P(0x200000), fw,
+                            ws, n.value, None) == L.MOE_ERR_INVALID_ARG        # dw_up missing
+    assert lib.moe_backward(c, C.byref(w), good, good, good, C.byref(grads), P(0x200000), fw - 256,
+                            ws, n.value, None) == L.MOE_ERR_WORKSPACE         # forward workspace
+    assert lib.moe_backward(c, *ok_args[:-3], ws, n.value - 256, None) == L.MOE_ERR_WORKSPACE
+    odd = _cfg(dtype="bf16", d_model=256, d_latent=128, d_ff=128, n_experts=48, n_shared=1,
+               d_ff_shared=128)                                                # E not /64
+    assert lib.moe_backward(C.byref(odd.c()), *ok_args) == L.MOE_ERR_UNSUPPORTED
+    f32 = _cfg(d_model=256, d_latent=128, d_ff=128, n_experts=64)
+    assert lib.moe_backward(C.byref(f32.c()), *ok_args) == L.MOE_ERR_UNSUPPORTED

@@ -616,3 +616,50 @@ def test_expert_backward_deterministic():
     b = _run_backward(c, E, L, F)
     for n in ("dx", "dw1", "dw3", "dw2"):
         assert torch.equal(a[n].view(torch.int16), b[n].view(torch.int16)), n
+
+
+# ---------------------------------------------------------------- layer backward ----
+
+def _layer_grads(shape, inp):
+    E, L, F, d = shape.n_experts, shape.d_latent, shape.d_ff, shape.d_model
+    S, Fs = shape.n_shared, shape.d_ff_shared
+    bf = dict(dtype=torch.bfloat16, device=DEV)
+    return {"dw_router": torch.full((d, E), 9.0, **bf),
+            "db_router": torch.full((E,), 9.0, dtype=torch.float32, device=DEV),
+            "dw_down": torch.full((d, L), 9.0, **bf),
+            "drms_gamma": torch.full((L,), 9.0, dtype=torch.float32, device=DEV),
+            "dw1": torch.full((E, L, F), 9.0, **bf), "dw3": torch.full((E, L, F), 9.0, **bf),
+            "dw2": torch.full((E, F, L), 9.0, **bf), "dw1_s": torch.full((S, d, Fs), 9.0, **bf),
+            "dw3_s": torch.full((S, d, Fs), 9.0, **bf), "dw2_s": torch.full((S, Fs, d), 9.0, **bf),
+            "dw_up": torch.full((L, d), 9.0, **bf)}
+
+
+@pytest.mark.parametrize("cap", [None, (1, 1)], ids=["nocap", "cf100"])
+def test_layer_backward(cap):
+    """dx and every weight gradient of the whole layer against the oracle's chain rule, after
+    the forward on the same inputs (with capacity drops in the second case)."""
+    shape = SHAPES["small_bf16"].with_(T=512, capacity=cap)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    cfg = m.LayerConfig.from_shape(shape)
+    T, d = shape.T, shape.d_model
+    fws = m.alloc_workspace(cfg, DEV)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    m.moe_forward(cfg, inp, inp["x"], y, fws)
+    g = torch.Generator().manual_seed(3)
+    dy = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    dx = torch.full((T, d), 9.0, dtype=torch.bfloat16, device=DEV)
+    grads = _layer_grads(shape, inp)
+    bws = m.alloc_layer_backward_workspace(cfg, DEV)
+    m.moe_backward(cfg, inp, inp["x"], dy.to(DEV), dx, grads, fws, bws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(bws)["status"] == 0
+    fwd = oracle_forward(shape, cpu)
+    if cap:
+        assert int(fwd["n_dropped"]) > 0
+    ref = moe_oracle.backward(cpu, fwd, dy, rms_eps=shape.rms_eps)
+    errs = {"dx": normwise(dx, ref["dx"])}
+    for n in grads:
+        errs[n] = normwise(grads[n].float(), ref[n])
+    bad = {n: e for n, e in errs.items() if not e <= 2e-2}
+    assert not bad, (bad, errs)
