@@ -754,7 +754,7 @@ moe_status_t moe_expert_ffn_backward(const moe_config_t* cfg, const void* x_perm
 struct LayerBwdLayout {
   BwdLayout e;
   size_t dc, gs, us, as2, dgs, dus, dy_perm, dgate, dx_perm, dz, dhz, dx32, dl32, dlbf, off01,
-      total;
+      colsum, total;
 };
 
 LayerBwdLayout make_layer_bwd_layout(const moe_config_t& c) {
@@ -784,6 +784,7 @@ LayerBwdLayout make_layer_bwd_layout(const moe_config_t& c) {
   L.dl32 = take(T * E * 4);
   L.dlbf = take(T * E * 2);
   L.off01 = take(2 * 4);
+  L.colsum = take((int64_t)COLSUM_CHUNKS * (Lt > E ? Lt : E) * 4);
   L.total = off;
   return L;
 }
@@ -957,15 +958,15 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_weights_t* w, const
                             w->rms_gamma, cfg->rms_eps, T, kk, L, P, at(B.dz),
                             static_cast<float*>(at(B.dhz)), k.st, k.pdl));
   if (g->drms_gamma)
-    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dhz)), T, L, g->drms_gamma, k.st,
-                            k.pdl));
+    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dhz)), T, L,
+                            static_cast<float*>(at(B.colsum)), g->drms_gamma, k.st, k.pdl));
   MOE_TRY_CUDA(gemm_tc(&dxp, 1, k.hdr(), k.st, k.pdl));
   MOE_TRY_CUDA(router_backward(idx, gate, static_cast<const float*>(at(B.dgate)), fat(FL.wrT),
                                static_cast<const float*>(at(B.dx32)), T, kk, E, d, dx,
                                static_cast<float*>(at(B.dl32)), at(B.dlbf), k.st, k.pdl));
   if (g->db_router)
-    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dl32)), T, E, g->db_router, k.st,
-                            k.pdl));
+    MOE_TRY_CUDA(column_sum(static_cast<const float*>(at(B.dl32)), T, E,
+                            static_cast<float*>(at(B.colsum)), g->db_router, k.st, k.pdl));
   MOE_TRY_CUDA(gemm_wgrad(w2g, n_w2, k.hdr(), k.st, k.pdl));
   return MOE_OK;
 }

@@ -146,13 +146,26 @@ __global__ void __launch_bounds__(256) router_backward_kernel(
   }
 }
 
-__global__ void __launch_bounds__(256) column_sum_kernel(const float* m, int64_t rows, int cols,
-                                                         float* out) {
+// Block (x, y): columns 256x.., rows of chunk y; partial[y][c] = the chunk's column sums.
+__global__ void __launch_bounds__(256) column_partial_kernel(const float* m, int64_t rows,
+                                                             int cols, float* partial) {
+  pdl_wait();
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  if (c >= cols) return;
+  const int64_t per = cdiv(rows, (int64_t)gridDim.y);
+  const int64_t r0 = blockIdx.y * per, r1 = imin64(rows, r0 + per);
+  float acc = 0.0f;
+  for (int64_t r = r0; r < r1; ++r) acc += m[r * cols + c];
+  partial[(int64_t)blockIdx.y * cols + c] = acc;
+}
+
+__global__ void __launch_bounds__(256) column_final_kernel(const float* partial, int chunks,
+                                                           int cols, float* out) {
   pdl_wait();
   const int c = blockIdx.x * 256 + threadIdx.x;
   if (c >= cols) return;
   float acc = 0.0f;
-  for (int64_t r = 0; r < rows; ++r) acc += m[r * cols + c];
+  for (int y = 0; y < chunks; ++y) acc += partial[(int64_t)y * cols + c];
   out[c] = acc;
 }
 
@@ -191,10 +204,14 @@ cudaError_t router_backward(const int32_t* idx, const float* gate, const float* 
                 dl32, static_cast<bf16*>(dlbf));
 }
 
-cudaError_t column_sum(const float* m, int64_t rows, int cols, float* out, cudaStream_t st,
-                       bool pdl) {
-  return launch(column_sum_kernel, dim3((unsigned)cdiv(cols, 256)), dim3(256), 0, st, pdl, m,
-                rows, cols, out);
+cudaError_t column_sum(const float* m, int64_t rows, int cols, float* partial, float* out,
+                       cudaStream_t st, bool pdl) {
+  const unsigned cx = (unsigned)cdiv(cols, 256);
+  cudaError_t e = launch(column_partial_kernel, dim3(cx, COLSUM_CHUNKS), dim3(256), 0, st, pdl,
+                         m, rows, cols, partial);
+  if (e != cudaSuccess) return e;
+  return launch(column_final_kernel, dim3(cx), dim3(256), 0, st, pdl, (const float*)partial,
+                COLSUM_CHUNKS, cols, out);
 }
 
 }  // namespace moe

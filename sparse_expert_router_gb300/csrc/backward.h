@@ -28,8 +28,10 @@ cudaError_t router_backward(const int32_t* idx, const float* gate, const float* 
 // p[0] = a, p[1] = b (device).
 cudaError_t write_int2(int32_t* p, int32_t a, int32_t b, cudaStream_t st, bool pdl);
 
-// out[c] = sum over r (in order) of m[r * cols + c], fp32.
-cudaError_t column_sum(const float* m, int64_t rows, int cols, float* out, cudaStream_t st,
-                       bool pdl);
+// out[c] = sum over r of m[r * cols + c], fp32, in a fixed order: COLSUM_CHUNKS row chunks are
+// summed in parallel into partial [COLSUM_CHUNKS, cols], then the chunks in order.
+constexpr int COLSUM_CHUNKS = 128;
+cudaError_t column_sum(const float* m, int64_t rows, int cols, float* partial, float* out,
+                       cudaStream_t st, bool pdl);
 
 }  // namespace moe

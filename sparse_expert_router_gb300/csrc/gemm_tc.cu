@@ -546,6 +546,19 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         }
         continue;
       }
+      if constexpr (BWD) {
+        if (q.epi == EPI_SWIGLU_BWD) {
+          // G and U of this item (nrows x 128 features, 256-byte row pieces) head for L2 while
+          // the main loop runs, so that the epilogue's loads of them hit L2
+          const int nl = it.nrows * 4;            // 2 tensors x 2 lines of 128 bytes per row
+          for (int i = threadIdx.x - 64; i < nl; i += 32 * EPI_WARPS) {
+            const int r = i >> 2, t2 = (i >> 1) & 1, line = i & 1;
+            const bf16* base_p = static_cast<const bf16*>(t2 ? q.aux_u : q.aux_g);
+            const bf16* ptr = base_p + (it.row0 + r) * q.ld_aux + it.m0 + line * 64;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+          }
+        }
+      }
       const int buf = ev % nacc;
       const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
       ++ev;
@@ -604,14 +617,22 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
             const bf16* gp = static_cast<const bf16*>(q.aux_g);
             const bf16* up = static_cast<const bf16*>(q.aux_u);
             const int valid = min(16, it.nrows - c0);
+            // all 32 loads first (packed in pairs), so that they are in flight together
+            __nv_bfloat162 gg[8], uu[8];
+            const bf16 zero = __float2bfloat16_rn(0.0f);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              bf16 g0 = zero, g1 = zero, u0 = zero, u1 = zero;
+              const int64_t o = (it.row0 + c0 + j) * q.ld_aux + f0 + lane;
+              if (fok && j < valid) { g0 = gp[o]; u0 = up[o]; }
+              if (fok && j + 1 < valid) { g1 = gp[o + q.ld_aux]; u1 = up[o + q.ld_aux]; }
+              gg[j / 2] = __halves2bfloat162(g0, g1);
+              uu[j / 2] = __halves2bfloat162(u0, u1);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              float g = 0.0f, u = 0.0f;
-              if (fok && j < valid) {
-                const int64_t o = (it.row0 + c0 + j) * q.ld_aux + f0 + lane;
-                g = __bfloat162float(gp[o]);
-                u = __bfloat162float(up[o]);
-              }
+              const float g = (j & 1) ? __high2float(gg[j / 2]) : __low2float(gg[j / 2]);
+              const float u = (j & 1) ? __high2float(uu[j / 2]) : __low2float(uu[j / 2]);
               const float sg = __fdiv_rn(1.0f, 1.0f + expf(-g));   // sigmoid(G)
               v3[j] = v[j] * u * (sg * (1.0f + g * (1.0f - sg)));
               v[j] = v[j] * (g * sg);
