@@ -239,7 +239,7 @@ def make_layer_inputs(shape: LayerShape, device="cpu", *, T: Optional[int] = Non
         "rms_gamma": torch.ones(L, dtype=torch.float32, device=device),
         "w1_s": _stacked_normal(S, d, Fs, d ** -0.5, dt, device, s.seed, "w1_s"),
         "w3_s": _stacked_normal(S, d, Fs, d ** -0.5, dt, device, s.seed, "w3_s"),
-        "w2_s": _stacked_normal(S, Fs, d, Fs ** -0.5, dt, device, s.seed, "w2_s"),
+        "w2_s": _stacked_normal(S, Fs, d, max(Fs, 1) ** -0.5, dt, device, s.seed, "w2_s"),
         "w_up": _normal((L, d), L ** -0.5, dt, device, tensor_seed(s.seed, "w_up")),
     }
     if s.expert_dtype == "fp8":

@@ -276,6 +276,8 @@ def shared_experts(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor,
 def shared_hidden(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor) -> torch.Tensor:
     """Shared experts' hidden activations, concatenated along the feature axis [T, S*F_s]."""
     x64 = to64(x)
+    if w1_s.shape[0] == 0:                       # no shared experts
+        return torch.zeros((x64.shape[0], 0), dtype=F64)
     return torch.cat([swiglu_hidden(x64, to64(w1_s[s]), to64(w3_s[s]))
                       for s in range(w1_s.shape[0])], dim=1)
 

@@ -663,3 +663,53 @@ def test_layer_backward(cap):
         errs[n] = normwise(grads[n].float(), ref[n])
     bad = {n: e for n, e in errs.items() if not e <= 2e-2}
     assert not bad, (bad, errs)
+
+
+# -------------------------------------------------------------------- edge cases ----
+
+from moe_workloads import LayerShape  # noqa: E402
+
+EDGE = {
+    # one token; every stage runs on a single row
+    "t1_f32": (LayerShape("t1_f32", T=1, d_model=256, d_latent=128, n_experts=16, top_k=2,
+                          d_ff=128, n_shared=1, d_ff_shared=256, dtype="f32"), 0),
+    "t1_bf16": (LayerShape("t1_bf16", T=1, d_model=256, d_latent=128, n_experts=64, top_k=8,
+                           d_ff=128, n_shared=1, d_ff_shared=256, dtype="bf16"), 0),
+    # k = E: every expert selected, gates = the full softmax
+    "k_eq_e": (LayerShape("k_eq_e", T=257, d_model=256, d_latent=128, n_experts=16, top_k=16,
+                          d_ff=128, n_shared=1, d_ff_shared=256, dtype="f32"), 0),
+    # k = 1 with a capacity of one row per expert and ragged token count
+    "k1_cap": (LayerShape("k1_cap", T=333, d_model=256, d_latent=128, n_experts=16, top_k=1,
+                          d_ff=128, n_shared=1, d_ff_shared=256, dtype="f32",
+                          capacity=(1, 21)), 0),
+    # the limits: 1024 experts, top-32, ragged T on the tensor-core path
+    "e1024_k32": (LayerShape("e1024_k32", T=300, d_model=256, d_latent=128, n_experts=1024,
+                             top_k=32, d_ff=128, n_shared=0, d_ff_shared=0, dtype="bf16"), 0),
+    "e1024_k32_simt": (LayerShape("e1024_k32_simt", T=129, d_model=256, d_latent=128,
+                                  n_experts=1024, top_k=32, d_ff=128, n_shared=0, d_ff_shared=0,
+                                  dtype="bf16"), m.MOE_FLAG_SIMT),
+    # no shared experts, latent == model width, T one past a 256-row token tile
+    "no_shared": (LayerShape("no_shared", T=257, d_model=128, d_latent=128, n_experts=64,
+                             top_k=4, d_ff=256, n_shared=0, d_ff_shared=0, dtype="bf16"), 0),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_case_forward(name):
+    """Every token's routing, dispatch and output against the oracle at the edges the method
+    allows: a single token, k = E, k = 1 with capacity 1, 1024 experts with top-32, no shared
+    experts, token counts one past a tile."""
+    shape, flags = EDGE[name]
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    got = run_forward(shape, inp, flags)
+    ref = oracle_forward(shape, cpu)
+    check_routing(got, ref, shape)
+    if shape.capacity:
+        assert int(ref["n_dropped"]) > 0
+    if shape.top_k == shape.n_experts:
+        assert torch.equal(got["topk_idx"].cpu(), torch.arange(shape.n_experts, dtype=torch.int32)
+                           .expand(shape.T, -1))
+    err = normwise(got["y"], ref["y"])
+    assert err <= (1e-5 if shape.dtype == "f32" else 2e-2), err
+    assert got["report"]["status"] == 0
