@@ -307,6 +307,19 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, co
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, void* y,
                          void* ws, size_t ws_bytes, void* stream, const moe_forward_aux_t* aux);
 
+/* Serving over host memory: moe_forward on n_batches batches, batch i reading x_host[i] and
+ * writing y_host[i] ([T, d] each in the layer dtype; pinned host memory makes the copies
+ * asynchronous). Batch i + 1's input is copied in on h2d_stream and batch i - 1's output copied
+ * out on d2h_stream while batch i runs on `stream`; x_stage and y_stage are device staging
+ * buffers of 2 * T * d elements each (two slots), ws as for moe_forward. The three streams must
+ * be distinct. Returns once everything is enqueued; `stream` completes after the last output
+ * copy. */
+MOE_API moe_status_t moe_forward_pipelined(const moe_config_t* cfg, const moe_weights_t* w,
+                                           int32_t n_batches, const void* const* x_host,
+                                           void* const* y_host, void* x_stage, void* y_stage,
+                                           void* ws, size_t ws_bytes, void* stream,
+                                           void* h2d_stream, void* d2h_stream);
+
 /* Waits for `stream`, then copies the device report out of the workspace into *out (host
  * memory). Returns MOE_ERR_CUDA if the wait or the copy fails. */
 MOE_API moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream,

@@ -22,6 +22,7 @@ __all__ = ["MoEError", "LayerConfig", "load", "workspace_size", "alloc_workspace
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
            "backward_workspace_size", "alloc_backward_workspace", "moe_expert_ffn_backward",
            "layer_backward_workspace_size", "alloc_layer_backward_workspace", "moe_backward",
+           "moe_forward_pipelined",
            "GRAD_NAMES",
            "moe_get_device_status", "moe_clear_device_status", "moe_route_noalloc",
            "moe_selftest_device_timeout",
@@ -225,6 +226,25 @@ def moe_forward(cfg, weights: Dict[str, torch.Tensor], x, y, ws, stream=None,
     _check("moe_forward", load().moe_forward(C.byref(cfg.c()), C.byref(w), _p(x), _p(y), _p(ws),
                                              ws.numel(), _stream(stream),
                                              C.byref(a) if a is not None else None))
+    del keep
+
+
+def moe_forward_pipelined(cfg, weights: Dict[str, torch.Tensor], x_hosts, y_hosts, x_stage,
+                          y_stage, ws, stream, h2d_stream, d2h_stream):
+    """moe_forward over host batches x_hosts[i] -> y_hosts[i] (pinned CPU tensors), copies
+    overlapped with the forwards on two more streams; x_stage / y_stage: [2, T, d] device."""
+    w = moe_weights_t(**{n: (weights[n].data_ptr() if weights.get(n) is not None else None)
+                         for n in WEIGHT_NAMES})
+    keep = None
+    if cfg.flags & MOE_FLAG_FP8_EXPERTS:
+        keep = _fp8({n: weights.get(n) for n in FP8_NAMES[:5]})
+        w.fp8 = keep
+    n = len(x_hosts)
+    xs = (C.c_void_p * n)(*[t.data_ptr() for t in x_hosts])
+    ys = (C.c_void_p * n)(*[t.data_ptr() for t in y_hosts])
+    _check("moe_forward_pipelined", load().moe_forward_pipelined(
+        C.byref(cfg.c()), C.byref(w), n, xs, ys, _p(x_stage), _p(y_stage), _p(ws), ws.numel(),
+        _stream(stream), _stream(h2d_stream), _stream(d2h_stream)))
     del keep
 
 

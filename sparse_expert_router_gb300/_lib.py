@@ -89,6 +89,9 @@ SIGNATURES = {
     "moe_expert_ffn_backward": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_forward": (C.c_int, [CFG, C.POINTER(moe_weights_t), P, P, P, C.c_size_t, P,
                               C.POINTER(moe_forward_aux_t)]),
+    "moe_forward_pipelined": (C.c_int, [CFG, C.POINTER(moe_weights_t), C.c_int32,
+                                        C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), P, P, P,
+                                        C.c_size_t, P, P, P]),
     "moe_get_device_status": (C.c_int, [P, C.c_size_t, P, C.POINTER(moe_device_report_t)]),
     "moe_clear_device_status": (C.c_int, [P, C.c_size_t, P]),
     "moe_route_noalloc": (C.c_int, [CFG, P, P, P, P, P, P, P]),

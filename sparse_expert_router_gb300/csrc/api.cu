@@ -1082,6 +1082,69 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   return MOE_OK;
 }
 
+moe_status_t moe_forward_pipelined(const moe_config_t* cfg, const moe_weights_t* w,
+                                   int32_t n_batches, const void* const* x_host,
+                                   void* const* y_host, void* x_stage, void* y_stage, void* ws,
+                                   size_t ws_bytes, void* stream, void* h2d_stream,
+                                   void* d2h_stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (n_batches < 1 || !x_host || !y_host || !w) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_batches; ++i)
+    if (!x_host[i] || !y_host[i]) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ptrs({x_stage, y_stage}, {})) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t up = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t dn = static_cast<cudaStream_t>(d2h_stream);
+  if (up == st || dn == st || up == dn) return MOE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)cfg->T * cfg->d_model * (cfg->dtype == MOE_BF16 ? 2 : 4);
+  unsigned char* xs = static_cast<unsigned char*>(x_stage);
+  unsigned char* ys = static_cast<unsigned char*>(y_stage);
+  // events: input copied in, forward done, output copied out (per batch)
+  const int n = n_batches;
+  cudaEvent_t* ev = new cudaEvent_t[3 * (size_t)n]();
+  auto cleanup = [&]() {
+    for (int i = 0; i < 3 * n; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);   // released once the recorded work completes
+    delete[] ev;
+  };
+  for (int i = 0; i < 3 * n; ++i)
+    if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+      ev[i] = nullptr;
+      cleanup();
+      return MOE_ERR_CUDA;
+    }
+  cudaEvent_t* in = ev;
+  cudaEvent_t* done = ev + n;
+  cudaEvent_t* out = ev + 2 * n;
+  moe_status_t rs = MOE_OK;
+  for (int i = 0; i < n && rs == MOE_OK; ++i) {
+    const size_t o = (size_t)(i & 1) * bytes;
+    auto step = [&]() -> moe_status_t {
+      // batch i's input into staging slot i % 2, once batch i - 2's forward has read it
+      if (i >= 2) MOE_TRY_CUDA(cudaStreamWaitEvent(up, done[i - 2], 0));
+      MOE_TRY_CUDA(cudaMemcpyAsync(xs + o, x_host[i], bytes, cudaMemcpyHostToDevice, up));
+      MOE_TRY_CUDA(cudaEventRecord(in[i], up));
+      // the forward, once its input has landed and batch i - 2's output has been copied out
+      MOE_TRY_CUDA(cudaStreamWaitEvent(st, in[i], 0));
+      if (i >= 2) MOE_TRY_CUDA(cudaStreamWaitEvent(st, out[i - 2], 0));
+      moe_status_t f = moe_forward(cfg, w, xs + o, ys + o, ws, ws_bytes, stream, nullptr);
+      if (f != MOE_OK) return f;
+      MOE_TRY_CUDA(cudaEventRecord(done[i], st));
+      // batch i's output back to the host
+      MOE_TRY_CUDA(cudaStreamWaitEvent(dn, done[i], 0));
+      MOE_TRY_CUDA(cudaMemcpyAsync(y_host[i], ys + o, bytes, cudaMemcpyDeviceToHost, dn));
+      MOE_TRY_CUDA(cudaEventRecord(out[i], dn));
+      return MOE_OK;
+    };
+    rs = step();
+  }
+  // the caller's stream completes after the last output copy
+  if (rs == MOE_OK && cudaStreamWaitEvent(st, out[n - 1], 0) != cudaSuccess) rs = MOE_ERR_CUDA;
+  cleanup();
+  return rs;
+}
+
 moe_status_t moe_get_device_status(const void* ws, size_t ws_bytes, void* stream,
                                    moe_device_report_t* out) {
   if (!ws || !out || ws_bytes < sizeof(DeviceHeader)) return MOE_ERR_INVALID_ARG;

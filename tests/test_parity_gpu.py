@@ -713,3 +713,27 @@ def test_edge_case_forward(name):
     err = normwise(got["y"], ref["y"])
     assert err <= (1e-5 if shape.dtype == "f32" else 2e-2), err
     assert got["report"]["status"] == 0
+
+
+def test_forward_pipelined_matches_forward():
+    """The host-buffer serving path gives, batch for batch, the bits moe_forward gives."""
+    shape = SHAPES["small_bf16"].with_(T=512)
+    inp = gpu_inputs(shape)
+    cfg = m.LayerConfig.from_shape(shape, flags=m.MOE_FLAG_PDL)
+    T, d = shape.T, shape.d_model
+    g = torch.Generator().manual_seed(4)
+    xs = [torch.randn(T, d, generator=g).to(torch.bfloat16).pin_memory() for _ in range(5)]
+    ys = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    ws = m.alloc_workspace(cfg, DEV)
+    x_stage = torch.empty((2, T, d), dtype=torch.bfloat16, device=DEV)
+    y_stage = torch.empty((2, T, d), dtype=torch.bfloat16, device=DEV)
+    st, h2d, d2h = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    m.moe_forward_pipelined(cfg, inp, xs, ys, x_stage, y_stage, ws, st, h2d, d2h)
+    st.synchronize()
+    for i in range(5):
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+        m.moe_forward(cfg, inp, xs[i].to(DEV), y, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i].view(torch.int16), y.cpu().view(torch.int16)), i
+    with pytest.raises(m.MoEError):      # the three streams must differ
+        m.moe_forward_pipelined(cfg, inp, xs, ys, x_stage, y_stage, ws, st, h2d, h2d)
