@@ -877,6 +877,32 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     if (is_glu(g.epi) || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
+  // Dense launches without fp32 k-chunked problems: choose the token tile height so that the
+  // items fill whole waves of the persistent grid, by the estimate (waves rounded up) x height.
+  // The back GEMM's 24 x 32 tiles of 256 rows are 5.05 waves on 152 SMs; 224-row tiles make
+  // 888 items, 5.84 waves, for 12% less estimated time.
+  bool any_kc = false;
+  for (int j = 0; j < n_probs; ++j) any_kc = any_kc || P.p[j].kchunk > 0;
+  if (P.grouped < 0 && !any_kc) {
+    const int64_t sms = num_sms_tc();
+    int best_bn = BN;
+    int64_t best_cost = -1;
+    // heights in whole 32-row TMA boxes: the B slot of a stage holds max_bn rows
+    for (int bn = BN; bn >= 160; bn -= B_BOX_ROWS) {
+      int64_t items = 0;
+      for (int j = 0; j < n_probs; ++j) items += (int64_t)P.p[j].m_tiles * cdiv(P.p[j].rows, bn);
+      const int64_t cost = cdiv(items, sms) * bn;
+      if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_bn = bn; }
+    }
+    base = 0;
+    for (int j = 0; j < n_probs; ++j) {
+      TcProblem& q = P.p[j];
+      q.bn = best_bn;
+      q.item_base = base;
+      q.n_items = q.m_tiles * cdiv(q.rows, q.bn);
+      base += q.n_items;
+    }
+  }
   int max_bn = 0, max_two_a_bn = 0;
   for (int j = 0; j < n_probs; ++j) {
     max_bn = max(max_bn, P.p[j].bn);
@@ -884,7 +910,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   }
   P.nacc = (max_two_a_bn > 128) ? 1 : 2;
   P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
-  P.b_bytes = max_bn * BK * 2;
+  P.b_bytes = (int)cdiv(max_bn, B_BOX_ROWS) * B_BOX_BYTES;   // whole boxes, as the producer loads
   const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
   // transpose tiles sized for the widest output of the launch
   P.epi_tile = 16 * 32 * 2;
