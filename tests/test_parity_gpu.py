@@ -634,18 +634,22 @@ def _layer_grads(shape, inp):
             "dw_up": torch.full((L, d), 9.0, **bf)}
 
 
-@pytest.mark.parametrize("cap", [None, (1, 1)], ids=["nocap", "cf100"])
-def test_layer_backward(cap):
+@pytest.mark.parametrize("cap,masked", [(None, False), ((1, 1), False), (None, True)],
+                         ids=["nocap", "cf100", "padding"])
+def test_layer_backward(cap, masked):
     """dx and every weight gradient of the whole layer against the oracle's chain rule, after
-    the forward on the same inputs (with capacity drops in the second case)."""
+    the forward on the same inputs (with capacity drops, or with padding tokens)."""
     shape = SHAPES["small_bf16"].with_(T=512, capacity=cap)
     cpu = make_layer_inputs(shape, "cpu")
+    if masked:
+        cpu["token_mask"] = padding_mask(shape.T, seq_len=128, seed=5)
     inp = {k: v.to(DEV) for k, v in cpu.items()}
     cfg = m.LayerConfig.from_shape(shape)
     T, d = shape.T, shape.d_model
     fws = m.alloc_workspace(cfg, DEV)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
-    m.moe_forward(cfg, inp, inp["x"], y, fws)
+    m.moe_forward(cfg, inp, inp["x"], y, fws,
+                  aux={"token_mask": inp["token_mask"]} if masked else None)
     g = torch.Generator().manual_seed(3)
     dy = torch.randn(T, d, generator=g).to(torch.bfloat16)
     dx = torch.full((T, d), 9.0, dtype=torch.bfloat16, device=DEV)
