@@ -138,6 +138,36 @@ __device__ void warp_stage1(const float* logits_t, const float* wnorm, float xn,
 template <typename T>
 __device__ __forceinline__ void load8f(const T* p, float v[8]) { ld8(p, v); }
 
+// 8 elements as loaded (16 B of bf16 or 32 B of fp32), converted to fp32 on use.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<bf16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const bf16* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void get(float v[8]) const {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void get(float v[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
 // Upper bound of ||x||_2 for a row of d elements (d a multiple of 8).
 template <typename T>
 __device__ float warp_norm_ub(const T* x, int d, float gam_d, int lane) {
@@ -183,23 +213,39 @@ __device__ void warp_dot2_multi(const T* x, const T* wrT, const int* cand, int n
     sa[j] = fabsf(b);
     wp[j] = wrT + (int64_t)e * d;
   }
-#pragma unroll 2
-  for (int i = lane * 8; i < d; i += 256) {
-    float xv[8];
-    load8f(x + i, xv);
+  // U consecutive 256-element steps per trip: all their loads are issued before any of their
+  // products, so U * (MC + 1) loads per lane are in flight (the sums keep their order)
+  constexpr int U = f32 ? 2 : 4;
+  for (int i0 = lane * 8; i0 < d; i0 += 256 * U) {
+    Raw8<T> xr[U], wr[U][MC];
 #pragma unroll
-    for (int j = 0; j < MC; ++j) {
-      float wv[8];
-      load8f(wp[j] + i, wv);
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + 256 * u;
+      if (i < d) {
+        xr[u].load(x + i);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float p = __fmul_rn(xv[q], wv[q]);
-        float ep = f32 ? fmaf(xv[q], wv[q], -p) : 0.0f;   // TwoProduct (exact when bf16)
-        float t, e;
-        two_sum(s[j], p, t, e);
-        s[j] = t;
-        c[j] = __fadd_rn(c[j], __fadd_rn(e, ep));
-        sa[j] = __fadd_rn(sa[j], fabsf(p));
+        for (int j = 0; j < MC; ++j) wr[u][j].load(wp[j] + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (i0 + 256 * u >= d) break;
+      float xv[8];
+      xr[u].get(xv);
+#pragma unroll
+      for (int j = 0; j < MC; ++j) {
+        float wv[8];
+        wr[u][j].get(wv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float p = __fmul_rn(xv[q], wv[q]);
+          float ep = f32 ? fmaf(xv[q], wv[q], -p) : 0.0f;   // TwoProduct (exact when bf16)
+          float t, e;
+          two_sum(s[j], p, t, e);
+          s[j] = t;
+          c[j] = __fadd_rn(c[j], __fadd_rn(e, ep));
+          sa[j] = __fadd_rn(sa[j], fabsf(p));
+        }
       }
     }
   }
@@ -444,6 +490,45 @@ router_select_kernel(RouterArgs a) {
   }
 }
 
+// Stage-3 work of the tokens whose stage-2 state the refine stage saved (the first n_saved of
+// the exact list) is spread over EXACT_PARTS blocks per token: each takes every EXACT_PARTS-th
+// undecided expert and publishes its exact value; the last block to arrive ranks them all.
+constexpr int EXACT_PARTS = 8;
+
+// The saved state of exact-list slot `it` inside RouterArgs::saved.
+struct SavedSlot {
+  float* bounds;               // [2, E]: lo, hi
+  unsigned long long* forms;   // [E, NB]: exact values of the undecided experts
+  int32_t* arrived;            // blocks of this token done with their experts
+};
+__device__ __forceinline__ SavedSlot saved_slot(const RouterArgs& a, int it) {
+  unsigned char* base = static_cast<unsigned char*>(a.saved);
+  const size_t nb = ((size_t)a.n_saved * 2 * a.E * 4 + 255) & ~(size_t)255;
+  const size_t nf = ((size_t)a.n_saved * a.E * NB * 8 + 255) & ~(size_t)255;
+  SavedSlot v;
+  v.bounds = reinterpret_cast<float*>(base) + (size_t)it * 2 * a.E;
+  v.forms = reinterpret_cast<unsigned long long*>(base + nb) + (size_t)it * a.E * NB;
+  v.arrived = reinterpret_cast<int32_t*>(base + nb + nf) + it;
+  return v;
+}
+
+// Stage-2 bounds of one token to and from its saved slot [lo[E], hi[E]].
+__device__ void copy_bounds(const float* lo, const float* hi, float* dst, int E,
+                                         int lane) {
+  for (int e = lane; e < E; e += 32) {
+    dst[e] = lo[e];
+    dst[E + e] = hi[e];
+  }
+}
+
+__device__ void restore_bounds(const float* src, float* lo, float* hi, int E,
+                                            int lane) {
+  for (int e = lane; e < E; e += 32) {
+    lo[e] = src[e];
+    hi[e] = src[E + e];
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(RT_WARPS * 32)
 router_refine_kernel(RouterArgs a) {
@@ -502,16 +587,28 @@ router_refine_kernel(RouterArgs a) {
     }
     if (n_in == a.k) {
       warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
-    } else if (lane == 0) {
-      int pos = atomicAdd(&a.hdr->n_exact, 1);
-      a.exact_list[pos] = (int32_t)t;
+    } else {
+      int pos = 0;
+      if (lane == 0) {
+        pos = atomicAdd(&a.hdr->n_exact, 1);
+        a.exact_list[pos] = (int32_t)t;
+      }
+      pos = __shfl_sync(~0u, pos, 0);
+      // the stage-2 bounds go with it, so that the exact stage starts from them
+      if (a.saved && pos < a.n_saved) {
+        const SavedSlot sv = saved_slot(a, pos);
+        copy_bounds(w.lo, w.hi, sv.bounds, a.E, lane);
+        if (lane == 0) *sv.arrived = 0;
+      }
     }
   }
 }
 
-// One block per token still undecided after stage 2. Warp 0 re-derives the stage-1
-// candidates; the 8 warps re-run their compensated dot products in parallel; only experts still
-// undecided then get exact logits, each computed by the whole block; the remaining top-k slots
+// Tokens still undecided after stage 2. Warp 0 re-derives the stage-1 logits and the candidate
+// list: from the stage-2 bounds the refine stage saved for the token (EXACT_PARTS blocks per
+// token, see above) or, past the saved slots, by re-running the compensated dot product of
+// every stage-1 candidate on the block's 8 warps (one block per token). Only experts still
+// undecided then get exact logits, each computed by a whole block; the remaining top-k slots
 // go to the largest exact values, ties to the lower index.
 template <typename T>
 __global__ void __launch_bounds__(RT_WARPS * 32)
@@ -526,14 +623,25 @@ router_exact_kernel(RouterArgs a) {
   int32_t* cand = reinterpret_cast<int32_t*>(red + RT_WARPS * NB);             // [E]
   float* cres = reinterpret_cast<float*>(cand + a.E);                           // [E]
   float* ceb = cres + a.E;                                                      // [E]
-  __shared__ int s_ncand, s_nin, s_ok;
+  __shared__ int s_ncand, s_nin, s_ok, s_last;
   const int n = min(a.hdr->n_exact, (int)a.T);
-  for (int it = blockIdx.x; it < n; it += gridDim.x) {
+  const int ns = a.saved ? min(n, a.n_saved) : 0;
+  const int n_items = ns * EXACT_PARTS + (n - ns);
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const bool split = item < ns * EXACT_PARTS;
+    const int it = split ? item / EXACT_PARTS : ns + (item - ns * EXACT_PARTS);
+    const int part = split ? item % EXACT_PARTS : 0;
     const int64_t t = a.exact_list[it];
     const T* x = static_cast<const T*>(a.x) + t * a.d;
+    SavedSlot sv{};
+    if (split) sv = saved_slot(a, it);
     if (warp == 0) {
       warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
-      warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+      if (split) {
+        restore_bounds(sv.bounds, w.lo, w.hi, a.E, lane);
+        __syncwarp();
+      }
+      const int n_in0 = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
       int base = 0;
       for (int e0 = 0; e0 < a.E; e0 += 32) {
         int e = e0 + lane;
@@ -542,60 +650,82 @@ router_exact_kernel(RouterArgs a) {
         if (on) cand[base + __popc(b & ((1u << lane) - 1u))] = e;
         base += __popc(b);
       }
-      if (lane == 0) { s_ncand = base; s_ok = 1; }
+      if (lane == 0) { s_ncand = base; s_ok = 1; s_nin = n_in0; }
     }
     __syncthreads();
-    // stage 2 for every candidate, one warp per candidate
-    const int nc = s_ncand;
-    for (int ci = warp; ci < nc; ci += RT_WARPS) {
-      float res[1], eb[1];
-      warp_dot2_multi<T, 1>(x, static_cast<const T*>(a.wrT), cand + ci, 1, a.d, a.bias, a.g2, lane,
-                            res, eb);
-      if (lane == 0) { cres[ci] = res[0]; ceb[ci] = eb[0]; }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      for (int ci = lane; ci < nc; ci += 32) {
-        const int e = cand[ci];
-        w.lo[e] = fmaxf(w.lo[e], __fsub_rd(cres[ci], ceb[ci]));
-        w.hi[e] = fminf(w.hi[e], __fadd_ru(cres[ci], ceb[ci]));
+    if (!split) {
+      // stage 2 for every candidate, one warp per candidate
+      const int nc = s_ncand;
+      for (int ci = warp; ci < nc; ci += RT_WARPS) {
+        float res[1], eb[1];
+        warp_dot2_multi<T, 1>(x, static_cast<const T*>(a.wrT), cand + ci, 1, a.d, a.bias, a.g2,
+                              lane, res, eb);
+        if (lane == 0) { cres[ci] = res[0]; ceb[ci] = eb[0]; }
       }
-      __syncwarp();
-      int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
-      int base = 0;
-      for (int e0 = 0; e0 < a.E; e0 += 32) {
-        int e = e0 + lane;
-        bool on = e < a.E && w.sel[e] == 2;
-        unsigned b = __ballot_sync(~0u, on);
-        if (on) cand[base + __popc(b & ((1u << lane) - 1u))] = e;
-        base += __popc(b);
+      __syncthreads();
+      if (warp == 0) {
+        for (int ci = lane; ci < nc; ci += 32) {
+          const int e = cand[ci];
+          w.lo[e] = fmaxf(w.lo[e], __fsub_rd(cres[ci], ceb[ci]));
+          w.hi[e] = fminf(w.hi[e], __fadd_ru(cres[ci], ceb[ci]));
+        }
+        __syncwarp();
+        int n_in = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
+        int base = 0;
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+          int e = e0 + lane;
+          bool on = e < a.E && w.sel[e] == 2;
+          unsigned b = __ballot_sync(~0u, on);
+          if (on) cand[base + __popc(b & ((1u << lane) - 1u))] = e;
+          base += __popc(b);
+        }
+        if (lane == 0) { s_ncand = base; s_nin = n_in; }
       }
-      if (lane == 0) { s_ncand = base; s_nin = n_in; }
+      __syncthreads();
     }
-    __syncthreads();
     // stage 3: exact values of the experts still undecided, one block-wide sum each
     const int nc2 = s_ncand;
-    for (int ci = 0; ci < nc2; ++ci) {
+    const int step = split ? EXACT_PARTS : 1;
+    for (int ci = part; ci < nc2; ci += step) {
       const int e = cand[ci];
       bool ok = block_exact(x, static_cast<const T*>(a.wrT) + (int64_t)e * a.d, a.d,
                             a.bias ? a.bias[e] : 0.0f, red, forms + (size_t)ci * NB);
       if (!ok && threadIdx.x == 0) s_ok = 0;
+      if (split && threadIdx.x < NB)
+        sv.forms[(size_t)e * NB + threadIdx.x] = forms[(size_t)ci * NB + threadIdx.x];
+    }
+    if (split) {
+      // publish this block's values; the last of the token's blocks reads everyone's and ranks
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) s_last = (atomicAdd(sv.arrived, 1) == EXACT_PARTS - 1);
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        for (int q = threadIdx.x; q < nc2 * NB; q += blockDim.x) {
+          const int ci = q / NB, i = q - ci * NB;
+          forms[q] = __ldcg(sv.forms + (size_t)cand[ci] * NB + i);
+        }
+      }
+      __syncthreads();
     }
     if (warp == 0) {
-      const int need = a.k - s_nin;
-      // rank each candidate among the candidates: larger exact value first, then lower index
-      for (int ci = lane; ci < nc2; ci += 32) {
-        int r = 0;
-        for (int cj = 0; cj < nc2; ++cj) {
-          if (cj == ci) continue;
-          int c = exact_cmp(forms + (size_t)cj * NB, forms + (size_t)ci * NB);
-          if (c > 0 || (c == 0 && cand[cj] < cand[ci])) ++r;
-        }
-        w.sel[cand[ci]] = (r < need) ? 1 : 0;
-      }
-      __syncwarp();
       if (!s_ok && lane == 0) report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
-      warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
+      if (!split || s_last) {
+        const int need = a.k - s_nin;
+        // rank each candidate among the candidates: larger exact value first, then lower index
+        for (int ci = lane; ci < nc2; ci += 32) {
+          int r = 0;
+          for (int cj = 0; cj < nc2; ++cj) {
+            if (cj == ci) continue;
+            int c = exact_cmp(forms + (size_t)cj * NB, forms + (size_t)ci * NB);
+            if (c > 0 || (c == 0 && cand[cj] < cand[ci])) ++r;
+          }
+          w.sel[cand[ci]] = (r < need) ? 1 : 0;
+        }
+        __syncwarp();
+        warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
+      }
     }
     __syncthreads();
   }
@@ -604,6 +734,13 @@ router_exact_kernel(RouterArgs a) {
 size_t warp_smem(int E) { return ((size_t)E * 18 + 15) & ~(size_t)15; }
 
 }  // namespace
+
+size_t router_saved_bytes(int E, int n_saved) {
+  // the layout of saved_slot: bounds, forms, arrival counters, each rounded up to 256 B
+  const size_t nb = ((size_t)n_saved * 2 * E * 4 + 255) & ~(size_t)255;
+  const size_t nf = ((size_t)n_saved * E * NB * 8 + 255) & ~(size_t)255;
+  return nb + nf + (size_t)n_saved * 4;
+}
 
 cudaError_t router_prepare(const RouterArgs& a, int dtype, cudaStream_t st, bool pdl) {
   dim3 tg(cdiv(a.E, 32), cdiv(a.d, 32)), tb(32, 8);

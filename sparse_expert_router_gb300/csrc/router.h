@@ -23,7 +23,14 @@ struct RouterArgs {
   int32_t* refine_list;   // [T] workspace
   int32_t* exact_list;    // [T] workspace
   DeviceHeader* hdr;
+  // router_saved_bytes(E, n_saved) of workspace, or NULL: the stage-2 state of the first
+  // n_saved tokens of the exact list (written by the refine stage), which lets the exact stage
+  // skip stage 2 and split stage 3 over several blocks per token
+  void* saved;
+  int n_saved;
 };
+
+size_t router_saved_bytes(int E, int n_saved);
 
 // W_r^T and the column-norm bounds (needed before router_select).
 cudaError_t router_prepare(const RouterArgs& a, int dtype, cudaStream_t st, bool pdl);

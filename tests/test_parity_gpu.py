@@ -162,9 +162,13 @@ def _near_tie_router(T=512, d=256, E=64, seed=3):
     return x, w
 
 
+@pytest.mark.parametrize("T", [48, 512])
 @pytest.mark.parametrize("path", list(BF16_PATHS))
-def test_router_exact_on_near_ties(path):
-    x, w = _near_tie_router()
+def test_router_exact_on_near_ties(path, T):
+    """Nearly every token reaches the exact stage. The library keeps the stage-2 state of the
+    first 64 of them and splits their exact stage over several blocks; the rest recompute
+    stage 2 on one block each: T=48 takes only the first way, T=512 both."""
+    x, w = _near_tie_router(T=T)
     T, d = x.shape
     E, k = w.shape[1], 8
     cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,
@@ -178,6 +182,8 @@ def test_router_exact_on_near_ties(path):
     assert torch.equal(idx.cpu().long(), ref["idx"])
     assert rep["status"] == 0
     assert rep["n_refined"] > 0 and rep["n_exact"] > 0, rep      # every stage exercised
+    if T > 64:
+        assert rep["n_exact"] > 64, rep                           # past the saved slots too
 
 
 # ------------------------------------------------------------ device-detected errors ----
