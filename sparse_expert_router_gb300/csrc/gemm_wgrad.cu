@@ -4,18 +4,25 @@
 // kernel of the ragged dot's custom VJP.
 //
 // Both operands are MN-major in shared memory: the contraction index is their row index, so a
-// stage holds 64 rows of a (two 64-feature boxes, 128 features) and of b (four 64-column boxes,
-// 256 columns). A group's rows start anywhere; its last stage may run past the group's end, so
-// the MMA warp zeroes the rows past the end in both tiles before it issues that stage's MMAs.
+// k step holds 64 rows of a (two 64-feature boxes, 128 features) and of b (four 64-column boxes,
+// 256 columns). A group's rows start anywhere; its last k step may run past the group's end, so
+// the MMA warp zeroes the rows past the end in both tiles before it issues that step's MMAs.
 //
-// Roles of the warps of a CTA (one CTA per SM, persistent over (problem, group, m tile, n tile)
-// items, n tiles fastest so the items of one group run together and share its rows in L2):
+// Work units are (problem, group, 256-column n tile, chunk of mc 128-row m tiles). The b tile of
+// a unit is the same for all its m tiles: when the group has at most WB_SLOTS * 64 rows it is
+// loaded once into the b slots and stays there for the whole unit, and only the a tiles stream
+// through their own ring (for an expert of 171 rows and mc = 24 this is 52 KB of operands per
+// 64 KB of output instead of 144 KB). Larger groups stream b through the same slots, one load per
+// m tile and k step.
+//
+// Roles of the warps of a CTA (one CTA per SM, persistent over units, n tiles fastest so the
+// units of one group run together and share its rows in L2):
 //   warp 0: TMA producer (one thread); warp 1: TMEM allocator and MMA issuer (the whole warp
 //   zeroes tail rows, one thread issues MMAs); warps 2..9: epilogue, the two warps of a lane
 //   quadrant each taking half of the 256 columns, 64 per tensor-memory load, and each thread
 //   writing its row's 64 values into a 128-byte-swizzled shared tile that one TMA bulk tensor
 //   store then copies out (whole 128-byte lines, no scattered stores). Accumulators are
-//   double-buffered (2 x 256 tensor-memory columns). Every wait is bounded.
+//   double-buffered (2 x 256 tensor-memory columns), one per m tile. Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -29,24 +36,26 @@ namespace {
 
 using namespace tc;
 
-constexpr int WM = 128;              // output rows (features of a) per item: MMA M, TMEM lanes
-constexpr int WN = 256;              // output columns per item: MMA N
-constexpr int WK = 64;               // contraction rows per stage
+constexpr int WM = 128;              // output rows (features of a) per m tile: MMA M, TMEM lanes
+constexpr int WN = 256;              // output columns per unit: MMA N
+constexpr int WK = 64;               // contraction rows per k step
 constexpr int W_EPI = 8;             // epilogue warps
 constexpr int W_THREADS = 64 + 32 * W_EPI;
 constexpr int WA_HALF = 64 * WK * 2; // one [64 rows][64 features] box: 8 KB
 constexpr int WA_BYTES = 2 * WA_HALF;
 constexpr int WB_ATOM = 64 * WK * 2; // one [64 rows][64 columns] box: 8 KB
 constexpr int WB_BYTES = 4 * WB_ATOM;
-constexpr int W_STAGE = WA_BYTES + WB_BYTES;   // 48 KB
-constexpr int W_STAGES = 4;
+constexpr int WA_STAGES = 4;         // a ring
+constexpr int WB_SLOTS = 4;          // b slots: groups of at most 256 rows keep b resident
 constexpr int W_MAX_PROBS = 6;
 constexpr int W_OUT_TILE = 32 * 64 * 2;   // one warp's store tile: 32 rows x 64 bf16 columns
+constexpr int W_SMEM = WB_SLOTS * WB_BYTES + WA_STAGES * WA_BYTES + W_EPI * W_OUT_TILE;
 
 struct WgProb {
   CUtensorMap a, b, o;
   const int32_t* offsets;
   int G, M, N, m_tiles, n_tiles;
+  int mc, m_chunks;                  // m tiles per unit, units per (group, n tile)
   int64_t rows;
   bf16* out;
   int64_t item_base;
@@ -59,30 +68,30 @@ struct WgParams {
   DeviceHeader* hdr;
 };
 
-struct WItem {
-  int p, g, m0, n0;
+struct WUnit {
+  int p, g, n0, mt0, nmt;
   int64_t lo, hi;   // the group's rows
 };
 
-__device__ __forceinline__ WItem wdecode(const WgParams& P, int64_t w) {
-  WItem it;
+__device__ __forceinline__ WUnit wdecode(const WgParams& P, int64_t w) {
+  WUnit u;
   int p = 0;
   while (p + 1 < P.n_probs && w >= P.p[p + 1].item_base) ++p;
   const WgProb& q = P.p[p];
   const int64_t local = w - q.item_base;
-  const int per_group = q.m_tiles * q.n_tiles;
-  it.p = p;
-  it.g = (int)(local / per_group);
+  const int per_group = q.n_tiles * q.m_chunks;
+  u.p = p;
+  u.g = (int)(local / per_group);
   const int rem = (int)(local % per_group);
-  it.m0 = (rem / q.n_tiles) * WM;
-  it.n0 = (rem % q.n_tiles) * WN;
-  const int64_t lo = imin64(imax64(q.offsets[it.g], 0), q.rows);
-  it.lo = lo;
-  it.hi = imin64(imax64(q.offsets[it.g + 1], lo), q.rows);
-  return it;
+  u.n0 = (rem % q.n_tiles) * WN;
+  u.mt0 = (rem / q.n_tiles) * q.mc;
+  u.nmt = q.mc;
+  const int64_t lo = imin64(imax64(q.offsets[u.g], 0), q.rows);
+  u.lo = lo;
+  u.hi = imin64(imax64(q.offsets[u.g + 1], lo), q.rows);
+  return u;
 }
 
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both MN-major (transposed), N, M=128.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -98,6 +107,7 @@ __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both MN-major (transposed), N, M=128.
 __device__ __forceinline__ uint32_t wg_idesc() {
   return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
          ((uint32_t)(WN >> 3) << 17) | ((uint32_t)(WM >> 4) << 24);
@@ -105,22 +115,25 @@ __device__ __forceinline__ uint32_t wg_idesc() {
 
 __global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_constant__ WgParams P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * W_STAGES + 4];
+  __shared__ __align__(8) uint64_t bars[2 * WA_STAGES + 2 * WB_SLOTS + 4];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  auto sA = [&](int s) { return base + s * W_STAGE; };
-  auto sB = [&](int s) { return base + s * W_STAGE + WA_BYTES; };
-  auto full = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty = [&](int s) { return smem_u32(&bars[W_STAGES + s]); };
-  auto tmem_full = [&](int b) { return smem_u32(&bars[2 * W_STAGES + b]); };
-  auto tmem_empty = [&](int b) { return smem_u32(&bars[2 * W_STAGES + 2 + b]); };
+  auto sB = [&](int s) { return base + s * WB_BYTES; };
+  auto sA = [&](int s) { return base + WB_SLOTS * WB_BYTES + s * WA_BYTES; };
+  auto a_full = [&](int s) { return smem_u32(&bars[s]); };
+  auto a_empty = [&](int s) { return smem_u32(&bars[WA_STAGES + s]); };
+  auto b_full = [&](int s) { return smem_u32(&bars[2 * WA_STAGES + s]); };
+  auto b_empty = [&](int s) { return smem_u32(&bars[2 * WA_STAGES + WB_SLOTS + s]); };
+  auto tmem_full = [&](int b) { return smem_u32(&bars[2 * WA_STAGES + 2 * WB_SLOTS + b]); };
+  auto tmem_empty = [&](int b) { return smem_u32(&bars[2 * WA_STAGES + 2 * WB_SLOTS + 2 + b]); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < W_STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int s = 0; s < WA_STAGES; ++s) { mbar_init(a_full(s), 1); mbar_init(a_empty(s), 1); }
+    for (int s = 0; s < WB_SLOTS; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(tmem_full(b), 1); mbar_init(tmem_empty(b), 32 * W_EPI); }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -141,137 +154,181 @@ __global__ void __launch_bounds__(W_THREADS, 1) wgrad_kernel(const __grid_consta
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
+    int as = 0;
+    uint32_t aph = 0;
+    uint32_t bl = 0;         // b loads issued: slot bl % WB_SLOTS, phase (bl / WB_SLOTS) & 1
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
-      const WItem it = wdecode(P, w);
-      const WgProb& q = P.p[it.p];
-      for (int64_t r0 = it.lo; r0 < it.hi; r0 += WK) {
-        if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 11)) { ok = false; break; }
-        mbar_expect_tx(full(stage), (uint32_t)W_STAGE);
-        const uint32_t a = smem_u32(sA(stage)), b = smem_u32(sB(stage));
-        tma_load_2d(a, &q.a, full(stage), it.m0, (int)r0);
-        tma_load_2d(a + WA_HALF, &q.a, full(stage), it.m0 + 64, (int)r0);
+    auto load_b = [&](const WgProb& q, int n0, int64_t r0) {
+      const int slot = (int)(bl % WB_SLOTS);
+      const uint32_t ph = (bl / WB_SLOTS) & 1u;
+      ++bl;
+      if (!mbar_wait(b_empty(slot), ph ^ 1u, &s_abort, P.hdr, 15)) return false;
+      mbar_expect_tx(b_full(slot), (uint32_t)WB_BYTES);
+      const uint32_t b = smem_u32(sB(slot));
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          tma_load_2d(b + i * WB_ATOM, &q.b, full(stage), it.n0 + 64 * i, (int)r0);
-        if (++stage == W_STAGES) { stage = 0; phase ^= 1u; }
+      for (int i = 0; i < 4; ++i)
+        tma_load_2d(b + i * WB_ATOM, &q.b, b_full(slot), n0 + 64 * i, (int)r0);
+      return true;
+    };
+    for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
+      const WUnit u = wdecode(P, w);
+      if (u.hi <= u.lo) continue;
+      const WgProb& q = P.p[u.p];
+      const int nk = (int)((u.hi - u.lo + WK - 1) / WK);
+      const bool resident = nk <= WB_SLOTS;
+      if (resident)
+        for (int k = 0; k < nk && ok; ++k) ok = load_b(q, u.n0, u.lo + (int64_t)k * WK);
+      for (int j = 0; j < u.nmt && ok; ++j) {
+        const int m0 = (u.mt0 + j) * WM;
+        for (int k = 0; k < nk; ++k) {
+          const int64_t r0 = u.lo + (int64_t)k * WK;
+          if (!resident && !(ok = load_b(q, u.n0, r0))) break;
+          if (!mbar_wait(a_empty(as), aph ^ 1u, &s_abort, P.hdr, 11)) { ok = false; break; }
+          mbar_expect_tx(a_full(as), (uint32_t)WA_BYTES);
+          const uint32_t a = smem_u32(sA(as));
+          tma_load_2d(a, &q.a, a_full(as), m0, (int)r0);
+          tma_load_2d(a + WA_HALF, &q.a, a_full(as), m0 + 64, (int)r0);
+          if (++as == WA_STAGES) { as = 0; aph ^= 1u; }
+        }
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp: tail zeroing) ----------------
-    int stage = 0;
-    uint32_t phase = 0;
+    int as = 0;
+    uint32_t aph = 0;
+    uint32_t bl = 0;
     int ev = 0;
     bool ok = true;
     const uint32_t idesc = wg_idesc();
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
-      const WItem it = wdecode(P, w);
-      if (it.hi <= it.lo) continue;                       // empty group: the epilogue writes zeros
-      const int buf = ev & 1;
-      const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
-      ++ev;
-      ok = mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 12);
-      if (!__all_sync(~0u, ok)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * WN);
-      uint32_t accumulate = 0;
-      for (int64_t r0 = it.lo; r0 < it.hi; r0 += WK) {
-        ok = mbar_wait(full(stage), phase, &s_abort, P.hdr, 13);
+      const WUnit u = wdecode(P, w);
+      if (u.hi <= u.lo) continue;                       // empty group: the epilogue writes zeros
+      const int nk = (int)((u.hi - u.lo + WK - 1) / WK);
+      const bool resident = nk <= WB_SLOTS;
+      const uint32_t b0 = bl;
+      for (int j = 0; j < u.nmt && ok; ++j) {
+        const int buf = ev & 1;
+        const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
+        ++ev;
+        ok = mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 12);
         if (!__all_sync(~0u, ok)) { ok = false; break; }
         tc_fence_after();
-        const int valid = (int)imin64(WK, it.hi - r0);
-        if (valid < WK) {
-          // rows past the group's end belong to the next group (or are padding): zero them in
-          // both tiles. A row is one 128-byte line per 64-wide box (swizzling permutes 16-byte
-          // pieces within the line only).
-          const int nz = WK - valid;
-          uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          for (int i = lane; i < nz * 6 * 8; i += 32) {
-            const int row = valid + i / 48, box = (i / 8) % 6, piece = i % 8;
-            unsigned char* line = (box < 2 ? sA(stage) + box * WA_HALF
-                                           : sB(stage) + (box - 2) * WB_ATOM) + row * 128;
-            *reinterpret_cast<uint4*>(line + piece * 16) = z;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * WN);
+        uint32_t accumulate = 0;
+        for (int k = 0; k < nk; ++k) {
+          const uint32_t bidx = resident ? b0 + (uint32_t)k : bl++;
+          const int slot = (int)(bidx % WB_SLOTS);
+          const bool fresh = !resident || j == 0;        // b slot loaded for this use
+          const bool last_use = !resident || j == u.nmt - 1;
+          ok = mbar_wait(b_full(slot), (bidx / WB_SLOTS) & 1u, &s_abort, P.hdr, 16);
+          if (ok) ok = mbar_wait(a_full(as), aph, &s_abort, P.hdr, 13);
+          if (!__all_sync(~0u, ok)) { ok = false; break; }
+          tc_fence_after();
+          // The group's rows in this k step: MMAs only for the 16-row slices holding some of them.
+          // Rows past the group's end belong to the next group (or are padding); the ones inside
+          // the last slice are zeroed in the a tile and, when it was just loaded, the b tile. A row
+          // is one 128-byte line per 64-wide box (swizzling permutes 16-byte pieces within the
+          // line only).
+          const int valid = (int)imin64(WK, u.hi - (u.lo + (int64_t)k * WK));
+          const int nk16 = (valid + 15) >> 4;
+          const int zr = (nk16 << 4) - valid;
+          if (zr > 0) {
+            unsigned char* ta = sA(as) + valid * 128;
+            for (int i = lane; i < zr * 16; i += 32)     // zr rows x 2 boxes x 8 pieces
+              *reinterpret_cast<uint4*>(ta + ((i >> 3) & 1) * WA_HALF + (i >> 4) * 128 +
+                                        (i & 7) * 16) = z;
+            if (fresh) {
+              unsigned char* tb = sB(slot) + valid * 128;
+              for (int i = lane; i < zr * 32; i += 32)   // zr rows x 4 boxes x 8 pieces
+                *reinterpret_cast<uint4*>(tb + ((i >> 3) & 3) * WB_ATOM + (i >> 5) * 128 +
+                                          (i & 7) * 16) = z;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (lane == 0) {
+            const uint32_t a = smem_u32(sA(as)), b = smem_u32(sB(slot));
+            for (int k16 = 0; k16 < nk16; ++k16) {
+              mma_bf16(d_tmem, smem_desc(a + k16 * 2048, WA_HALF, 1024),
+                       smem_desc(b + k16 * 2048, WB_ATOM, 1024), idesc, accumulate);
+              accumulate = 1;
+            }
+            mma_commit(a_empty(as));
+            if (last_use) mma_commit(b_empty(slot));
+          }
           __syncwarp();
+          if (++as == WA_STAGES) { as = 0; aph ^= 1u; }
         }
-        if (lane == 0) {
-          const uint32_t a = smem_u32(sA(stage)), b = smem_u32(sB(stage));
-#pragma unroll
-          for (int k16 = 0; k16 < WK / 16; ++k16) {
-            mma_bf16(d_tmem, smem_desc(a + k16 * 2048, WA_HALF, 1024),
-                     smem_desc(b + k16 * 2048, WB_ATOM, 1024), idesc, accumulate);
-            accumulate = 1;
-          }
-          mma_commit(empty(stage));
-        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(tmem_full(buf));
         __syncwarp();
-        if (++stage == W_STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(tmem_full(buf));
-      __syncwarp();
+      if (resident) bl = b0 + (uint32_t)nk;
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); the two warps of a quadrant
     // take the two halves of the columns.
     const int quad = warp & 3, half = (warp - 2) >> 2;
-    unsigned char* otile = base + W_STAGES * W_STAGE + (warp - 2) * W_OUT_TILE;
+    unsigned char* otile = base + WB_SLOTS * WB_BYTES + WA_STAGES * WA_BYTES +
+                           (warp - 2) * W_OUT_TILE;
     int ev = 0;
-    for (int64_t w = blockIdx.x; w < P.total; w += gridDim.x) {
-      const WItem it = wdecode(P, w);
-      const WgProb& q = P.p[it.p];
-      const int m = it.m0 + quad * 32 + lane;
-      bf16* orow = q.out + ((int64_t)it.g * q.M + m) * q.N;
-      const bool mok = m < q.M;
-      if (it.hi <= it.lo) {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < P.total && ok; w += gridDim.x) {
+      const WUnit u = wdecode(P, w);
+      const WgProb& q = P.p[u.p];
+      for (int j = 0; j < u.nmt; ++j) {
+        const int m0 = (u.mt0 + j) * WM;
+        const int m = m0 + quad * 32 + lane;
+        bf16* orow = q.out + ((int64_t)u.g * q.M + m) * q.N;
+        const bool mok = m < q.M;
+        if (u.hi <= u.lo) {
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int c0 = half * (WN / 2); c0 < (half + 1) * (WN / 2); c0 += 64) {
+            const int n = u.n0 + c0;
+            if (mok && n < q.N) {
+#pragma unroll
+              for (int p8 = 0; p8 < 8; ++p8) *reinterpret_cast<uint4*>(orow + n + 8 * p8) = z;
+            }
+          }
+          continue;
+        }
+        const int buf = ev & 1;
+        const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
+        ++ev;
+        if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 14)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t lane_addr =
+            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * WN);
+        // this warp's half of the columns, 64 at a time: one tensor-memory load and one wait per
+        // 64 columns; each thread puts its row's 128 bytes into the shared tile in the 128-byte
+        // swizzle (16-byte piece p of row r at piece p ^ (r % 8)), then one bulk tensor store
         for (int c0 = half * (WN / 2); c0 < (half + 1) * (WN / 2); c0 += 64) {
-          const int n = it.n0 + c0;
-          if (mok && n < q.N) {
+          float v[64];
+          tmem_ld64(lane_addr + c0, v);
+          tmem_wait_ld();
+          const int n = u.n0 + c0;
+          if (n < q.N) {
+            if (lane == 0) bulk_wait_read0();       // the tile's previous store has read it
+            __syncwarp();
 #pragma unroll
-            for (int p8 = 0; p8 < 8; ++p8) *reinterpret_cast<uint4*>(orow + n + 8 * p8) = z;
+            for (int p8 = 0; p8 < 8; ++p8) {
+              uint4 pk;
+              __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                h[i] = __floats2bfloat162_rn(v[8 * p8 + 2 * i], v[8 * p8 + 2 * i + 1]);
+              *reinterpret_cast<uint4*>(otile + lane * 128 + ((p8 ^ (lane & 7)) << 4)) = pk;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&q.o, smem_u32(otile), n, u.g * q.M + m0 + quad * 32);
           }
         }
-        continue;
+        tc_fence_before();
+        mbar_arrive(tmem_empty(buf));
       }
-      const int buf = ev & 1;
-      const uint32_t acc_phase = (uint32_t)(ev >> 1) & 1u;
-      ++ev;
-      if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 14)) break;
-      tc_fence_after();
-      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * WN);
-      // this warp's half of the columns, 64 at a time: one tensor-memory load and one wait per
-      // 64 columns; each thread puts its row's 128 bytes into the shared tile in the 128-byte
-      // swizzle (16-byte piece p of row r at piece p ^ (r % 8)), then one bulk tensor store
-      for (int c0 = half * (WN / 2); c0 < (half + 1) * (WN / 2); c0 += 64) {
-        float v[64];
-        tmem_ld64(lane_addr + c0, v);
-        tmem_wait_ld();
-        const int n = it.n0 + c0;
-        if (n < q.N) {
-          if (lane == 0) bulk_wait_read0();       // the tile's previous store has read it
-          __syncwarp();
-#pragma unroll
-          for (int p8 = 0; p8 < 8; ++p8) {
-            uint4 u;
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              h[i] = __floats2bfloat162_rn(v[8 * p8 + 2 * i], v[8 * p8 + 2 * i + 1]);
-            *reinterpret_cast<uint4*>(otile + lane * 128 + ((p8 ^ (lane & 7)) << 4)) = u;
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0)
-            tma_store_2d(&q.o, smem_u32(otile), n, it.g * q.M + it.m0 + quad * 32);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(tmem_empty(buf));
     }
     if (lane == 0) bulk_wait0();                 // every store of this warp has completed
     __syncwarp();
@@ -341,6 +398,10 @@ cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
   static WgParams P;
   memset(&P, 0, sizeof(P));
   P.hdr = static_cast<DeviceHeader*>(dev_header);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
   int64_t base = 0;
   for (int j = 0; j < n_probs; ++j) {
     const WgradProblem& g = probs[j];
@@ -356,21 +417,27 @@ cudaError_t gemm_wgrad(const WgradProblem* probs, int n_probs, void* dev_header,
     q.N = g.N;
     q.m_tiles = g.M / WM;
     q.n_tiles = (int)cdiv(g.N, WN);
+    // m tiles per unit: as many as keep at least 8 units per SM (a resident b tile then serves
+    // them all), one when even that leaves fewer units
+    q.mc = 1;
+    for (int mc = q.m_tiles; mc > 1; --mc)
+      if (q.m_tiles % mc == 0 && (int64_t)g.G * q.n_tiles * (q.m_tiles / mc) >= 8ll * sms) {
+        q.mc = mc;
+        break;
+      }
+    q.m_chunks = q.m_tiles / q.mc;
     q.rows = g.rows;
     q.out = static_cast<bf16*>(g.out);
     q.item_base = base;
-    base += (int64_t)g.G * q.m_tiles * q.n_tiles;
+    base += (int64_t)g.G * q.n_tiles * q.m_chunks;
   }
   P.n_probs = n_probs;
   P.total = base;
-  const size_t smem = (size_t)W_STAGES * W_STAGE + (size_t)W_EPI * W_OUT_TILE + 1024;
+  const size_t smem = (size_t)W_SMEM + 1024;
   cudaError_t e = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = (int)imin64(sms > 0 ? sms : 148, base);
+  const int grid = (int)imin64(sms, base);
   if (grid < 1) return cudaSuccess;
   return launch(wgrad_kernel, dim3(grid), dim3(W_THREADS), smem, stream, pdl, P);
 }

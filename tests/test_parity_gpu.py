@@ -614,6 +614,49 @@ def test_expert_backward(E, L, F, counts):
                 assert float(g[e].abs().max()) == 0.0, (n, e)
 
 
+def _many_expert_counts(E=320):
+    """Rows per expert for a grouped problem large enough that the weight-gradient kernel gives
+    each work unit several m tiles: empty experts, groups of 1-4 k steps with tails (their b
+    tile stays in shared memory across the unit's m tiles) and groups above 256 rows (b
+    streamed)."""
+    counts = []
+    for e in range(E):
+        if e % 10 == 0:
+            counts.append(0)
+        elif e % 16 == 3:
+            counts.append(257 + (e * 37) % 200)
+        elif e % 5 == 1:
+            counts.append(193 + (e * 13) % 64)
+        elif e % 9 == 4:
+            counts.append(129 + (e * 11) % 64)
+        else:
+            counts.append(1 + (e * 29) % 128)
+    return tuple(counts)
+
+
+def test_expert_backward_many_experts():
+    """320 experts, L = F = 512: the weight-gradient units hold 2 m tiles each, so a resident b
+    tile serves two accumulators; gradients against the oracle, empty experts exactly zero."""
+    E, L, F = 320, 512, 512
+    counts = _many_expert_counts(E)
+    c = _backward_case(E, L, F, counts, seed=9)
+    got = _run_backward(c, E, L, F)
+    ref = moe_oracle.grouped_experts_backward(c["x"][:c["R"]], c["offs"], c["w1"], c["w3"],
+                                              c["w2"], c["dy"][:c["R"]])
+    assert got["report"]["status"] == 0
+    assert normwise(got["dx"][:c["R"]], ref["dx"]) <= 2e-2
+    for n in ("dw1", "dw3", "dw2"):
+        g = got[n].float()
+        err = normwise(g, ref[n])
+        assert err <= 2e-2, (n, err)
+        # per-expert check as well: a wrong m tile or unit shows in a single expert
+        for e in range(0, E, 7):
+            if counts[e]:
+                assert normwise(g[e], ref[n][e]) <= 3e-2, (n, e, counts[e])
+        zero = [e for e, cnt in enumerate(counts) if cnt == 0]
+        assert float(g[zero].abs().max()) == 0.0, n
+
+
 def test_expert_backward_deterministic():
     """Two runs give bitwise equal gradients (fixed accumulation order, no atomics)."""
     E, L, F, counts = 4, 256, 256, (100, 37, 0, 300)
