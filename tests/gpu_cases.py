@@ -97,3 +97,24 @@ def e4m3_codes_match(got_vals: torch.Tensor, exact: torch.Tensor, atol: float):
                                  f"atol {atol:.1e})")
     assert bool(one_step.all()), "codes differ by more than one step"
     return int(bad.numel())
+
+
+def near_tie_router(T=512, d=256, E=64, seed=3):
+    """bf16 router inputs built to defeat fp32 logits: duplicated expert columns (exact
+    ties, to be broken by the lower index) and columns that differ only in an element
+    weighted by 2^-30 (gaps far below fp32 resolution), plus reordered columns."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, d, generator=g)
+    x[:, -1] = 2.0 ** -30                           # a tiny coordinate shared by all tokens
+    x = x.to(torch.bfloat16)
+    base = torch.randn(d, 8, generator=g) * d ** -0.5
+    cols = []
+    for e in range(E):
+        c = base[:, e % 8].clone()
+        if e % 3 == 1:
+            c[-1] += 1.0                          # larger by 2^-30 in exact arithmetic
+        if e % 5 == 2:
+            c[:-1] = c[:-1][torch.randperm(d - 1, generator=g)]
+        cols.append(c)
+    w = torch.stack(cols, 1).to(torch.bfloat16)
+    return x, w

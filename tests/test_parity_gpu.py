@@ -11,9 +11,8 @@ import sparse_expert_router_gb300 as m
 from moe_workloads import SHAPES, SLICE_C5B, make_layer_inputs, make_slice_inputs, padding_mask
 from oracle import moe_oracle
 
-from gpu_cases import (DEV, check_routing, e4m3_codes_match, gpu_inputs, normwise, oracle_forward,
-                       run_forward,
-                       sample_tokens)
+from gpu_cases import (DEV, check_routing, e4m3_codes_match, gpu_inputs, near_tie_router, normwise,
+                       oracle_forward, run_forward, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -141,34 +140,13 @@ def test_split_calls_tiny_f32():
 
 # ----------------------------------------------------------- router exactness stress ----
 
-def _near_tie_router(T=512, d=256, E=64, seed=3):
-    """bf16 router inputs built to defeat fp32 logits: duplicated expert columns (exact
-    ties, to be broken by the lower index) and columns that differ only in an element
-    weighted by 2^-30 (gaps far below fp32 resolution), plus reordered columns."""
-    g = torch.Generator().manual_seed(seed)
-    x = torch.randn(T, d, generator=g)
-    x[:, -1] = 2.0 ** -30                           # a tiny coordinate shared by all tokens
-    x = x.to(torch.bfloat16)
-    base = torch.randn(d, 8, generator=g) * d ** -0.5
-    cols = []
-    for e in range(E):
-        c = base[:, e % 8].clone()
-        if e % 3 == 1:
-            c[-1] += 1.0                          # larger by 2^-30 in exact arithmetic
-        if e % 5 == 2:
-            c[:-1] = c[:-1][torch.randperm(d - 1, generator=g)]
-        cols.append(c)
-    w = torch.stack(cols, 1).to(torch.bfloat16)
-    return x, w
-
-
 @pytest.mark.parametrize("T", [48, 512])
 @pytest.mark.parametrize("path", list(BF16_PATHS))
 def test_router_exact_on_near_ties(path, T):
     """Nearly every token reaches the exact stage. The library keeps the stage-2 state of the
     first 64 of them and splits their exact stage over several blocks; the rest recompute
     stage 2 on one block each: T=48 takes only the first way, T=512 both."""
-    x, w = _near_tie_router(T=T)
+    x, w = near_tie_router(T=T)
     T, d = x.shape
     E, k = w.shape[1], 8
     cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,

@@ -11,7 +11,9 @@ import pytest
 import torch
 
 import sparse_expert_router_gb300 as m
+from gpu_cases import near_tie_router
 from moe_workloads import SHAPES, make_router_inputs
+from oracle import moe_oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -52,6 +54,30 @@ def test_noalloc_matches_moe_route_on_two_calls(name, flags):
         assert float((gate - gate_ref).abs().max()) <= tol, (name, call)
         assert rep[0] == 0, rep
         assert rep[2] == rep_ref["n_refined"] and rep[3] == rep_ref["n_exact"], (rep, rep_ref)
+
+
+def test_noalloc_exact_stage_on_near_ties():
+    """Inputs where nearly every token needs exact logits (more than the 64 tokens whose stage-2
+    state the library hands to the exact stage), on scratch left behind by a previous call:
+    indices equal to the oracle's exact top-k and to moe_route's."""
+    x, w = near_tie_router(T=512)
+    T, d = x.shape
+    E, k = w.shape[1], 8
+    cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,
+                        d_ff_shared=0, dtype="bf16")
+    idx = torch.full((T, k), -1, dtype=torch.int32, device=DEV)
+    gate = torch.zeros((T, k), dtype=torch.float32, device=DEV)
+    report = torch.full((4,), -1, dtype=torch.int32, device=DEV)
+    m.moe_route_noalloc(cfg, x.to(DEV), w.to(DEV), None, idx, gate, report)
+    torch.cuda.synchronize()
+    rep = report.cpu().tolist()
+    ref = moe_oracle.route(x, w, None, k)
+    assert torch.equal(idx.cpu().long(), ref["idx"])
+    assert rep[0] == 0 and rep[3] > 64, rep
+    ws = m.alloc_workspace(cfg, DEV)
+    idx2 = torch.empty_like(idx)
+    m.moe_route(cfg, x.to(DEV), w.to(DEV), None, idx2, torch.empty_like(gate), ws)
+    assert torch.equal(idx, idx2)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
