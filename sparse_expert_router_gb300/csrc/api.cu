@@ -850,7 +850,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_weights_t* w, const
     shr.out2 = at(B.gs);
     shr.out3 = at(B.us);
   }
-  // 2. dc = dy W_up^T and the shared experts' dA = dy W2s^T with their SwiGLU backward
+  // 2. dc = dy W_up^T and the shared experts' dA = dy W2s^T with their SwiGLU backward, in two
+  // launches: dc's 256-feature items fill tensor memory with one accumulator buffer, and in a
+  // shared launch the SwiGLU-backward items would lose the second buffer that hides their
+  // epilogue's loads of G and U behind the next item's main loop
   GemmProblem d1[2];
   d1[0].epi = EPI_STORE;
   d1[0].M = L;
@@ -953,7 +956,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_weights_t* w, const
   MOE_TRY_CUDA(header_reset(k.hdr(), false, k.st, false));
   MOE_TRY_CUDA(write_int2(off01, 0, (int32_t)T, k.st, k.pdl));
   if (S > 0) MOE_TRY_CUDA(gemm_tc(&shr, 1, k.hdr(), k.st, k.pdl));
-  MOE_TRY_CUDA(gemm_tc(d1, S > 0 ? 2 : 1, k.hdr(), k.st, k.pdl));
+  MOE_TRY_CUDA(gemm_tc(&d1[0], 1, k.hdr(), k.st, k.pdl));
+  if (S > 0) MOE_TRY_CUDA(gemm_tc(&d1[1], 1, k.hdr(), k.st, k.pdl));
   MOE_TRY_CUDA(gemm_wgrad(w1g, S > 0 ? 2 : 1, k.hdr(), k.st, k.pdl));
   MOE_TRY_CUDA(combine_backward(at(B.dc), fat(FL.y_perm), slot_of, gate, T, kk, L, P,
                                 at(B.dy_perm), static_cast<float*>(at(B.dgate)), k.st, k.pdl));

@@ -548,11 +548,12 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       }
       if constexpr (BWD) {
         if (q.epi == EPI_SWIGLU_BWD) {
-          // G and U of this item (nrows x 128 features, 256-byte row pieces) head for L2 while
-          // the main loop runs, so that the epilogue's loads of them hit L2
-          const int nl = it.nrows * 4;            // 2 tensors x 2 lines of 128 bytes per row
+          // G and U of this item (nrows x 128 or, dual, 256 features, 128-byte lines) head for
+          // L2 while the main loop runs, so that the epilogue's loads of them hit L2
+          const int lpr = q.dual ? 4 : 2;         // lines of 128 bytes per row and tensor
+          const int nl = it.nrows * 2 * lpr;
           for (int i = threadIdx.x - 64; i < nl; i += 32 * EPI_WARPS) {
-            const int r = i >> 2, t2 = (i >> 1) & 1, line = i & 1;
+            const int r = i / (2 * lpr), t2 = (i / lpr) & 1, line = i % lpr;
             const bf16* base_p = static_cast<const bf16*>(t2 ? q.aux_u : q.aux_g);
             const bf16* ptr = base_p + (it.row0 + r) * q.ld_aux + it.m0 + line * 64;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -822,10 +823,12 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     // twice the weight bytes in flight per stage
     q.kchunk = g.kchunk;
     q.bn = g.kchunk ? BN_CHUNKED : BN;
-    // (not for the backward's SwiGLU epilogue: its global loads of G and U are better hidden
-    // behind the next item's main loop, which double-buffered accumulators allow)
-    q.dual = (!g.kchunk && !is_glu(g.epi) && g.epi != EPI_SWIGLU_BWD && g.group != GROUP_COLS &&
-              g.M % (2 * BM) == 0)
+    // (for the backward's SwiGLU epilogue only on dense problems: on the grouped expert dA, which
+    // streams its weights from HBM, its global loads of G and U are better hidden behind the next
+    // item's main loop, which double-buffered accumulators allow; a dense dA is bound by the
+    // operand ingest of single 128-feature items instead)
+    q.dual = (!g.kchunk && !is_glu(g.epi) && g.group != GROUP_COLS && g.M % (2 * BM) == 0 &&
+              (g.epi != EPI_SWIGLU_BWD || g.group == GROUP_NONE))
                  ? 1 : 0;
     if (q.dual) q.m_tiles = (int)(g.M / (2 * BM));
     q.rows = g.rows;
