@@ -395,6 +395,78 @@ def run_layer_backward(args, shape):
         "clocks": clocks, "device_report": m.moe_get_device_status(bws)}))
 
 
+def run_slice(args):
+    """One expert-parallel rank's slice of the 535B layer: 49,152 rows that arrive tagged with
+    6 local experts (Dirichlet(0.5) shares) in a padded pool of 56,576, run through the grouped
+    SwiGLU expert MLP (moe_expert_ffn) and the gate-weighted un-permute back to arrival order
+    (moe_combine without an up-projection). One GPU; no routing, no shared experts."""
+    import sparse_expert_router_gb300 as m
+    from moe_workloads import SLICE_C5B, make_slice_inputs
+    m.load()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    sh = SLICE_C5B
+    cfg = m.LayerConfig(T=sh.rows, d_model=sh.d_latent, d_latent=sh.d_latent,
+                        n_experts=sh.n_local, top_k=1, d_ff=sh.d_ff, n_shared=0, d_ff_shared=0,
+                        dtype=sh.dtype, pool_rows=sh.pool_rows,
+                        flags=0 if args.no_pdl else m.MOE_FLAG_PDL)
+    inp = make_slice_inputs(sh, dev)
+    ws = m.alloc_workspace(cfg, dev)
+    y_perm = torch.empty((sh.pool_rows, sh.d_latent), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((sh.rows, sh.d_latent), dtype=torch.bfloat16, device=dev)
+    slot, gate = inp["slot_of"].view(-1, 1), inp["gate"].view(-1, 1)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step():
+        ev[0].record(st)
+        m.moe_expert_ffn(cfg, inp["pool"], inp["expert_offsets"], inp["w1"], inp["w3"],
+                         inp["w2"], y_perm, ws=ws, stream=st)
+        ev[1].record(st)
+        m.moe_combine(cfg, y_perm, slot, gate, out, ws, stream=st)
+        ev[2].record(st)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(0)
+    clk.start()
+    tot = ffn = comb = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+        ev[2].synchronize()
+        ffn += ev[0].elapsed_time(ev[1])
+        comb += ev[1].elapsed_time(ev[2])
+    clocks = clk.stop()
+    ffn /= args.steps
+    comb /= args.steps
+    ms = ffn + comb
+    R, L, F = sh.rows, sh.d_latent, sh.d_ff
+    flops = 6.0 * R * L * F                 # gate, up (4RLF) and down (2RFL) projections
+    pk = peaks()
+    ach = flops / (ffn * 1e-3) / 1e12
+    comb_bytes = 2 * (R * L + R * L) + 8 * R   # rows read, outputs written, gates and slots
+    print(json.dumps({
+        "metric": "expert-slice rows/s", "value": round(R / (ms * 1e-3), 1), "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded rows, Dirichlet(0.5) expert shares, U(0,1] gates)",
+        "config": {"workload": f"{sh.name}: rows={R} pool={sh.pool_rows} L={L} F={F} "
+                               f"local experts={sh.n_local}", "pdl": not args.no_pdl,
+                   "l2": "flushed between timed steps (256 MB write)"},
+        "stages": {"expert_ffn": {"ms": round(ffn, 4), "tflop_s": round(ach, 1)},
+                   "combine": {"ms": round(comb, 4),
+                               "gb_s": round(comb_bytes / (comb * 1e-3) / 1e9, 1)}},
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
+                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
+                     "kernel": "expert_ffn", "traffic": None,
+                     "peak_source": pk["source"] + " (bf16 sustained)"},
+        "gpu_launches": 4 * args.steps, "clocks": clocks,   # offsets check, 2 GEMMs, combine
+        "device_report": m.moe_get_device_status(ws)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,6 +484,8 @@ def main():
                     help="time the routed experts' backward (moe_expert_ffn_backward) instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the whole layer's backward (moe_backward) instead")
+    ap.add_argument("--slice", action="store_true",
+                    help="time the expert-parallel slice workload (grouped expert MLP + un-permute)")
     args = ap.parse_args()
     shape = SHAPES[args.workload]
     if args.impl == "reference":
@@ -422,6 +496,9 @@ def main():
         return
     if args.backward:
         run_layer_backward(args, shape)
+        return
+    if args.slice:
+        run_slice(args)
         return
 
     import sparse_expert_router_gb300 as m
