@@ -34,7 +34,7 @@ int64_t pool_rows_of(const moe_config_t& c) {
 size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, ebnd, idx, gate, z, chist, cbase, counts,
+  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, rsaved, idx, gate, z, chist, cbase, counts,
       offsets, ndrop, slot_of, perm, x_perm, hid, y_perm, a_s, c, total;
 };
 
@@ -57,7 +57,7 @@ Layout make_layout(const moe_config_t& c) {
   L.xnorm = take(T * 4);
   L.rlist = take(T * 4);
   L.elist = take(T * 4);
-  L.ebnd = take((int64_t)router_saved_bytes(E, ROUTER_SAVED));
+  L.rsaved = take((int64_t)router_saved_bytes(E, ROUTER_SAVED));
   L.idx = take(T * k * 4);
   L.gate = take(T * k * 4);
   L.z = take(T * Lt * 4);
@@ -277,7 +277,7 @@ RouterArgs router_args(const Call& k, const void* x, const void* w_router, const
   a.gate = gate;
   a.refine_list = k.at<int32_t>(k.L.rlist);
   a.exact_list = k.at<int32_t>(k.L.elist);
-  a.saved = k.at<unsigned char>(k.L.ebnd);
+  a.saved = k.at<unsigned char>(k.L.rsaved);
   a.n_saved = ROUTER_SAVED;
   a.hdr = k.hdr();
   return a;
@@ -469,7 +469,7 @@ void* noalloc_scratch_address() {
 
 // Layout of the routing scratch inside the fixed array (the same regions moe_route uses).
 struct NoallocLayout {
-  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, ebnd, total;
+  size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, rsaved, total;
 };
 NoallocLayout noalloc_layout(const moe_config_t& c) {
   NoallocLayout L{};
@@ -487,7 +487,7 @@ NoallocLayout noalloc_layout(const moe_config_t& c) {
   L.xnorm = take(c.T * 4);
   L.rlist = take(c.T * 4);
   L.elist = take(c.T * 4);
-  L.ebnd = take((int64_t)router_saved_bytes(c.n_experts, ROUTER_SAVED));
+  L.rsaved = take((int64_t)router_saved_bytes(c.n_experts, ROUTER_SAVED));
   L.total = off;
   return L;
 }
@@ -1207,7 +1207,7 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x, const voi
   k.L.xnorm = NL.xnorm;
   k.L.rlist = NL.rlist;
   k.L.elist = NL.elist;
-  k.L.ebnd = NL.ebnd;
+  k.L.rsaved = NL.rsaved;
   GemmProblem p = router_problem(k, x, w_router, b_router);
   if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
   RouterArgs ra = router_args(k, x, w_router, b_router, topk_idx, topk_gate);
