@@ -414,8 +414,8 @@ def silu_grad(v: torch.Tensor) -> torch.Tensor:
 
 
 def grouped_experts_backward(rows: torch.Tensor, offsets: Sequence[int], w1: torch.Tensor,
-                             w3: torch.Tensor, w2: torch.Tensor, dy: torch.Tensor
-                             ) -> Dict[str, torch.Tensor]:
+                             w3: torch.Tensor, w2: torch.Tensor, dy: torch.Tensor, *,
+                             weight_grads: bool = True) -> Dict[str, torch.Tensor]:
     """Gradients of the grouped expert MLP (grouped_experts) given dy = dL/dy_perm.
 
     For expert e with rows X = rows[offsets[e]:offsets[e+1]], G = X W1_e, U = X W3_e,
@@ -425,13 +425,16 @@ def grouped_experts_backward(rows: torch.Tensor, offsets: Sequence[int], w1: tor
       dW1_e = X^T dG,  dW3_e = X^T dU,  dW2_e = A^T dY.
     Experts without rows get zero weight gradients; rows past offsets[-1] get no dX. All fp64.
     Returns dx [n_active, L], dw1, dw3 [E, L, F], dw2 [E, F, L] and the intermediates
-    g, u, a, da, dg, du [n_active, F]."""
+    g, u, a, da, dg, du [n_active, F]. With weight_grads=False the three weight gradients are
+    neither formed nor returned (a check of dx alone on a large expert bank)."""
     x64, dy64 = to64(rows), to64(dy)
     n_act = int(offsets[-1])
     E, L, F = w1.shape
-    out = {"dx": torch.zeros((n_act, L), dtype=F64),
-           "dw1": torch.zeros((E, L, F), dtype=F64), "dw3": torch.zeros((E, L, F), dtype=F64),
-           "dw2": torch.zeros((E, F, w2.shape[2]), dtype=F64)}
+    out = {"dx": torch.zeros((n_act, L), dtype=F64)}
+    if weight_grads:
+        out.update({"dw1": torch.zeros((E, L, F), dtype=F64),
+                    "dw3": torch.zeros((E, L, F), dtype=F64),
+                    "dw2": torch.zeros((E, F, w2.shape[2]), dtype=F64)})
     for n in ("g", "u", "a", "da", "dg", "du"):
         out[n] = torch.zeros((n_act, F), dtype=F64)
     for e in range(E):
@@ -446,9 +449,10 @@ def grouped_experts_backward(rows: torch.Tensor, offsets: Sequence[int], w1: tor
         dG = dA * U * silu_grad(G)
         dU = dA * silu(G)
         out["dx"][lo:hi] = dG @ W1.T + dU @ W3.T
-        out["dw1"][e] = X.T @ dG
-        out["dw3"][e] = X.T @ dU
-        out["dw2"][e] = A.T @ dY
+        if weight_grads:
+            out["dw1"][e] = X.T @ dG
+            out["dw3"][e] = X.T @ dU
+            out["dw2"][e] = A.T @ dY
         for n, v in (("g", G), ("u", U), ("a", A), ("da", dA), ("dg", dG), ("du", dU)):
             out[n][lo:hi] = v
     return out
@@ -527,7 +531,7 @@ def forward(inp: Dict[str, torch.Tensor], *, top_k: int, rms_eps: float,
 # --------------------------------------------------------------- layer backward ----
 
 def backward(inp: Dict[str, torch.Tensor], fwd: Dict[str, torch.Tensor], dy: torch.Tensor, *,
-             rms_eps: float) -> Dict[str, torch.Tensor]:
+             rms_eps: float, expert_weight_grads: bool = True) -> Dict[str, torch.Tensor]:
     """Gradients of <dy, y> for the whole layer (16-bit or fp32 expert banks), by the chain
     rule through the forward's definition, given ``fwd`` = forward(inp, ...) over all tokens.
 
@@ -544,7 +548,9 @@ def backward(inp: Dict[str, torch.Tensor], fwd: Dict[str, torch.Tensor], dy: tor
       z = x W_down                          -> dW_down = x^T dz, dx += dz W_down^T
       logits = x W_r + b                    -> dW_r = x^T dl, db = sum_t dl, dx += dl W_r^T
       shared: a_s = silu(x W1_s) (x W3_s)   -> as the expert MLP, dx += ...
-    Returns every gradient in fp64 (names d<weight>, dx)."""
+    Returns every gradient in fp64 (names d<weight>, dx). expert_weight_grads=False leaves out
+    dw1, dw3 and dw2 of the routed experts (whose fp64 banks would be 87 GB for the 535B layer);
+    everything else, dx included, is unchanged."""
     x64, dy64 = to64(inp["x"]), to64(dy)
     T, d = x64.shape
     E = inp["w_router"].shape[1]
@@ -592,8 +598,10 @@ def backward(inp: Dict[str, torch.Tensor], fwd: Dict[str, torch.Tensor], dy: tor
     rows = torch.stack([h[t] for _, t, _ in order]) if order else torch.zeros((0, L), dtype=F64)
     dys = (torch.stack([gate[t, j] * dc[t] for _, t, j in order]) if order
            else torch.zeros((0, L), dtype=F64))
-    eb = grouped_experts_backward(rows, offsets, inp["w1"], inp["w3"], inp["w2"], dys)
-    out["dw1"], out["dw3"], out["dw2"] = eb["dw1"], eb["dw3"], eb["dw2"]
+    eb = grouped_experts_backward(rows, offsets, inp["w1"], inp["w3"], inp["w2"], dys,
+                                  weight_grads=expert_weight_grads)
+    if expert_weight_grads:
+        out["dw1"], out["dw3"], out["dw2"] = eb["dw1"], eb["dw3"], eb["dw2"]
     dh = torch.zeros((T, L), dtype=F64)
     for n, (_, t, _) in enumerate(order):
         dh[t] += eb["dx"][n]

@@ -538,7 +538,19 @@ def pin_layer_backward_finite_differences():
             assert abs(fd - an) <= 1e-6 * (1 + abs(fd)), (cap, gname, index, fd, an)
 
 
-ALL_PINS = [pin_layer_backward_finite_differences, pin_expert_backward_autograd, pin_expert_backward_finite_differences,
+def pin_layer_backward_dx_without_expert_weight_grads():
+    """Leaving out the routed experts' weight gradients (for a dx check on a bank too large for
+    fp64 copies) changes no other output: every remaining gradient is identical."""
+    inp, dy, kw = _tiny_layer(cap=None)
+    fwd = O.forward(inp, **kw)
+    full = O.backward(inp, fwd, dy, rms_eps=kw["rms_eps"])
+    part = O.backward(inp, fwd, dy, rms_eps=kw["rms_eps"], expert_weight_grads=False)
+    assert set(full) - set(part) == {"dw1", "dw3", "dw2"}
+    for n in part:
+        assert torch.equal(part[n], full[n]), n
+
+
+ALL_PINS = [pin_layer_backward_dx_without_expert_weight_grads, pin_layer_backward_finite_differences, pin_expert_backward_autograd, pin_expert_backward_finite_differences,
             pin_silu_grad_closed_form, pin_mask_all_ones_is_no_mask, pin_mask_padding_keeps_shared_only,
             pin_mask_frees_capacity, pin_fp8_expert_golden, pin_e4m3_rounding, pin_fp8_quantize_in_fp32,
             pin_fp8_layer_grid, pin_forward_drop_skips_expert, pin_topk_bruteforce, pin_topk_exact_near_tie, pin_logit_bound_holds, pin_gates,
@@ -659,11 +671,11 @@ def _mut_silu_grad_no_inner(monkeypatch):
 def _mut_backward_dw2_from_g(monkeypatch):
     orig = O.grouped_experts_backward
 
-    def bad(rows, offsets, w1, w3, w2, dy):
-        out = orig(rows, offsets, w1, w3, w2, dy)
+    def bad(rows, offsets, w1, w3, w2, dy, **kw):
+        out = orig(rows, offsets, w1, w3, w2, dy, **kw)
         for e in range(len(offsets) - 1):
             lo, hi = int(offsets[e]), int(offsets[e + 1])
-            if hi > lo:
+            if hi > lo and "dw2" in out:
                 out["dw2"][e] = out["g"][lo:hi].T @ O.to64(dy)[lo:hi]
         return out
     monkeypatch.setattr(O, "grouped_experts_backward", bad)
@@ -672,8 +684,8 @@ def _mut_backward_dw2_from_g(monkeypatch):
 def _mut_backward_dx_no_w3(monkeypatch):
     orig = O.grouped_experts_backward
 
-    def bad(rows, offsets, w1, w3, w2, dy):
-        out = orig(rows, offsets, w1, w3, w2, dy)
+    def bad(rows, offsets, w1, w3, w2, dy, **kw):
+        out = orig(rows, offsets, w1, w3, w2, dy, **kw)
         for e in range(len(offsets) - 1):
             lo, hi = int(offsets[e]), int(offsets[e + 1])
             if hi > lo:
@@ -685,8 +697,8 @@ def _mut_backward_dx_no_w3(monkeypatch):
 def _mut_router_grad_full_softmax(monkeypatch):
     orig = O.backward
 
-    def bad(inp, fwd, dy, *, rms_eps):
-        out = orig(inp, fwd, dy, rms_eps=rms_eps)
+    def bad(inp, fwd, dy, *, rms_eps, **kw):
+        out = orig(inp, fwd, dy, rms_eps=rms_eps, **kw)
         # forget the normalisation over the selected experts: dl_j = g_j dg_j
         dl = torch.zeros((fwd["idx"].shape[0], inp["w_router"].shape[1]), dtype=F64)
         for j in range(fwd["idx"].shape[1]):
@@ -699,8 +711,8 @@ def _mut_router_grad_full_softmax(monkeypatch):
 def _mut_rmsnorm_grad_no_projection(monkeypatch):
     orig = O.backward
 
-    def bad(inp, fwd, dy, *, rms_eps):
-        out = orig(inp, fwd, dy, rms_eps=rms_eps)
+    def bad(inp, fwd, dy, *, rms_eps, **kw):
+        out = orig(inp, fwd, dy, rms_eps=rms_eps, **kw)
         z = fwd["z"]
         rstd = 1.0 / torch.sqrt((z * z).mean(dim=1, keepdim=True) + rms_eps)
         dz = rstd * out["dh"] * O.to64(inp["rms_gamma"])         # drops the mean term

@@ -696,6 +696,85 @@ def test_layer_backward(cap, masked):
     assert not bad, (bad, errs)
 
 
+def test_expert_backward_full_size_sampled():
+    """The routed experts' backward at the 535B layer's full size, in the launch configuration the
+    bench times (the workload's own routing, PDL on; 24 m tiles per weight-gradient work unit):
+    the weight gradients of three experts (the largest group, a middle one and the smallest
+    non-empty one) and their rows' dx against the oracle's chain rule for those experts alone."""
+    shape = SHAPES["l535b_t8192"]
+    cfg = m.LayerConfig.from_shape(shape, flags=m.MOE_FLAG_PDL)
+    T, k, E, L = shape.T, shape.top_k, shape.n_experts, shape.d_latent
+    inp = make_layer_inputs(shape, DEV)
+    ws = m.alloc_workspace(cfg, DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(cfg, inp["x"], inp["w_router"], inp["b_router"], idx, gate, ws)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    slot = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ndrop = torch.empty(1, dtype=torch.int32, device=DEV)
+    xp = torch.empty((T * k, L), dtype=torch.bfloat16, device=DEV)
+    m.moe_permute(cfg, inp["x"], inp["w_down"], inp["rms_gamma"], idx, counts, offs, perm, slot,
+                  ndrop, xp, ws)
+    g = torch.Generator(device=DEV).manual_seed(7)
+    dy = torch.randn((T * k, L), generator=g, device=DEV).to(torch.bfloat16)
+    dx = torch.empty_like(xp)
+    dw1, dw3, dw2 = (torch.empty_like(inp[n]) for n in ("w1", "w3", "w2"))
+    bws = m.alloc_backward_workspace(cfg, DEV)
+    m.moe_expert_ffn_backward(cfg, xp, offs, inp["w1"], inp["w3"], inp["w2"], dy, dx, dw1, dw3,
+                              dw2, bws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(bws)["status"] == 0
+    c, o = counts.cpu(), offs.cpu()
+    nz = (c > 0).nonzero().flatten()
+    order = nz[c[nz].argsort()]
+    for e in (int(order[-1]), int(order[len(order) // 2]), int(order[0])):
+        lo, hi = int(o[e]), int(o[e + 1])
+        ref = moe_oracle.grouped_experts_backward(xp[lo:hi], [0, hi - lo], inp["w1"][e:e + 1],
+                                                  inp["w3"][e:e + 1], inp["w2"][e:e + 1],
+                                                  dy[lo:hi])
+        for n, got in (("dw1", dw1[e]), ("dw3", dw3[e]), ("dw2", dw2[e])):
+            err = normwise(got.float(), ref[n][0])
+            assert err <= 2e-2, (n, e, hi - lo, err)
+        assert normwise(dx[lo:hi], ref["dx"]) <= 2e-2, (e, hi - lo)
+    del inp, dw1, dw3, dw2
+    torch.cuda.empty_cache()
+
+
+def test_layer_backward_full_size_sampled_dx():
+    """The whole layer's backward at the 535B layer's full size (PDL on, as the bench times it):
+    dx of sampled tokens against the oracle's chain rule on those tokens alone. A token's dx
+    depends only on its own row, and without a capacity its routing is its own."""
+    shape = SHAPES["l535b_t8192"]
+    cfg = m.LayerConfig.from_shape(shape, flags=m.MOE_FLAG_PDL)
+    T, d, L, E = shape.T, shape.d_model, shape.d_latent, shape.n_experts
+    inp = make_layer_inputs(shape, DEV)
+    fws = m.alloc_workspace(cfg, DEV)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    m.moe_forward(cfg, inp, inp["x"], y, fws)
+    g = torch.Generator(device=DEV).manual_seed(7)
+    dy = torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16)
+    dx = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    grads = {n: torch.empty_like(inp[n[1:]]) for n in m.GRAD_NAMES
+             if n not in ("db_router", "drms_gamma")}
+    grads["db_router"] = torch.empty(E, dtype=torch.float32, device=DEV)
+    grads["drms_gamma"] = torch.empty(L, dtype=torch.float32, device=DEV)
+    bws = m.alloc_layer_backward_workspace(cfg, DEV)
+    m.moe_backward(cfg, inp, inp["x"], dy, dx, grads, fws, bws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(bws)["status"] == 0
+    toks = sample_tokens(T, 4)
+    sub = dict(inp)
+    sub["x"] = inp["x"][toks]
+    fwd = moe_oracle.forward(sub, top_k=shape.top_k, rms_eps=shape.rms_eps)
+    ref = moe_oracle.backward(sub, fwd, dy[toks], rms_eps=shape.rms_eps, expert_weight_grads=False)
+    err = normwise(dx[toks], ref["dx"])
+    assert err <= 2e-2, err
+    del inp, grads
+    torch.cuda.empty_cache()
+
+
 # -------------------------------------------------------------------- edge cases ----
 
 from moe_workloads import LayerShape  # noqa: E402
