@@ -227,31 +227,47 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
 
 // c[t] = sum_j gate[t, j] * y_perm[slot_of[t, j]] over kept j, in order j = 0..k-1.
 template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+// One block per `tpb` consecutive tokens (several when k is small, so that a block moves enough
+// bytes). Each token's kept rows are summed in the fixed order j = 0..k-1; the loads of up to four
+// rows are issued together before their products are accumulated in that order.
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a, int tpb) {
   pdl_wait();
-  const int64_t t = blockIdx.x;
-  int32_t slots[32];
-  float gates[32];
-  int ns = 0;
-  for (int j = 0; j < a.k; ++j) {
-    int32_t s = a.slot_of[t * a.k + j];
-    if (s >= a.pool_rows || s < -1) {
-      if (threadIdx.x == 0) report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
-      continue;
-    }
-    if (s >= 0) { slots[ns] = s; gates[ns] = a.gate[t * a.k + j]; ++ns; }
-  }
   const T* yp = static_cast<const T*>(a.y_perm);
   T* out = static_cast<T*>(a.out);
-  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < ns; ++j) {
-      float v[8];
-      ld8(yp + (int64_t)slots[j] * a.L + i, v);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(gates[j], v[q], acc[q]);
+  const int64_t t_end = imin64(a.T, ((int64_t)blockIdx.x + 1) * tpb);
+  for (int64_t t = (int64_t)blockIdx.x * tpb; t < t_end; ++t) {
+    int32_t slots[32];
+    float gates[32];
+    int ns = 0;
+    for (int j = 0; j < a.k; ++j) {
+      int32_t s = a.slot_of[t * a.k + j];
+      if (s >= a.pool_rows || s < -1) {
+        if (threadIdx.x == 0) report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
+        continue;
+      }
+      if (s >= 0) { slots[ns] = s; gates[ns] = a.gate[t * a.k + j]; ++ns; }
     }
-    st8(out + t * a.ld_out + i, acc);
+    for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      int j = 0;
+      for (; j + 4 <= ns; j += 4) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ld8(yp + (int64_t)slots[j + u] * a.L + i, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(gates[j + u], v[u][q], acc[q]);
+        }
+      }
+      for (; j < ns; ++j) {
+        float v[8];
+        ld8(yp + (int64_t)slots[j] * a.L + i, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(gates[j], v[q], acc[q]);
+      }
+      st8(out + t * a.ld_out + i, acc);
+    }
   }
 }
 
@@ -293,8 +309,11 @@ cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool
 }
 
 cudaError_t combine_run(const CombineArgs& a, int dtype, cudaStream_t st, bool pdl) {
-  if (dtype == DT_BF16) return launch(combine_kernel<bf16>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
-  return launch(combine_kernel<float>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
+  // tokens per block: at least ~4 rows of input per block
+  const int tpb = a.k >= 4 ? 1 : (a.k == 1 ? 4 : 2);
+  const dim3 grid((unsigned)cdiv(a.T, tpb));
+  if (dtype == DT_BF16) return launch(combine_kernel<bf16>, grid, dim3(128), 0, st, pdl, a, tpb);
+  return launch(combine_kernel<float>, grid, dim3(128), 0, st, pdl, a, tpb);
 }
 
 cudaError_t validate_offsets(const int32_t* off, int G, int64_t rows, DeviceHeader* h,
