@@ -526,6 +526,27 @@ def test_token_mask_small_bf16():
     assert got["report"]["status"] == 0
 
 
+def test_fp8_with_capacity_and_padding():
+    """fp8 experts together with a capacity that drops assignments and attention-mask padding:
+    routing, drops and slots bit-exact, outputs (dropped and padding tokens included) against
+    the oracle's fp8 layer."""
+    shape = SHAPES["small_fp8"].with_(T=2048, capacity=(1, 2))
+    inp = gpu_inputs(shape)
+    mask = padding_mask(shape.T, seq_len=256, seed=4)
+    got = run_forward(shape, inp, token_mask=mask)
+    pads = (mask == 0).nonzero().flatten()[:6].tolist()
+    dropped = (got["slot_of"].cpu() < 0).any(1).nonzero().flatten()
+    dropped = [t for t in dropped.tolist() if int(mask[t])][:6]
+    toks = sample_tokens(shape.T, 64, extra=pads + dropped)
+    ref = oracle_forward(shape, dict({k: v.cpu() for k, v in inp.items()}, token_mask=mask),
+                         tokens=toks)
+    check_routing(got, ref, shape)
+    assert int(ref["n_dropped"]) > 0 and len(dropped) > 0
+    err = normwise(got["y"][toks], ref["y"])
+    assert err <= 2e-2, err
+    assert got["report"]["status"] == 0
+
+
 # ---------------------------------------------------------- expert MLP backward ----
 
 def _backward_case(E, L, F, counts, seed=21, pad=64):
