@@ -99,14 +99,14 @@ def e4m3_codes_match(got_vals: torch.Tensor, exact: torch.Tensor, atol: float):
     return int(bad.numel())
 
 
-def near_tie_router(T=512, d=256, E=64, seed=3):
-    """bf16 router inputs built to defeat fp32 logits: duplicated expert columns (exact
-    ties, to be broken by the lower index) and columns that differ only in an element
-    weighted by 2^-30 (gaps far below fp32 resolution), plus reordered columns."""
+def near_tie_router(T=512, d=256, E=64, seed=3, dtype=torch.bfloat16):
+    """Router inputs (bf16, or fp32 with dtype) built to defeat fp32 logits: duplicated expert
+    columns (exact ties, to be broken by the lower index) and columns that differ only in an
+    element weighted by 2^-30 (gaps far below fp32 resolution), plus reordered columns."""
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(T, d, generator=g)
     x[:, -1] = 2.0 ** -30                           # a tiny coordinate shared by all tokens
-    x = x.to(torch.bfloat16)
+    x = x.to(dtype)
     base = torch.randn(d, 8, generator=g) * d ** -0.5
     cols = []
     for e in range(E):
@@ -116,5 +116,5 @@ def near_tie_router(T=512, d=256, E=64, seed=3):
         if e % 5 == 2:
             c[:-1] = c[:-1][torch.randperm(d - 1, generator=g)]
         cols.append(c)
-    w = torch.stack(cols, 1).to(torch.bfloat16)
+    w = torch.stack(cols, 1).to(dtype)
     return x, w

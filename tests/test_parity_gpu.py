@@ -164,6 +164,26 @@ def test_router_exact_on_near_ties(path, T):
         assert rep["n_exact"] > 64, rep                           # past the saved slots too
 
 
+def test_router_exact_on_near_ties_f32():
+    """The same near ties with fp32 router inputs: stage 2 then needs TwoProduct for the exact
+    products of fp32 values, and stage 3 integer products of 24-bit significands."""
+    x, w = near_tie_router(T=512, dtype=torch.float32)
+    T, d = x.shape
+    E, k = w.shape[1], 8
+    cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,
+                        d_ff_shared=0, dtype="f32")
+    ws = m.alloc_workspace(cfg, DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(cfg, x.to(DEV), w.to(DEV), None, idx, gate, ws)
+    rep = m.moe_get_device_status(ws)
+    ref = moe_oracle.route(x, w, None, k)
+    assert torch.equal(idx.cpu().long(), ref["idx"])
+    assert float((gate.cpu().double() - ref["gate"]).abs().max()) <= 1e-6
+    assert rep["status"] == 0
+    assert rep["n_refined"] > 0 and rep["n_exact"] > 64, rep      # both exact-stage paths
+
+
 # ------------------------------------------------------------ device-detected errors ----
 
 def test_bad_routing_is_reported_not_faulted():
