@@ -866,9 +866,10 @@ def test_edge_case_forward(name):
     assert got["report"]["status"] == 0
 
 
-def test_forward_pipelined_matches_forward():
+@pytest.mark.parametrize("name", ["small_bf16", "small_fp8"])
+def test_forward_pipelined_matches_forward(name):
     """The host-buffer serving path gives, batch for batch, the bits moe_forward gives."""
-    shape = SHAPES["small_bf16"].with_(T=512)
+    shape = SHAPES[name].with_(T=512)
     inp = gpu_inputs(shape)
     cfg = m.LayerConfig.from_shape(shape, flags=m.MOE_FLAG_PDL)
     T, d = shape.T, shape.d_model
