@@ -58,6 +58,8 @@ def test_small_bf16_forward(path):
 
 
 def test_forward_deterministic():
+    """Two runs give the same bits: bf16 on both GEMM paths, and fp8 experts (whose amax
+    reductions are order-independent maxima)."""
     shape = SHAPES["small_bf16"].with_(T=1024)
     inp = gpu_inputs(shape)
     for flags in BF16_PATHS.values():
@@ -65,6 +67,11 @@ def test_forward_deterministic():
         b = run_forward(shape, inp, flags)
         assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
         assert torch.equal(a["topk_gate"], b["topk_gate"])
+    shape = SHAPES["small_fp8"].with_(T=1024)
+    inp = gpu_inputs(shape)
+    a, b = run_forward(shape, inp), run_forward(shape, inp)
+    assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
+    assert float(a["x_amax"]) == float(b["x_amax"]) and float(a["h_amax"]) == float(b["h_amax"])
 
 
 # ---------------------------------------------------------------------- split calls ----
