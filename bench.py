@@ -484,6 +484,8 @@ def main():
                     help="time the routed experts' backward (moe_expert_ffn_backward) instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the whole layer's backward (moe_backward) instead")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one captured CUDA graph of moe_forward per timed step")
     ap.add_argument("--slice", action="store_true",
                     help="time the expert-parallel slice workload (grouped expert MLP + un-permute)")
     args = ap.parse_args()
@@ -528,6 +530,16 @@ def main():
     for _ in range(max(3, args.warmup)):
         m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
     torch.cuda.synchronize(dev)
+    graph = None
+    if args.graph:
+        # the whole forward (its kernels, PDL edges and stage events) as one CUDA graph
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            m.moe_forward(cfg, inp, inp["x"], y, ws, stream=torch.cuda.current_stream(dev),
+                          aux=aux)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
     rep = m.moe_get_device_status(ws)
     if rep["status"] != 0:
         raise RuntimeError(f"device report after warm-up: {rep}")
@@ -542,7 +554,10 @@ def main():
     t_wall = time.perf_counter()
     for _ in range(args.steps):
         flush.zero_()                                   # L2 flushed between timed steps
-        m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
+        if graph is not None:
+            graph.replay()
+        else:
+            m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
         evs[-1].synchronize()
         step_ms.append(evs[0].elapsed_time(evs[-1]))
         for i, s in enumerate(STAGES):
@@ -637,6 +652,7 @@ def main():
                                f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gemm_path": "simt" if args.simt else "tcgen05", "pdl": not args.no_pdl,
+                   "launch": "cuda graph replay" if args.graph else "eager",
                    "expert_weights": shape.expert_dtype,
                    "l2": "flushed between timed steps (256 MB write); weights "
                          f"({weight_bytes(shape) / 1e9:.1f} GB) exceed L2"},

@@ -151,7 +151,11 @@ typedef struct {
 /* Optional extras of moe_forward; every pointer may be NULL. Device buffers receive copies of
  * the routing results. stage_events, when not NULL, holds MOE_FORWARD_STAGES + 1 cudaEvent_t
  * handles created by the caller; event i is recorded on `stream` before stage i and the last
- * one after the final stage, so that the caller can time stages without a profiler. */
+ * one after the final stage, so that the caller can time stages without a profiler. Under
+ * stream capture they are recorded as external event nodes: every replay of the graph records
+ * them, and the caller can synchronize on them and time them as usual.
+ * moe_forward may be captured in a CUDA graph (its kernels, their programmatic-dependent-launch
+ * edges and these events) and replayed; the graph keeps the buffers it was captured with. */
 #define MOE_FORWARD_STAGES 8   /* prep, front GEMM, router select, dispatch, expert GEMM 1,
                                   expert GEMM 2, combine, back GEMM */
 typedef struct {

@@ -439,9 +439,15 @@ CombineArgs combine_args(const Call& k, const void* y_perm, const int32_t* slot_
   return a;
 }
 
+// Stage event i on st. Under stream capture the record becomes an external event node of the
+// graph, so that the caller can still synchronize on and time the events of each replay.
 void record(const moe_forward_aux_t* aux, int i, cudaStream_t st) {
-  if (aux && aux->stage_events && aux->stage_events[i])
-    cudaEventRecord(static_cast<cudaEvent_t>(aux->stage_events[i]), st);
+  if (!aux || !aux->stage_events || !aux->stage_events[i]) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+  cudaEventRecordWithFlags(static_cast<cudaEvent_t>(aux->stage_events[i]), st,
+                           cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                               : cudaEventRecordDefault);
 }
 
 // ---- routing without caller-allocated scratch -------------------------------------------

@@ -873,6 +873,46 @@ def test_edge_case_forward(name):
     assert got["report"]["status"] == 0
 
 
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16", "small_fp8"])
+def test_forward_cuda_graph_replay(name):
+    """moe_forward captured in a CUDA graph (PDL edges included) and replayed on new inputs
+    copied into the captured buffer gives the bits of an eager call on the same inputs."""
+    shape = SHAPES[name]
+    inp = gpu_inputs(shape)
+    flags = m.MOE_FLAG_PDL
+    cfg = m.LayerConfig.from_shape(shape, flags=flags)
+    T, d = shape.T, shape.d_model
+    ws = m.alloc_workspace(cfg, DEV)
+    x = inp["x"].clone()
+    y = torch.empty((T, d), dtype=shape.torch_dtype, device=DEV)
+    st = torch.cuda.Stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_FORWARD_STAGES + 1)]
+    for e in evs:
+        e.record(st)
+    aux = {"stage_events": evs}
+    with torch.cuda.stream(st):
+        m.moe_forward(cfg, inp, x, y, ws, stream=st, aux=aux)   # first call outside the capture
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        m.moe_forward(cfg, inp, x, y, ws, stream=st, aux=aux)
+    gen = torch.Generator().manual_seed(9)
+    for _ in range(3):
+        xn = torch.randn(T, d, generator=gen).to(shape.torch_dtype).to(DEV)
+        x.copy_(xn)
+        g.replay()
+        evs[-1].synchronize()                                   # the stage events are replayed too
+        assert evs[0].elapsed_time(evs[-1]) > 0
+        torch.cuda.synchronize()
+        y_graph = y.clone()
+        y_eager = torch.empty_like(y)
+        m.moe_forward(cfg, inp, xn, y_eager, ws)
+        torch.cuda.synchronize()
+        bits = torch.int16 if shape.dtype == "bf16" else torch.int32
+        assert torch.equal(y_graph.view(bits), y_eager.view(bits))
+    assert m.moe_get_device_status(ws)["status"] == 0
+
+
 @pytest.mark.parametrize("name", ["small_bf16", "small_fp8"])
 def test_forward_pipelined_matches_forward(name):
     """The host-buffer serving path gives, batch for batch, the bits moe_forward gives."""
