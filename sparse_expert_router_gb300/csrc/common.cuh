@@ -85,11 +85,20 @@ __device__ __forceinline__ void st8(float* p, const float v[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// silu(u) * v with an accurate exponential and IEEE division (the approximate fused SwiGLU of
-// the Marin summary for the week of 2026-07-06, #7024, caused a ~2.6% output mismatch).
+// silu(u) * v for a hidden stored in bf16 or E4M3. The exponential and the division are the
+// hardware approximations __expf (at most 2 + floor(1.173 |u|) ulp) and __fdividef (2 ulp),
+// about 2e-6 relative for |u| <= 10: three orders of magnitude below the 2^-9 rounding of the
+// bf16 hidden. The approximate fused SwiGLU of the Marin summary for the week of 2026-07-06
+// (#7024) caused a ~2.6% output mismatch, an error at the scale of the stored precision.
 __device__ __forceinline__ float swiglu(float u, float v) {
+  return __fdividef(u, 1.0f + __expf(-u)) * v;
+}
+// The same for an fp32 hidden (the fp32 layer): accurate exponential and IEEE division.
+__device__ __forceinline__ float swiglu_ieee(float u, float v) {
   return __fdiv_rn(u, 1.0f + expf(-u)) * v;
 }
+// sigmoid(g) for the SwiGLU backward of a bf16 hidden, with the same approximations as swiglu.
+__device__ __forceinline__ float sigmoid_bf16(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // ---- programmatic dependent launch ----------------------------------------------------
 // Every thread of a consumer kernel executes pdl_wait() before it reads anything a preceding

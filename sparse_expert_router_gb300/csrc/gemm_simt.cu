@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
         if (p.bias) v = __fadd_rn(v, p.bias[c]);
         static_cast<float*>(p.out)[o] = v;
       } else if (p.epi == EPI_SWIGLU) {
-        st_f(static_cast<T*>(p.out), o, swiglu(acc[i][j], acc3[i][j]));
+        st_f(static_cast<T*>(p.out), o,
+             sizeof(T) == 4 ? swiglu_ieee(acc[i][j], acc3[i][j]) : swiglu(acc[i][j], acc3[i][j]));
       } else {
         st_f(static_cast<T*>(p.out), o, acc[i][j]);
       }

@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
             for (int j = 0; j < 16; ++j) {
               const float g = (j & 1) ? __high2float(gg[j / 2]) : __low2float(gg[j / 2]);
               const float u = (j & 1) ? __high2float(uu[j / 2]) : __low2float(uu[j / 2]);
-              const float sg = __fdiv_rn(1.0f, 1.0f + expf(-g));   // sigmoid(G)
+              const float sg = sigmoid_bf16(g);                      // sigmoid(G)
               v3[j] = v[j] * u * (sg * (1.0f + g * (1.0f - sg)));
               v[j] = v[j] * (g * sg);
             }
