@@ -50,21 +50,25 @@ def peaks():
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "tc_gemm_grouped_l535b_e64_t1368.md")
 
 
+# the sources the grouped GEMM kernel is compiled from: a change to any of them voids the counters
+PROFILED_SOURCES = ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "gemm.h")
+
+
 def profiled_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, or None
-    when there is none or the GEMM source changed since the counters were taken."""
+    when there is none or a source of the GEMM changed since the counters were taken."""
     import hashlib
     try:
         text = open(PROFILE_SUMMARY).read()
-        src = open(os.path.join(ROOT, "sparse_expert_router_gb300", "csrc", "gemm_tc.cu"), "rb").read()
+        shas = {f: hashlib.sha256(open(os.path.join(ROOT, "sparse_expert_router_gb300", "csrc", f),
+                                       "rb").read()).hexdigest()[:16] for f in PROFILED_SOURCES}
     except OSError:
         return None
-    sha = hashlib.sha256(src).hexdigest()[:16]
-    ok_sha = any(ln.split() == ["source_sha256_prefix", "gemm_tc.cu", sha] for ln in text.splitlines())
-    if not ok_sha:
-        return None
-    for ln in text.splitlines():
-        parts = ln.split()
+    lines = [ln.split() for ln in text.splitlines()]
+    for f, sha in shas.items():
+        if ["source_sha256_prefix", f, sha] not in lines:
+            return None
+    for parts in lines:
         if len(parts) == 4 and parts[0] == "traffic_per_launch" and parts[1] == workload \
                 and parts[2] == kernel:
             return float(parts[3])
