@@ -563,6 +563,22 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       const int buf = ev % nacc;
       const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
       ++ev;
+      // fp8: dequantization factor of each accumulator, fp32(1 / activation scale) times the
+      // feature's weight scale in this expert (w, and w3 for the up projection). Loaded before
+      // the wait for the accumulator, so that their latency hides behind the main loop.
+      float sc1s[2] = {1.0f, 1.0f}, sc3s[2] = {1.0f, 1.0f}, osc = 1.0f;
+      if constexpr (FP8) {
+        const float da = __fdiv_rn(1.0f, *q.act_scale);
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int f0 = it.m0 + sub * BM + quad * 32;
+          const bool fok = (sub == 0 || q.dual) && f0 + lane < q.M;
+          const int64_t fs = (int64_t)it.wg * q.M + f0 + lane;
+          sc1s[sub] = fok ? __fmul_rn(da, q.w_scale[fs]) : 0.0f;
+          sc3s[sub] = (fok && q.w3_scale) ? __fmul_rn(da, q.w3_scale[fs]) : 0.0f;
+        }
+        if (q.out_fp8) osc = *q.out_scale;
+      }
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
       for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
@@ -572,16 +588,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       const bool f32out = (q.epi == EPI_F32);
       const bool fok = f0 + lane < q.M;
       const float bias = (f32out && q.bias && fok) ? q.bias[f0 + lane] : 0.0f;
-      // fp8: dequantization factor of each accumulator, fp32(1 / activation scale) times the
-      // feature's weight scale in this expert (w, and w3 for the up projection)
-      const int64_t fs = (int64_t)it.wg * q.M + f0 + lane;
-      float sc1 = 1.0f, sc3 = 1.0f, osc = 1.0f;
-      if constexpr (FP8) {
-        const float da = __fdiv_rn(1.0f, *q.act_scale);
-        sc1 = fok ? __fmul_rn(da, q.w_scale[fs]) : 0.0f;
-        sc3 = (fok && q.w3_scale) ? __fmul_rn(da, q.w3_scale[fs]) : 0.0f;
-        if (q.out_fp8) osc = *q.out_scale;
-      }
+      const float sc1 = sub ? sc1s[1] : sc1s[0], sc3 = sub ? sc3s[1] : sc3s[0];
       for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
         float v[16], v3[16];
         tmem_ld16(lane_addr + c0, v);

@@ -145,6 +145,10 @@ template <>
 struct Raw8<bf16> {
   uint4 u;
   __device__ __forceinline__ void load(const bf16* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ bf16 raw(int q) const {   // element q
+    const uint32_t wd = q < 2 ? u.x : q < 4 ? u.y : q < 6 ? u.z : u.w;
+    return __ushort_as_bfloat16((unsigned short)((q & 1) ? (wd >> 16) : (wd & 0xFFFFu)));
+  }
   __device__ __forceinline__ void get(float v[8]) const {
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -161,6 +165,11 @@ struct Raw8<float> {
   __device__ __forceinline__ void load(const float* p) {
     a = *reinterpret_cast<const float4*>(p);
     b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ float raw(int q) const {   // element q
+    const float4& h = q < 4 ? a : b;
+    const int r = q & 3;
+    return r == 0 ? h.x : r == 1 ? h.y : r == 2 ? h.z : h.w;
   }
   __device__ __forceinline__ void get(float v[8]) const {
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -294,10 +303,21 @@ __device__ __forceinline__ bool decompose<bf16>(bf16 v, uint32_t& M, int& q, uin
   return true;
 }
 
+// a[u] for a runtime u < N without dynamic indexing (the array stays in registers)
+template <typename R, int N>
+__device__ __forceinline__ R pick(const R (&a)[N], int u) {
+  R r = a[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i)
+    if (u == i) r = a[i];
+  return r;
+}
+
 // Block-wide exact x . w + bias (blockDim = RT_WARPS * 32) into canonical form `out`. Every
 // thread accumulates its products in 20 register limbs (updated with predicated adds, so the
-// limbs stay in registers); warps add their limbs with shuffles, thread 0 adds the warps' limbs
-// (from `red`, RT_WARPS * NB int64 of shared memory) and propagates the carries.
+// limbs stay in registers); warps add their limbs with shuffles, warp 0 adds the warps' limbs
+// (from `red`, RT_WARPS * NB int64 of shared memory), one limb per lane, and lane 0 propagates
+// the carries. Requires d % 8 == 0 and 16-byte aligned rows.
 template <typename T>
 __device__ bool block_exact(const T* x, const T* w, int d, float bias,
                             long long* red, unsigned long long* out) {
@@ -320,13 +340,33 @@ __device__ bool block_exact(const T* x, const T* w, int d, float bias,
     for (int i = 0; i < NB; ++i)
       bins[i] += (i == bi) ? c0 : (i == bi + 1) ? c1 : (i == bi + 2) ? c2 : 0ll;
   };
-  for (int i = tid; i < d; i += RT_WARPS * 32) {
-    uint32_t Mx = 0, Mw = 0, sx = 0, sw = 0;
-    int qx = 0, qw = 0;
-    bool fx = decompose<T>(x[i], Mx, qx, sx);
-    bool fw = decompose<T>(w[i], Mw, qw, sw);
-    ok &= fx && fw;
-    if (fx && fw) add((uint64_t)Mx * (uint64_t)Mw, qx + qw, sx ^ sw);
+  // XB groups of 8 elements per thread per trip, all their loads issued before any product;
+  // the limb sums are exact, so how elements are assigned to threads does not change them
+  constexpr int XB = 4;
+  const int nv = d >> 3;
+  for (int v0 = tid; v0 < nv; v0 += RT_WARPS * 32 * XB) {
+    Raw8<T> xr[XB], wr[XB];
+#pragma unroll
+    for (int u = 0; u < XB; ++u) {
+      const int v = v0 + RT_WARPS * 32 * u;
+      if (v < nv) {
+        xr[u].load(x + 8 * v);
+        wr[u].load(w + 8 * v);
+      }
+    }
+    // one compact loop over the loaded elements: the kernel runs once per step, from a cold
+    // instruction cache, so its code size matters more than its instruction count
+    const int nu = min(XB, (nv - v0 + RT_WARPS * 32 - 1) / (RT_WARPS * 32));
+#pragma unroll 1
+    for (int uq = 0; uq < nu * 8; ++uq) {
+      const int u = uq >> 3, q = uq & 7;
+      uint32_t Mx = 0, Mw = 0, sx = 0, sw = 0;
+      int qx = 0, qw = 0;
+      const bool fx = decompose<T>(pick(xr, u).raw(q), Mx, qx, sx);
+      const bool fw = decompose<T>(pick(wr, u).raw(q), Mw, qw, sw);
+      ok &= fx && fw;
+      if (fx && fw) add((uint64_t)Mx * (uint64_t)Mw, qx + qw, sx ^ sw);
+    }
   }
   if (tid == 0) {
     uint32_t Mb = 0, sb = 0;
@@ -343,16 +383,27 @@ __device__ bool block_exact(const T* x, const T* w, int d, float bias,
     if (lane == 0) red[warp * NB + i] = v;
   }
   ok = __syncthreads_and(ok);
-  if (tid == 0) {
-    long long carry = 0;
-    for (int i = 0; i < NB; ++i) {
-      long long v = carry;
-      for (int wv = 0; wv < RT_WARPS; ++wv) v += red[wv * NB + i];
-      if (i < NB - 1) {
-        out[i] = (unsigned long long)(v & 0xFFFFFFFFll);
-        carry = v >> 32;   // arithmetic shift: floor division
-      } else {
-        out[i] = (unsigned long long)v;
+  // lane i of warp 0 adds limb i over the warps, then lane 0 propagates the carries
+  if (warp == 0) {
+    long long v = 0;
+    if (lane < NB) {
+#pragma unroll
+      for (int wv = 0; wv < RT_WARPS; ++wv) v += red[wv * NB + lane];
+    }
+    __syncwarp();
+    if (lane < NB) red[lane] = v;
+    __syncwarp();
+    if (lane == 0) {
+      long long carry = 0;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const long long t = carry + red[i];
+        if (i < NB - 1) {
+          out[i] = (unsigned long long)(t & 0xFFFFFFFFll);
+          carry = t >> 32;   // arithmetic shift: floor division
+        } else {
+          out[i] = (unsigned long long)t;
+        }
       }
     }
   }
