@@ -171,6 +171,36 @@ def test_router_exact_on_near_ties(path, T):
         assert rep["n_exact"] > 64, rep                           # past the saved slots too
 
 
+@pytest.mark.parametrize("E,k,dtype,path", [(64, 8, "bf16", "tc"), (64, 8, "bf16", "simt"),
+                                             (64, 8, "f32", "tc"), (1024, 32, "bf16", "tc")],
+                         ids=["e64_bf16_tc", "e64_bf16_simt", "e64_f32", "e1024_k32_bf16"])
+def test_router_tied_logits(E, k, dtype, path):
+    """The degenerate router: zero weights, so every logit is its bias, and the biases repeat
+    in four levels. The top level holds E/4 exactly equal logits; the k lowest indices among
+    them win, and the gates are all 1/k. Every expert of the top level is undecided until the
+    exact stage."""
+    T, d = 40, 256
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(T, d, generator=g).to(tdt)
+    w = torch.zeros(d, E, dtype=tdt)
+    b = (torch.arange(E) % 4).float() * 0.5
+    cfg = m.LayerConfig(T=T, d_model=d, d_latent=64, n_experts=E, top_k=k, d_ff=64, n_shared=0,
+                        d_ff_shared=0, dtype=dtype, flags=BF16_PATHS[path])
+    ws = m.alloc_workspace(cfg, DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(cfg, x.to(DEV), w.to(DEV), b.to(DEV), idx, gate, ws)
+    rep = m.moe_get_device_status(ws)
+    ref = moe_oracle.route(x, w, b, k)
+    want = torch.arange(3, 4 * k, 4).expand(T, -1)
+    assert torch.equal(ref["idx"], want)                          # the oracle's own reading
+    assert torch.equal(idx.cpu().long(), want)
+    assert float((gate.cpu() - 1.0 / k).abs().max()) <= 1e-7
+    assert rep["status"] == 0
+    assert rep["n_exact"] == T, rep
+
+
 def test_router_exact_on_near_ties_f32():
     """The same near ties with fp32 router inputs: stage 2 then needs TwoProduct for the exact
     products of fp32 values, and stage 3 integer products of 24-bit significands."""
