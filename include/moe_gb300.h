@@ -348,9 +348,9 @@ MOE_API moe_status_t moe_selftest_device_timeout(void* ws, size_t ws_bytes, uint
  * fixed array of 32 MiB inside the library, present on every GPU that loads the library until
  * the process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Sizes: the routing scratch (256 B + T*E*4 + E*d*elem + E*4 + 3*T*4 bytes, plus
- *     64*(E*168 + 4) bytes of exact-stage state, each region rounded up to 256 B) must fit in
+ *     64*(E*161 + 8) bytes of exact-stage state, each region rounded up to 256 B) must fit in
  *     32 MiB, else MOE_ERR_WORKSPACE and nothing is enqueued; the 535B-shaped router
- *     (T = 8192, E = 384, d = 6144, bf16) needs 21.5 MB.
+ *     (T = 8192, E = 384, d = 6144, bf16) needs 21.4 MB.
  *   - Set-up: the first call on a device looks up the array's device address (with that device
  *     current); make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array and leaves its contents behind; each

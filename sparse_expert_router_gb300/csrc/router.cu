@@ -121,22 +121,35 @@ __device__ void warp_write_selection(const float* lg, const uint8_t* sel, int E,
 }
 
 // Load a token's logits and stage-1 intervals into per-warp shared arrays.
+// Loops over a token's experts take EU experts per lane per trip and issue all their global
+// loads before any shared-memory store, so that a trip costs one memory latency, not EU.
+constexpr int EU = 4;
+
 __device__ void warp_stage1(const float* logits_t, const float* wnorm, float xn, float cgam,
                             int E, int lane, float* lg, float* lo, float* hi) {
   const float cx = __fmul_ru(cgam, xn);
-  for (int e = lane; e < E; e += 32) {
-    float l = logits_t[e];
-    float b = __fadd_ru(__fmul_ru(cx, wnorm[e]), __fmul_ru(2.0f * U32, fabsf(l)));
-    b = __fadd_ru(b, 1e-30f);
-    lg[e] = l;
-    lo[e] = __fsub_rd(l, b);
-    hi[e] = __fadd_ru(l, b);
+  for (int e0 = lane; e0 < E; e0 += 32 * EU) {
+    float l[EU], wn[EU];
+#pragma unroll
+    for (int u = 0; u < EU; ++u) {
+      const int e = e0 + 32 * u;
+      l[u] = e < E ? logits_t[e] : 0.0f;
+      wn[u] = e < E ? wnorm[e] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < EU; ++u) {
+      const int e = e0 + 32 * u;
+      if (e < E) {
+        float b = __fadd_ru(__fmul_ru(cx, wn[u]), __fmul_ru(2.0f * U32, fabsf(l[u])));
+        b = __fadd_ru(b, 1e-30f);
+        lg[e] = l[u];
+        lo[e] = __fsub_rd(l[u], b);
+        hi[e] = __fadd_ru(l[u], b);
+      }
+    }
   }
   __syncwarp();
 }
-
-template <typename T>
-__device__ __forceinline__ void load8f(const T* p, float v[8]) { ld8(p, v); }
 
 // 8 elements as loaded (16 B of bf16 or 32 B of fp32), converted to fp32 on use.
 template <typename T>
@@ -178,15 +191,25 @@ struct Raw8<float> {
 };
 
 // Upper bound of ||x||_2 for a row of d elements (d a multiple of 8).
+// Each lane issues the loads of XU groups of 8 elements before it adds any of them (the sum
+// keeps its order).
 template <typename T>
 __device__ float warp_norm_ub(const T* x, int d, float gam_d, int lane) {
+  constexpr int XU = 8;
   float s = 0.0f;
-#pragma unroll 4
-  for (int i = lane * 8; i < d; i += 256) {
-    float v[8];
-    load8f(x + i, v);
+  for (int i0 = lane * 8; i0 < d; i0 += 256 * XU) {
+    Raw8<T> r[XU];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s = fmaf(v[j], v[j], s);
+    for (int u = 0; u < XU; ++u)
+      if (i0 + 256 * u < d) r[u].load(x + i0 + 256 * u);
+#pragma unroll
+    for (int u = 0; u < XU; ++u) {
+      if (i0 + 256 * u >= d) break;
+      float v[8];
+      r[u].get(v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s = fmaf(v[j], v[j], s);
+    }
   }
   s = warp_sum_f(s);
   // s~ >= (1 - gamma_d) s, so s <= s~ (1 + 2 gamma_d) for gamma_d <= 1/2
@@ -484,12 +507,24 @@ router_select_kernel(RouterArgs a) {
   if (lane == 0) a.xnorm[t] = xn;
   const float* lt = a.logits + t * a.E;
   float wmax = 0.0f, amax = 0.0f;
-  for (int e = lane; e < a.E; e += 32) {
-    const float l = lt[e];
-    w.lg[e] = l;
-    w.work[e] = l;
-    wmax = fmaxf(wmax, a.wnorm[e]);
-    amax = fmaxf(amax, fabsf(l));
+  for (int e0 = lane; e0 < a.E; e0 += 32 * EU) {
+    float l[EU], wn[EU];
+#pragma unroll
+    for (int u = 0; u < EU; ++u) {
+      const int e = e0 + 32 * u;
+      l[u] = e < a.E ? lt[e] : 0.0f;
+      wn[u] = e < a.E ? a.wnorm[e] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < EU; ++u) {
+      const int e = e0 + 32 * u;
+      if (e < a.E) {
+        w.lg[e] = l[u];
+        w.work[e] = l[u];
+        wmax = fmaxf(wmax, wn[u]);
+        amax = fmaxf(amax, fabsf(l[u]));
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -546,38 +581,26 @@ router_select_kernel(RouterArgs a) {
 // undecided expert and publishes its exact value; the last block to arrive ranks them all.
 constexpr int EXACT_PARTS = 8;
 
-// The saved state of exact-list slot `it` inside RouterArgs::saved.
+// The saved state of exact-list slot `it` inside RouterArgs::saved: the refine stage's final
+// classification of the token, and the exact values the exact stage's blocks publish.
 struct SavedSlot {
-  float* bounds;               // [2, E]: lo, hi
+  uint8_t* sel;                // [E]: 1 surely in, 0 surely out, 2 undecided after stage 2
+  int32_t* n_in;               // experts surely in
   unsigned long long* forms;   // [E, NB]: exact values of the undecided experts
   int32_t* arrived;            // blocks of this token done with their experts
 };
+__host__ __device__ __forceinline__ size_t al256z(size_t b) { return (b + 255) & ~(size_t)255; }
 __device__ __forceinline__ SavedSlot saved_slot(const RouterArgs& a, int it) {
   unsigned char* base = static_cast<unsigned char*>(a.saved);
-  const size_t nb = ((size_t)a.n_saved * 2 * a.E * 4 + 255) & ~(size_t)255;
-  const size_t nf = ((size_t)a.n_saved * a.E * NB * 8 + 255) & ~(size_t)255;
+  const size_t ns = al256z((size_t)a.n_saved * a.E);
+  const size_t nn = al256z((size_t)a.n_saved * 4);
+  const size_t nf = al256z((size_t)a.n_saved * a.E * NB * 8);
   SavedSlot v;
-  v.bounds = reinterpret_cast<float*>(base) + (size_t)it * 2 * a.E;
-  v.forms = reinterpret_cast<unsigned long long*>(base + nb) + (size_t)it * a.E * NB;
-  v.arrived = reinterpret_cast<int32_t*>(base + nb + nf) + it;
+  v.sel = base + (size_t)it * a.E;
+  v.n_in = reinterpret_cast<int32_t*>(base + ns) + it;
+  v.forms = reinterpret_cast<unsigned long long*>(base + ns + nn) + (size_t)it * a.E * NB;
+  v.arrived = reinterpret_cast<int32_t*>(base + ns + nn + nf) + it;
   return v;
-}
-
-// Stage-2 bounds of one token to and from its saved slot [lo[E], hi[E]].
-__device__ void copy_bounds(const float* lo, const float* hi, float* dst, int E,
-                                         int lane) {
-  for (int e = lane; e < E; e += 32) {
-    dst[e] = lo[e];
-    dst[E + e] = hi[e];
-  }
-}
-
-__device__ void restore_bounds(const float* src, float* lo, float* hi, int E,
-                                            int lane) {
-  for (int e = lane; e < E; e += 32) {
-    lo[e] = src[e];
-    hi[e] = src[E + e];
-  }
 }
 
 template <typename T>
@@ -588,7 +611,9 @@ router_refine_kernel(RouterArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpArrays w = warp_arrays(smem, a.E, warp);
   const int n = min(a.hdr->n_refine, (int)a.T);
-  for (int it = blockIdx.x * RT_WARPS + warp; it < n; it += gridDim.x * RT_WARPS) {
+  // consecutive list entries go to consecutive blocks (one per SM), so that a short list still
+  // spreads over every SM
+  for (int it = warp * gridDim.x + blockIdx.x; it < n; it += gridDim.x * RT_WARPS) {
     const int64_t t = a.refine_list[it];
     const T* x = static_cast<const T*>(a.x) + t * a.d;
     warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
@@ -645,11 +670,14 @@ router_refine_kernel(RouterArgs a) {
         a.exact_list[pos] = (int32_t)t;
       }
       pos = __shfl_sync(~0u, pos, 0);
-      // the stage-2 bounds go with it, so that the exact stage starts from them
+      // its classification goes with it, so that the exact stage starts from it
       if (a.saved && pos < a.n_saved) {
         const SavedSlot sv = saved_slot(a, pos);
-        copy_bounds(w.lo, w.hi, sv.bounds, a.E, lane);
-        if (lane == 0) *sv.arrived = 0;
+        for (int e = lane; e < a.E; e += 32) sv.sel[e] = w.sel[e];
+        if (lane == 0) {
+          *sv.n_in = n_in;
+          *sv.arrived = 0;
+        }
       }
     }
   }
@@ -687,12 +715,23 @@ router_exact_kernel(RouterArgs a) {
     SavedSlot sv{};
     if (split) sv = saved_slot(a, it);
     if (warp == 0) {
-      warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
+      int n_in0;
       if (split) {
-        restore_bounds(sv.bounds, w.lo, w.hi, a.E, lane);
+        // the refine stage's classification of the token
+        for (int e0 = lane; e0 < a.E; e0 += 32 * EU) {
+          uint8_t c[EU];
+#pragma unroll
+          for (int u = 0; u < EU; ++u) c[u] = (e0 + 32 * u < a.E) ? sv.sel[e0 + 32 * u] : 0;
+#pragma unroll
+          for (int u = 0; u < EU; ++u)
+            if (e0 + 32 * u < a.E) w.sel[e0 + 32 * u] = c[u];
+        }
+        n_in0 = *sv.n_in;
         __syncwarp();
+      } else {
+        warp_stage1(a.logits + t * a.E, a.wnorm, a.xnorm[t], a.cgam, a.E, lane, w.lg, w.lo, w.hi);
+        n_in0 = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
       }
-      const int n_in0 = warp_classify(w.lo, w.hi, w.work, w.sel, a.E, a.k, lane);
       int base = 0;
       for (int e0 = 0; e0 < a.E; e0 += 32) {
         int e = e0 + lane;
@@ -763,6 +802,11 @@ router_exact_kernel(RouterArgs a) {
     if (warp == 0) {
       if (!s_ok && lane == 0) report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
       if (!split || s_last) {
+        if (split) {
+          const float* lt = a.logits + t * a.E;
+          for (int e = lane; e < a.E; e += 32) w.lg[e] = lt[e];
+          __syncwarp();
+        }
         const int need = a.k - s_nin;
         // rank each candidate among the candidates: larger exact value first, then lower index
         for (int ci = lane; ci < nc2; ci += 32) {
@@ -787,10 +831,10 @@ size_t warp_smem(int E) { return ((size_t)E * 18 + 15) & ~(size_t)15; }
 }  // namespace
 
 size_t router_saved_bytes(int E, int n_saved) {
-  // the layout of saved_slot: bounds, forms, arrival counters, each rounded up to 256 B
-  const size_t nb = ((size_t)n_saved * 2 * E * 4 + 255) & ~(size_t)255;
-  const size_t nf = ((size_t)n_saved * E * NB * 8 + 255) & ~(size_t)255;
-  return nb + nf + (size_t)n_saved * 4;
+  // the layout of saved_slot: classifications, sure-in counts, exact values and arrival
+  // counters, the first three rounded up to 256 B
+  return al256z((size_t)n_saved * E) + al256z((size_t)n_saved * 4) +
+         al256z((size_t)n_saved * E * NB * 8) + (size_t)n_saved * 4;
 }
 
 cudaError_t router_prepare(const RouterArgs& a, int dtype, cudaStream_t st, bool pdl) {
@@ -824,7 +868,7 @@ cudaError_t router_select(const RouterArgs& a, int dtype, int num_sms, cudaStrea
   cudaFuncSetAttribute(ex, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_exact);
   err = launch(sel, dim3((unsigned)cdiv(a.T, RT_WARPS)), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(ref, dim3(num_sms * 4), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
+  err = launch(ref, dim3(num_sms), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
   if (err != cudaSuccess) return err;
   return launch(ex, dim3(num_sms), dim3(RT_WARPS * 32), sm_exact, st, pdl, a);
 }
