@@ -191,11 +191,11 @@ struct Raw8<float> {
 };
 
 // Upper bound of ||x||_2 for a row of d elements (d a multiple of 8).
-// Each lane issues the loads of XU groups of 8 elements before it adds any of them (the sum
-// keeps its order).
+// Each lane issues the loads of XU groups of 8 elements (128 bytes) before it adds any of them
+// (the sum keeps its order).
 template <typename T>
 __device__ float warp_norm_ub(const T* x, int d, float gam_d, int lane) {
-  constexpr int XU = 8;
+  constexpr int XU = sizeof(T) == 4 ? 4 : 8;
   float s = 0.0f;
   for (int i0 = lane * 8; i0 < d; i0 += 256 * XU) {
     Raw8<T> r[XU];
@@ -491,17 +491,16 @@ __device__ __forceinline__ WarpArrays warp_arrays(unsigned char* base, int E, in
 
 // Stage 1 for every token. Every expert's logit gets the same, token-wide error bound beta
 // (the largest of the per-expert bounds), so one extraction of the k+1 largest fp32 logits
-// decides: an expert is surely in when l_e - beta > l_(k+1) + beta, surely out when
-// l_e + beta < l_(k) - beta. Tokens with an undecided expert go to the refine list.
+// decides. Tokens with an undecided expert go to the refine list.
 template <typename T>
-__global__ void __launch_bounds__(RT_WARPS * 32)
+__global__ void __launch_bounds__(RT_WARPS * 32, 5)
 router_select_kernel(RouterArgs a) {
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * RT_WARPS + warp;
   if (t >= a.T) return;
-  WarpArrays w = warp_arrays(smem, a.E, warp);
+  float* work = reinterpret_cast<float*>(smem) + (size_t)warp * a.E;   // this warp's logits
   const T* x = static_cast<const T*>(a.x) + t * a.d;
   const float xn = warp_norm_ub(x, a.d, a.gam_d, lane);
   if (lane == 0) a.xnorm[t] = xn;
@@ -519,8 +518,7 @@ router_select_kernel(RouterArgs a) {
     for (int u = 0; u < EU; ++u) {
       const int e = e0 + 32 * u;
       if (e < a.E) {
-        w.lg[e] = l[u];
-        w.work[e] = l[u];
+        work[e] = l[u];
         wmax = fmaxf(wmax, wn[u]);
         amax = fmaxf(amax, fabsf(l[u]));
       }
@@ -534,14 +532,16 @@ router_select_kernel(RouterArgs a) {
   float beta = __fadd_ru(__fmul_ru(__fmul_ru(a.cgam, xn), wmax), __fmul_ru(2.0f * U32, amax));
   beta = __fadd_ru(beta, 1e-30f);
   __syncwarp();
-  // the k-th and (k+1)-th largest fp32 logits (with multiplicity)
-  float lk = -INFINITY, lk1 = -INFINITY;
+  // the k+1 largest fp32 logits (with multiplicity, ties to the lower index), lane j keeping
+  // the j-th of them
+  float lk = -INFINITY, lk1 = -INFINITY, my_v = -INFINITY;
+  int my_i = INT_MAX;
   const int kk = min(a.k + 1, a.E);
   for (int it = 0; it < kk; ++it) {
     float best = -INFINITY;
     int bi = INT_MAX;
     for (int e = lane; e < a.E; e += 32) {
-      const float v = w.work[e];
+      const float v = work[e];
       if (v > best) { best = v; bi = e; }
     }
 #pragma unroll
@@ -550,26 +550,27 @@ router_select_kernel(RouterArgs a) {
       const int oi = __shfl_xor_sync(~0u, bi, o);
       if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
     }
+    if (lane == it && it < a.k) { my_v = best; my_i = bi; }
     if (it == a.k - 1) lk = best;
     if (it == a.k) lk1 = best;
-    if (bi != INT_MAX && (bi & 31) == lane) w.work[bi] = -INFINITY;
+    if (bi != INT_MAX && (bi & 31) == lane) work[bi] = -INFINITY;
     __syncwarp();
   }
-  const float in_thr = __fadd_ru(__fadd_ru(lk1, beta), beta);    // l_e - beta > l_(k+1) + beta
-  const float out_thr = __fsub_rd(__fsub_rd(lk, beta), beta);    // l_e + beta < l_(k) - beta
-  int n_in = 0, n_amb = 0;
-  for (int e = lane; e < a.E; e += 32) {
-    const float l = w.lg[e];
-    uint8_t sl = 2;
-    if (l > in_thr) { sl = 1; ++n_in; }
-    else if (l < out_thr) sl = 0;
-    n_amb += (sl == 2);
-    w.sel[e] = sl;
-  }
-  __syncwarp();
-  n_in = warp_sum_i(n_in);
-  if (n_in == a.k) {
-    warp_write_selection(w.lg, w.sel, a.E, a.k, lane, a.idx + t * a.k, a.gate + t * a.k);
+  // An expert is surely in when l_e - beta > l_(k+1) + beta and surely out when
+  // l_e + beta < l_(k) - beta. Every expert above l_(k+1) is one of the k largest, so the
+  // token is decided exactly when the k-th largest is surely in; its top-k is then the k
+  // logits found above.
+  const float in_thr = __fadd_ru(__fadd_ru(lk1, beta), beta);
+  if (lk > in_thr) {
+    const float m = __shfl_sync(~0u, my_v, 0);            // the largest logit
+    const float ex = lane < a.k ? expf(my_v - m) : 0.0f;
+    const float sum = warp_sum_f(ex);
+    int pos = 0;                                          // rank by expert index
+    for (int j = 0; j < a.k; ++j) pos += (__shfl_sync(~0u, my_i, j) < my_i) ? 1 : 0;
+    if (lane < a.k) {
+      a.idx[t * a.k + pos] = my_i;
+      a.gate[t * a.k + pos] = __fdiv_rn(ex, sum);
+    }
   } else if (lane == 0) {
     int pos = atomicAdd(&a.hdr->n_refine, 1);
     a.refine_list[pos] = (int32_t)t;
@@ -856,7 +857,8 @@ cudaError_t router_prepare(const RouterArgs& a, int dtype, cudaStream_t st, bool
 }
 
 cudaError_t router_select(const RouterArgs& a, int dtype, int num_sms, cudaStream_t st, bool pdl) {
-  size_t sm_sel = warp_smem(a.E) * RT_WARPS;
+  const size_t sm_sel = (size_t)a.E * 4 * RT_WARPS;
+  const size_t sm_ref = warp_smem(a.E) * RT_WARPS;
   size_t sm_exact = warp_smem(a.E) + (size_t)a.E * NB * 8 + (size_t)RT_WARPS * NB * 8 +
                     (size_t)a.E * 12;
   cudaError_t err;
@@ -864,11 +866,11 @@ cudaError_t router_select(const RouterArgs& a, int dtype, int num_sms, cudaStrea
   auto ref = (dtype == DT_BF16) ? router_refine_kernel<bf16> : router_refine_kernel<float>;
   auto ex = (dtype == DT_BF16) ? router_exact_kernel<bf16> : router_exact_kernel<float>;
   cudaFuncSetAttribute(sel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
-  cudaFuncSetAttribute(ref, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
+  cudaFuncSetAttribute(ref, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_ref);
   cudaFuncSetAttribute(ex, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_exact);
   err = launch(sel, dim3((unsigned)cdiv(a.T, RT_WARPS)), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(ref, dim3(num_sms), dim3(RT_WARPS * 32), sm_sel, st, pdl, a);
+  err = launch(ref, dim3(num_sms), dim3(RT_WARPS * 32), sm_ref, st, pdl, a);
   if (err != cudaSuccess) return err;
   return launch(ex, dim3(num_sms), dim3(RT_WARPS * 32), sm_exact, st, pdl, a);
 }
