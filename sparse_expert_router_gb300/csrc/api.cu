@@ -23,7 +23,7 @@ constexpr float TC_BOUND_FACTOR = 2.0f;
 // sums the chunk results in fp32 (error bound c*gamma_256 per chunk plus gamma_nchunks over the
 // chunk sums, instead of c*gamma_d).
 constexpr int ROUTER_KCHUNK = 4;
-// Tokens of the exact stage whose stage-2 state the refine stage hands over (the rest, if ever
+// Tokens of the exact stage whose classification the refine stage hands over (the rest, if ever
 // more, recompute it, one block per token).
 constexpr int ROUTER_SAVED = 64;
 

@@ -577,7 +577,7 @@ router_select_kernel(RouterArgs a) {
   }
 }
 
-// Stage-3 work of the tokens whose stage-2 state the refine stage saved (the first n_saved of
+// Stage-3 work of the tokens whose classification the refine stage saved (the first n_saved of
 // the exact list) is spread over EXACT_PARTS blocks per token: each takes every EXACT_PARTS-th
 // undecided expert and publishes its exact value; the last block to arrive ranks them all.
 constexpr int EXACT_PARTS = 8;
@@ -684,10 +684,10 @@ router_refine_kernel(RouterArgs a) {
   }
 }
 
-// Tokens still undecided after stage 2. Warp 0 re-derives the stage-1 logits and the candidate
-// list: from the stage-2 bounds the refine stage saved for the token (EXACT_PARTS blocks per
-// token, see above) or, past the saved slots, by re-running the compensated dot product of
-// every stage-1 candidate on the block's 8 warps (one block per token). Only experts still
+// Tokens still undecided after stage 2. Warp 0 builds the candidate list: from the
+// classification the refine stage saved for the token (EXACT_PARTS blocks per token, see
+// above) or, past the saved slots, from stage 1 and the compensated dot product of every
+// stage-1 candidate on the block's 8 warps (one block per token). Only experts still
 // undecided then get exact logits, each computed by a whole block; the remaining top-k slots
 // go to the largest exact values, ties to the lower index.
 template <typename T>

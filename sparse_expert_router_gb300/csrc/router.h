@@ -23,9 +23,9 @@ struct RouterArgs {
   int32_t* refine_list;   // [T] workspace
   int32_t* exact_list;    // [T] workspace
   DeviceHeader* hdr;
-  // router_saved_bytes(E, n_saved) of workspace, or NULL: the stage-2 state of the first
-  // n_saved tokens of the exact list (written by the refine stage), which lets the exact stage
-  // skip stage 2 and split stage 3 over several blocks per token
+  // router_saved_bytes(E, n_saved) of workspace, or NULL: the final classification of the
+  // first n_saved tokens of the exact list (written by the refine stage), which lets the exact
+  // stage skip stages 1 and 2 and split stage 3 over several blocks per token
   void* saved;
   int n_saved;
 };
