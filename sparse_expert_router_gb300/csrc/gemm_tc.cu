@@ -441,6 +441,35 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     // v[j] = token c0 + j) to out[row][col0 + feature] through the transpose tile, so that every
     // lane stores whole 16-byte pieces of output rows. kind: 0 fp32, 1 bf16, 2 E4M3 (v already
     // multiplied by its quantization scale).
+    // Writes the transpose tile's 16 token rows x 32 E4M3 codes (byte j * 32 + lane = token j,
+    // feature lane) to out: lane -> (row lane / 2, 16-byte half lane % 2).
+    auto store_e4m3_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
+                               int M) {
+      const int rows_here = min(16, it.nrows - c0);
+      const int row = lane >> 1, part = lane & 1;
+      if (f0 + part * 16 < M && row < rows_here) {
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 32 + part * 16);
+        const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 16;
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + o) = val;
+      }
+    };
+    // Writes the transpose tile's 16 token rows x 32 bf16 values (element j * 32 + lane = token
+    // j, feature lane) to out: lane -> (rows lane / 4 and lane / 4 + 8, 16-byte part lane % 4).
+    auto store_bf16_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
+                               int M) {
+      const int rows_here = min(16, it.nrows - c0);
+      const int part = lane & 3;
+      const bool ok = f0 + part * 8 < M;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = (lane >> 2) + 8 * r;
+        if (ok && row < rows_here) {
+          const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
+          const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 8;
+          *reinterpret_cast<uint4*>(static_cast<bf16*>(out) + o) = val;
+        }
+      }
+    };
     auto store_rows = [&](void* out, int64_t ld, int col0, int kind, const Item& it, int c0,
                           int f0, int M, const float* v) {
       if (kind == 0) {
@@ -462,13 +491,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       __syncwarp();
       const int rows_here = min(16, it.nrows - c0);
       if (FP8 && kind == 2) {
-        // 16 token rows x 32 bytes: lane -> (row lane / 2, 16-byte half lane % 2)
-        const int row = lane >> 1, part = lane & 1;
-        if (f0 + part * 16 < M && row < rows_here) {
-          const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 32 + part * 16);
-          const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 16;
-          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + o) = val;
-        }
+        store_e4m3_tile(out, ld, col0, it, c0, f0, M);
       } else if (kind == 0) {
         const int part = lane & 7;
         const bool ok = f0 + part * 4 < M;
@@ -482,17 +505,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
           }
         }
       } else {
-        const int part = lane & 3;
-        const bool ok = f0 + part * 8 < M;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int row = (lane >> 2) + 8 * r;
-          if (ok && row < rows_here) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
-            const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 8;
-            *reinterpret_cast<uint4*>(static_cast<bf16*>(out) + o) = val;
-          }
-        }
+        store_bf16_tile(out, ld, col0, it, c0, f0, M);
       }
       __syncwarp();
     };
@@ -581,6 +594,114 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       }
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
+      if constexpr (FP8) {
+        if (q.out_fp8 && is_glu(q.epi)) {
+          // E4M3 hidden: the SwiGLU of every chunk of this warp is computed and packed into
+          // registers first, then the accumulators are released, so that the next item's MMAs
+          // run while this warp writes its codes out
+          constexpr int CPW = (BN / 16 + EPI_WARPS / 4 - 1) / (EPI_WARPS / 4);   // chunks per warp
+          const int f0 = it.m0 + quad * 32;
+          const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                     (uint32_t)(buf * BN);
+          const bool fok = f0 + lane < q.M;
+          const float sc1 = sc1s[0], sc3 = sc3s[0];
+          uint32_t pk[CPW][4];
+#pragma unroll
+          for (int i = 0; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+              float v[16], v3[16];
+              tmem_ld16(lane_addr + c0, v);
+              tmem_ld16(lane_addr + acc2 + c0, v3);
+              tmem_wait_ld();
+              const int valid = min(16, it.nrows - c0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float h = swiglu(__fmul_rn(v[j], sc1), __fmul_rn(v3[j], sc3));
+                if (fok && j < valid) amax = fmaxf(amax, fabsf(h));
+                v[j] = __fmul_rn(h, osc);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; j += 4)
+                pk[i][j / 4] = e4m3x2(v[j + 1], v[j]) | (e4m3x2(v[j + 3], v[j + 2]) << 16);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(tmem_empty(buf));
+          uint8_t* stg_b = reinterpret_cast<uint8_t*>(stg);
+#pragma unroll
+          for (int i = 0; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                stg_b[j * 32 + lane] = (uint8_t)((pk[i][j / 4] >> (8 * (j % 4))) & 0xFFu);
+              __syncwarp();
+              store_e4m3_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
+              __syncwarp();
+            }
+          }
+          continue;
+        }
+      }
+      if constexpr (!FP8 && !KC && !BWD) {
+        if (q.epi == EPI_SWIGLU) {
+          // bf16 hidden: as for E4M3 above, the SwiGLU of a warp's first CPR chunks is packed
+          // into registers before the accumulators are released; chunks past those (tiles of
+          // more than 192 tokens) are written out first, in place
+          constexpr int CPW = (BN / 16 + EPI_WARPS / 4 - 1) / (EPI_WARPS / 4);   // chunks per warp
+          constexpr int CPR = CPW < 4 ? CPW : 4;
+          const int f0 = it.m0 + quad * 32;
+          const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                     (uint32_t)(buf * BN);
+          for (int i = CPR; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+              float v[16], v3[16];
+              tmem_ld16(lane_addr + c0, v);
+              tmem_ld16(lane_addr + acc2 + c0, v3);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
+              store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
+            }
+          }
+          uint32_t pk[CPR][8];
+#pragma unroll
+          for (int i = 0; i < CPR; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+              float v[16], v3[16];
+              tmem_ld16(lane_addr + c0, v);
+              tmem_ld16(lane_addr + acc2 + c0, v3);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(swiglu(v[j], v3[j]),
+                                                                swiglu(v[j + 1], v3[j + 1]));
+                pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(tmem_empty(buf));
+#pragma unroll
+          for (int i = 0; i < CPR; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                stg_h[j * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] & 0xFFFFu));
+                stg_h[(j + 1) * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] >> 16));
+              }
+              __syncwarp();
+              store_bf16_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
+              __syncwarp();
+            }
+          }
+          continue;
+        }
+      }
       for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
       const int f0 = it.m0 + sub * BM + quad * 32;       // first feature of this warp
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
