@@ -437,10 +437,6 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
     float* stg_f = reinterpret_cast<float*>(stg);
     bf16* stg_h = reinterpret_cast<bf16*>(stg);
-    // Writes one 16-token x 32-feature chunk of this warp (values final: lane = feature,
-    // v[j] = token c0 + j) to out[row][col0 + feature] through the transpose tile, so that every
-    // lane stores whole 16-byte pieces of output rows. kind: 0 fp32, 1 bf16, 2 E4M3 (v already
-    // multiplied by its quantization scale).
     // Writes the transpose tile's 16 token rows x 32 E4M3 codes (byte j * 32 + lane = token j,
     // feature lane) to out: lane -> (row lane / 2, 16-byte half lane % 2).
     auto store_e4m3_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
@@ -470,29 +466,21 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         }
       }
     };
+    // Writes one 16-token x 32-feature chunk of this warp (values final: lane = feature,
+    // v[j] = token c0 + j) to out[row][col0 + feature] through the transpose tile, so that every
+    // lane stores whole 16-byte pieces of output rows. kind: 0 fp32, 1 bf16.
     auto store_rows = [&](void* out, int64_t ld, int col0, int kind, const Item& it, int c0,
                           int f0, int M, const float* v) {
       if (kind == 0) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = v[j];
-      } else if (FP8 && kind == 2) {
-        // pairs of tokens share one conversion
-        uint8_t* stg_b = reinterpret_cast<uint8_t*>(stg);
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const uint32_t c = e4m3x2(v[j + 1], v[j]);
-          stg_b[j * 32 + lane] = (uint8_t)(c & 0xFFu);
-          stg_b[(j + 1) * 32 + lane] = (uint8_t)(c >> 8);
-        }
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
       }
       __syncwarp();
       const int rows_here = min(16, it.nrows - c0);
-      if (FP8 && kind == 2) {
-        store_e4m3_tile(out, ld, col0, it, c0, f0, M);
-      } else if (kind == 0) {
+      if (kind == 0) {
         const int part = lane & 7;
         const bool ok = f0 + part * 4 < M;
 #pragma unroll
@@ -722,19 +710,6 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         if constexpr (FP8) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) { v[j] = __fmul_rn(v[j], sc1); v3[j] = __fmul_rn(v3[j], sc3); }
-        }
-        if (FP8 && q.out_fp8) {
-          // SwiGLU in fp32, running max of |hidden| over this thread's stored values, then the
-          // quantization multiplier; store_rows rounds to E4M3
-          const int valid = min(16, it.nrows - c0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h = swiglu(v[j], v3[j]);
-            if (fok && j < valid) amax = fmaxf(amax, fabsf(h));
-            v[j] = __fmul_rn(h, osc);
-          }
-          store_rows(q.out, q.ld_out, q.out_col0, 2, it, c0, f0, q.M, v);
-          continue;
         }
         if constexpr (BWD) {
           if (q.epi == EPI_SWIGLU_SAVE) {
