@@ -22,7 +22,7 @@ The layer, as the pages state it:
   * Teardown, section "A sphere for every matrix": expert banks are stacked
     [experts, d_in, d_out].
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   R1 the router reads the block input x (width d);
   R2 routing is the top-k of the EXACT real-valued logits x.W_r + b of the
      stored inputs, ties to the lowest expert index; indices are reported in
