@@ -102,7 +102,10 @@ typedef struct {
   float*       h_amax;    /* [1] or NULL: max |hidden| over the active rows */
 } moe_fp8_t;
 
-/* Limits: 1 <= top_k <= 32, top_k <= n_experts <= 1024, T * top_k < 2^31. */
+/* Limits: 1 <= top_k <= 32, top_k <= n_experts <= 1024, T * top_k < 2^31. The tensor-core
+ * GEMMs (bf16 layers without MOE_FLAG_SIMT, and every fp8-expert layer) also need n_experts,
+ * d_model, d_latent and d_ff of at least 64, and d_ff_shared a multiple of 128 when n_shared > 0;
+ * other sizes return MOE_ERR_UNSUPPORTED before any launch (MOE_FLAG_SIMT runs them). */
 
 typedef struct {
   int64_t  T;            /* tokens */

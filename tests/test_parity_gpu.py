@@ -879,6 +879,17 @@ EDGE = {
     # no shared experts, latent == model width, T one past a 256-row token tile
     "no_shared": (LayerShape("no_shared", T=257, d_model=128, d_latent=128, n_experts=64,
                              top_k=4, d_ff=256, n_shared=0, d_ff_shared=0, dtype="bf16"), 0),
+    # the fp8 expert path at the same edges: one token (most experts empty, one-row groups),
+    # 1024 experts with top-32 (groups of ~9 rows), k = 1 with capacity 1 per expert
+    "t1_fp8": (LayerShape("t1_fp8", T=1, d_model=256, d_latent=128, n_experts=64, top_k=8,
+                          d_ff=128, n_shared=1, d_ff_shared=256, dtype="bf16",
+                          expert_dtype="fp8"), 0),
+    "e1024_k32_fp8": (LayerShape("e1024_k32_fp8", T=300, d_model=256, d_latent=128,
+                                 n_experts=1024, top_k=32, d_ff=128, n_shared=0, d_ff_shared=0,
+                                 dtype="bf16", expert_dtype="fp8"), 0),
+    "k1_cap_fp8": (LayerShape("k1_cap_fp8", T=333, d_model=256, d_latent=128, n_experts=64,
+                              top_k=1, d_ff=128, n_shared=1, d_ff_shared=256, dtype="bf16",
+                              capacity=(1, 21), expert_dtype="fp8"), 0),
 }
 
 
@@ -886,7 +897,7 @@ EDGE = {
 def test_edge_case_forward(name):
     """Every token's routing, dispatch and output against the oracle at the edges the method
     allows: a single token, k = E, k = 1 with capacity 1, 1024 experts with top-32, no shared
-    experts, token counts one past a tile."""
+    experts, token counts one past a tile; the fp8 expert path at three of them."""
     shape, flags = EDGE[name]
     cpu = make_layer_inputs(shape, "cpu")
     inp = {k: v.to(DEV) for k, v in cpu.items()}
