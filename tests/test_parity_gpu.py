@@ -455,6 +455,35 @@ def test_small_fp8_forward():
     assert float(got["h_amax"]) < 448.0 / float(inp["h_scale"][0])
 
 
+def test_bf16_expert_ffn_with_shared_experts():
+    """moe_expert_ffn on a bf16 layer with the shared experts in the same call: one tensor-core
+    launch holds the grouped SwiGLU GEMM and the dense shared one. Both hiddens' SwiGLU
+    epilogues hold their results in registers across the accumulator release; y_perm and the
+    shared hidden against the oracle, rows past the groups untouched."""
+    shape = SHAPES["small_bf16"].with_(T=512)
+    cpu = make_layer_inputs(shape, "cpu")
+    inp = {k: v.to(DEV) for k, v in cpu.items()}
+    cfg = m.LayerConfig.from_shape(shape)
+    T, k, L = shape.T, shape.top_k, shape.d_latent
+    ref = oracle_forward(shape, cpu)
+    R = int(ref["offsets"][-1])
+    tok = ref["perm"] // k
+    xp = torch.zeros((T * k + 64, L), dtype=torch.bfloat16, device=DEV)
+    xp[:R] = ref["h"][tok].to(torch.bfloat16).to(DEV)
+    y_perm = torch.zeros((T * k + 64, L), dtype=torch.bfloat16, device=DEV)
+    a_s = torch.empty((T, shape.n_shared * shape.d_ff_shared), dtype=torch.bfloat16, device=DEV)
+    ws = m.alloc_workspace(cfg, DEV)
+    offs = ref["offsets"].to(torch.int32).to(DEV)
+    m.moe_expert_ffn(cfg, xp, offs, inp["w1"], inp["w3"], inp["w2"], y_perm, inp["x"],
+                     inp["w1_s"], inp["w3_s"], a_s, ws)
+    _, o_ref = moe_oracle.grouped_experts(xp[:R].cpu(), ref["offsets"].tolist(), cpu["w1"],
+                                          cpu["w3"], cpu["w2"])
+    assert normwise(y_perm[:R], o_ref) <= 2e-2
+    assert float(y_perm[R:].float().abs().max()) == 0.0
+    assert normwise(a_s, ref["a_s"]) <= 2e-2
+    assert m.moe_get_device_status(ws)["status"] == 0
+
+
 def test_fp8_split_calls():
     """moe_permute's E4M3 rows and amax against the oracle's quantization; moe_expert_ffn on the
     oracle's codes (with the shared experts in the same call) and its hidden amax."""
