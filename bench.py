@@ -128,10 +128,11 @@ def weight_bytes(shape) -> int:
     return bank + scales + 2 * (d * E + 2 * d * L + 3 * d * SF) + 4 * (E + L)
 
 
-def tc_peak(pk, stage) -> float:
-    """Tensor-core peak (TFLOP/s) of a stage: the measured sustained bf16 rate, doubled for E4M3
-    operands (the nominal dense ratio 4.5 / 2.25 PFLOP/s)."""
-    return pk["bf16_sustained"] * (2.0 if stage.get("tc_peak") == "fp8" else 1.0)
+def tc_peak(pk, stage, which="bf16_burst") -> float:
+    """Tensor-core peak (TFLOP/s) of a stage: the measured bf16 rate (burst by default: the timed
+    loops here last a fraction of a second; "bf16_sustained" for the seconds-long rate under the
+    power cap), doubled for E4M3 operands (the nominal dense ratio 4.5 / 2.25 PFLOP/s)."""
+    return pk[which] * (2.0 if stage.get("tc_peak") == "fp8" else 1.0)
 
 
 class ClockSampler:
@@ -226,7 +227,7 @@ def run_reference(args, shape):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
-        "config": {"workload": shape.name, "T": shape.T, "parallelism": "replicas"},
+        "config": forward_config(shape, args, world),
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": torch.get_num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -309,15 +310,16 @@ def run_expert_backward(args, shape):
     # then read (G, U by dA; A by dW2; dG, dU by dX and by dW1 / dW3: 7x)
     by = 2 * 5 * active * L * F + 2 * 3 * active * L * F + 2 * R * 6 * L + 2 * R * 12 * F
     pk = peaks()
-    if by / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_sustained"] * 1e12):
+    if by / (pk["hbm_gbs"] * 1e9) >= flops / (pk["bf16_burst"] * 1e12):
         ach = by / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (HBM copy)"}
     else:
         ach = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
-                "peak_source": pk["source"] + " (bf16 sustained)"}
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_burst"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_burst"], 4),
+                "sustained_frac": round(ach / pk["bf16_sustained"], 4),
+                "peak_source": pk["source"] + " (bf16 burst)"}
     roof["traffic"] = None
     print(json.dumps({
         "metric": "routed-expert MLP backward tokens/s", "value": round(T / (ms * 1e-3), 1),
@@ -393,9 +395,10 @@ def run_layer_backward(args, shape):
                                f"k={shape.top_k} F={F} shared={S}x{Fs}",
                    "pdl": not args.no_pdl, "l2": "flushed between timed steps (256 MB write)"},
         "tflop_s": round(ach, 1),
-        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
-                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
-                     "traffic": None, "peak_source": pk["source"] + " (bf16 sustained)"},
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_burst"],
+                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_burst"], 4),
+                     "sustained_frac": round(ach / pk["bf16_sustained"], 4),
+                     "traffic": None, "peak_source": pk["source"] + " (bf16 burst)"},
         "clocks": clocks, "device_report": m.moe_get_device_status(bws)}))
 
 
@@ -463,12 +466,29 @@ def run_slice(args):
         "stages": {"expert_ffn": {"ms": round(ffn, 4), "tflop_s": round(ach, 1)},
                    "combine": {"ms": round(comb, 4),
                                "gb_s": round(comb_bytes / (comb * 1e-3) / 1e9, 1)}},
-        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_sustained"],
-                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_sustained"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_burst"],
+                     "unit": "TFLOP/s", "frac": round(ach / pk["bf16_burst"], 4),
+                     "sustained_frac": round(ach / pk["bf16_sustained"], 4),
                      "kernel": "expert_ffn", "traffic": None,
-                     "peak_source": pk["source"] + " (bf16 sustained)"},
+                     "peak_source": pk["source"] + " (bf16 burst)"},
         "gpu_launches": 4 * args.steps, "clocks": clocks,   # offsets check, 2 GEMMs, combine
-        "device_report": m.moe_get_device_status(ws)}))
+        "device_report": m.moe_get_device_status(ws),
+        **({} if args.no_cpu_baseline else {"cpu_baseline": slice_cpu_baseline(inp, 1024)})}))
+
+
+def slice_cpu_baseline(inp_gpu, n_rows):
+    """The oracle's slice on a bounded sample of arrival positions (every expert's rows)."""
+    from oracle import moe_oracle
+    host = {k: v.cpu() for k, v in inp_gpu.items()}
+    n = host["slot_of"].numel()
+    pos = torch.linspace(0, n - 1, n_rows).round().long().tolist()
+    t0 = time.perf_counter()
+    moe_oracle.slice_rows(host, pos)
+    dt = time.perf_counter() - t0
+    return {"value": n_rows / dt, "unit": "rows/s", "cores": torch.get_num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{n_rows} evenly spaced arrival positions of the slice (grouped SwiGLU "
+                      f"expert MLP and gate-weighted un-permute)"}
 
 
 def main():
@@ -480,7 +500,7 @@ def main():
     ap.add_argument("--workload", default="l535b_t8192", choices=sorted(SHAPES))
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -492,6 +512,9 @@ def main():
                     help="replay one captured CUDA graph of moe_forward per timed step")
     ap.add_argument("--slice", action="store_true",
                     help="time the expert-parallel slice workload (grouped expert MLP + un-permute)")
+    ap.add_argument("--all", action="store_true",
+                    help="one line per workload (every layer size, fp8 experts, the slice), each "
+                         "with the oracle timed on the host cores")
     args = ap.parse_args()
     shape = SHAPES[args.workload]
     if args.impl == "reference":
@@ -515,7 +538,43 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
+    if args.all:
+        if world > 1:
+            raise SystemExit("--all runs on one GPU")
+        run_all(args, m, dev)
+        return
+    line = bench_forward(args, shape, m, world, rank, local, dev)
+    if line is not None:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(shape, args.cpu_tokens, line.pop("_inp"))
+        line.pop("_inp", None)
+        print(json.dumps(line), flush=True)
+    else:
+        torch.distributed.destroy_process_group()
+        return
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
+
+def forward_config(shape, args, world):
+    """The `config` object of a forward line (the reference arm prints the same one)."""
+    return {"workload": f"{shape.name}: T={shape.T} d={shape.d_model} "
+                        f"latent={shape.d_latent} E={shape.n_experts} k={shape.top_k} "
+                        f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}"
+                        + (f" capacity={shape.capacity[0]}/{shape.capacity[1]}"
+                           if shape.capacity else "")
+                        + (" zipf" if shape.routing == "zipf" else ""),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "gemm_path": "simt" if args.simt else "tcgen05", "pdl": not args.no_pdl,
+            "launch": "cuda graph replay" if args.graph else "eager",
+            "expert_weights": shape.expert_dtype,
+            "l2": "flushed between timed steps (256 MB write); weights "
+                  f"({weight_bytes(shape) / 1e9:.1f} GB) exceed L2"}
+
+
+def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
+    """Times args.steps forwards of `shape` (after the warm-up) and returns rank 0's JSON line as
+    a dict (None on the other ranks); "_inp" holds the workload's inputs for the CPU baseline."""
     flags = (m.MOE_FLAG_SIMT if args.simt else 0) | (0 if args.no_pdl else m.MOE_FLAG_PDL)
     cfg = m.LayerConfig.from_shape(shape, flags=flags)
     inp = make_layer_inputs(shape.with_(seed=shape.seed), dev)
@@ -581,7 +640,7 @@ def main():
 
     # end to end through the C ABI with host buffers: H2D of x, forward, D2H of y
     e2e = None
-    if not args.no_e2e:
+    if (not args.no_e2e) if e2e_on is None else e2e_on:
         # the serving path: moe_forward_pipelined over host batches, each batch's input copied in
         # and output copied out inside the timed region, overlapped with the other batches'
         # forwards on two copy streams
@@ -608,8 +667,7 @@ def main():
                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()}
 
     if rank != 0:
-        torch.distributed.destroy_process_group()
-        return
+        return None
 
     pk = peaks()
     alg = algorithmic(shape, counts.cpu().tolist())
@@ -622,9 +680,10 @@ def main():
             st["gb_s"] = round(by / (ms * 1e-3) / 1e9, 1)
             st["hbm_frac"] = round(st["gb_s"] / pk["hbm_gbs"], 3)
             if f:
-                tp = tc_peak(pk, alg[s])
+                tp, tps = tc_peak(pk, alg[s]), tc_peak(pk, alg[s], "bf16_sustained")
                 st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 1)
                 st[alg[s].get("tc_peak", "bf16") + "_frac"] = round(st["tflop_s"] / tp, 3)
+                st[alg[s].get("tc_peak", "bf16") + "_sustained_frac"] = round(st["tflop_s"] / tps, 3)
         stages[s] = st
     dom = max((s for s in STAGES if s in alg), key=lambda s: stage_ms[s])
     f, by = alg[dom]["flops"], alg[dom]["bytes"]
@@ -638,28 +697,21 @@ def main():
     else:
         ach = f / (ms_dom * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(tp, 1),
-                "unit": "TFLOP/s", "frac": round(ach / tp, 4)}
+                "unit": "TFLOP/s", "frac": round(ach / tp, 4),
+                "sustained_frac": round(ach / tc_peak(pk, alg[dom], "bf16_sustained"), 4)}
     roof.update({"kernel": dom, "traffic": profiled_traffic(shape.name, dom),
                  "peak_source": pk["source"]
-                 + ((" (bf16 sustained" + (" x 2, the nominal E4M3/bf16 ratio)"
-                                           if alg[dom].get("tc_peak") == "fp8" else ")"))
+                 + ((" (bf16 burst" + (" x 2, the nominal E4M3/bf16 ratio)"
+                                       if alg[dom].get("tc_peak") == "fp8" else ")"))
                     if roof["bound"] == "tensor" else " (HBM copy)")})
-    line = {
+    return {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.expert_dtype == "bf16" else "bf16; expert MLP e4m3 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, near-uniform "
                 "routing unless the workload is Zipf-skewed)",
-        "config": {"workload": f"{shape.name}: T={shape.T} d={shape.d_model} "
-                               f"latent={shape.d_latent} E={shape.n_experts} k={shape.top_k} "
-                               f"F={shape.d_ff} shared={shape.n_shared}x{shape.d_ff_shared}",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "gemm_path": "simt" if args.simt else "tcgen05", "pdl": not args.no_pdl,
-                   "launch": "cuda graph replay" if args.graph else "eager",
-                   "expert_weights": shape.expert_dtype,
-                   "l2": "flushed between timed steps (256 MB write); weights "
-                         f"({weight_bytes(shape) / 1e9:.1f} GB) exceed L2"},
+        "config": forward_config(shape, args, world),
         "layer_tflop_s": round(sum(shape.flops().values()) / (ms_step * 1e-3) / 1e12, 1),
         "stages": stages,
         "roofline": roof,
@@ -668,12 +720,38 @@ def main():
         "clocks": clk,
         "wall_s": round(wall, 3),
         "device_report": rep,
+        "_inp": inp,
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shape, args.cpu_tokens, inp)
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+
+
+# Every workload of the layer, one JSON line each in --all mode, with the number of tokens of
+# the oracle's bounded CPU sample (all threads) and, for the two smallest layers, of a second
+# sample timed on one thread.
+ALL_WORKLOADS = [("tiny_f32", 256, 256), ("small_bf16", 256, 32), ("l535b_t8192", 256, 0),
+                 ("l535b_t8192_fp8", 256, 0), ("l535b_zipf_t16384", 256, 0),
+                 ("l535b_zipf_t16384_cf110", 256, 0), ("l535b_t65536", 256, 0)]
+
+
+def run_all(args, m, dev):
+    """One line per workload (the layer at every size, the fp8 expert MLP, the expert-parallel
+    slice), each with the oracle timed on the host cores beside it."""
+    for name, n_cpu, n_single in ALL_WORKLOADS:
+        shape = SHAPES[name]
+        line = bench_forward(args, shape, m, 1, 0, 0, dev, e2e_on=False)
+        inp = line.pop("_inp")
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(shape, min(n_cpu, shape.T), inp)
+            if n_single:
+                nt = torch.get_num_threads()
+                torch.set_num_threads(1)
+                try:
+                    line["cpu_baseline_single_core"] = cpu_baseline(shape, n_single, inp)
+                finally:
+                    torch.set_num_threads(nt)
+        print(json.dumps(line), flush=True)
+        del inp, line
+        torch.cuda.empty_cache()
+    run_slice(args)
 
 
 if __name__ == "__main__":

@@ -196,6 +196,21 @@ MOE_API int32_t moe_last_cuda_error(const char** name);
  * The workspace must be 256-byte aligned device memory owned by the caller. */
 MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
+/* Byte offsets, from the start of the workspace, of the intermediates that moe_forward leaves
+ * there after its call (stream-ordered): the fp32 latent z [T, L] before the RMSNorm, the
+ * expert-grouped rows x_perm [pool_rows, L] (bf16, fp32 for an fp32 layer, or E4M3 codes with
+ * MOE_FLAG_FP8_EXPERTS), the routed SwiGLU hidden [pool_rows, F] (same type), the routed experts'
+ * outputs y_perm [pool_rows, L], the shared experts' hidden a_shared [T, S*F_s], the combine
+ * c [T, L] (16-bit or fp32 like the layer), perm [pool_rows] int32 and the group offsets
+ * [E + 1] int32. Rows of x_perm, hidden and y_perm at or past expert_offsets[E] are padding that
+ * no kernel writes. For inspection and testing; the regions are overwritten by the next call that
+ * uses the workspace. Returns MOE_ERR_INVALID_ARG for a NULL argument and the configuration
+ * errors of moe_workspace_size. */
+typedef struct {
+  size_t z, x_perm, hidden, y_perm, a_shared, combined, perm, expert_offsets;
+} moe_workspace_regions_t;
+MOE_API moe_status_t moe_workspace_regions(const moe_config_t* cfg, moe_workspace_regions_t* out);
+
 /* Router: logits = x W_r + b_r, then per token the top_k experts by the exact real value of
  * the logit (ties to the lowest index), written in ascending expert order to topk_idx [T, k],
  * and gates topk_gate [T, k] = softmax over the selected logits. The router weight and bias
@@ -354,8 +369,12 @@ MOE_API moe_status_t moe_selftest_device_timeout(void* ws, size_t ws_bytes, uint
  *     64*(E*161 + 8) bytes of exact-stage state, each region rounded up to 256 B) must fit in
  *     32 MiB, else MOE_ERR_WORKSPACE and nothing is enqueued; the 535B-shaped router
  *     (T = 8192, E = 384, d = 6144, bf16) needs 21.4 MB.
- *   - Set-up: the first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *   - Set-up: every call looks up the array's device address in the current device's context.
+ *     The array's memory is committed when the library's device code is first loaded on a
+ *     device (with lazy module loading, the default, that is the first call into the library on
+ *     that device), and that load can synchronise the device. Callers that cannot accept this
+ *     mid-run make one library call on each device during their set-up, before any stream
+ *     capture, e.g. one moe_route_noalloc on a small input.
  *   - Sharing: every call on a device uses the same array and leaves its contents behind; each
  *     call clears what must start at zero. Calls whose GPU work overlaps (other streams, other
  *     host threads) race on the array: serialise them.

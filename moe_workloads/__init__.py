@@ -43,8 +43,8 @@ __all__ = [
 # itself, the plain reading of "router logits biased by a Zipf(s=1.1) expert
 # popularity". At seed 0 and T=16384 on the 535B-shaped layer the hottest
 # expert then gets 46x the mean load (the top-8 ceiling is 48x) and 162 of 384
-# experts get no token; ``python -m moe_workloads.zipf_load`` prints the load
-# statistics for other scales.
+# experts get no token. Smaller scales that bring the hottest expert near 20x
+# the mean leave no expert empty.
 ZIPF_BETA = 1.0
 
 

@@ -263,16 +263,6 @@ def swiglu_hidden(h: torch.Tensor, w1: torch.Tensor, w3: torch.Tensor) -> torch.
     return silu(h @ w1) * (h @ w3)
 
 
-def shared_experts(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor,
-                   w2_s: torch.Tensor) -> torch.Tensor:
-    """Sum over the S shared experts of SwiGLU_s(x); they read x, not the latent (R7)."""
-    x64 = to64(x)
-    out = torch.zeros((x64.shape[0], to64(w2_s[0]).shape[1]), dtype=F64)
-    for s in range(w1_s.shape[0]):
-        out += swiglu_mlp(x64, to64(w1_s[s]), to64(w3_s[s]), to64(w2_s[s]))
-    return out
-
-
 def shared_hidden(x: torch.Tensor, w1_s: torch.Tensor, w3_s: torch.Tensor) -> torch.Tensor:
     """Shared experts' hidden activations, concatenated along the feature axis [T, S*F_s]."""
     x64 = to64(x)

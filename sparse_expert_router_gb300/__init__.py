@@ -114,6 +114,24 @@ def workspace_size(cfg: LayerConfig) -> int:
     return n.value
 
 
+def workspace_regions(cfg: LayerConfig) -> Dict[str, int]:
+    """Byte offsets in the workspace of the intermediates moe_forward leaves there."""
+    r = _lib.moe_workspace_regions_t()
+    _check("moe_workspace_regions", load().moe_workspace_regions(C.byref(cfg.c()), C.byref(r)))
+    return {n: int(getattr(r, n)) for n in _lib.REGION_NAMES}
+
+
+def workspace_view(ws: torch.Tensor, cfg: LayerConfig, name: str, dtype: torch.dtype,
+                   shape) -> torch.Tensor:
+    """A tensor view of one region of the workspace (see workspace_regions)."""
+    off = workspace_regions(cfg)[name]
+    n = 1
+    for s in shape:
+        n *= int(s)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype).view(*shape)
+
+
 def alloc_workspace(cfg: LayerConfig, device="cuda") -> torch.Tensor:
     """A caller-owned, zero-filled workspace of the right size (torch's allocator aligns it to
     256 bytes); zero fill clears the device report it starts with."""

@@ -62,6 +62,14 @@ class moe_forward_aux_t(C.Structure):
                                           "stage_events", "token_mask")]
 
 
+REGION_NAMES = ("z", "x_perm", "hidden", "y_perm", "a_shared", "combined", "perm",
+                "expert_offsets")
+
+
+class moe_workspace_regions_t(C.Structure):
+    _fields_ = [(n, C.c_size_t) for n in REGION_NAMES]
+
+
 class moe_device_report_t(C.Structure):
     _fields_ = [("status", C.c_int32), ("detail", C.c_int32), ("n_refined", C.c_int32),
                 ("n_exact", C.c_int32)]
@@ -76,6 +84,7 @@ SIGNATURES = {
     "moe_status_string": (C.c_char_p, [C.c_int]),
     "moe_last_cuda_error": (C.c_int32, [C.POINTER(C.c_char_p)]),
     "moe_workspace_size": (C.c_int, [CFG, C.POINTER(C.c_size_t)]),
+    "moe_workspace_regions": (C.c_int, [CFG, C.POINTER(moe_workspace_regions_t)]),
     "moe_route": (C.c_int, [CFG, P, P, P, P, P, P, C.c_size_t, P]),
     "moe_permute": (C.c_int, [CFG, P, P, P, P, P, P, P, P, P, P, P, C.POINTER(moe_fp8_t), P,
                               C.c_size_t, P]),

@@ -456,21 +456,13 @@ void record(const moe_forward_aux_t* aux, int i, cudaStream_t st) {
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)32 << 20;
 static __device__ __align__(256) unsigned char g_route_scratch[NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_route_scratch for the current device (looked up once per device: in host
-// code the array's name is only a host-side stand-in). NULL if the lookup failed.
-void* noalloc_scratch_address() {
-  constexpr int kMaxDev = 64;
-  static void* addr[kMaxDev] = {nullptr};
-  static bool looked_up[kMaxDev] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  if (!looked_up[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-    looked_up[dev] = true;
-  }
-  return addr[dev];
+// Device address of g_route_scratch in the current device's context (in host code the array's
+// name is only a host-side stand-in). Looked up on every call: the lookup allocates nothing, is
+// safe from several host threads at once, and stays right after a context is torn down and
+// re-created. On failure returns the CUDA error and leaves *addr NULL.
+cudaError_t noalloc_scratch_address(void** addr) {
+  *addr = nullptr;
+  return cudaGetSymbolAddress(addr, g_route_scratch);
 }
 
 // Layout of the routing scratch inside the fixed array (the same regions moe_route uses).
@@ -537,6 +529,22 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
   if (s != MOE_OK) return s;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_regions(const moe_config_t* cfg, moe_workspace_regions_t* out) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*cfg);
+  out->z = L.z;
+  out->x_perm = L.x_perm;
+  out->hidden = L.hid;
+  out->y_perm = L.y_perm;
+  out->a_shared = L.a_s;
+  out->combined = L.c;
+  out->perm = L.perm;
+  out->expert_offsets = L.offsets;
   return MOE_OK;
 }
 
@@ -1201,8 +1209,9 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x, const voi
     return s;
   const NoallocLayout NL = noalloc_layout(*cfg);
   if (NL.total > NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
-  unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch_address());
-  if (!scratch) return MOE_ERR_CUDA;
+  void* scratch_addr = nullptr;
+  MOE_TRY_CUDA(noalloc_scratch_address(&scratch_addr));
+  unsigned char* scratch = static_cast<unsigned char*>(scratch_addr);
   // The routing stages index the workspace through a Layout; point the regions they use into
   // the fixed array (the other regions are not touched by routing).
   Call k = make_call(cfg, scratch, stream);

@@ -201,3 +201,23 @@ def test_layer_backward_argument_errors(lib):
     assert lib.moe_backward(C.byref(odd.c()), *ok_args) == L.MOE_ERR_UNSUPPORTED
     f32 = _cfg(d_model=256, d_latent=128, d_ff=128, n_experts=64)
     assert lib.moe_backward(C.byref(f32.c()), *ok_args) == L.MOE_ERR_UNSUPPORTED
+
+
+def test_workspace_regions(lib):
+    """The intermediates' offsets lie inside the workspace, 256-byte aligned, each region large
+    enough for its tensor and none overlapping the next."""
+    import sparse_expert_router_gb300 as m
+    from sparse_expert_router_gb300 import _lib as L
+    cfg = _cfg(dtype="bf16", T=300, pool_rows=0)
+    r = m.workspace_regions(cfg)
+    total = _ws(lib, cfg)
+    T, Lt, F, k, E = 300, 128, 128, 2, 16
+    sizes = {"z": T * Lt * 4, "x_perm": T * k * Lt * 2, "hidden": T * k * F * 2,
+             "y_perm": T * k * Lt * 2, "a_shared": T * 256 * 2, "combined": T * Lt * 2,
+             "perm": T * k * 4, "expert_offsets": (E + 1) * 4}
+    spans = sorted((r[n], r[n] + sizes[n], n) for n in sizes)
+    for (lo, hi, n), nxt in zip(spans, spans[1:] + [(total, total, "end")]):
+        assert lo % 256 == 0 and hi <= nxt[0], (n, lo, hi, nxt)
+    assert lib.moe_workspace_regions(C.byref(cfg.c()), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_regions(None, C.byref(L.moe_workspace_regions_t())) == \
+        L.MOE_ERR_INVALID_ARG

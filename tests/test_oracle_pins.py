@@ -237,23 +237,49 @@ def pin_combine_drop_not_renormalised():
     assert c.tolist() == [[0.25, 0.5], [5.5, 11.0]]
 
 
-def pin_slice_rowwise():
-    """The grouped slice equals a per-row loop that looks up each row's expert."""
-    g = torch.Generator().manual_seed(9)
+def _tiny_slice(seed=9):
+    g = torch.Generator().manual_seed(seed)
     E, L, F, P = 3, 6, 5, 14
     offs = [0, 4, 4, 10]                      # an empty expert; rows 10..13 are padding
     inp = {"pool": torch.randn(P, L, generator=g), "expert_offsets": torch.tensor(offs),
            "w1": torch.randn(E, L, F, generator=g), "w3": torch.randn(E, L, F, generator=g),
            "w2": torch.randn(E, F, L, generator=g),
            "gate": torch.rand(10, generator=g), "slot_of": torch.randperm(10, generator=g)}
+    inp["pool"][10:] = float("nan")           # padding must never be read
+    return inp, offs
+
+
+def _slice_row_by_hand(inp, offs, i):
+    """Arrival position i by hand: its pool row, that row's expert (the group whose half-open
+    range holds it), SwiGLU, gate."""
+    r = int(inp["slot_of"][i])
+    e = [ee for ee in range(len(offs) - 1) if offs[ee] <= r < offs[ee + 1]]
+    assert len(e) == 1
+    v = inp["pool"][r].double()
+    W1, W3, W2 = (inp[n][e[0]].double() for n in ("w1", "w3", "w2"))
+    return float(inp["gate"][i]) * ((Fn.silu(v @ W1) * (v @ W3)) @ W2)
+
+
+def pin_slice_rowwise():
+    """The grouped slice, whole (slice_forward) and for chosen positions (slice_rows), equals a
+    per-row loop that looks up each row's expert; rows at group boundaries (pool rows 0, 3, 4
+    and 9, next to the empty expert) are among the positions."""
+    inp, offs = _tiny_slice()
     out = O.slice_forward(inp)["out"]
+    assert not bool(torch.isnan(out).any())
+    # the positions whose pool rows sit at group boundaries, in no particular order
+    pos = [int((inp["slot_of"] == r).nonzero()) for r in (4, 0, 9, 3, 6)]
+    part = O.slice_rows(inp, pos)
+    assert part["rows"].tolist() == [4, 0, 9, 3, 6]
     for i in range(10):
-        r = int(inp["slot_of"][i])
-        e = max(ee for ee in range(E) if offs[ee] <= r < offs[ee + 1])
-        v = inp["pool"][r].double()
-        hid = Fn.silu(v @ inp["w1"][e].double()) * (v @ inp["w3"][e].double())
-        ref = float(inp["gate"][i]) * (hid @ inp["w2"][e].double())
+        ref = _slice_row_by_hand(inp, offs, i)
         assert torch.allclose(out[i], ref, atol=1e-12, rtol=0)
+    for n, i in enumerate(pos):
+        ref = _slice_row_by_hand(inp, offs, i)
+        assert torch.allclose(part["out"][n], ref, atol=1e-12, rtol=0), (i, n)
+        r = int(inp["slot_of"][i])
+        assert torch.allclose(part["y_perm"][n] * float(inp["gate"][i]), ref, atol=1e-12, rtol=0)
+        assert torch.equal(part["y_perm"][n], O.slice_forward(inp)["y_perm"][r])
 
 
 def pin_forward_drop_skips_expert():
@@ -734,6 +760,35 @@ def _mut_unstable_perm(monkeypatch):
     monkeypatch.setattr(O, "dispatch", bad)
 
 
+def _mut_slice_rows_boundary(monkeypatch):
+    """slice_rows assigns a pool row to the first group whose end is >= the row (an off-by-one
+    at a group boundary)."""
+    def bad(inp, positions):
+        offs = [int(v) for v in inp["expert_offsets"].tolist()]
+        pos = [int(p) for p in positions]
+        rows = [int(inp["slot_of"][p]) for p in pos]
+        o = torch.zeros((len(pos), inp["w2"].shape[2]), dtype=F64)
+        for n, r in enumerate(rows):
+            e = min(g for g in range(len(offs) - 1) if offs[g + 1] >= r)
+            v = O.to64(inp["pool"][[r]])
+            o[n] = O.swiglu_mlp(v, O.expert_weight(inp, "w1", e), O.expert_weight(inp, "w3", e),
+                                O.expert_weight(inp, "w2", e))[0]
+        g = O.to64(inp["gate"][pos]).unsqueeze(1)
+        return {"rows": torch.tensor(rows), "y_perm": o, "out": g * o}
+    monkeypatch.setattr(O, "slice_rows", bad)
+
+
+def _mut_slice_rows_gate_by_row(monkeypatch):
+    """slice_rows weights by the gate of the pool row instead of the arrival position."""
+    orig = O.slice_rows
+
+    def bad(inp, positions):
+        res = orig(inp, positions)
+        g_row = O.to64(inp["gate"][res["rows"].clamp(max=inp["gate"].numel() - 1)]).unsqueeze(1)
+        return {**res, "out": g_row * res["y_perm"]}
+    monkeypatch.setattr(O, "slice_rows", bad)
+
+
 def _mut_transposed_up(monkeypatch):
     orig = O.forward
 
@@ -752,7 +807,7 @@ MUTATIONS = [_mut_silu_no_sigmoid, _mut_tie_high_index, _mut_float_capacity, _mu
              _mut_silu_grad_no_inner, _mut_backward_dw2_from_g, _mut_backward_dx_no_w3,
              _mut_router_grad_full_softmax, _mut_rmsnorm_grad_no_projection,
              _mut_unstable_perm,
-             _mut_transposed_up]
+             _mut_transposed_up, _mut_slice_rows_boundary, _mut_slice_rows_gate_by_row]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__[5:] for m in MUTATIONS])

@@ -16,8 +16,12 @@ from gpu_cases import (DEV, check_routing, e4m3_codes_match, gpu_inputs, near_ti
 
 pytestmark = pytest.mark.gpu
 
-# the bf16 GEMM paths under test: tensor cores (default) and the CUDA-core cross-check
-BF16_PATHS = {"tc": 0, "simt": m.MOE_FLAG_SIMT}
+# the bf16 GEMM paths under test: tensor cores (default), tensor cores with programmatic
+# dependent launch (the bench configuration) and the CUDA-core cross-check
+BF16_PATHS = {"tc": 0, "tc_pdl": m.MOE_FLAG_PDL, "simt": m.MOE_FLAG_SIMT}
+# The bench configuration runs with programmatic dependent launch on (MOE_FLAG_PDL); the
+# full-size and edge-case forwards run both with and without it.
+PDL_FLAGS = {"nopdl": 0, "pdl": m.MOE_FLAG_PDL}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,11 +34,12 @@ def _built():
 
 # ------------------------------------------------------------------ full layer, small ----
 
+@pytest.mark.parametrize("flags", [0, m.MOE_FLAG_PDL], ids=["nopdl", "pdl"])
 @pytest.mark.parametrize("cap", [None, (11, 10), (1, 2)], ids=["nocap", "cf110", "cf050"])
-def test_tiny_f32_forward(cap):
+def test_tiny_f32_forward(cap, flags):
     shape = SHAPES["tiny_f32"].with_(capacity=cap)
     inp = gpu_inputs(shape)
-    got = run_forward(shape, inp)
+    got = run_forward(shape, inp, flags)
     ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()})
     check_routing(got, ref, shape)
     if cap == (1, 2):
@@ -284,31 +289,135 @@ LARGE = ["l535b_t8192", "l535b_zipf_t16384", "l535b_zipf_t16384_cf110", "l535b_t
          "l535b_t8192_fp8"]
 
 
+def _chosen_experts(offs):
+    """The three experts with the most grouped rows, the one with the fewest (non-empty) and the
+    one in the middle of the non-empty experts ordered by rows."""
+    rows = offs[1:] - offs[:-1]
+    nz = (rows > 0).nonzero().flatten()
+    order = nz[rows[nz].argsort(stable=True)]
+    picks = [int(order[-1]), int(order[-2]), int(order[-3]), int(order[0]),
+             int(order[len(order) // 2])]
+    return list(dict.fromkeys(picks))
+
+
+def _check_expert_rows(shape, inp, cfg, ws, offs, name):
+    """Every grouped row of the chosen experts, read from the forward's workspace: the rows the
+    gather wrote (x_perm) against the oracle's normalised latent of their tokens, the SwiGLU
+    hidden and the expert outputs (y_perm) against the oracle's expert MLP on those same rows.
+    Per-expert and per-row normwise bounds."""
+    P, L, F, k = shape.T * shape.top_k, shape.d_latent, shape.d_ff, shape.top_k
+    fp8 = shape.expert_dtype == "fp8"
+    xdt = torch.uint8 if fp8 else torch.bfloat16
+    xp = m.workspace_view(ws, cfg, "x_perm", xdt, (P, L))
+    hid = m.workspace_view(ws, cfg, "hidden", xdt, (P, F))
+    yp = m.workspace_view(ws, cfg, "y_perm", torch.bfloat16, (P, L))
+    perm = m.workspace_view(ws, cfg, "perm", torch.int32, (P,))
+    scales = {n: inp[n] for n in ("w1_scale", "w3_scale", "w2_scale", "x_scale", "h_scale")} \
+        if fp8 else None
+    checked = 0
+    for e in _chosen_experts(offs):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        tok = (perm[lo:hi].long() // k).cpu()
+        if fp8:
+            rows = xp[lo:hi].view(torch.float8_e4m3fn).to(torch.float64).cpu()
+        else:
+            rows = xp[lo:hi]
+            _, h = moe_oracle.latent(inp["x"][tok.to(DEV)], inp["w_down"], inp["rms_gamma"],
+                                     shape.rms_eps)
+            r64 = rows.double().cpu()
+            err_h = (r64 - h).norm(dim=1) / h.norm(dim=1).clamp_min(1e-300)
+            assert float(err_h.max()) <= 4e-3, (name, e, "x_perm", float(err_h.max()))
+        a, o = moe_oracle.grouped_experts(
+            rows, [0, hi - lo], inp["w1"][e:e + 1], inp["w3"][e:e + 1], inp["w2"][e:e + 1],
+            fp8={**scales, **{n: scales[n][e:e + 1] for n in ("w1_scale", "w3_scale", "w2_scale")}}
+            if fp8 else None)
+        got = yp[lo:hi].double().cpu()
+        assert normwise(got, o) <= 2e-2, (name, e, hi - lo)
+        per_row = ((got - o).norm(dim=1) / o.norm(dim=1).clamp_min(1e-300))
+        assert float(per_row.max()) <= 2e-2, (name, e, hi - lo, float(per_row.max()))
+        if not fp8:
+            assert normwise(hid[lo:hi], a) <= 2e-2, (name, e, "hidden")
+        checked += hi - lo
+    return checked
+
+
 @pytest.mark.parametrize("name", LARGE)
 def test_large_layer(name):
-    """Full routing and dispatch checked bit-exactly on every token; outputs on a seeded
-    sample of tokens (each token's output depends only on its own row and routing), with the
-    hottest expert's first tokens and dropped tokens added to the sample."""
+    """Full routing and dispatch checked bit-exactly on every token, with and without PDL, and the
+    two outputs bitwise equal. Outputs of 256 seeded tokens plus the hottest expert's first tokens
+    and dropped tokens against the oracle (each token's output depends only on its own row and
+    routing), normwise over the sample and per token. Every grouped row of five experts (the
+    three hottest, the smallest and a middle one) read from the PDL forward's workspace: gathered
+    rows, hidden and expert outputs against the oracle."""
     shape = SHAPES[name]
     inp = gpu_inputs(shape)
-    got = run_forward(shape, inp, BF16_PATHS["tc"])
+    runs = {f: run_forward(shape, inp, PDL_FLAGS[f]) for f in PDL_FLAGS}
+    got = runs["pdl"]
+    assert torch.equal(runs["pdl"]["y"].view(torch.int16), runs["nopdl"]["y"].view(torch.int16))
     counts = got["expert_counts"].cpu()
     hot = int(counts.argmax())
     hot_tokens = (got["topk_idx"].cpu() == hot).any(1).nonzero().flatten()[:4].tolist()
     dropped = (got["slot_of"].cpu() < 0).any(1).nonzero().flatten()[:4].tolist()
-    toks = sample_tokens(shape.T, 12, extra=hot_tokens + dropped)
+    toks = sample_tokens(shape.T, 256, extra=hot_tokens + dropped)
     ref = oracle_forward(shape, inp, tokens=toks)
-    check_routing(got, ref, shape)
+    for f in PDL_FLAGS:
+        check_routing(runs[f], ref, shape)
+        assert runs[f]["report"]["status"] == 0
     if shape.routing == "zipf":
         assert int((counts == 0).sum()) > 0                      # experts with no rows
         assert float(counts.max()) > 20 * shape.T * shape.top_k / shape.n_experts
     if shape.capacity:
         assert int(ref["n_dropped"]) > 0
-    err = normwise(got["y"][toks], ref["y"])
-    assert err <= 2e-2, err
-    assert got["report"]["status"] == 0
-    del inp, got
+    ys = got["y"][toks].double().cpu()
+    assert normwise(ys, ref["y"]) <= 2e-2
+    per_tok = (ys - ref["y"]).norm(dim=1) / ref["y"].norm(dim=1).clamp_min(1e-300)
+    assert float(per_tok.max()) <= 2e-2, float(per_tok.max())
+    cfg = m.LayerConfig.from_shape(shape, flags=PDL_FLAGS["pdl"])
+    n_rows = _check_expert_rows(shape, inp, cfg, got["ws"], got["expert_offsets"].cpu(), name)
+    assert n_rows > 0
+    del inp, got, runs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("path", ["tc", "tc_pdl", "f32"])
+def test_swiglu_epilogue_wide_range(path):
+    """The grouped GEMM's SwiGLU epilogue on its own, over gate pre-activations u1 in [-30, 30] and
+    up pre-activations u3 in [-4, 4]: one-hot rows (row r is e_{r mod L}) make u1 = W1[r mod L, f]
+    and u3 = W3[r mod L, f] exactly, so the stored hidden silu(u1) * u3 is compared element by
+    element with the oracle's fp64 value. Bar: the rounding to the stored type (bf16: 2^-9
+    relative) plus 2e-5 relative for the epilogue's own arithmetic; fp32 layer: 2e-6 relative."""
+    R, L, F, E = 300, 128, 256, 64
+    dt = torch.float32 if path == "f32" else torch.bfloat16
+    cfg = m.LayerConfig(T=R, d_model=L, d_latent=L, n_experts=E, top_k=1, d_ff=F, n_shared=0,
+                        d_ff_shared=0, dtype="f32" if path == "f32" else "bf16", pool_rows=320,
+                        flags=BF16_PATHS.get(path, 0))
+    g = torch.Generator().manual_seed(17)
+    w1 = torch.zeros((E, L, F), dtype=dt)
+    w3 = torch.zeros((E, L, F), dtype=dt)
+    w1[0] = torch.linspace(-30.0, 30.0, L * F)[torch.randperm(L * F, generator=g)].view(L, F)
+    w3[0] = torch.linspace(-4.0, 4.0, L * F)[torch.randperm(L * F, generator=g)].view(L, F)
+    w2 = (torch.randn((E, F, L), generator=g) * F ** -0.5).to(dt)
+    rows = torch.zeros((320, L), dtype=dt)
+    rows[torch.arange(R), torch.arange(R) % L] = 1.0
+    rows[R:] = float("nan")                                   # padding is never read
+    offs = torch.tensor([0] + [R] * E, dtype=torch.int32)     # every row in expert 0
+    ws = m.alloc_workspace(cfg, DEV)
+    y_perm = torch.zeros((320, L), dtype=dt, device=DEV)
+    m.moe_expert_ffn(cfg, rows.to(DEV), offs.to(DEV), w1.to(DEV), w3.to(DEV), w2.to(DEV), y_perm,
+                     ws=ws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(ws)["status"] == 0
+    hid = m.workspace_view(ws, cfg, "hidden", dt, (320, F))[:R].double().cpu()
+    ref = moe_oracle.swiglu_hidden(rows[:R].double(), w1[0].double(), w3[0].double())
+    u1 = w1[0].double()[torch.arange(R) % L]
+    assert float(u1.min()) <= -29.9 and float(u1.max()) >= 29.9
+    rel = 2e-6 if path == "f32" else 2.0 ** -9 + 2e-5
+    err = (hid - ref).abs() - rel * ref.abs()
+    worst = int(err.flatten().argmax())
+    assert float(err.max()) <= 1e-30, (path, float(hid.flatten()[worst]), float(ref.flatten()[worst]),
+                                       float(u1.flatten()[worst]))
+    _, o = moe_oracle.grouped_experts(rows[:R], [0, R], w1[:1], w3[:1], w2[:1])
+    assert normwise(y_perm[:R], o) <= (1e-5 if path == "f32" else 2e-2)
 
 
 def test_expert_slice():
@@ -922,15 +1031,16 @@ EDGE = {
 }
 
 
+@pytest.mark.parametrize("pdl", list(PDL_FLAGS))
 @pytest.mark.parametrize("name", list(EDGE))
-def test_edge_case_forward(name):
+def test_edge_case_forward(name, pdl):
     """Every token's routing, dispatch and output against the oracle at the edges the method
     allows: a single token, k = E, k = 1 with capacity 1, 1024 experts with top-32, no shared
     experts, token counts one past a tile; the fp8 expert path at three of them."""
     shape, flags = EDGE[name]
     cpu = make_layer_inputs(shape, "cpu")
     inp = {k: v.to(DEV) for k, v in cpu.items()}
-    got = run_forward(shape, inp, flags)
+    got = run_forward(shape, inp, flags | PDL_FLAGS[pdl])
     ref = oracle_forward(shape, cpu)
     check_routing(got, ref, shape)
     if shape.capacity:
