@@ -47,31 +47,35 @@ def peaks():
                 "source": "fallback"}
 
 
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "tc_gemm_grouped_l535b_e64_t1368.md")
-
-
-# the sources the grouped GEMM kernel is compiled from: a change to any of them voids the counters
-PROFILED_SOURCES = ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "gemm.h")
+# ncu summaries with per-launch DRAM traffic, each with the sources its kernels are compiled from:
+# a change to any of them voids that summary's counters
+PROFILE_SUMMARIES = (
+    (os.path.join(ROOT, "profiles", "tc_gemm_grouped_l535b_e64_t1368.md"),
+     ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "gemm.h")),
+    (os.path.join(ROOT, "profiles", "memory_kernels_l535b_f128_t8192.md"),
+     ("dispatch.cu", "router.cu", "common.cuh")),
+)
 
 
 def profiled_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, or None
-    when there is none or a source of the GEMM changed since the counters were taken."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summaries, or None
+    when there is none or a source of the kernel changed since the counters were taken."""
     import hashlib
-    try:
-        text = open(PROFILE_SUMMARY).read()
-        shas = {f: hashlib.sha256(open(os.path.join(ROOT, "sparse_expert_router_gb300", "csrc", f),
-                                       "rb").read()).hexdigest()[:16] for f in PROFILED_SOURCES}
-    except OSError:
-        return None
-    lines = [ln.split() for ln in text.splitlines()]
-    for f, sha in shas.items():
-        if ["source_sha256_prefix", f, sha] not in lines:
-            return None
-    for parts in lines:
-        if len(parts) == 4 and parts[0] == "traffic_per_launch" and parts[1] == workload \
-                and parts[2] == kernel:
-            return float(parts[3])
+    for path, sources in PROFILE_SUMMARIES:
+        try:
+            text = open(path).read()
+            shas = {f: hashlib.sha256(open(os.path.join(ROOT, "sparse_expert_router_gb300", "csrc",
+                                                        f), "rb").read()).hexdigest()[:16]
+                    for f in sources}
+        except OSError:
+            continue
+        lines = [ln.split() for ln in text.splitlines()]
+        if any(["source_sha256_prefix", f, sha] not in lines for f, sha in shas.items()):
+            continue
+        for parts in lines:
+            if len(parts) == 4 and parts[0] == "traffic_per_launch" and parts[1] == workload \
+                    and parts[2] == kernel:
+                return float(parts[3])
     return None
 
 
@@ -85,19 +89,21 @@ def max_over_ranks(x: float, device) -> float:
     return float(t)
 
 
-def algorithmic(shape, counts):
-    """Algorithmic flops and bytes per stage of one forward: bf16 storage, except that an
-    fp8-expert layer keeps its expert banks (plus one fp32 scale per output column), grouped
-    rows and hidden in E4M3 (one byte). "tc_peak" names the tensor-core rate a stage runs at."""
+def algorithmic(shape, kept):
+    """Algorithmic flops and bytes per stage of one forward, given the rows each expert keeps
+    after the capacity clamp (`kept`, the differences of the group offsets): bf16 storage,
+    except that an fp8-expert layer keeps its expert banks (plus one fp32 scale per output
+    column), grouped rows and hidden in E4M3 (one byte). "tc_peak" names the tensor-core rate a
+    stage runs at."""
     T, d, L, E, k = shape.T, shape.d_model, shape.d_latent, shape.n_experts, shape.top_k
     F, SF = shape.d_ff, shape.n_shared * shape.d_ff_shared
-    es = 2
+    es = 4 if shape.dtype == "f32" else 2
     fp8 = getattr(shape, "expert_dtype", "bf16") == "fp8"
     wb = 1 if fp8 else es                              # bytes per expert-bank weight
     ab = 1 if fp8 else es                              # bytes per grouped-row / hidden value
     xp = "fp8" if fp8 else "bf16"
-    R = int(min(sum(counts), T * k))
-    active = sum(1 for c in counts if c > 0)
+    R = int(sum(kept))
+    active = sum(1 for c in kept if c > 0)
     fl = shape.flops()
     fl["expert_up"] = 2.0 * R * L * 2 * F
     fl["expert_down"] = 2.0 * R * F * L
@@ -500,7 +506,7 @@ def main():
     ap.add_argument("--workload", default="l535b_t8192", choices=sorted(SHAPES))
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -583,12 +589,13 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
     ws = m.alloc_workspace(cfg, dev)
     y = torch.empty((shape.T, shape.d_model), dtype=shape.torch_dtype, device=dev)
     counts = torch.zeros(shape.n_experts, dtype=torch.int32, device=dev)
+    offsets = torch.zeros(shape.n_experts + 1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
     stream = torch.cuda.current_stream(dev)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
     for e in evs:
         e.record(stream)          # creates the CUDA events before their handles are passed on
-    aux = {"stage_events": evs, "expert_counts": counts}
+    aux = {"stage_events": evs, "expert_counts": counts, "expert_offsets": offsets}
 
     for _ in range(max(3, args.warmup)):
         m.moe_forward(cfg, inp, inp["x"], y, ws, stream=stream, aux=aux)
@@ -670,7 +677,7 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
         return None
 
     pk = peaks()
-    alg = algorithmic(shape, counts.cpu().tolist())
+    alg = algorithmic(shape, (offsets[1:] - offsets[:-1]).cpu().tolist())
     stages = {}
     for s in STAGES:
         ms = stage_ms[s] / args.steps
@@ -679,6 +686,9 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
             f, by = alg[s]["flops"], alg[s]["bytes"]
             st["gb_s"] = round(by / (ms * 1e-3) / 1e9, 1)
             st["hbm_frac"] = round(st["gb_s"] / pk["hbm_gbs"], 3)
+            tr = profiled_traffic(shape.name, s)
+            if tr is not None:
+                st["traffic"] = tr
             if f:
                 tp, tps = tc_peak(pk, alg[s]), tc_peak(pk, alg[s], "bf16_sustained")
                 st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 1)
@@ -727,9 +737,9 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
 # Every workload of the layer, one JSON line each in --all mode, with the number of tokens of
 # the oracle's bounded CPU sample (all threads) and, for the two smallest layers, of a second
 # sample timed on one thread.
-ALL_WORKLOADS = [("tiny_f32", 256, 256), ("small_bf16", 256, 32), ("l535b_t8192", 256, 0),
-                 ("l535b_t8192_fp8", 256, 0), ("l535b_zipf_t16384", 256, 0),
-                 ("l535b_zipf_t16384_cf110", 256, 0), ("l535b_t65536", 256, 0)]
+ALL_WORKLOADS = [("tiny_f32", 256, 256), ("small_bf16", 1024, 128), ("l535b_t8192", 1024, 0),
+                 ("l535b_t8192_fp8", 1024, 0), ("l535b_zipf_t16384", 2048, 0),
+                 ("l535b_zipf_t16384_cf110", 2048, 0), ("l535b_t65536", 1024, 0)]
 
 
 def run_all(args, m, dev):

@@ -138,6 +138,12 @@ SHAPES: Dict[str, LayerShape] = {
     "l535b_e64_t1368": LayerShape("l535b_e64_t1368", T=1368, d_model=6144, d_latent=3072,
                                   n_experts=64, top_k=8, d_ff=3072, n_shared=2,
                                   d_ff_shared=3072, dtype="bf16"),
+    # Profiling case of the routing, dispatch and combine kernels (2.5 GB on the device): the
+    # 535B layer at T=8192 with the routed experts' d_ff cut to 128. Router, dispatch and combine
+    # see exactly the bench workload's sizes (T, d, latent, E, k), and their inputs exceed L2.
+    "l535b_f128_t8192": LayerShape("l535b_f128_t8192", T=8192, d_model=6144, d_latent=3072,
+                                   n_experts=384, top_k=8, d_ff=128, n_shared=2,
+                                   d_ff_shared=3072, dtype="bf16"),
 }
 
 # fp8 expert weights (E4M3 with a power-of-two scale per expert output column), everything

@@ -20,7 +20,8 @@ struct DeviceHeader {
   int32_t n_exact;     // exact-token list length (router stage 3)
   uint32_t amax_x;     // fp8 experts: bits of max |row| quantized by the gather (fp32, >= 0)
   uint32_t amax_h;     // fp8 experts: bits of max |hidden| quantized by expert GEMM 1
-  int32_t reserved[58];
+  uint32_t dispatch_ticket;   // blocks of the dispatch scan that have finished (reset per call)
+  int32_t reserved[57];
 };
 static_assert(sizeof(DeviceHeader) == 256, "header is 256 bytes");
 

@@ -18,7 +18,12 @@
 namespace moe {
 namespace {
 
-constexpr int CH = 128;   // tokens per dispatch chunk (one thread per token)
+// Tokens per dispatch chunk: one warp lane per token. A token's slot for expert e is
+// offsets[e] + (tokens of earlier chunks that chose e: the chunk base) + (earlier tokens of its
+// own chunk that chose e: a 32-bit mask and a popcount), so slots are stable in token order and
+// need no atomics.
+constexpr int CH = 32;
+constexpr int HIST_WARPS = 4;   // chunks per histogram block
 
 __global__ void header_reset_kernel(DeviceHeader* h, int clear_status, int amax_mask) {
   pdl_wait();
@@ -37,30 +42,39 @@ __device__ __forceinline__ bool valid_assignment(const int32_t* row, int j, int 
   return e >= 0 && e < E && (j == 0 || row[j - 1] < e);
 }
 
-__global__ void __launch_bounds__(CH) hist_kernel(DispatchArgs a) {
+// Per-chunk expert counts: each warp counts one 32-token chunk in shared memory. Also zeroes the
+// ticket of the scan that follows.
+__global__ void __launch_bounds__(32 * HIST_WARPS) hist_kernel(DispatchArgs a) {
   pdl_wait();
-  extern __shared__ int s_cnt[];
-  for (int e = threadIdx.x; e < a.E; e += CH) s_cnt[e] = 0;
+  extern __shared__ int s_cnt[];   // [HIST_WARPS][E]
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->dispatch_ticket = 0u;
+  for (int i = threadIdx.x; i < HIST_WARPS * a.E; i += 32 * HIST_WARPS) s_cnt[i] = 0;
   __syncthreads();
-  int64_t t = (int64_t)blockIdx.x * CH + threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c = (int64_t)blockIdx.x * HIST_WARPS + warp;
+  const int64_t t = c * CH + lane;
+  int* cnt = s_cnt + warp * a.E;
   if (t < a.T && (!a.mask || a.mask[t])) {   // padding tokens are not dispatched
     const int32_t* row = a.idx + t * a.k;
     for (int j = 0; j < a.k; ++j) {
-      if (valid_assignment(row, j, a.E)) atomicAdd(&s_cnt[row[j]], 1);
+      if (valid_assignment(row, j, a.E)) atomicAdd(&cnt[row[j]], 1);
       else report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < a.E; e += CH)
-    a.chunk_hist[(int64_t)blockIdx.x * a.E + e] = s_cnt[e];
+  __syncwarp();
+  if (c < a.n_chunks)
+    for (int e = lane; e < a.E; e += 32) a.chunk_hist[c * a.E + e] = cnt[e];
 }
 
 // One block per expert: exclusive scan of the expert's per-chunk counts (the base of each
-// chunk's ranks) and the expert's total count.
-__global__ void __launch_bounds__(256) scan_chunks_kernel(DispatchArgs a) {
+// chunk's ranks) and the expert's total count. The last block to finish (a ticket in the device
+// report) then clamps every expert to the capacity, scans the kept counts into the group
+// offsets and counts the drops.
+__global__ void __launch_bounds__(256) scan_kernel(DispatchArgs a) {
   pdl_wait();
   __shared__ int s_warp[8];
   __shared__ int s_carry;
+  __shared__ int s_last;
   const int e = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
@@ -93,85 +107,59 @@ __global__ void __launch_bounds__(256) scan_chunks_kernel(DispatchArgs a) {
     if (threadIdx.x == 255) s_carry = excl + v;
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.counts[e] = s_carry;
-}
-
-// One block: capacity clamp, exclusive scan of the kept counts into the group offsets, drops.
-__global__ void __launch_bounds__(1024) scan_offsets_kernel(DispatchArgs a) {
-  pdl_wait();
-  __shared__ int s_warp[32];
-  __shared__ int s_drop[32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  const int cnt = (e < a.E) ? a.counts[e] : 0;
-  int kept = (a.cap >= 0) ? min(cnt, a.cap) : cnt;
-  int drop = cnt - kept;
-  int incl = kept;
+  if (threadIdx.x == 0) {
+    a.counts[e] = s_carry;
+    __threadfence();                       // the count is visible before the ticket is taken
+    s_last = atomicAdd(&a.hdr->dispatch_ticket, 1u) == (unsigned)(a.E - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // the last block: capacity clamp and exclusive scan of the kept counts, E <= 1024 experts as
+  // four consecutive experts per thread
+  constexpr int PER = 4;
+  int kept[PER], sum = 0, drop = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int ee = threadIdx.x * PER + i;
+    const int cnt = (ee < a.E) ? __ldcg(a.counts + ee) : 0;
+    kept[i] = (a.cap >= 0) ? min(cnt, a.cap) : cnt;
+    drop += cnt - kept[i];
+    sum += kept[i];
+  }
+  int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(~0u, incl, o);
-    if (lane >= o) incl += v;
+    int u = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += u;
   }
   int wdrop = drop;
 #pragma unroll
   for (int o = 16; o; o >>= 1) wdrop += __shfl_xor_sync(~0u, wdrop, o);
-  if (lane == 31) s_warp[warp] = incl;
-  if (lane == 0) s_drop[warp] = wdrop;
+  __shared__ int s_wsum[8], s_wdrop[8];
+  if (lane == 31) s_wsum[warp] = incl;
+  if (lane == 0) s_wdrop[warp] = wdrop;
   __syncthreads();
-  if (warp == 0) {
-    int v = s_warp[lane], dv = s_drop[lane];
-    int iv = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(~0u, iv, o);
-      if (lane >= o) iv += u;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) dv += __shfl_xor_sync(~0u, dv, o);
-    s_warp[lane] = iv - v;   // exclusive prefix of warp totals
-    if (lane == 0) s_drop[0] = dv;
+  int wbase = 0, dtot = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) wbase += s_wsum[w];
+    dtot += s_wdrop[w];
   }
-  __syncthreads();
-  int excl = s_warp[warp] + incl - kept;
-  if (e < a.E) a.offsets[e] = excl;
-  if (e == a.E - 1) a.offsets[a.E] = excl + kept;
-  if (e == 0 && a.n_dropped) *a.n_dropped = s_drop[0];
+  int run = wbase + incl - sum;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int ee = threadIdx.x * PER + i;
+    if (ee < a.E) a.offsets[ee] = run;
+    run += kept[i];
+    if (ee == a.E - 1) a.offsets[a.E] = run;
+  }
+  if (threadIdx.x == 0 && a.n_dropped) *a.n_dropped = dtot;
 }
 
-// Slots: stable rank of each token among the tokens of its chunk that chose the same expert
-// (bitmask per expert and popcount), plus the chunk's base.
-__global__ void __launch_bounds__(CH) rank_kernel(DispatchArgs a) {
-  pdl_wait();
-  extern __shared__ uint32_t s_mask[];   // [E][CH / 32]
-  constexpr int W = CH / 32;
-  for (int i = threadIdx.x; i < a.E * W; i += CH) s_mask[i] = 0u;
-  __syncthreads();
-  const int tl = threadIdx.x;
-  const int64_t t = (int64_t)blockIdx.x * CH + tl;
-  const int32_t* row = a.idx + t * a.k;
-  const bool real = t < a.T && (!a.mask || a.mask[t]);
-  if (real)
-    for (int j = 0; j < a.k; ++j)
-      if (valid_assignment(row, j, a.E)) atomicOr(&s_mask[row[j] * W + (tl >> 5)], 1u << (tl & 31));
-  __syncthreads();
-  if (t >= a.T) return;
-  for (int j = 0; j < a.k; ++j) {
-    int32_t slot = -1;
-    if (real && valid_assignment(row, j, a.E)) {
-      const int e = row[j];
-      int r = __popc(s_mask[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u));
-      for (int w = 0; w < (tl >> 5); ++w) r += __popc(s_mask[e * W + w]);
-      r += a.chunk_base[(int64_t)blockIdx.x * a.E + e];
-      if (a.cap < 0 || r < a.cap) {
-        slot = a.offsets[e] + r;
-        if (slot >= a.pool_rows) { report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t); slot = -1; }
-        else a.perm[slot] = (int32_t)(t * a.k + j);
-      }
-    }
-    a.slot_of[t * a.k + j] = slot;
-  }
-}
-
-// h = z * rsqrt(mean(z^2) + eps) * gamma written to every kept slot of the token. With E4M3
+// One block per token. Warp 0 first gives the token its slots: the chunk's 32 tokens mark, per
+// expert, a 32-bit mask of the tokens that chose it; the token's rank among them is the popcount
+// below its lane, plus the chunk base. Slots past the expert's capacity are -1 (dropped). Then
+// h = z * rsqrt(mean(z^2) + eps) * gamma is written to every kept slot of the token. With E4M3
 // output the rows hold the codes of h * x_scale (round to nearest even, saturating) and the
 // block's max |h| joins the layer's amax when the token has a kept slot.
 template <typename T>
@@ -179,7 +167,43 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
   constexpr bool kFp8 = std::is_same<T, e4m3>::value;
   pdl_wait();
   __shared__ float s_red[4];
+  __shared__ uint32_t s_mask[1024];          // E <= 1024
+  __shared__ int32_t s_slot[32];             // k <= 32
   const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    for (int e = lane; e < a.E; e += 32) s_mask[e] = 0u;
+    __syncwarp();
+    const int64_t c = t / CH;
+    const int tl = (int)(t % CH);
+    const int64_t tt = c * CH + lane;           // this lane's token of the chunk
+    if (tt < a.T && (!a.mask || a.mask[tt])) {
+      const int32_t* rowl = a.idx + tt * a.k;
+      for (int j = 0; j < a.k; ++j)
+        if (valid_assignment(rowl, j, a.E)) atomicOr(&s_mask[rowl[j]], 1u << lane);
+    }
+    __syncwarp();
+    if (lane < a.k) {                           // lane j: the token's assignment j
+      const int j = lane;
+      const int32_t* row = a.idx + t * a.k;
+      int32_t slot = -1;
+      if ((!a.mask || a.mask[t]) && valid_assignment(row, j, a.E)) {
+        const int e = row[j];
+        const int r = __popc(s_mask[e] & ((1u << tl) - 1u)) + a.chunk_base[c * a.E + e];
+        if (a.cap < 0 || r < a.cap) {
+          slot = a.offsets[e] + r;
+          if (slot < 0 || slot >= a.pool_rows) {
+            report_error(a.hdr, MOE_ERR_BAD_ROUTING, (int)t);
+            slot = -1;
+          } else {
+            a.perm[slot] = (int32_t)(t * a.k + j);
+          }
+        }
+      }
+      a.slot_of[t * a.k + j] = slot;
+      s_slot[j] = slot;
+    }
+  }
   const float* z = a.z + t * a.L;
   float ss = 0.0f;
   for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
@@ -190,16 +214,13 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(~0u, ss, o);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  if (lane == 0) s_red[warp] = ss;
   __syncthreads();
+  if (a.x_perm == nullptr) return;
   ss = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
   const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)a.L), a.eps)));
-  int32_t slots[32];
   int ns = 0;
-  for (int j = 0; j < a.k; ++j) {
-    int32_t s = a.slot_of[t * a.k + j];
-    if (s >= 0 && s < a.pool_rows) slots[ns++] = s;
-  }
+  for (int j = 0; j < a.k; ++j) ns += s_slot[j] >= 0;
   T* xp = static_cast<T*>(a.x_perm);
   const float qs = kFp8 ? *a.x_scale : 1.0f;
   float amax = 0.0f;
@@ -216,7 +237,10 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
         v[q] = v[q] * qs;
       }
     }
-    for (int j = 0; j < ns; ++j) st8(xp + (int64_t)slots[j] * a.L + i, v);
+    for (int j = 0; j < a.k; ++j) {
+      const int32_t sl = s_slot[j];
+      if (sl >= 0) st8(xp + (int64_t)sl * a.L + i, v);
+    }
   }
   if (kFp8 && ns > 0) {
 #pragma unroll
@@ -291,17 +315,14 @@ cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bo
 int64_t dispatch_chunks(int64_t T) { return cdiv(T, CH); }
 
 cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool pdl) {
+  if (a.E > 1024 || a.k > 32) return cudaErrorInvalidValue;
   cudaError_t err;
-  const unsigned nch = (unsigned)a.n_chunks;
-  err = launch(hist_kernel, dim3(nch), dim3(CH), (size_t)a.E * 4, st, pdl, a);
+  const unsigned nhb = (unsigned)cdiv(a.n_chunks, HIST_WARPS);
+  err = launch(hist_kernel, dim3(nhb), dim3(32 * HIST_WARPS), (size_t)HIST_WARPS * a.E * 4, st,
+               pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(scan_chunks_kernel, dim3(a.E), dim3(256), 0, st, pdl, a);
+  err = launch(scan_kernel, dim3(a.E), dim3(256), 0, st, pdl, a);
   if (err != cudaSuccess) return err;
-  err = launch(scan_offsets_kernel, dim3(1), dim3(1024), 0, st, pdl, a);
-  if (err != cudaSuccess) return err;
-  err = launch(rank_kernel, dim3(nch), dim3(CH), (size_t)a.E * (CH / 32) * 4, st, pdl, a);
-  if (err != cudaSuccess) return err;
-  if (a.x_perm == nullptr) return cudaSuccess;
   if (a.xperm_fp8)
     return launch(gather_kernel<e4m3>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);
   if (dtype == DT_BF16) return launch(gather_kernel<bf16>, dim3((unsigned)a.T), dim3(128), 0, st, pdl, a);

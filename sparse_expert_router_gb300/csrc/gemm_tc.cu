@@ -23,7 +23,13 @@
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing work, frees its tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 #include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include <cuda_fp16.h>
 
@@ -42,6 +48,10 @@ using namespace tc;
 #ifndef MOE_TC_SMEM_BUDGET
 #define MOE_TC_SMEM_BUDGET (220 * 1024)   // dynamic shared memory per CTA, bytes
 #endif
+// Pair launches: a sixth stage of 32 KB fits next to the epilogue tiles within the 227 KB a CTA
+// may use (static shared memory included), so that as many weight bytes are in flight per SM as
+// with three 64 KB stages.
+constexpr int PAIR_SMEM_BUDGET = 225 * 1024;
 constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
 constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem
@@ -56,7 +66,7 @@ constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte ro
 // quadrant take alternate 16-token chunks. Keeping the instances apart keeps each one's
 // registers within what its warp count allows (three or four warps share one sub-partition's
 // 16K registers).
-template <bool FP8, bool KC, bool BWD> struct Inst {
+template <bool FP8, bool KC, bool BWD, bool PAIR = false> struct Inst {
   static constexpr int EW = KC ? 8 : MOE_TC_EPI_WARPS;
 };
 constexpr int EPI_TILE_MAX = 16 * 32 * 4;   // transpose tile of one warp: 16 tokens x 32 fp32
@@ -126,11 +136,12 @@ struct TcParams {
 // Instruction descriptor: fp32 accumulator (bits 4..5 = 1), A and B formats at bits 7..9 and
 // 10..12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3), A MN-major (transposed, bit 15),
 // B K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-__device__ __forceinline__ uint32_t make_idesc(int n, bool fp8, bool a_kmajor = false) {
+__device__ __forceinline__ uint32_t make_idesc(int n, bool fp8, bool a_kmajor = false,
+                                               int m = BM) {
   const uint32_t ab = fp8 ? 0u : 1u;
   const uint32_t ta = a_kmajor ? 0u : 1u;
   return (1u << 4) | (ab << 7) | (ab << 10) | (ta << 15) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(m >> 4) << 24);
 }
 
 // Problems whose items carry two weight tiles (gate and up) and two accumulators.
@@ -197,20 +208,33 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
 // Two instances: FP8 = false (bf16 operands, k-chunked fp32 problems) and FP8 = true (E4M3
 // operands, scales and the E4M3 SwiGLU output), so that neither carries the other's registers:
 // with 10 warps per CTA three warps share one sub-partition's 16K registers, 168 per thread.
-template <bool FP8, bool KC, bool BWD>
-__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
+// PAIR: a cluster of two CTAs runs each item with tcgen05.mma.cta_group::2 (M = 256: 128 weight
+// rows from each CTA; each CTA loads half of the token tile). Every item of a pair launch has two
+// weight tiles: a dual item's 256 features split 128 + 128 between the CTAs; a SwiGLU item's
+// 128 output features split 64 + 64, each CTA stacking the gate (W1) and up (W3) tiles of its 64
+// features into one 128-row A tile. Each CTA's accumulator is then one N-column buffer, so two
+// buffers fit in tensor memory and the epilogue of one item overlaps the MMAs of the next.
+template <bool FP8, bool KC, bool BWD, bool PAIR = false>
+__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams P) {
-  constexpr int EPI_WARPS = Inst<FP8, KC, BWD>::EW;
+  constexpr int EPI_WARPS = Inst<FP8, KC, BWD, PAIR>::EW;
+  static_assert(!PAIR || (!FP8 && !KC && !BWD), "pair launches: bf16 forward problems");
+  constexpr int XPAIRS = EPI_WARPS / 2;          // gate/up warp pairs of a pair SwiGLU epilogue
+  constexpr int XB0 = 2 * 8 + 4;                 // first exchange barrier
   const int EPI_STAGE_BYTES = P.epi_tile;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 4 + 2 * XPAIRS];
   __shared__ int64_t s_total;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int stages = P.stages;
-  const bool glu = P.glu != 0;
+  const bool glu = P.glu != 0 && !PAIR;     // two A tiles per stage (a pair CTA holds one)
+  // pair launches: this CTA's rank in its pair, the pair's index and the number of pairs
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int64_t unit = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+  const int64_t n_units = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int stage_bytes = (glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
@@ -248,22 +272,33 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tmem_full(b), 1);
-      mbar_init(tmem_empty(b), 32 * EPI_WARPS);
+      // pair launches: rank 0's barrier, released by the epilogue threads of both CTAs
+      mbar_init(tmem_empty(b), (PAIR ? 2 : 1) * 32 * EPI_WARPS);
     }
+    if (PAIR)
+      for (int i = 0; i < 2 * XPAIRS; ++i) mbar_init(smem_u32(&bars[XB0 + i]), 32);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int p = 0; p < P.n_probs; ++p)
       for (int s = 0; s < P.p[p].n_seg; ++s) {
         prefetch_map(&P.p[p].seg[s].a1);
         prefetch_map(&P.p[p].seg[s].b);
-        if (glu) prefetch_map(&P.p[p].seg[s].a3);
+        if (P.glu) prefetch_map(&P.p[p].seg[s].a3);
       }
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                     smem_u32(&s_tmem))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {
+      // one warp of each CTA of the pair allocates, collectively, the same columns in both
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                       smem_u32(&s_tmem))
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                       smem_u32(&s_tmem))
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
 
   // Every thread waits for the preceding kernel before it reads the group offsets.
@@ -308,11 +343,47 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // pair launches: both CTAs' barriers are initialised before either signals the other's
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
   const int64_t total = s_total;
 
-  if (warp == 0 && lane == 0) {
+  if (PAIR && warp == 0 && lane == 0) {
+    // ---------------- TMA producer of a pair CTA ----------------
+    // Loads this CTA's 128 weight rows and its half (N / 2 rows) of the token tile; the bytes of
+    // both CTAs complete on rank 0's full barrier, which rank 0 arms with their sum.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t w = unit; w < total && ok; w += n_units) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const int half_rows = ((it.nrows + 15) / 16) * 8;
+      const int nb = (half_rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
+      const uint32_t bytes = 2u * (uint32_t)(A_BYTES + nb * B_BOX_BYTES);
+      const int64_t my_row0 = it.row0 + (int64_t)rank * half_rows;
+      const bool gl = is_glu(q.epi);
+      // SwiGLU: gate and up tiles of features m_w + 64 rank ..; dual: features m_w + 128 rank ..
+      const int mx0 = it.m_w + (gl ? 64 : BM) * (int)rank;
+      for (int s = 0; s < q.n_seg && ok; ++s) {
+        const TcSeg& sg = q.seg[s];
+        for (int kb = 0; kb < sg.kblocks; ++kb) {
+          const int k0 = kb * BK;
+          if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
+          const uint32_t fb = mapa_shared(full(stage), 0);
+          if (rank == 0) mbar_expect_tx(full(stage), bytes);
+          tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx0, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA1(stage)) + A_HALF, gl ? &sg.a3 : &sg.a1, fb,
+                           gl ? mx0 : mx0 + 64, k0, it.wg);
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d_pair(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, fb, k0,
+                             (int)(my_row0 + b * B_BOX_ROWS));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (!PAIR && warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
@@ -363,19 +434,20 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (in a pair, rank 0 issues for both CTAs) ----------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     int ev = 0;      // accumulator events of this CTA: one per item, or one per k-chunk
-    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int64_t w = unit; w < total && ok; w += n_units) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      const bool sw = is_glu(q.epi) || q.dual;   // second A tile -> second accumulator
+      // second A tile -> second accumulator (a pair CTA holds one A tile)
+      const bool sw = !PAIR && (is_glu(q.epi) || q.dual);
       const int n = ((it.nrows + 15) / 16) * 16;
       const bool akm = BWD && q.a_kmajor;
-      const uint32_t idesc = make_idesc(n, fp8, akm);
+      const uint32_t idesc = make_idesc(n, fp8, akm, PAIR ? 2 * BM : BM);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
       const int per_ev = q.kchunk ? q.kchunk : kb_total;
@@ -383,7 +455,11 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         const int buf = ev % nacc;
         const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-        if (!mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) { ok = false; break; }
+        if (PAIR ? !mbar_wait_cluster(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)
+                 : !mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         uint32_t accumulate = 0;
         const int kb_end = min(kb0 + per_ev, kb_total);
@@ -413,17 +489,23 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
 #pragma unroll
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-              mma_bf16(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc, accumulate);
-              if (sw)
-                mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * astep, alb, asbo), bd, idesc,
-                         accumulate);
+              if constexpr (PAIR) {
+                mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc,
+                              accumulate);
+              } else {
+                mma_bf16(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc, accumulate);
+                if (sw)
+                  mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * astep, alb, asbo), bd, idesc,
+                           accumulate);
+              }
               accumulate = 1;
             }
           }
-          mma_commit(empty(stage));
+          // pair: frees the stage in both CTAs
+          if constexpr (PAIR) mma_commit_pair(empty(stage), 3); else mma_commit(empty(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
-        mma_commit(tmem_full(buf));
+        if constexpr (PAIR) mma_commit_pair(tmem_full(buf), 3); else mma_commit(tmem_full(buf));
       }
     }
   } else if (warp >= 2) {
@@ -499,7 +581,14 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     };
     int ev = 0;
     float amax = 0.0f;                                   // fp8 output: this thread's max |value|
-    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    uint32_t xc = 0;                                     // pair SwiGLU: chunks exchanged so far
+    // pair launches: the epilogue threads of both CTAs release rank 0's accumulator buffer
+    auto release = [&](int b) {
+      tc_fence_before();
+      if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(tmem_empty(b), 0));
+      else mbar_arrive(tmem_empty(b));
+    };
+    for (int64_t w = unit; w < total; w += n_units) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       if (KC && q.kchunk) {
@@ -582,6 +671,99 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       }
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
+      if constexpr (PAIR) {
+        if (is_glu(q.epi)) {
+          // Lanes 0..63 of this CTA's accumulator hold the gate (x W1) and lanes 64..127 the up
+          // projection (x W3) of the same 64 features. Each warp of quadrant 2 or 3 (up) hands
+          // its 16-token chunks, one at a time, through shared memory to the warp of quadrant 0
+          // or 1 of the same half (same lane = same feature), which computes the SwiGLU and
+          // writes the bf16 hidden. Hand-overs wait on mbarriers with bounded waits.
+          constexpr int HW = EPI_WARPS / 4;                     // warps per quadrant
+          constexpr int CPW = (BN / 16 + HW - 1) / HW;          // chunks per warp
+          constexpr int CPR = CPW < 4 ? CPW : 4;                // chunks held in registers
+          const int xp = half * 2 + (quad & 1);
+          const uint32_t xfull = smem_u32(&bars[XB0 + xp]);
+          const uint32_t xempty = smem_u32(&bars[XB0 + XPAIRS + xp]);
+          float* xbuf = reinterpret_cast<float*>(epi_stage +
+                                                 (4 * half + (quad & 1)) * EPI_STAGE_BYTES);
+          const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                     (uint32_t)(buf * BN);
+          const int f0 = it.m0 + 64 * (int)rank + (quad & 1) * 32;
+          bool ok = true;
+          if (quad >= 2) {
+            for (int i = 0; i < CPW; ++i) {
+              const int c0 = half * 16 + i * 16 * HW;
+              if (c0 < it.nrows) {
+                float v3[16];
+                tmem_ld16(lane_addr + c0, v3);
+                tmem_wait_ld();
+                if (!mbar_wait(xempty, (xc & 1u) ^ 1u, &s_abort, P.hdr, 5)) { ok = false; break; }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) xbuf[j * 32 + lane] = v3[j];
+                mbar_arrive(xfull);
+                ++xc;
+              }
+            }
+            release(buf);
+            if (!ok) break;
+            continue;
+          }
+          // gate warp: the first CPR chunks are packed into registers and written after the
+          // release, later chunks (tiles of more than 192 tokens) are written in place
+          uint32_t pk[CPR][8];
+          auto take = [&](int c0, float v[16]) -> bool {
+            float v3[16];
+            tmem_ld16(lane_addr + c0, v);
+            tmem_wait_ld();
+            if (!mbar_wait(xfull, xc & 1u, &s_abort, P.hdr, 6)) return false;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v3[j] = xbuf[j * 32 + lane];
+            mbar_arrive(xempty);
+            ++xc;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
+            return true;
+          };
+#pragma unroll
+          for (int i = 0; i < CPR; ++i) {
+            const int c0 = half * 16 + i * 16 * HW;
+            if (ok && c0 < it.nrows) {
+              float v[16];
+              ok = take(c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j], v[j + 1]);
+                pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            }
+          }
+          for (int i = CPR; i < CPW && ok; ++i) {
+            const int c0 = half * 16 + i * 16 * HW;
+            if (c0 < it.nrows) {
+              float v[16];
+              if (!(ok = take(c0, v))) break;
+              store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
+            }
+          }
+          release(buf);
+          if (!ok) break;
+#pragma unroll
+          for (int i = 0; i < CPR; ++i) {
+            const int c0 = half * 16 + i * 16 * HW;
+            if (c0 < it.nrows) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                stg_h[j * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] & 0xFFFFu));
+                stg_h[(j + 1) * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] >> 16));
+              }
+              __syncwarp();
+              store_bf16_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
+              __syncwarp();
+            }
+          }
+          continue;
+        }
+      }
       if constexpr (FP8) {
         if (q.out_fp8 && is_glu(q.epi)) {
           // E4M3 hidden: the SwiGLU of every chunk of this warp is computed and packed into
@@ -632,7 +814,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
           continue;
         }
       }
-      if constexpr (!FP8 && !KC && !BWD) {
+      if constexpr (!FP8 && !KC && !BWD && !PAIR) {
         if (q.epi == EPI_SWIGLU) {
           // bf16 hidden: as for E4M3 above, the SwiGLU of a warp's first CPR chunks is packed
           // into registers before the accumulators are released; chunks past those (tiles of
@@ -690,8 +872,9 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
           continue;
         }
       }
-      for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
-      const int f0 = it.m0 + sub * BM + quad * 32;       // first feature of this warp
+      // a pair CTA holds one 128-feature half of a dual item
+      for (int sub = 0; sub < ((q.dual && !PAIR) ? 2 : 1); ++sub) {
+      const int f0 = it.m0 + (PAIR ? (int)rank : sub) * BM + quad * 32;   // this warp's first feature
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                  (uint32_t)(buf * BN) + (uint32_t)sub * acc2;
       const bool f32out = (q.epi == EPI_F32);
@@ -753,8 +936,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
       }
       }
-      tc_fence_before();
-      mbar_arrive(tmem_empty(buf));
+      release(buf);
     }
     if (FP8 && P.amax) {
 #pragma unroll
@@ -765,10 +947,24 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // After a timeout, copies and MMAs this CTA or its pair issued may still be in flight:
+    // give them 20 ms (they take microseconds) before either CTA frees its shared or tensor
+    // memory. Then neither CTA leaves while the other can still signal its barriers.
+    if (s_abort) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 20000000ull) __nanosleep(1000);
+    }
+    cluster_sync();
+  }
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                   : "memory");
   }
 }
 
@@ -859,6 +1055,77 @@ int num_sms_tc() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 148;
+}
+
+// Which launches use CTA pairs: MOE_TC_PAIR in the environment selects none ("0", the default),
+// launches with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1");
+// no launch uses them once a query finds that no pair fits on the GPU.
+enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3 };
+std::atomic<int> g_pair_mode{-1};
+int pair_mode() {
+  int m = g_pair_mode.load(std::memory_order_relaxed);
+  if (m < 0) {
+    const char* e = getenv("MOE_TC_PAIR");
+    m = PAIR_NONE;
+    if (e && !strcmp(e, "1")) m = PAIR_ALL;
+    else if (e && !strcmp(e, "dual")) m = PAIR_DUAL;
+    else if (e && !strcmp(e, "glu")) m = PAIR_GLU;
+    g_pair_mode.store(m, std::memory_order_relaxed);
+  }
+  return m;
+}
+void pair_disable() { g_pair_mode.store(PAIR_NONE, std::memory_order_relaxed); }
+
+cudaLaunchConfig_t pair_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                               cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = 2;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cfg;
+}
+
+// Pairs (clusters of two CTAs, one CTA per SM) of the pair kernel that fit on the GPU at once,
+// cached per device: the persistent grid of a pair launch.
+int max_pairs(void (*kern)(TcParams), dim3 block) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BUDGET) ==
+      cudaSuccess) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(dim3(2), block, PAIR_SMEM_BUDGET, nullptr, false, attr);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();   // a failed query leaves no error behind
+  cache[dev] = n;
+  return n;
+}
+
+cudaError_t launch_pair(void (*kern)(TcParams), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t stream, bool pdl, const TcParams& P) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(grid, block, smem, stream, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace
@@ -983,14 +1250,36 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     if (is_glu(g.epi) || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
+  bool kc = false, bwd = false;
+  for (int j = 0; j < n_probs; ++j) {
+    kc = kc || P.p[j].kchunk > 0;
+    bwd = bwd || P.p[j].a_kmajor || P.p[j].epi == EPI_SWIGLU_SAVE || P.p[j].epi == EPI_SWIGLU_BWD;
+  }
+  if (kc && bwd) return cudaErrorNotSupported;
+  // CTA pairs (cta_group::2) for bf16 launches whose every item has two weight tiles
+  const int pmode = pair_mode();
+  bool pair = pmode != PAIR_NONE && !P.fp8 && !kc && !bwd;
+  for (int j = 0; j < n_probs; ++j) {
+    const TcProblem& q = P.p[j];
+    pair = pair && (is_glu(q.epi) || q.dual) &&
+           (q.epi == EPI_SWIGLU || q.epi == EPI_STORE || q.epi == EPI_F32) &&
+           !(pmode == PAIR_DUAL && is_glu(q.epi)) && !(pmode == PAIR_GLU && q.dual);
+  }
+  const dim3 block(64 + 32 * (P.fp8 ? Inst<true, false, false>::EW
+                                    : (kc ? Inst<false, true, false>::EW
+                                          : (bwd ? Inst<false, false, true>::EW
+                                                 : Inst<false, false, false>::EW))));
+  const int n_pairs = pair ? max_pairs(tc_gemm_kernel<false, false, false, true>, block) : 0;
+  if (pair && n_pairs < 1) {   // no CTA pair fits: this and later launches run without pairs
+    pair_disable();
+    pair = false;
+  }
   // Dense launches without fp32 k-chunked problems: choose the token tile height so that the
   // items fill whole waves of the persistent grid, by the estimate (waves rounded up) x height.
   // The back GEMM's 24 x 32 tiles of 256 rows are 5.05 waves on 152 SMs; 224-row tiles make
-  // 888 items, 5.84 waves, for 12% less estimated time.
-  bool any_kc = false;
-  for (int j = 0; j < n_probs; ++j) any_kc = any_kc || P.p[j].kchunk > 0;
-  if (P.grouped < 0 && !any_kc) {
-    const int64_t sms = num_sms_tc();
+  // 888 items, 5.84 waves, for 12% less estimated time. A pair of SMs runs one item at a time.
+  if (P.grouped < 0 && !kc) {
+    const int64_t sms = pair ? n_pairs : num_sms_tc();
     int best_bn = BN;
     int64_t best_cost = -1;
     // heights in whole 32-row TMA boxes: the B slot of a stage holds max_bn rows
@@ -1014,20 +1303,18 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     max_bn = max(max_bn, P.p[j].bn);
     if (is_glu(P.p[j].epi) || P.p[j].dual) max_two_a_bn = max(max_two_a_bn, P.p[j].bn);
   }
-  P.nacc = (max_two_a_bn > 128) ? 1 : 2;
+  // a pair CTA's accumulator is one buffer of the item's token columns: always two buffers
+  P.nacc = (max_two_a_bn > 128 && !pair) ? 1 : 2;
   P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
-  P.b_bytes = (int)cdiv(max_bn, B_BOX_ROWS) * B_BOX_BYTES;   // whole boxes, as the producer loads
-  const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
-  // transpose tiles sized for the widest output of the launch
+  // token rows of a stage's B slot (a pair CTA loads half of the 16-rounded tile), whole boxes
+  const int64_t b_rows = pair ? cdiv(max_bn, 16) * 8 : max_bn;
+  P.b_bytes = (int)cdiv(b_rows, B_BOX_ROWS) * B_BOX_BYTES;
+  const int stage_bytes = ((P.glu && !pair) ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
+  // transpose tiles sized for the widest output of the launch; in a pair SwiGLU launch the up
+  // warps' tiles carry a 16 x 32 fp32 chunk to the gate warps
   P.epi_tile = 16 * 32 * 2;
   for (int j = 0; j < n_probs; ++j)
-    if (P.p[j].epi == EPI_F32) P.epi_tile = EPI_TILE_MAX;
-  bool kc = false, bwd = false;
-  for (int j = 0; j < n_probs; ++j) {
-    kc = kc || P.p[j].kchunk > 0;
-    bwd = bwd || P.p[j].a_kmajor || P.p[j].epi == EPI_SWIGLU_SAVE || P.p[j].epi == EPI_SWIGLU_BWD;
-  }
-  if (kc && bwd) return cudaErrorNotSupported;
+    if (P.p[j].epi == EPI_F32 || (pair && is_glu(P.p[j].epi))) P.epi_tile = EPI_TILE_MAX;
   const int ew = P.fp8 ? Inst<true, false, false>::EW
                        : (kc ? Inst<false, true, false>::EW
                              : (bwd ? Inst<false, false, true>::EW : Inst<false, false, false>::EW));
@@ -1036,23 +1323,30 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   {
     const size_t fixed = 1024 + epi_bytes +
                          (size_t)(3 * ((P.grouped >= 0) ? P.p[P.grouped].G : 0) + 1) * 4;
-    const size_t budget = (size_t)MOE_TC_SMEM_BUDGET;
+    const size_t budget = pair ? (size_t)PAIR_SMEM_BUDGET : (size_t)MOE_TC_SMEM_BUDGET;
     int st = (int)((budget - fixed) / (size_t)stage_bytes);
     P.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
   }
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024 +
                       epi_bytes + (size_t)(3 * G + 1) * 4;
-  auto kern = P.fp8 ? tc_gemm_kernel<true, false, false>
-                    : (kc ? tc_gemm_kernel<false, true, false>
-                          : (bwd ? tc_gemm_kernel<false, false, true>
-                                 : tc_gemm_kernel<false, false, false>));
+  auto kern = pair ? tc_gemm_kernel<false, false, false, true>
+             : P.fp8 ? tc_gemm_kernel<true, false, false>
+                     : (kc ? tc_gemm_kernel<false, true, false>
+                           : (bwd ? tc_gemm_kernel<false, false, true>
+                                  : tc_gemm_kernel<false, false, false>));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (pair) {
+    int units = n_pairs;
+    if (P.grouped < 0) units = (int)imin64(units, base);
+    if (units < 1) return cudaSuccess;
+    return launch_pair(kern, dim3(2 * units), block, smem, stream, pdl, P);
+  }
   int grid = num_sms_tc();
   if (P.grouped < 0) grid = (int)imin64(grid, base);
   if (grid < 1) return cudaSuccess;
-  return launch(kern, dim3(grid), dim3(64 + 32 * ew), smem, stream, pdl, P);
+  return launch(kern, dim3(grid), block, smem, stream, pdl, P);
 }
 
 cudaError_t bounded_wait_selftest(void* dev_header, uint64_t limit_ns, cudaStream_t stream) {

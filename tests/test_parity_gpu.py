@@ -384,8 +384,9 @@ def test_swiglu_epilogue_wide_range(path):
     """The grouped GEMM's SwiGLU epilogue on its own, over gate pre-activations u1 in [-30, 30] and
     up pre-activations u3 in [-4, 4]: one-hot rows (row r is e_{r mod L}) make u1 = W1[r mod L, f]
     and u3 = W3[r mod L, f] exactly, so the stored hidden silu(u1) * u3 is compared element by
-    element with the oracle's fp64 value. Bar: the rounding to the stored type (bf16: 2^-9
-    relative) plus 2e-5 relative for the epilogue's own arithmetic; fp32 layer: 2e-6 relative."""
+    element with the oracle's fp64 value. Bar: the rounding to the stored type (bf16, with its
+    8-bit significand: at most 2^-8 relative) plus 2e-5 relative for the epilogue's own
+    arithmetic; fp32 layer: 2e-6 relative."""
     R, L, F, E = 300, 128, 256, 64
     dt = torch.float32 if path == "f32" else torch.bfloat16
     cfg = m.LayerConfig(T=R, d_model=L, d_latent=L, n_experts=E, top_k=1, d_ff=F, n_shared=0,
@@ -411,7 +412,7 @@ def test_swiglu_epilogue_wide_range(path):
     ref = moe_oracle.swiglu_hidden(rows[:R].double(), w1[0].double(), w3[0].double())
     u1 = w1[0].double()[torch.arange(R) % L]
     assert float(u1.min()) <= -29.9 and float(u1.max()) >= 29.9
-    rel = 2e-6 if path == "f32" else 2.0 ** -9 + 2e-5
+    rel = 2e-6 if path == "f32" else 2.0 ** -8 + 2e-5
     err = (hid - ref).abs() - rel * ref.abs()
     worst = int(err.flatten().argmax())
     assert float(err.max()) <= 1e-30, (path, float(hid.flatten()[worst]), float(ref.flatten()[worst]),
