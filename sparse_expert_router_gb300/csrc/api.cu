@@ -1,5 +1,6 @@
 // The C ABI: argument validation, workspace layout and the stage sequence of the layer.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "backward.h"
@@ -33,9 +34,22 @@ int64_t pool_rows_of(const moe_config_t& c) {
 
 size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Token tiles of the back GEMM (at least 128 rows each) whose combined rows a fused combine counts.
+int64_t ready_tiles(int64_t T) { return (T + 127) / 128; }
+
+// The combine runs inside the back GEMM's launch (the shared experts' K segment first, while the
+// epilogue warps combine) unless MOE_FUSED_COMBINE=0 is set in the environment.
+bool fused_combine_enabled() {
+  static const int on = [] {
+    const char* e = getenv("MOE_FUSED_COMBINE");
+    return (e && e[0] == '0') ? 0 : 1;
+  }();
+  return on != 0;
+}
+
 struct Layout {
   size_t hdr, logits, wrT, wnorm, xnorm, rlist, elist, rsaved, idx, gate, z, chist, cbase, counts,
-      offsets, ndrop, slot_of, perm, x_perm, hid, y_perm, a_s, c, total;
+      offsets, ndrop, slot_of, perm, x_perm, hid, y_perm, a_s, c, cready, total;
 };
 
 Layout make_layout(const moe_config_t& c) {
@@ -73,6 +87,7 @@ Layout make_layout(const moe_config_t& c) {
   L.y_perm = take(P * Lt * es);
   L.a_s = take(T * (SF > 0 ? SF : 1) * es);
   L.c = take(T * Lt * es);
+  L.cready = take(ready_tiles(T) * 4);
   L.total = off;
   return L;
 }
@@ -369,6 +384,33 @@ GemmProblem expert_down_problem(const Call& k, const int32_t* offsets, const voi
   p.out = y_perm;
   p.ld_out = k.c.d_latent;
   p.dtype = k.c.dtype;
+  return p;
+}
+
+// The back GEMM with the combine inside its launch: the shared experts' segment first, then
+// the combine's, whose rows the launch's epilogue warps write into c_buf before they drain any
+// accumulator (the tensor cores run the first segment meanwhile).
+GemmProblem back_problem_fused(const Call& k, void* c_buf, const void* w_up, const void* a_s,
+                               const void* w2_s, void* y, const void* y_perm,
+                               const int32_t* slot_of, const float* gate, uint32_t* ready) {
+  GemmProblem p;
+  p.epi = EPI_STORE;
+  p.group = GROUP_NONE;
+  p.M = k.c.d_model;
+  p.seg[0] = {a_s, w2_s, nullptr, k.c.n_shared * k.c.d_ff_shared};
+  p.seg[1] = {c_buf, w_up, nullptr, k.c.d_latent};
+  p.n_seg = 2;
+  p.rows = k.c.T;
+  p.out = y;
+  p.ld_out = k.c.d_model;
+  p.dtype = k.c.dtype;
+  p.cmb_seg = 1;
+  p.cmb_y_perm = y_perm;
+  p.cmb_slot = slot_of;
+  p.cmb_gate = gate;
+  p.cmb_k = k.c.top_k;
+  p.cmb_pool_rows = pool_rows_of(k.c);
+  p.cmb_ready = ready;
   return p;
 }
 
@@ -1011,6 +1053,16 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int3
     return MOE_OK;
   }
   if (cfg->n_shared > 0 && (!a_shared || !w2_s)) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && k.tc && fused_combine_enabled()) {
+    // the combine inside the up-projection's launch
+    uint32_t* ready = k.at<uint32_t>(k.L.cready);
+    GemmProblem p = back_problem_fused(k, k.at<void>(k.L.c), w_up, a_shared, w2_s, out, y_perm,
+                                       slot_of, topk_gate, ready);
+    if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
+    MOE_TRY_CUDA(cudaMemsetAsync(ready, 0, (size_t)ready_tiles(cfg->T) * 4, k.st));
+    MOE_TRY_CUDA(run_gemms(k, &p, 1));
+    return MOE_OK;
+  }
   GemmProblem p = back_problem(k, k.at<void>(k.L.c), w_up, a_shared, w2_s, out);
   if ((s = check_tc(k, &p, 1)) != MOE_OK) return s;
   CombineArgs ca = combine_args(k, y_perm, slot_of, topk_gate, k.at<void>(k.L.c));
@@ -1053,8 +1105,13 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   if (shared) front[n_front++] = shared_problem(k, x, w->w1_s, w->w3_s, a_s);
   GemmProblem up = expert_up_problem(k, k.at<void>(L.x_perm), offsets, w->w1, w->w3, w->fp8);
   GemmProblem down = expert_down_problem(k, offsets, w->w2, k.at<void>(L.y_perm), w->fp8);
-  GemmProblem back = back_problem(k, k.at<void>(L.c), w->w_up, shared ? a_s : nullptr,
-                                  shared ? w->w2_s : nullptr, y);
+  // the combine inside the back GEMM's launch (tensor-core layers with shared experts)
+  const bool fuse = shared && k.tc && fused_combine_enabled();
+  uint32_t* ready = k.at<uint32_t>(L.cready);
+  GemmProblem back = fuse ? back_problem_fused(k, k.at<void>(L.c), w->w_up, a_s, w->w2_s, y,
+                                               k.at<void>(L.y_perm), slot_of, gate, ready)
+                          : back_problem(k, k.at<void>(L.c), w->w_up, shared ? a_s : nullptr,
+                                         shared ? w->w2_s : nullptr, y);
   if ((s = check_tc(k, front, n_front)) != MOE_OK) return s;
   if ((s = check_tc(k, &up, 1)) != MOE_OK) return s;
   if ((s = check_tc(k, &down, 1)) != MOE_OK) return s;
@@ -1069,7 +1126,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
 
   record(aux, 0, k.st);
   const bool f8 = fp8_experts(*cfg);
-  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false, f8 ? 3 : 0));
+  MOE_TRY_CUDA(header_reset(k.hdr(), true, k.st, false, f8 ? 3 : 0, fuse ? ready : nullptr,
+                            fuse ? (int)ready_tiles(cfg->T) : 0));
   MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
   record(aux, 1, k.st);
   MOE_TRY_CUDA(run_gemms(k, front, n_front));
@@ -1082,7 +1140,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   record(aux, 5, k.st);
   MOE_TRY_CUDA(run_gemms(k, &down, 1));
   record(aux, 6, k.st);
-  MOE_TRY_CUDA(combine_run(ca, cfg->dtype, k.st, k.pdl));
+  if (!fuse) MOE_TRY_CUDA(combine_run(ca, cfg->dtype, k.st, k.pdl));
   record(aux, 7, k.st);
   MOE_TRY_CUDA(run_gemms(k, &back, 1));
   record(aux, 8, k.st);

@@ -25,7 +25,8 @@ namespace {
 constexpr int CH = 32;
 constexpr int HIST_WARPS = 4;   // chunks per histogram block
 
-__global__ void header_reset_kernel(DeviceHeader* h, int clear_status, int amax_mask) {
+__global__ void header_reset_kernel(DeviceHeader* h, int clear_status, int amax_mask,
+                                    uint32_t* zero, int n_zero) {
   pdl_wait();
   if (threadIdx.x == 0) {
     if (clear_status) { h->status = 0; h->detail = 0; }
@@ -34,6 +35,7 @@ __global__ void header_reset_kernel(DeviceHeader* h, int clear_status, int amax_
     if (amax_mask & 1) h->amax_x = 0;
     if (amax_mask & 2) h->amax_h = 0;
   }
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0u;
 }
 
 // An assignment (t, j) is valid when its expert id is in range and the token's ids ascend.
@@ -307,9 +309,9 @@ __global__ void validate_offsets_kernel(const int32_t* off, int G, int64_t rows,
 }  // namespace
 
 cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl,
-                         int amax_mask) {
-  return launch(header_reset_kernel, dim3(1), dim3(32), 0, st, pdl, h, clear_status ? 1 : 0,
-                amax_mask);
+                         int amax_mask, uint32_t* zero, int n_zero) {
+  return launch(header_reset_kernel, dim3(1), dim3(256), 0, st, pdl, h, clear_status ? 1 : 0,
+                amax_mask, zero, n_zero);
 }
 
 int64_t dispatch_chunks(int64_t T) { return cdiv(T, CH); }

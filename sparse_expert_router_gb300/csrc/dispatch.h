@@ -44,9 +44,9 @@ struct CombineArgs {
 };
 
 // Zeroes the router counters, and the status (clear_status) and the amax fields named by
-// amax_mask (bit 0: amax_x, bit 1: amax_h).
+// amax_mask (bit 0: amax_x, bit 1: amax_h), and n_zero words at `zero`.
 cudaError_t header_reset(DeviceHeader* h, bool clear_status, cudaStream_t st, bool pdl,
-                         int amax_mask = 0);
+                         int amax_mask = 0, uint32_t* zero = nullptr, int n_zero = 0);
 int64_t dispatch_chunks(int64_t T);
 cudaError_t dispatch_run(const DispatchArgs& a, int dtype, cudaStream_t st, bool pdl);
 cudaError_t combine_run(const CombineArgs& a, int dtype, cudaStream_t st, bool pdl);

@@ -73,6 +73,18 @@ struct GemmProblem {
   const void* aux_g = nullptr;
   const void* aux_u = nullptr;
   int64_t ld_aux = 0;
+  // tcgen05 only, one dense bf16 problem per launch: segment cmb_seg's activations (bf16
+  // [rows, K]) are the gate-weighted combine c[t] = sum over kept j, in order, of
+  // gate[t, j] * y_perm[slot_of[t, j]], computed in the same launch by the epilogue warps before
+  // they drain any accumulator. A token tile of that segment is loaded only after
+  // cmb_ready[tile] (zeroed before the launch, [ceil(rows / 128)]) counts all of its rows.
+  int cmb_seg = -1;
+  const void* cmb_y_perm = nullptr;
+  const int32_t* cmb_slot = nullptr;
+  const float* cmb_gate = nullptr;
+  int cmb_k = 0;
+  int64_t cmb_pool_rows = 0;
+  uint32_t* cmb_ready = nullptr;
 };
 
 // CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).

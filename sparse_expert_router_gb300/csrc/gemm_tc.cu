@@ -118,8 +118,24 @@ struct TcProblem {
   int64_t n_items;             // dense: m_tiles * n_tiles (grouped: filled on device)
 };
 
+// The combine computed inside a dense launch (GemmProblem::cmb_*).
+struct TcCombine {
+  int active;
+  int seg;                     // segment of problem 0 whose activations are c
+  const bf16* y_perm;          // [pool_rows, L]
+  const int32_t* slot;         // [T, k]
+  const float* gate;           // [T, k]
+  bf16* c;                     // [T, L]
+  int64_t T;
+  int k, L;
+  int64_t pool_rows;
+  uint32_t* ready;             // rows of c written, per token tile
+  int bn;                      // token rows per tile of the launch
+};
+
 struct TcParams {
   TcProblem p[MAX_PROBS];
+  TcCombine cmb;
   int n_probs;
   int grouped;                 // index of the grouped problem (always the last) or -1
   int glu;                     // any problem uses two A tiles per stage (SwiGLU or dual)
@@ -201,6 +217,103 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
     it.nrows = (int)imin64(q.bn, q.rows - it.row0);
   }
   return it;
+}
+
+// ---- the combine of a dense launch -------------------------------------------------------
+
+// c rows of this CTA's share of the tokens: each of the launch's epilogue warps takes one token
+// at a time. Every element is sum over the token's kept assignments, in order j = 0..k-1, of
+// fmaf(gate, y_perm value, acc) in fp32, rounded once to bf16, with the loads of up to four rows
+// in flight: the same arithmetic as the separate combine kernel, so c is bitwise the same. After
+// a token's row is written, lane 0 counts it in its tile's ready counter (release).
+__device__ void combine_rows(const TcCombine& C, int w, int n_w, int lane, DeviceHeader* hdr) {
+  const int64_t per = cdiv(C.T, (int64_t)gridDim.x);
+  const int64_t t0 = (int64_t)blockIdx.x * per, t1 = imin64(C.T, t0 + per);
+  for (int64_t t = t0 + w; t < t1; t += n_w) {
+    int32_t s = -1;
+    float g = 0.0f;
+    if (lane < C.k) {
+      s = C.slot[t * C.k + lane];
+      g = C.gate[t * C.k + lane];
+      if (s >= C.pool_rows || s < -1) {
+        report_error(hdr, MOE_ERR_BAD_ROUTING, (int)t);
+        s = -1;
+      }
+    }
+    const unsigned kept = __ballot_sync(~0u, s >= 0);
+    // every lane runs every iteration (the shuffles below take the whole warp); lanes past the
+    // row's end only skip their loads and stores
+    for (int i0 = 0; i0 < C.L; i0 += 256) {
+      const int i = i0 + lane * 8;
+      const bool on = i < C.L;
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      unsigned m = kept;
+      while (m) {
+        int js[4];
+        int nn = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (m) {
+            js[u] = __ffs(m) - 1;
+            m &= m - 1;
+            ++nn;
+          }
+        }
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (u < nn) {
+            const int32_t sj = __shfl_sync(~0u, s, js[u]);
+            if (on) ld8(C.y_perm + (int64_t)sj * C.L + i, v[u]);
+            else
+#pragma unroll
+              for (int q = 0; q < 8; ++q) v[u][q] = 0.0f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (u < nn) {
+            const float gj = __shfl_sync(~0u, g, js[u]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(gj, v[u][q], acc[q]);
+          }
+        }
+      }
+      if (on) st8(C.c + t * C.L + i, acc);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(C.ready + t / C.bn, 1u);
+    }
+  }
+}
+
+// Waits (bounded) until the combine has written all `rows` rows of token tile `tile`; then orders
+// the TMA loads that follow after those writes. False when the kernel is aborting.
+__device__ bool wait_combined(const TcCombine& C, int64_t tile, int rows, volatile int* abort_flag,
+                              DeviceHeader* hdr) {
+  const uint32_t* p = C.ready + tile;
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= (uint32_t)rows) break;
+    if (*abort_flag) return false;
+    __nanosleep(64);
+    if ((i & 63u) == 63u) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TIMEOUT_NS) {
+        report_error(hdr, MOE_ERR_DEVICE_TIMEOUT, 7);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
@@ -368,6 +481,11 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
       const int mx0 = it.m_w + (gl ? 64 : BM) * (int)rank;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
+        if (P.cmb.active && s == P.cmb.seg &&
+            !wait_combined(P.cmb, it.row0 / P.cmb.bn, it.nrows, &s_abort, P.hdr)) {
+          ok = false;
+          break;
+        }
         for (int kb = 0; kb < sg.kblocks; ++kb) {
           const int k0 = kb * BK;
           if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
@@ -397,6 +515,11 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
       const uint32_t bytes = (two_a ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
+        if (P.cmb.active && s == P.cmb.seg &&
+            !wait_combined(P.cmb, it.row0 / P.cmb.bn, it.nrows, &s_abort, P.hdr)) {
+          ok = false;
+          break;
+        }
         for (int kb = 0; kb < sg.kblocks; ++kb) {
           const int k0 = kb * bk;
           if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
@@ -582,6 +705,9 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
     int ev = 0;
     float amax = 0.0f;                                   // fp8 output: this thread's max |value|
     uint32_t xc = 0;                                     // pair SwiGLU: chunks exchanged so far
+    if constexpr (!FP8 && !KC && !BWD) {
+      if (P.cmb.active) combine_rows(P.cmb, warp - 2, EPI_WARPS, lane, P.hdr);
+    }
     // pair launches: the epilogue threads of both CTAs release rank 0's accumulator buffer
     auto release = [&](int b) {
       tc_fence_before();
@@ -1057,17 +1183,23 @@ int num_sms_tc() {
   return n > 0 ? n : 148;
 }
 
-// Which launches use CTA pairs: MOE_TC_PAIR in the environment selects none ("0", the default),
-// launches with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1");
-// no launch uses them once a query finds that no pair fits on the GPU.
-enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3 };
+// Which launches use CTA pairs. By default ("auto") only the dual launches where pairs measured
+// faster on GB300: the grouped GEMM 2 with at most two 256-row token tiles per expert on average
+// (the 535B layer at T=8192: 1.29 -> 1.26 ms; T=4096 small layer: 0.097 -> 0.088 ms) and dense
+// launches of at least 32K rows (the back GEMM at T=65536: 6.4 -> 5.6 ms). SwiGLU items, whose
+// pair CTAs each stack 64 gate and 64 up features, measured slower at every size (their main loop
+// alone: 2.18 -> 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
+// with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1"); no launch
+// uses them once a query finds that no pair fits on the GPU.
+enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3, PAIR_AUTO = 4 };
 std::atomic<int> g_pair_mode{-1};
 int pair_mode() {
   int m = g_pair_mode.load(std::memory_order_relaxed);
   if (m < 0) {
     const char* e = getenv("MOE_TC_PAIR");
-    m = PAIR_NONE;
-    if (e && !strcmp(e, "1")) m = PAIR_ALL;
+    m = PAIR_AUTO;
+    if (e && !strcmp(e, "0")) m = PAIR_NONE;
+    else if (e && !strcmp(e, "1")) m = PAIR_ALL;
     else if (e && !strcmp(e, "dual")) m = PAIR_DUAL;
     else if (e && !strcmp(e, "glu")) m = PAIR_GLU;
     g_pair_mode.store(m, std::memory_order_relaxed);
@@ -1161,6 +1293,12 @@ bool gemm_tc_supported(const GemmProblem& p) {
   if (p.out_fp8 && (!p.w_fp8 || p.epi != EPI_SWIGLU || !p.out_scale || (p.M % 16) ||
                     (p.ld_out % 16) || (p.out_col0 % 16)))
     return false;
+  if (p.cmb_seg >= 0) {   // a combine inside the launch: dense bf16, c written in place of act
+    if (p.cmb_seg >= p.n_seg || p.group != GROUP_NONE || p.w_fp8 || p.a_kmajor || p.kchunk ||
+        !p.cmb_y_perm || !p.cmb_slot || !p.cmb_gate || !p.cmb_ready || p.cmb_k < 1 ||
+        p.cmb_k > 32 || p.seg[p.cmb_seg].ld || (p.seg[p.cmb_seg].K % 8))
+      return false;
+  }
   return true;
 }
 
@@ -1250,6 +1388,23 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     if (is_glu(g.epi) || q.dual) P.glu = 1;
   }
   P.n_probs = n_probs;
+  bool any_cmb = false;
+  for (int j = 0; j < n_probs; ++j) any_cmb = any_cmb || probs[j].cmb_seg >= 0;
+  if (any_cmb) {
+    if (n_probs != 1) return cudaErrorNotSupported;   // the combine needs the launch to itself
+    const GemmProblem& g = probs[0];
+    P.cmb.active = 1;
+    P.cmb.seg = g.cmb_seg;
+    P.cmb.y_perm = static_cast<const bf16*>(g.cmb_y_perm);
+    P.cmb.slot = g.cmb_slot;
+    P.cmb.gate = g.cmb_gate;
+    P.cmb.c = static_cast<bf16*>(const_cast<void*>(g.seg[g.cmb_seg].act));
+    P.cmb.T = g.rows;
+    P.cmb.k = g.cmb_k;
+    P.cmb.L = g.seg[g.cmb_seg].K;
+    P.cmb.pool_rows = g.cmb_pool_rows;
+    P.cmb.ready = g.cmb_ready;
+  }
   bool kc = false, bwd = false;
   for (int j = 0; j < n_probs; ++j) {
     kc = kc || P.p[j].kchunk > 0;
@@ -1264,6 +1419,9 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     pair = pair && (is_glu(q.epi) || q.dual) &&
            (q.epi == EPI_SWIGLU || q.epi == EPI_STORE || q.epi == EPI_F32) &&
            !(pmode == PAIR_DUAL && is_glu(q.epi)) && !(pmode == PAIR_GLU && q.dual);
+    if (pmode == PAIR_AUTO)
+      pair = pair && q.dual &&
+             (q.group == GROUP_ROWS ? q.rows <= (int64_t)2 * BN * q.G : q.rows >= 32768);
   }
   const dim3 block(64 + 32 * (P.fp8 ? Inst<true, false, false>::EW
                                     : (kc ? Inst<false, true, false>::EW
@@ -1298,6 +1456,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       base += q.n_items;
     }
   }
+  if (P.cmb.active) P.cmb.bn = P.p[0].bn;
   int max_bn = 0, max_two_a_bn = 0;
   for (int j = 0; j < n_probs; ++j) {
     max_bn = max(max_bn, P.p[j].bn);

@@ -19,6 +19,30 @@ pytestmark = pytest.mark.gpu
 # the bf16 GEMM paths under test: tensor cores (default), tensor cores with programmatic
 # dependent launch (the bench configuration) and the CUDA-core cross-check
 BF16_PATHS = {"tc": 0, "tc_pdl": m.MOE_FLAG_PDL, "simt": m.MOE_FLAG_SIMT}
+def _check_combine(shape, cfg, got):
+    """The combine c the forward left in its workspace (computed inside the back GEMM's launch
+    for tensor-core layers with shared experts) against the separate combine kernel on the same
+    y_perm, slots and gates (moe_combine without an up-projection), bit for bit, and against the
+    oracle's combine of those rows in fp64 (bf16 rounding of c: at most 2^-8 per element)."""
+    T, L = shape.T, shape.d_latent
+    P = T * shape.top_k
+    ws = got["ws"]
+    c = m.workspace_view(ws, cfg, "combined", torch.bfloat16, (T, L)).clone()
+    yp = m.workspace_view(ws, cfg, "y_perm", torch.bfloat16, (P, L))
+    gate = got["topk_gate"]
+    sep = torch.empty((T, L), dtype=torch.bfloat16, device=DEV)
+    m.moe_combine(cfg, yp, got["slot_of"], gate, sep, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16), sep.view(torch.int16))
+    toks = sample_tokens(T, 64)
+    slots = got["slot_of"].cpu().long()[toks]                  # [64, k], -1 = dropped
+    rows = yp[slots.clamp(min=0).flatten().to(DEV)]            # the rows those slots name
+    local = torch.where(slots >= 0, torch.arange(slots.numel()).view(slots.shape), -1)
+    ref = moe_oracle.combine(rows, local, gate.cpu()[toks])
+    err = (c[toks].double().cpu() - ref).abs() - 2.0 ** -8 * ref.abs()
+    assert float(err.max()) <= 1e-6, float(err.max())
+
+
 # The bench configuration runs with programmatic dependent launch on (MOE_FLAG_PDL); the
 # full-size and edge-case forwards run both with and without it.
 PDL_FLAGS = {"nopdl": 0, "pdl": m.MOE_FLAG_PDL}
@@ -54,6 +78,8 @@ def test_small_bf16_forward(path):
     shape = SHAPES["small_bf16"]
     inp = gpu_inputs(shape)
     got = run_forward(shape, inp, BF16_PATHS[path])
+    if path != "simt":
+        _check_combine(shape, m.LayerConfig.from_shape(shape, flags=BF16_PATHS[path]), got)
     toks = sample_tokens(shape.T, 256)
     ref = oracle_forward(shape, {k: v.cpu() for k, v in inp.items()}, tokens=toks)
     check_routing(got, ref, shape)
@@ -375,6 +401,7 @@ def test_large_layer(name):
     cfg = m.LayerConfig.from_shape(shape, flags=PDL_FLAGS["pdl"])
     n_rows = _check_expert_rows(shape, inp, cfg, got["ws"], got["expert_offsets"].cpu(), name)
     assert n_rows > 0
+    _check_combine(shape, cfg, got)
     del inp, got, runs
     torch.cuda.empty_cache()
 
