@@ -38,7 +38,9 @@ def launches_per_forward(shape, simt: bool) -> int:
     back GEMM (one launch when the combine runs inside the tensor-core back GEMM)."""
     tc = shape.dtype == "bf16" and not simt
     front = 1 if tc else 2 + (1 if shape.n_shared > 0 else 0)
-    fused = tc and shape.n_shared > 0 and os.environ.get("MOE_FUSED_COMBINE", "1") != "0"
+    env = os.environ.get("MOE_FUSED_COMBINE")
+    rows_bytes = shape.T * shape.top_k * shape.d_latent * 2
+    fused = tc and shape.n_shared > 0 and (rows_bytes <= (96 << 20) if env is None else env != "0")
     return 1 + 2 + front + 3 + 3 + 2 + (1 if fused else 2)
 METRIC = "MoE-layer tokens/s"
 

@@ -37,14 +37,21 @@ size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 // Token tiles of the back GEMM (at least 128 rows each) whose combined rows a fused combine counts.
 int64_t ready_tiles(int64_t T) { return (T + 127) / 128; }
 
-// The combine runs inside the back GEMM's launch (the shared experts' K segment first, while the
-// epilogue warps combine) unless MOE_FUSED_COMBINE=0 is set in the environment.
-bool fused_combine_enabled() {
-  static const int on = [] {
+// Whether the combine runs inside the back GEMM's launch (the shared experts' K segment first,
+// while the launch's epilogue warps combine). There the combine is latency-bound: twelve warps per
+// SM gather y_perm. It pays only while y_perm, just written by expert GEMM 2, is still in L2 (the
+// small bf16 layer, 67 MB of rows: 0.091 -> 0.079 ms for combine and up-projection); with rows
+// from HBM the separate combine kernel, spread over one block per token, is faster (the 535B layer
+// at T=8192, 403 MB: 0.735 -> 0.826 ms). MOE_FUSED_COMBINE in the environment forces it on ("1")
+// or off ("0").
+bool fused_combine_enabled(const moe_config_t& c) {
+  static const int mode = [] {
     const char* e = getenv("MOE_FUSED_COMBINE");
-    return (e && e[0] == '0') ? 0 : 1;
+    return !e ? -1 : (e[0] == '0' ? 0 : 1);
   }();
-  return on != 0;
+  if (mode >= 0) return mode == 1;
+  const int64_t es = (c.dtype == MOE_BF16) ? 2 : 4;
+  return pool_rows_of(c) * (int64_t)c.d_latent * es <= ((int64_t)96 << 20);
 }
 
 struct Layout {
@@ -1053,7 +1060,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int3
     return MOE_OK;
   }
   if (cfg->n_shared > 0 && (!a_shared || !w2_s)) return MOE_ERR_INVALID_ARG;
-  if (cfg->n_shared > 0 && k.tc && fused_combine_enabled()) {
+  if (cfg->n_shared > 0 && k.tc && fused_combine_enabled(*cfg)) {
     // the combine inside the up-projection's launch
     uint32_t* ready = k.at<uint32_t>(k.L.cready);
     GemmProblem p = back_problem_fused(k, k.at<void>(k.L.c), w_up, a_shared, w2_s, out, y_perm,
@@ -1106,7 +1113,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
   GemmProblem up = expert_up_problem(k, k.at<void>(L.x_perm), offsets, w->w1, w->w3, w->fp8);
   GemmProblem down = expert_down_problem(k, offsets, w->w2, k.at<void>(L.y_perm), w->fp8);
   // the combine inside the back GEMM's launch (tensor-core layers with shared experts)
-  const bool fuse = shared && k.tc && fused_combine_enabled();
+  const bool fuse = shared && k.tc && fused_combine_enabled(*cfg);
   uint32_t* ready = k.at<uint32_t>(L.cready);
   GemmProblem back = fuse ? back_problem_fused(k, k.at<void>(L.c), w->w_up, a_s, w->w2_s, y,
                                                k.at<void>(L.y_perm), slot_of, gate, ready)

@@ -1184,11 +1184,12 @@ int num_sms_tc() {
 }
 
 // Which launches use CTA pairs. By default ("auto") only the dual launches where pairs measured
-// faster on GB300: the grouped GEMM 2 with at most two 256-row token tiles per expert on average
-// (the 535B layer at T=8192: 1.29 -> 1.26 ms; T=4096 small layer: 0.097 -> 0.088 ms) and dense
-// launches of at least 32K rows (the back GEMM at T=65536: 6.4 -> 5.6 ms). SwiGLU items, whose
-// pair CTAs each stack 64 gate and 64 up features, measured slower at every size (their main loop
-// alone: 2.18 -> 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
+// faster on GB300: the grouped GEMM 2 with at most one 256-row token tile per expert on average
+// (the 535B layer at T=8192: 1.29 -> 1.26 ms; with Zipf-skewed routing at T=16384, whose hot
+// experts fill many full tiles, pairs were slower: 2.19 -> 2.37 ms) and dense launches of at
+// least 32K rows (the back GEMM at T=65536: 6.4 -> 5.9 ms). SwiGLU items, whose pair CTAs each
+// stack 64 gate and 64 up features, measured slower at every size (their main loop alone: 2.18 ->
+// 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
 // with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1"); no launch
 // uses them once a query finds that no pair fits on the GPU.
 enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3, PAIR_AUTO = 4 };
@@ -1421,7 +1422,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
            !(pmode == PAIR_DUAL && is_glu(q.epi)) && !(pmode == PAIR_GLU && q.dual);
     if (pmode == PAIR_AUTO)
       pair = pair && q.dual &&
-             (q.group == GROUP_ROWS ? q.rows <= (int64_t)2 * BN * q.G : q.rows >= 32768);
+             (q.group == GROUP_ROWS ? q.rows <= (int64_t)BN * q.G : q.rows >= 32768);
   }
   const dim3 block(64 + 32 * (P.fp8 ? Inst<true, false, false>::EW
                                     : (kc ? Inst<false, true, false>::EW
