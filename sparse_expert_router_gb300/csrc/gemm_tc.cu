@@ -66,7 +66,7 @@ constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte ro
 // quadrant take alternate 16-token chunks. Keeping the instances apart keeps each one's
 // registers within what its warp count allows (three or four warps share one sub-partition's
 // 16K registers).
-template <bool FP8, bool KC, bool BWD, bool PAIR = false> struct Inst {
+template <bool FP8, bool KC, bool BWD> struct Inst {
   static constexpr int EW = KC ? 8 : MOE_TC_EPI_WARPS;
 };
 constexpr int EPI_TILE_MAX = 16 * 32 * 4;   // transpose tile of one warp: 16 tokens x 32 fp32
@@ -321,33 +321,27 @@ __device__ bool wait_combined(const TcCombine& C, int64_t tile, int rows, volati
 // Two instances: FP8 = false (bf16 operands, k-chunked fp32 problems) and FP8 = true (E4M3
 // operands, scales and the E4M3 SwiGLU output), so that neither carries the other's registers:
 // with 10 warps per CTA three warps share one sub-partition's 16K registers, 168 per thread.
-// PAIR: a cluster of two CTAs runs each item with tcgen05.mma.cta_group::2 (M = 256: 128 weight
-// rows from each CTA; each CTA loads half of the token tile). Every item of a pair launch has two
-// weight tiles: a dual item's 256 features split 128 + 128 between the CTAs; a SwiGLU item's
-// 128 output features split 64 + 64, each CTA stacking the gate (W1) and up (W3) tiles of its 64
-// features into one 128-row A tile. Each CTA's accumulator is then one N-column buffer, so two
-// buffers fit in tensor memory and the epilogue of one item overlaps the MMAs of the next.
-template <bool FP8, bool KC, bool BWD, bool PAIR = false>
-__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
+// Two instances: FP8 = false (bf16 operands, k-chunked fp32 problems) and FP8 = true (E4M3
+// operands, scales and the E4M3 SwiGLU output), so that neither carries the other's registers:
+// with 10 warps per CTA three warps share one sub-partition's 16K registers, 168 per thread.
+// CMB: the launch's epilogue warps first compute the combine that one segment's activations are
+// (TcCombine), and the producer loads a token tile of that segment once its rows are written;
+// an instance of its own, so that the other launches carry none of that code.
+template <bool FP8, bool KC, bool BWD, bool CMB = false>
+__global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams P) {
-  constexpr int EPI_WARPS = Inst<FP8, KC, BWD, PAIR>::EW;
-  static_assert(!PAIR || (!FP8 && !KC && !BWD), "pair launches: bf16 forward problems");
-  constexpr int XPAIRS = EPI_WARPS / 2;          // gate/up warp pairs of a pair SwiGLU epilogue
-  constexpr int XB0 = 2 * 8 + 4;                 // first exchange barrier
+  constexpr int EPI_WARPS = Inst<FP8, KC, BWD>::EW;
+  static_assert(!CMB || (!FP8 && !KC && !BWD), "combine launches: bf16 dense problems");
   const int EPI_STAGE_BYTES = P.epi_tile;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * 8 + 4 + 2 * XPAIRS];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
   __shared__ int64_t s_total;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int stages = P.stages;
-  const bool glu = P.glu != 0 && !PAIR;     // two A tiles per stage (a pair CTA holds one)
-  // pair launches: this CTA's rank in its pair, the pair's index and the number of pairs
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int64_t unit = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
-  const int64_t n_units = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+  const bool glu = P.glu != 0;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int stage_bytes = (glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
@@ -385,33 +379,22 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tmem_full(b), 1);
-      // pair launches: rank 0's barrier, released by the epilogue threads of both CTAs
-      mbar_init(tmem_empty(b), (PAIR ? 2 : 1) * 32 * EPI_WARPS);
+      mbar_init(tmem_empty(b), 32 * EPI_WARPS);
     }
-    if (PAIR)
-      for (int i = 0; i < 2 * XPAIRS; ++i) mbar_init(smem_u32(&bars[XB0 + i]), 32);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int p = 0; p < P.n_probs; ++p)
       for (int s = 0; s < P.p[p].n_seg; ++s) {
         prefetch_map(&P.p[p].seg[s].a1);
         prefetch_map(&P.p[p].seg[s].b);
-        if (P.glu) prefetch_map(&P.p[p].seg[s].a3);
+        if (glu) prefetch_map(&P.p[p].seg[s].a3);
       }
   }
   if (warp == 1) {
-    if constexpr (PAIR) {
-      // one warp of each CTA of the pair allocates, collectively, the same columns in both
-      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                       smem_u32(&s_tmem))
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                       smem_u32(&s_tmem))
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
   // Every thread waits for the preceding kernel before it reads the group offsets.
@@ -456,52 +439,11 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // pair launches: both CTAs' barriers are initialised before either signals the other's
-  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
   const int64_t total = s_total;
 
-  if (PAIR && warp == 0 && lane == 0) {
-    // ---------------- TMA producer of a pair CTA ----------------
-    // Loads this CTA's 128 weight rows and its half (N / 2 rows) of the token tile; the bytes of
-    // both CTAs complete on rank 0's full barrier, which rank 0 arms with their sum.
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int64_t w = unit; w < total && ok; w += n_units) {
-      Item it = decode(P, S, w);
-      const TcProblem& q = P.p[it.p];
-      const int half_rows = ((it.nrows + 15) / 16) * 8;
-      const int nb = (half_rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
-      const uint32_t bytes = 2u * (uint32_t)(A_BYTES + nb * B_BOX_BYTES);
-      const int64_t my_row0 = it.row0 + (int64_t)rank * half_rows;
-      const bool gl = is_glu(q.epi);
-      // SwiGLU: gate and up tiles of features m_w + 64 rank ..; dual: features m_w + 128 rank ..
-      const int mx0 = it.m_w + (gl ? 64 : BM) * (int)rank;
-      for (int s = 0; s < q.n_seg && ok; ++s) {
-        const TcSeg& sg = q.seg[s];
-        if (P.cmb.active && s == P.cmb.seg &&
-            !wait_combined(P.cmb, it.row0 / P.cmb.bn, it.nrows, &s_abort, P.hdr)) {
-          ok = false;
-          break;
-        }
-        for (int kb = 0; kb < sg.kblocks; ++kb) {
-          const int k0 = kb * BK;
-          if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
-          const uint32_t fb = mapa_shared(full(stage), 0);
-          if (rank == 0) mbar_expect_tx(full(stage), bytes);
-          tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx0, k0, it.wg);
-          tma_load_3d_pair(smem_u32(sA1(stage)) + A_HALF, gl ? &sg.a3 : &sg.a1, fb,
-                           gl ? mx0 : mx0 + 64, k0, it.wg);
-          for (int b = 0; b < nb; ++b)
-            tma_load_2d_pair(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, fb, k0,
-                             (int)(my_row0 + b * B_BOX_ROWS));
-          if (++stage == stages) { stage = 0; phase ^= 1u; }
-        }
-      }
-    }
-  } else if (!PAIR && warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
@@ -515,10 +457,12 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
       const uint32_t bytes = (two_a ? 2 * A_BYTES : A_BYTES) + nb * B_BOX_BYTES;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
-        if (P.cmb.active && s == P.cmb.seg &&
-            !wait_combined(P.cmb, it.row0 / P.cmb.bn, it.nrows, &s_abort, P.hdr)) {
-          ok = false;
-          break;
+        if constexpr (CMB) {
+          if (s == P.cmb.seg &&
+              !wait_combined(P.cmb, it.row0 / P.cmb.bn, it.nrows, &s_abort, P.hdr)) {
+            ok = false;
+            break;
+          }
         }
         for (int kb = 0; kb < sg.kblocks; ++kb) {
           const int k0 = kb * bk;
@@ -557,20 +501,19 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
         }
       }
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
-    // ---------------- MMA issuer (in a pair, rank 0 issues for both CTAs) ----------------
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     int ev = 0;      // accumulator events of this CTA: one per item, or one per k-chunk
-    for (int64_t w = unit; w < total && ok; w += n_units) {
+    for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      // second A tile -> second accumulator (a pair CTA holds one A tile)
-      const bool sw = !PAIR && (is_glu(q.epi) || q.dual);
+      const bool sw = is_glu(q.epi) || q.dual;   // second A tile -> second accumulator
       const int n = ((it.nrows + 15) / 16) * 16;
       const bool akm = BWD && q.a_kmajor;
-      const uint32_t idesc = make_idesc(n, fp8, akm, PAIR ? 2 * BM : BM);
+      const uint32_t idesc = make_idesc(n, fp8, akm);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
       const int per_ev = q.kchunk ? q.kchunk : kb_total;
@@ -578,11 +521,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
         const int buf = ev % nacc;
         const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-        if (PAIR ? !mbar_wait_cluster(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)
-                 : !mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) { ok = false; break; }
         tc_fence_after();
         uint32_t accumulate = 0;
         const int kb_end = min(kb0 + per_ev, kb_total);
@@ -612,23 +551,17 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
 #pragma unroll
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-              if constexpr (PAIR) {
-                mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc,
-                              accumulate);
-              } else {
-                mma_bf16(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc, accumulate);
-                if (sw)
-                  mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * astep, alb, asbo), bd, idesc,
-                           accumulate);
-              }
+              mma_bf16(d_tmem, smem_desc(a1 + k16 * astep, alb, asbo), bd, idesc, accumulate);
+              if (sw)
+                mma_bf16(d_tmem + acc2, smem_desc(a3 + k16 * astep, alb, asbo), bd, idesc,
+                         accumulate);
               accumulate = 1;
             }
           }
-          // pair: frees the stage in both CTAs
-          if constexpr (PAIR) mma_commit_pair(empty(stage), 3); else mma_commit(empty(stage));
+          mma_commit(empty(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
-        if constexpr (PAIR) mma_commit_pair(tmem_full(buf), 3); else mma_commit(tmem_full(buf));
+        mma_commit(tmem_full(buf));
       }
     }
   } else if (warp >= 2) {
@@ -704,17 +637,8 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
     };
     int ev = 0;
     float amax = 0.0f;                                   // fp8 output: this thread's max |value|
-    uint32_t xc = 0;                                     // pair SwiGLU: chunks exchanged so far
-    if constexpr (!FP8 && !KC && !BWD) {
-      if (P.cmb.active) combine_rows(P.cmb, warp - 2, EPI_WARPS, lane, P.hdr);
-    }
-    // pair launches: the epilogue threads of both CTAs release rank 0's accumulator buffer
-    auto release = [&](int b) {
-      tc_fence_before();
-      if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(tmem_empty(b), 0));
-      else mbar_arrive(tmem_empty(b));
-    };
-    for (int64_t w = unit; w < total; w += n_units) {
+    if constexpr (CMB) combine_rows(P.cmb, warp - 2, EPI_WARPS, lane, P.hdr);
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
       Item it = decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       if (KC && q.kchunk) {
@@ -797,99 +721,6 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
       }
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
-      if constexpr (PAIR) {
-        if (is_glu(q.epi)) {
-          // Lanes 0..63 of this CTA's accumulator hold the gate (x W1) and lanes 64..127 the up
-          // projection (x W3) of the same 64 features. Each warp of quadrant 2 or 3 (up) hands
-          // its 16-token chunks, one at a time, through shared memory to the warp of quadrant 0
-          // or 1 of the same half (same lane = same feature), which computes the SwiGLU and
-          // writes the bf16 hidden. Hand-overs wait on mbarriers with bounded waits.
-          constexpr int HW = EPI_WARPS / 4;                     // warps per quadrant
-          constexpr int CPW = (BN / 16 + HW - 1) / HW;          // chunks per warp
-          constexpr int CPR = CPW < 4 ? CPW : 4;                // chunks held in registers
-          const int xp = half * 2 + (quad & 1);
-          const uint32_t xfull = smem_u32(&bars[XB0 + xp]);
-          const uint32_t xempty = smem_u32(&bars[XB0 + XPAIRS + xp]);
-          float* xbuf = reinterpret_cast<float*>(epi_stage +
-                                                 (4 * half + (quad & 1)) * EPI_STAGE_BYTES);
-          const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
-                                     (uint32_t)(buf * BN);
-          const int f0 = it.m0 + 64 * (int)rank + (quad & 1) * 32;
-          bool ok = true;
-          if (quad >= 2) {
-            for (int i = 0; i < CPW; ++i) {
-              const int c0 = half * 16 + i * 16 * HW;
-              if (c0 < it.nrows) {
-                float v3[16];
-                tmem_ld16(lane_addr + c0, v3);
-                tmem_wait_ld();
-                if (!mbar_wait(xempty, (xc & 1u) ^ 1u, &s_abort, P.hdr, 5)) { ok = false; break; }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) xbuf[j * 32 + lane] = v3[j];
-                mbar_arrive(xfull);
-                ++xc;
-              }
-            }
-            release(buf);
-            if (!ok) break;
-            continue;
-          }
-          // gate warp: the first CPR chunks are packed into registers and written after the
-          // release, later chunks (tiles of more than 192 tokens) are written in place
-          uint32_t pk[CPR][8];
-          auto take = [&](int c0, float v[16]) -> bool {
-            float v3[16];
-            tmem_ld16(lane_addr + c0, v);
-            tmem_wait_ld();
-            if (!mbar_wait(xfull, xc & 1u, &s_abort, P.hdr, 6)) return false;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v3[j] = xbuf[j * 32 + lane];
-            mbar_arrive(xempty);
-            ++xc;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
-            return true;
-          };
-#pragma unroll
-          for (int i = 0; i < CPR; ++i) {
-            const int c0 = half * 16 + i * 16 * HW;
-            if (ok && c0 < it.nrows) {
-              float v[16];
-              ok = take(c0, v);
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j], v[j + 1]);
-                pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-            }
-          }
-          for (int i = CPR; i < CPW && ok; ++i) {
-            const int c0 = half * 16 + i * 16 * HW;
-            if (c0 < it.nrows) {
-              float v[16];
-              if (!(ok = take(c0, v))) break;
-              store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
-            }
-          }
-          release(buf);
-          if (!ok) break;
-#pragma unroll
-          for (int i = 0; i < CPR; ++i) {
-            const int c0 = half * 16 + i * 16 * HW;
-            if (c0 < it.nrows) {
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {
-                stg_h[j * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] & 0xFFFFu));
-                stg_h[(j + 1) * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] >> 16));
-              }
-              __syncwarp();
-              store_bf16_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
-              __syncwarp();
-            }
-          }
-          continue;
-        }
-      }
       if constexpr (FP8) {
         if (q.out_fp8 && is_glu(q.epi)) {
           // E4M3 hidden: the SwiGLU of every chunk of this warp is computed and packed into
@@ -940,7 +771,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
           continue;
         }
       }
-      if constexpr (!FP8 && !KC && !BWD && !PAIR) {
+      if constexpr (!FP8 && !KC && !BWD) {
         if (q.epi == EPI_SWIGLU) {
           // bf16 hidden: as for E4M3 above, the SwiGLU of a warp's first CPR chunks is packed
           // into registers before the accumulators are released; chunks past those (tiles of
@@ -998,9 +829,8 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
           continue;
         }
       }
-      // a pair CTA holds one 128-feature half of a dual item
-      for (int sub = 0; sub < ((q.dual && !PAIR) ? 2 : 1); ++sub) {
-      const int f0 = it.m0 + (PAIR ? (int)rank : sub) * BM + quad * 32;   // this warp's first feature
+      for (int sub = 0; sub < (q.dual ? 2 : 1); ++sub) {
+      const int f0 = it.m0 + sub * BM + quad * 32;       // first feature of this warp
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                  (uint32_t)(buf * BN) + (uint32_t)sub * acc2;
       const bool f32out = (q.epi == EPI_F32);
@@ -1062,7 +892,8 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
         store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
       }
       }
-      release(buf);
+      tc_fence_before();
+      mbar_arrive(tmem_empty(buf));
     }
     if (FP8 && P.amax) {
 #pragma unroll
@@ -1073,25 +904,394 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD, PAIR>::EW, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (PAIR) {
-    // After a timeout, copies and MMAs this CTA or its pair issued may still be in flight:
-    // give them 20 ms (they take microseconds) before either CTA frees its shared or tensor
-    // memory. Then neither CTA leaves while the other can still signal its barriers.
-    if (s_abort) {
-      const uint64_t t0 = globaltimer();
-      while (globaltimer() - t0 < 20000000ull) __nanosleep(1000);
-    }
-    cluster_sync();
-  }
   tc_fence_after();
   if (warp == 1) {
-    if constexpr (PAIR)
-      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
-                   : "memory");
-    else
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
-                   : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                 : "memory");
   }
+}
+
+// ---- the CTA-pair kernel ------------------------------------------------------------------
+//
+// A cluster of two CTAs runs each item with tcgen05.mma.cta_group::2 (M = 256: 128 weight rows
+// from each CTA; each CTA loads half of the token tile). Every item of a pair launch has two
+// weight tiles: a dual item's 256 features split 128 + 128 between the CTAs; a SwiGLU item's 128
+// output features split 64 + 64, each CTA stacking the gate (W1) and up (W3) tiles of its 64
+// features into one 128-row A tile. Each CTA's accumulator is then one N-column buffer, so two
+// buffers fit in tensor memory and the epilogue of one item overlaps the MMAs of the next.
+// bf16 forward problems only (EPI_SWIGLU, EPI_STORE, EPI_F32); no combine.
+__global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcParams P) {
+  constexpr int EPI_WARPS = MOE_TC_EPI_WARPS;
+  constexpr int XPAIRS = EPI_WARPS / 2;          // gate/up warp pairs of a SwiGLU epilogue
+  constexpr int XB0 = 2 * 8 + 4;                 // first exchange barrier
+  const int EPI_STAGE_BYTES = P.epi_tile;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 4 + 2 * XPAIRS];
+  __shared__ int64_t s_total;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stages = P.stages;
+  const uint32_t rank = cluster_ctarank();                 // this CTA in its pair
+  const int64_t unit = blockIdx.x >> 1, n_units = gridDim.x >> 1;
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int stage_bytes = A_BYTES + P.b_bytes;             // one 128-row A tile per CTA
+  auto sA = [&](int s) { return base + s * stage_bytes; };
+  auto sB = [&](int s) { return base + s * stage_bytes + A_BYTES; };
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
+  auto full = [&](int s) { return full0 + 8u * s; };
+  auto empty = [&](int s) { return empty0 + 8u * s; };
+  auto tmem_full = [&](int b) { return smem_u32(&bars[16 + b]); };
+  auto tmem_empty = [&](int b) { return smem_u32(&bars[18 + b]); };
+  unsigned char* epi_stage = base + (size_t)stages * stage_bytes;   // [EPI_WARPS][EPI_STAGE_BYTES]
+  Sched S;
+  {
+    int32_t* sp = reinterpret_cast<int32_t*>(epi_stage + EPI_WARPS * EPI_STAGE_BYTES);
+    const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
+    S.glo = sp;
+    S.ghi = sp + G;
+    S.gitem = sp + 2 * G;
+  }
+
+  // set-up that reads nothing a preceding kernel writes
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tmem_full(b), 1);
+      mbar_init(tmem_empty(b), 2 * 32 * EPI_WARPS);      // rank 0's: both CTAs' epilogues
+    }
+    for (int i = 0; i < 2 * XPAIRS; ++i) mbar_init(smem_u32(&bars[XB0 + i]), 32);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int p = 0; p < P.n_probs; ++p)
+      for (int s = 0; s < P.p[p].n_seg; ++s) {
+        prefetch_map(&P.p[p].seg[s].a1);
+        prefetch_map(&P.p[p].seg[s].b);
+        if (is_glu(P.p[p].epi)) prefetch_map(&P.p[p].seg[s].a3);
+      }
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates, collectively, the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+
+  // Every thread waits for the preceding kernel before it reads the group offsets.
+  pdl_wait();
+
+  // schedule of the grouped problem (as in tc_gemm_kernel)
+  if (P.grouped >= 0) {
+    const TcProblem& q = P.p[P.grouped];
+    if (warp == 0) {
+      const int G = q.G;
+      const int per = (G + 31) / 32;
+      int64_t sum = 0;
+      for (int i = 0; i < per; ++i) {
+        int g = lane * per + i;
+        if (g < G) {
+          int64_t lo = imin64(imax64(q.offsets[g], 0), q.rows);
+          int64_t hi = imin64(imax64(q.offsets[g + 1], lo), q.rows);
+          S.glo[g] = (int32_t)lo;
+          S.ghi[g] = (int32_t)hi;
+          sum += cdiv(hi - lo, q.bn) * q.m_tiles;
+        }
+      }
+      int64_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int64_t v = __shfl_up_sync(~0u, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int64_t run = incl - sum + q.item_base;
+      for (int i = 0; i < per; ++i) {
+        int g = lane * per + i;
+        if (g < G) {
+          S.gitem[g] = (int32_t)run;
+          run += cdiv((int64_t)S.ghi[g] - S.glo[g], q.bn) * q.m_tiles;
+        }
+      }
+      if (lane == 31) { S.gitem[G] = (int32_t)run; s_total = run; }
+    }
+  } else if (threadIdx.x == 0) {
+    const TcProblem& q = P.p[P.n_probs - 1];
+    s_total = q.item_base + q.n_items;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();      // both CTAs' barriers are initialised before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int64_t total = s_total;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    // This CTA's 128 weight rows and its half (N / 2 rows) of the token tile; the bytes of both
+    // CTAs complete on rank 0's full barrier, which rank 0 arms with their sum.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t w = unit; w < total && ok; w += n_units) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const int half_rows = ((it.nrows + 15) / 16) * 8;
+      const int nb = (half_rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
+      const uint32_t bytes = 2u * (uint32_t)(A_BYTES + nb * B_BOX_BYTES);
+      const int64_t my_row0 = it.row0 + (int64_t)rank * half_rows;
+      const bool gl = is_glu(q.epi);
+      // SwiGLU: gate and up tiles of features m_w + 64 rank ..; dual: features m_w + 128 rank ..
+      const int mx0 = it.m_w + (gl ? 64 : BM) * (int)rank;
+      for (int s = 0; s < q.n_seg && ok; ++s) {
+        const TcSeg& sg = q.seg[s];
+        for (int kb = 0; kb < sg.kblocks; ++kb) {
+          const int k0 = kb * BK;
+          if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
+          const uint32_t fb = mapa_shared(full(stage), 0);
+          if (rank == 0) mbar_expect_tx(full(stage), bytes);
+          tma_load_3d_pair(smem_u32(sA(stage)), &sg.a1, fb, mx0, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA(stage)) + A_HALF, gl ? &sg.a3 : &sg.a1, fb,
+                           gl ? mx0 : mx0 + 64, k0, it.wg);
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d_pair(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, fb, k0,
+                             (int)(my_row0 + b * B_BOX_ROWS));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer: rank 0 issues for both CTAs ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int ev = 0;      // accumulator events: one per item
+    for (int64_t w = unit; w < total && ok; w += n_units) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const int n = ((it.nrows + 15) / 16) * 16;
+      const uint32_t idesc = make_idesc(n, false, false, 2 * BM);
+      int kb_total = 0;
+      for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
+      const int buf = ev % 2;
+      const uint32_t acc_phase = (uint32_t)(ev / 2) & 1u;
+      ++ev;
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      if (!mbar_wait_cluster(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
+      tc_fence_after();
+      uint32_t accumulate = 0;
+      for (int kk = 0; kk < kb_total; ++kk) {
+        if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a1 = smem_u32(sA(stage)), b = smem_u32(sB(stage));
+        // MN-major A (LBO: the two 64-feature atoms, SBO: 8-row k groups), K-major B
+#pragma unroll
+        for (int k16 = 0; k16 < BK / 16; ++k16) {
+          mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * 2048u, (uint32_t)A_HALF, 1024u),
+                        smem_desc(b + k16 * 32, 16, 1024), idesc, accumulate);
+          accumulate = 1;
+        }
+        mma_commit_pair(empty(stage), 3);         // frees the stage in both CTAs
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      mma_commit_pair(tmem_full(buf), 3);
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); the warps of a quadrant take
+    // alternate 16-token chunks, transposed through a per-warp shared-memory tile so that every
+    // lane writes whole 16-byte pieces of output rows.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+    float* stg_f = reinterpret_cast<float*>(stg);
+    bf16* stg_h = reinterpret_cast<bf16*>(stg);
+    auto store_bf16_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
+                               int M) {
+      const int rows_here = min(16, it.nrows - c0);
+      const int part = lane & 3;
+      const bool ok = f0 + part * 8 < M;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = (lane >> 2) + 8 * r;
+        if (ok && row < rows_here) {
+          const uint4 val = *reinterpret_cast<const uint4*>(stg_h + row * 32 + part * 8);
+          const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 8;
+          *reinterpret_cast<uint4*>(static_cast<bf16*>(out) + o) = val;
+        }
+      }
+    };
+    // one 16-token x 32-feature chunk (lane = feature, v[j] = token c0 + j); kind 0 fp32, 1 bf16
+    auto store_rows = [&](void* out, int64_t ld, int col0, int kind, const Item& it, int c0,
+                          int f0, int M, const float* v) {
+      if (kind == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg_f[j * 32 + lane] = v[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg_h[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+      }
+      __syncwarp();
+      const int rows_here = min(16, it.nrows - c0);
+      if (kind == 0) {
+        const int part = lane & 7;
+        const bool ok = f0 + part * 4 < M;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = (lane >> 3) + 4 * r;
+          if (ok && row < rows_here) {
+            const float4 val = *reinterpret_cast<const float4*>(stg_f + row * 32 + part * 4);
+            const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 4;
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = val;
+          }
+        }
+      } else {
+        store_bf16_tile(out, ld, col0, it, c0, f0, M);
+      }
+      __syncwarp();
+    };
+    // releases rank 0's accumulator buffer (remote arrive from rank 1)
+    auto release = [&](int b) {
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(tmem_empty(b), 0));
+    };
+    int ev = 0;
+    uint32_t xc = 0;                                     // SwiGLU: chunks exchanged so far
+    for (int64_t w = unit; w < total; w += n_units) {
+      Item it = decode(P, S, w);
+      const TcProblem& q = P.p[it.p];
+      const int buf = ev % 2;
+      const uint32_t acc_phase = (uint32_t)(ev / 2) & 1u;
+      ++ev;
+      if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
+      tc_fence_after();
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+      if (is_glu(q.epi)) {
+        // Lanes 0..63 of this CTA's accumulator hold the gate (x W1) and lanes 64..127 the up
+        // projection (x W3) of the same 64 features. Each warp of quadrant 2 or 3 (up) hands its
+        // 16-token chunks, one at a time, through shared memory to the warp of quadrant 0 or 1
+        // of the same half (same lane = same feature), which computes the SwiGLU and writes the
+        // bf16 hidden. Hand-overs wait on mbarriers with bounded waits.
+        constexpr int HW = EPI_WARPS / 4;                     // warps per quadrant
+        constexpr int CPW = (BN / 16 + HW - 1) / HW;          // chunks per warp
+        constexpr int CPR = CPW < 4 ? CPW : 4;                // chunks held in registers
+        const int xp = half * 2 + (quad & 1);
+        const uint32_t xfull = smem_u32(&bars[XB0 + xp]);
+        const uint32_t xempty = smem_u32(&bars[XB0 + XPAIRS + xp]);
+        float* xbuf = reinterpret_cast<float*>(epi_stage + (4 * half + (quad & 1)) * EPI_STAGE_BYTES);
+        const int f0 = it.m0 + 64 * (int)rank + (quad & 1) * 32;
+        bool ok = true;
+        if (quad >= 2) {
+          for (int i = 0; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * HW;
+            if (c0 < it.nrows) {
+              float v3[16];
+              tmem_ld16(lane_addr + c0, v3);
+              tmem_wait_ld();
+              if (!mbar_wait(xempty, (xc & 1u) ^ 1u, &s_abort, P.hdr, 5)) { ok = false; break; }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xbuf[j * 32 + lane] = v3[j];
+              mbar_arrive(xfull);
+              ++xc;
+            }
+          }
+          release(buf);
+          if (!ok) break;
+          continue;
+        }
+        // gate warp: the first CPR chunks are packed into registers and written after the
+        // release, later chunks (tiles of more than 192 tokens) are written in place
+        uint32_t pk[CPR][8];
+        auto take = [&](int c0, float v[16]) -> bool {
+          float v3[16];
+          tmem_ld16(lane_addr + c0, v);
+          tmem_wait_ld();
+          if (!mbar_wait(xfull, xc & 1u, &s_abort, P.hdr, 6)) return false;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v3[j] = xbuf[j * 32 + lane];
+          mbar_arrive(xempty);
+          ++xc;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
+          return true;
+        };
+#pragma unroll
+        for (int i = 0; i < CPR; ++i) {
+          const int c0 = half * 16 + i * 16 * HW;
+          if (ok && c0 < it.nrows) {
+            float v[16];
+            ok = take(c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j], v[j + 1]);
+              pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+          }
+        }
+        for (int i = CPR; i < CPW && ok; ++i) {
+          const int c0 = half * 16 + i * 16 * HW;
+          if (c0 < it.nrows) {
+            float v[16];
+            if (!(ok = take(c0, v))) break;
+            store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
+          }
+        }
+        release(buf);
+        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < CPR; ++i) {
+          const int c0 = half * 16 + i * 16 * HW;
+          if (c0 < it.nrows) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              stg_h[j * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] & 0xFFFFu));
+              stg_h[(j + 1) * 32 + lane] = __ushort_as_bfloat16((unsigned short)(pk[i][j / 2] >> 16));
+            }
+            __syncwarp();
+            store_bf16_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
+            __syncwarp();
+          }
+        }
+        continue;
+      }
+      // a dual item: this CTA holds features m0 + 128 rank .. of the item's 256
+      const int f0 = it.m0 + (int)rank * BM + quad * 32;
+      const bool f32out = (q.epi == EPI_F32);
+      const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+      for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
+        float v[16];
+        tmem_ld16(lane_addr + c0, v);
+        tmem_wait_ld();
+        if (f32out) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
+        }
+        store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
+      }
+      release(buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // After a timeout, copies and MMAs either CTA issued may still be in flight: give them 20 ms
+  // (they take microseconds) before either CTA frees its shared or tensor memory. Then neither
+  // CTA leaves while the other can still signal its barriers.
+  if (s_abort) {
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 20000000ull) __nanosleep(1000);
+  }
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base)
+                 : "memory");
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing arrives at, with
@@ -1183,13 +1383,12 @@ int num_sms_tc() {
   return n > 0 ? n : 148;
 }
 
-// Which launches use CTA pairs. By default ("auto") only the dual launches where pairs measured
-// faster on GB300: the grouped GEMM 2 with at most one 256-row token tile per expert on average
-// (the 535B layer at T=8192: 1.29 -> 1.26 ms; with Zipf-skewed routing at T=16384, whose hot
-// experts fill many full tiles, pairs were slower: 2.19 -> 2.37 ms) and dense launches of at
-// least 32K rows (the back GEMM at T=65536: 6.4 -> 5.9 ms). SwiGLU items, whose pair CTAs each
-// stack 64 gate and 64 up features, measured slower at every size (their main loop alone: 2.18 ->
-// 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
+// Which launches use CTA pairs. By default ("auto") only dense dual launches of at least 32K rows,
+// where pairs measured faster on GB300 than single CTAs (the back GEMM at T=65536: 6.0 -> 5.6-5.9
+// ms). Grouped dual launches measured even at best (GEMM 2 of the 535B layer at T=8192: 1.26 ms
+// both ways) and slower with skewed routing (Zipf, T=16384: 2.19 -> 2.37 ms); SwiGLU items, whose
+// pair CTAs each stack 64 gate and 64 up features, measured slower at every size (their main loop
+// alone: 2.18 -> 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
 // with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1"); no launch
 // uses them once a query finds that no pair fits on the GPU.
 enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3, PAIR_AUTO = 4 };
@@ -1414,21 +1613,19 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   if (kc && bwd) return cudaErrorNotSupported;
   // CTA pairs (cta_group::2) for bf16 launches whose every item has two weight tiles
   const int pmode = pair_mode();
-  bool pair = pmode != PAIR_NONE && !P.fp8 && !kc && !bwd;
+  bool pair = pmode != PAIR_NONE && !P.fp8 && !kc && !bwd && !P.cmb.active;
   for (int j = 0; j < n_probs; ++j) {
     const TcProblem& q = P.p[j];
     pair = pair && (is_glu(q.epi) || q.dual) &&
            (q.epi == EPI_SWIGLU || q.epi == EPI_STORE || q.epi == EPI_F32) &&
            !(pmode == PAIR_DUAL && is_glu(q.epi)) && !(pmode == PAIR_GLU && q.dual);
-    if (pmode == PAIR_AUTO)
-      pair = pair && q.dual &&
-             (q.group == GROUP_ROWS ? q.rows <= (int64_t)BN * q.G : q.rows >= 32768);
+    if (pmode == PAIR_AUTO) pair = pair && q.dual && q.group != GROUP_ROWS && q.rows >= 32768;
   }
   const dim3 block(64 + 32 * (P.fp8 ? Inst<true, false, false>::EW
                                     : (kc ? Inst<false, true, false>::EW
                                           : (bwd ? Inst<false, false, true>::EW
                                                  : Inst<false, false, false>::EW))));
-  const int n_pairs = pair ? max_pairs(tc_gemm_kernel<false, false, false, true>, block) : 0;
+  const int n_pairs = pair ? max_pairs(tc_gemm_pair_kernel, block) : 0;
   if (pair && n_pairs < 1) {   // no CTA pair fits: this and later launches run without pairs
     pair_disable();
     pair = false;
@@ -1490,7 +1687,8 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024 +
                       epi_bytes + (size_t)(3 * G + 1) * 4;
-  auto kern = pair ? tc_gemm_kernel<false, false, false, true>
+  auto kern = pair ? tc_gemm_pair_kernel
+             : P.cmb.active ? tc_gemm_kernel<false, false, false, true>
              : P.fp8 ? tc_gemm_kernel<true, false, false>
                      : (kc ? tc_gemm_kernel<false, true, false>
                            : (bwd ? tc_gemm_kernel<false, false, true>

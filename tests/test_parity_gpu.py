@@ -448,6 +448,49 @@ def test_swiglu_epilogue_wide_range(path):
     assert normwise(y_perm[:R], o) <= (1e-5 if path == "f32" else 2e-2)
 
 
+_PAIR_CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+import sparse_expert_router_gb300 as m
+from moe_workloads import SHAPES, make_layer_inputs
+from oracle import moe_oracle
+for name, T in (("small_bf16", 1000), ("l535b_e64_t1368", 1368)):
+    shape = SHAPES[name].with_(T=T)
+    cfg = m.LayerConfig.from_shape(shape, flags=m.MOE_FLAG_PDL)
+    inp = make_layer_inputs(shape, "cpu")
+    dinp = {k: v.to("cuda") for k, v in inp.items()}
+    y = torch.empty((T, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, shape.top_k), dtype=torch.int32, device="cuda")
+    ws = m.alloc_workspace(cfg)
+    m.moe_forward(cfg, dinp, dinp["x"], y, ws, aux={"topk_idx": idx})
+    rep = m.moe_get_device_status(ws)
+    toks = list(range(0, T, 8))
+    ref = moe_oracle.forward(inp, top_k=shape.top_k, rms_eps=shape.rms_eps, tokens=toks)
+    assert rep["status"] == 0, rep
+    assert torch.equal(idx.cpu().long(), ref["idx"])
+    ys = y[toks].double().cpu()
+    err = float((ys - ref["y"]).norm() / ref["y"].norm())
+    per_row = float(((ys - ref["y"]).norm(dim=1) / ref["y"].norm(dim=1)).max())
+    assert err <= 2e-2 and per_row <= 2e-2, (name, err, per_row)
+    print(name, "ok", err, per_row)
+"""
+
+
+def test_pair_kernels_forced():
+    """Every launch that can run as CTA pairs does (MOE_TC_PAIR=1: the SwiGLU GEMM 1 with its
+    gate/up hand-over, the grouped dual GEMM 2, the dense dual back GEMM), in a child process
+    because the switch is read once per process; outputs against the oracle, routing exact."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_TC_PAIR="1")
+    r = subprocess.run([sys.executable, "-c", _PAIR_CHILD, root], env=env, cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.count(" ok ") == 2, r.stdout
+
+
 def test_expert_slice():
     """One expert-parallel rank's slice: grouped GEMMs over the active rows of a padded pool,
     then the gate-weighted un-permute back to arrival order."""
