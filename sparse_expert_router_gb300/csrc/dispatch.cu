@@ -206,13 +206,34 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
       s_slot[j] = slot;
     }
   }
+  // Rows of up to ZC * 1024 features stay in registers between the two passes (all of a
+  // thread's loads in flight at once); longer rows are read again. Either way each thread sums
+  // its squares in the same order.
+  constexpr int ZC = 4;
+  const bool cached = a.L <= ZC * 1024;
   const float* z = a.z + t * a.L;
+  float zc[ZC][8];
   float ss = 0.0f;
-  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
-    float v[8];
-    ld8(z + i, v);
+  if (cached) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+    for (int u = 0; u < ZC; ++u) {
+      const int i = threadIdx.x * 8 + u * 1024;
+      if (i < a.L) ld8(z + i, zc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < ZC; ++u) {
+      if (threadIdx.x * 8 + u * 1024 < a.L) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ss = fmaf(zc[u][q], zc[u][q], ss);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+      float v[8];
+      ld8(z + i, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(~0u, ss, o);
@@ -226,9 +247,8 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
   T* xp = static_cast<T*>(a.x_perm);
   const float qs = kFp8 ? *a.x_scale : 1.0f;
   float amax = 0.0f;
-  for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
-    float v[8], g[8];
-    ld8(z + i, v);
+  auto emit = [&](int i, float v[8]) {
+    float g[8];
     ld8(a.gamma + i, g);
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = v[q] * rstd * g[q];
@@ -242,6 +262,19 @@ __global__ void __launch_bounds__(128) gather_kernel(DispatchArgs a) {
     for (int j = 0; j < a.k; ++j) {
       const int32_t sl = s_slot[j];
       if (sl >= 0) st8(xp + (int64_t)sl * a.L + i, v);
+    }
+  };
+  if (cached) {
+#pragma unroll
+    for (int u = 0; u < ZC; ++u) {
+      const int i = threadIdx.x * 8 + u * 1024;
+      if (i < a.L) emit(i, zc[u]);
+    }
+  } else {
+    for (int i = threadIdx.x * 8; i < a.L; i += 1024) {
+      float v[8];
+      ld8(z + i, v);
+      emit(i, v);
     }
   }
   if (kFp8 && ns > 0) {
