@@ -913,21 +913,57 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
 
 // ---- the CTA-pair kernel ------------------------------------------------------------------
 //
-// A cluster of two CTAs runs each item with tcgen05.mma.cta_group::2 (M = 256: 128 weight rows
-// from each CTA; each CTA loads half of the token tile). Every item of a pair launch has two
-// weight tiles: a dual item's 256 features split 128 + 128 between the CTAs; a SwiGLU item's 128
-// output features split 64 + 64, each CTA stacking the gate (W1) and up (W3) tiles of its 64
-// features into one 128-row A tile. Each CTA's accumulator is then one N-column buffer, so two
-// buffers fit in tensor memory and the epilogue of one item overlaps the MMAs of the next.
+// A cluster of two CTAs runs each item with tcgen05.mma.cta_group::2: an MMA of M = 256 takes
+// 128 weight rows from each CTA and the token tile from both, each CTA loading half of it (N / 2
+// rows); each CTA's tensor memory receives its own 128 rows of the accumulator over all N
+// columns. Every item keeps two weight tiles per CTA, as in tc_gemm_kernel, so a pair item spans
+// twice the features of a single-CTA item: a SwiGLU item 256 output features (each CTA the gate
+// and up tiles of its 128), a dual item 512 (each CTA two 128-feature tiles). The token tile is
+// loaded once per pair instead of once per CTA: 46 KB per k-block and SM instead of 60 KB for the
+// same MMAs, where L2-to-SM ingest is what bounds the dense GEMMs.
 // bf16 forward problems only (EPI_SWIGLU, EPI_STORE, EPI_F32); no combine.
+
+// Item w of a pair launch: SwiGLU items of 256 features, dual items of 512.
+__device__ __forceinline__ Item pair_decode(const TcParams& P, const Sched& S, int64_t w) {
+  Item it;
+  int p = 0;
+  while (p + 1 < P.n_probs && w >= P.p[p + 1].item_base) ++p;
+  const TcProblem& q = P.p[p];
+  const int pw = q.dual ? 4 * BM : 2 * BM;             // features of a pair item
+  int64_t local = w - (p == P.grouped ? (int64_t)S.gitem[0] : q.item_base);
+  it.p = p;
+  if (q.group == GROUP_ROWS) {
+    int lo = 0, hi = q.G;
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if ((int64_t)S.gitem[mid] - S.gitem[0] <= local) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int64_t within = local - ((int64_t)S.gitem[g] - S.gitem[0]);
+    const int n_t = (int)(within / q.m_tiles), m_t = (int)(within % q.m_tiles);
+    it.wg = g;
+    it.m0 = m_t * pw;
+    it.m_w = it.m0;
+    it.row0 = S.glo[g] + (int64_t)n_t * q.bn;
+    it.nrows = (int)imin64(q.bn, (int64_t)S.ghi[g] - it.row0);
+  } else {
+    const int64_t n_tiles = cdiv(q.rows, q.bn);
+    const int n_t = (int)(local % n_tiles), m_t = (int)(local / n_tiles);   // token tiles fastest
+    it.m0 = m_t * pw;
+    if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
+    else { it.wg = 0; it.m_w = it.m0; }
+    it.row0 = (int64_t)n_t * q.bn;
+    it.nrows = (int)imin64(q.bn, q.rows - it.row0);
+  }
+  return it;
+}
+
 __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams P) {
   constexpr int EPI_WARPS = MOE_TC_EPI_WARPS;
-  constexpr int XPAIRS = EPI_WARPS / 2;          // gate/up warp pairs of a SwiGLU epilogue
-  constexpr int XB0 = 2 * 8 + 4;                 // first exchange barrier
   const int EPI_STAGE_BYTES = P.epi_tile;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * 8 + 4 + 2 * XPAIRS];
+  __shared__ __align__(8) uint64_t bars[2 * 8 + 4];
   __shared__ int64_t s_total;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -938,14 +974,17 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
   const int64_t unit = blockIdx.x >> 1, n_units = gridDim.x >> 1;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int stage_bytes = A_BYTES + P.b_bytes;             // one 128-row A tile per CTA
-  auto sA = [&](int s) { return base + s * stage_bytes; };
-  auto sB = [&](int s) { return base + s * stage_bytes + A_BYTES; };
+  const int stage_bytes = 2 * A_BYTES + P.b_bytes;         // two weight tiles, half a token tile
+  auto sA1 = [&](int s) { return base + s * stage_bytes; };
+  auto sA3 = [&](int s) { return base + s * stage_bytes + A_BYTES; };
+  auto sB = [&](int s) { return base + s * stage_bytes + 2 * A_BYTES; };
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
   auto full = [&](int s) { return full0 + 8u * s; };
   auto empty = [&](int s) { return empty0 + 8u * s; };
   auto tmem_full = [&](int b) { return smem_u32(&bars[16 + b]); };
   auto tmem_empty = [&](int b) { return smem_u32(&bars[18 + b]); };
+  const int nacc = P.nacc;
+  const uint32_t acc2 = (uint32_t)P.acc2_off;
   unsigned char* epi_stage = base + (size_t)stages * stage_bytes;   // [EPI_WARPS][EPI_STAGE_BYTES]
   Sched S;
   {
@@ -966,7 +1005,6 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
       mbar_init(tmem_full(b), 1);
       mbar_init(tmem_empty(b), 2 * 32 * EPI_WARPS);      // rank 0's: both CTAs' epilogues
     }
-    for (int i = 0; i < 2 * XPAIRS; ++i) mbar_init(smem_u32(&bars[XB0 + i]), 32);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int p = 0; p < P.n_probs; ++p)
@@ -1033,31 +1071,35 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    // This CTA's 128 weight rows and its half (N / 2 rows) of the token tile; the bytes of both
-    // CTAs complete on rank 0's full barrier, which rank 0 arms with their sum.
+    // This CTA's two 128-row weight tiles and its half (N / 2 rows) of the token tile; the bytes
+    // of both CTAs complete on rank 0's full barrier, which rank 0 arms with their sum.
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int64_t w = unit; w < total && ok; w += n_units) {
-      Item it = decode(P, S, w);
+      Item it = pair_decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int half_rows = ((it.nrows + 15) / 16) * 8;
       const int nb = (half_rows + B_BOX_ROWS - 1) / B_BOX_ROWS;
-      const uint32_t bytes = 2u * (uint32_t)(A_BYTES + nb * B_BOX_BYTES);
+      const uint32_t bytes = 2u * (uint32_t)(2 * A_BYTES + nb * B_BOX_BYTES);
       const int64_t my_row0 = it.row0 + (int64_t)rank * half_rows;
       const bool gl = is_glu(q.epi);
-      // SwiGLU: gate and up tiles of features m_w + 64 rank ..; dual: features m_w + 128 rank ..
-      const int mx0 = it.m_w + (gl ? 64 : BM) * (int)rank;
+      // SwiGLU: gate (W1) and up (W3) tiles of features m_w + 128 rank ..; dual: features
+      // m_w + 256 rank .. and .. + 128 of the one weight matrix
+      const int mx1 = it.m_w + (gl ? BM : 2 * BM) * (int)rank;
+      const int mx3 = gl ? mx1 : mx1 + BM;
       for (int s = 0; s < q.n_seg && ok; ++s) {
         const TcSeg& sg = q.seg[s];
+        const CUtensorMap* m3 = gl ? &sg.a3 : &sg.a1;
         for (int kb = 0; kb < sg.kblocks; ++kb) {
           const int k0 = kb * BK;
           if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
           const uint32_t fb = mapa_shared(full(stage), 0);
           if (rank == 0) mbar_expect_tx(full(stage), bytes);
-          tma_load_3d_pair(smem_u32(sA(stage)), &sg.a1, fb, mx0, k0, it.wg);
-          tma_load_3d_pair(smem_u32(sA(stage)) + A_HALF, gl ? &sg.a3 : &sg.a1, fb,
-                           gl ? mx0 : mx0 + 64, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx1, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA1(stage)) + A_HALF, &sg.a1, fb, mx1 + 64, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA3(stage)), m3, fb, mx3, k0, it.wg);
+          tma_load_3d_pair(smem_u32(sA3(stage)) + A_HALF, m3, fb, mx3 + 64, k0, it.wg);
           for (int b = 0; b < nb; ++b)
             tma_load_2d_pair(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, fb, k0,
                              (int)(my_row0 + b * B_BOX_ROWS));
@@ -1072,14 +1114,14 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
     bool ok = true;
     int ev = 0;      // accumulator events: one per item
     for (int64_t w = unit; w < total && ok; w += n_units) {
-      Item it = decode(P, S, w);
+      Item it = pair_decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int n = ((it.nrows + 15) / 16) * 16;
       const uint32_t idesc = make_idesc(n, false, false, 2 * BM);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
-      const int buf = ev % 2;
-      const uint32_t acc_phase = (uint32_t)(ev / 2) & 1u;
+      const int buf = ev % nacc;
+      const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
       ++ev;
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       if (!mbar_wait_cluster(tmem_empty(buf), acc_phase ^ 1u, &s_abort, P.hdr, 2)) break;
@@ -1088,12 +1130,16 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
       for (int kk = 0; kk < kb_total; ++kk) {
         if (!mbar_wait(full(stage), phase, &s_abort, P.hdr, 3)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a1 = smem_u32(sA(stage)), b = smem_u32(sB(stage));
+        const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)),
+                       b = smem_u32(sB(stage));
         // MN-major A (LBO: the two 64-feature atoms, SBO: 8-row k groups), K-major B
 #pragma unroll
         for (int k16 = 0; k16 < BK / 16; ++k16) {
-          mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * 2048u, (uint32_t)A_HALF, 1024u),
-                        smem_desc(b + k16 * 32, 16, 1024), idesc, accumulate);
+          const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
+          mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd, idesc,
+                        accumulate);
+          mma_bf16_pair(d_tmem + acc2, smem_desc(a3 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd,
+                        idesc, accumulate);
           accumulate = 1;
         }
         mma_commit_pair(empty(stage), 3);         // frees the stage in both CTAs
@@ -1104,9 +1150,9 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
-    // Warp w reads tensor-memory lanes 32*(w%4).. (its quadrant); the warps of a quadrant take
-    // alternate 16-token chunks, transposed through a per-warp shared-memory tile so that every
-    // lane writes whole 16-byte pieces of output rows.
+    // As in tc_gemm_kernel: warp w reads tensor-memory lanes 32*(w%4).. (its quadrant), the
+    // warps of a quadrant take alternate 16-token chunks, transposed through a per-warp
+    // shared-memory tile so that every lane writes whole 16-byte pieces of output rows.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
@@ -1156,97 +1202,61 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
       }
       __syncwarp();
     };
-    // releases rank 0's accumulator buffer (remote arrive from rank 1)
+    // releases rank 0's accumulator buffer (a remote arrive from rank 1)
     auto release = [&](int b) {
       tc_fence_before();
       mbar_arrive_cluster(mapa_shared(tmem_empty(b), 0));
     };
     int ev = 0;
-    uint32_t xc = 0;                                     // SwiGLU: chunks exchanged so far
     for (int64_t w = unit; w < total; w += n_units) {
-      Item it = decode(P, S, w);
+      Item it = pair_decode(P, S, w);
       const TcProblem& q = P.p[it.p];
-      const int buf = ev % 2;
-      const uint32_t acc_phase = (uint32_t)(ev / 2) & 1u;
+      const int buf = ev % nacc;
+      const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
       ++ev;
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
       if (is_glu(q.epi)) {
-        // Lanes 0..63 of this CTA's accumulator hold the gate (x W1) and lanes 64..127 the up
-        // projection (x W3) of the same 64 features. Each warp of quadrant 2 or 3 (up) hands its
-        // 16-token chunks, one at a time, through shared memory to the warp of quadrant 0 or 1
-        // of the same half (same lane = same feature), which computes the SwiGLU and writes the
-        // bf16 hidden. Hand-overs wait on mbarriers with bounded waits.
-        constexpr int HW = EPI_WARPS / 4;                     // warps per quadrant
-        constexpr int CPW = (BN / 16 + HW - 1) / HW;          // chunks per warp
-        constexpr int CPR = CPW < 4 ? CPW : 4;                // chunks held in registers
-        const int xp = half * 2 + (quad & 1);
-        const uint32_t xfull = smem_u32(&bars[XB0 + xp]);
-        const uint32_t xempty = smem_u32(&bars[XB0 + XPAIRS + xp]);
-        float* xbuf = reinterpret_cast<float*>(epi_stage + (4 * half + (quad & 1)) * EPI_STAGE_BYTES);
-        const int f0 = it.m0 + 64 * (int)rank + (quad & 1) * 32;
-        bool ok = true;
-        if (quad >= 2) {
-          for (int i = 0; i < CPW; ++i) {
-            const int c0 = half * 16 + i * 16 * HW;
-            if (c0 < it.nrows) {
-              float v3[16];
-              tmem_ld16(lane_addr + c0, v3);
-              tmem_wait_ld();
-              if (!mbar_wait(xempty, (xc & 1u) ^ 1u, &s_abort, P.hdr, 5)) { ok = false; break; }
+        // bf16 hidden of this CTA's 128 features: the SwiGLU of a warp's first CPR chunks is
+        // packed into registers before the accumulators are released; chunks past those (tiles
+        // of more than 192 tokens) are written out first, in place
+        constexpr int CPW = (BN / 16 + EPI_WARPS / 4 - 1) / (EPI_WARPS / 4);   // chunks per warp
+        constexpr int CPR = CPW < 4 ? CPW : 4;
+        const int f0 = it.m0 + (int)rank * BM + quad * 32;
+        for (int i = CPR; i < CPW; ++i) {
+          const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+          if (c0 < it.nrows) {
+            float v[16], v3[16];
+            tmem_ld16(lane_addr + c0, v);
+            tmem_ld16(lane_addr + acc2 + c0, v3);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) xbuf[j * 32 + lane] = v3[j];
-              mbar_arrive(xfull);
-              ++xc;
-            }
+            for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
+            store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
           }
-          release(buf);
-          if (!ok) break;
-          continue;
         }
-        // gate warp: the first CPR chunks are packed into registers and written after the
-        // release, later chunks (tiles of more than 192 tokens) are written in place
         uint32_t pk[CPR][8];
-        auto take = [&](int c0, float v[16]) -> bool {
-          float v3[16];
-          tmem_ld16(lane_addr + c0, v);
-          tmem_wait_ld();
-          if (!mbar_wait(xfull, xc & 1u, &s_abort, P.hdr, 6)) return false;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v3[j] = xbuf[j * 32 + lane];
-          mbar_arrive(xempty);
-          ++xc;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = swiglu(v[j], v3[j]);
-          return true;
-        };
 #pragma unroll
         for (int i = 0; i < CPR; ++i) {
-          const int c0 = half * 16 + i * 16 * HW;
-          if (ok && c0 < it.nrows) {
-            float v[16];
-            ok = take(c0, v);
+          const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+          if (c0 < it.nrows) {
+            float v[16], v3[16];
+            tmem_ld16(lane_addr + c0, v);
+            tmem_ld16(lane_addr + acc2 + c0, v3);
+            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j], v[j + 1]);
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(swiglu(v[j], v3[j]),
+                                                              swiglu(v[j + 1], v3[j + 1]));
               pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
           }
         }
-        for (int i = CPR; i < CPW && ok; ++i) {
-          const int c0 = half * 16 + i * 16 * HW;
-          if (c0 < it.nrows) {
-            float v[16];
-            if (!(ok = take(c0, v))) break;
-            store_rows(q.out, q.ld_out, q.out_col0, 1, it, c0, f0, q.M, v);
-          }
-        }
         release(buf);
-        if (!ok) break;
 #pragma unroll
         for (int i = 0; i < CPR; ++i) {
-          const int c0 = half * 16 + i * 16 * HW;
+          const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
           if (c0 < it.nrows) {
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
@@ -1260,19 +1270,23 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
         }
         continue;
       }
-      // a dual item: this CTA holds features m0 + 128 rank .. of the item's 256
-      const int f0 = it.m0 + (int)rank * BM + quad * 32;
+      // a dual item: this CTA holds features m0 + 256 rank .. (first accumulator) and .. + 128
+      // (second)
       const bool f32out = (q.epi == EPI_F32);
-      const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
-      for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
-        float v[16];
-        tmem_ld16(lane_addr + c0, v);
-        tmem_wait_ld();
-        if (f32out) {
+      for (int sub = 0; sub < 2; ++sub) {
+        const int f0 = it.m0 + (int)rank * 2 * BM + sub * BM + quad * 32;
+        const uint32_t la = lane_addr + (uint32_t)sub * acc2;
+        const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+        for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
+          float v[16];
+          tmem_ld16(la + c0, v);
+          tmem_wait_ld();
+          if (f32out) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
+            for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
+          }
+          store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
         }
-        store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
       }
       release(buf);
     }
@@ -1383,23 +1397,20 @@ int num_sms_tc() {
   return n > 0 ? n : 148;
 }
 
-// Which launches use CTA pairs. By default ("auto") only dense dual launches of at least 32K rows,
-// where pairs measured faster on GB300 than single CTAs (the back GEMM at T=65536: 6.0 -> 5.6-5.9
-// ms). Grouped dual launches measured even at best (GEMM 2 of the 535B layer at T=8192: 1.26 ms
-// both ways) and slower with skewed routing (Zipf, T=16384: 2.19 -> 2.37 ms); SwiGLU items, whose
-// pair CTAs each stack 64 gate and 64 up features, measured slower at every size (their main loop
-// alone: 2.18 -> 2.38 ms at T=8192). MOE_TC_PAIR in the environment selects none ("0"), launches
-// with dual items only ("dual"), launches with SwiGLU items only ("glu") or both ("1"); no launch
+// Which launches use CTA pairs: by default every launch whose items all have two weight tiles
+// (SwiGLU or dual) of bf16 forward problems, where pairs measured faster at every size on GB300
+// (the 535B layer at T=8192: GEMM 1 2.31 -> 2.24 ms, GEMM 2 1.26 -> 1.18 ms, the back GEMM 0.60
+// -> 0.50 ms). MOE_TC_PAIR in the environment selects none ("0"), launches with dual items only
+// ("dual"), launches with SwiGLU items only ("glu") or all of them ("1", the default); no launch
 // uses them once a query finds that no pair fits on the GPU.
-enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3, PAIR_AUTO = 4 };
+enum PairMode { PAIR_NONE = 0, PAIR_ALL = 1, PAIR_DUAL = 2, PAIR_GLU = 3 };
 std::atomic<int> g_pair_mode{-1};
 int pair_mode() {
   int m = g_pair_mode.load(std::memory_order_relaxed);
   if (m < 0) {
     const char* e = getenv("MOE_TC_PAIR");
-    m = PAIR_AUTO;
+    m = PAIR_ALL;
     if (e && !strcmp(e, "0")) m = PAIR_NONE;
-    else if (e && !strcmp(e, "1")) m = PAIR_ALL;
     else if (e && !strcmp(e, "dual")) m = PAIR_DUAL;
     else if (e && !strcmp(e, "glu")) m = PAIR_GLU;
     g_pair_mode.store(m, std::memory_order_relaxed);
@@ -1616,10 +1627,12 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   bool pair = pmode != PAIR_NONE && !P.fp8 && !kc && !bwd && !P.cmb.active;
   for (int j = 0; j < n_probs; ++j) {
     const TcProblem& q = P.p[j];
+    const int Mw = (q.group == GROUP_COLS) ? q.Mg : q.M;
+    // a pair item spans 256 (SwiGLU) or 512 (dual) features, within one weight group
     pair = pair && (is_glu(q.epi) || q.dual) &&
            (q.epi == EPI_SWIGLU || q.epi == EPI_STORE || q.epi == EPI_F32) &&
+           (is_glu(q.epi) ? (Mw % (2 * BM) == 0 && q.M % (2 * BM) == 0) : q.M % (4 * BM) == 0) &&
            !(pmode == PAIR_DUAL && is_glu(q.epi)) && !(pmode == PAIR_GLU && q.dual);
-    if (pmode == PAIR_AUTO) pair = pair && q.dual && q.group != GROUP_ROWS && q.rows >= 32768;
   }
   const dim3 block(64 + 32 * (P.fp8 ? Inst<true, false, false>::EW
                                     : (kc ? Inst<false, true, false>::EW
@@ -1629,6 +1642,19 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   if (pair && n_pairs < 1) {   // no CTA pair fits: this and later launches run without pairs
     pair_disable();
     pair = false;
+  }
+  if (pair) {   // items of the pair width, and the dense problems' item ranges again
+    int64_t pbase = 0;
+    for (int j = 0; j < n_probs; ++j) {
+      TcProblem& q = P.p[j];
+      q.m_tiles = (int)(q.M / (q.dual ? 4 * BM : 2 * BM));
+      q.item_base = pbase;
+      if (q.group != GROUP_ROWS) {
+        q.n_items = q.m_tiles * cdiv(q.rows, q.bn);
+        pbase += q.n_items;
+      }
+    }
+    base = pbase;
   }
   // Dense launches without fp32 k-chunked problems: choose the token tile height so that the
   // items fill whole waves of the persistent grid, by the estimate (waves rounded up) x height.
@@ -1660,18 +1686,16 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     max_bn = max(max_bn, P.p[j].bn);
     if (is_glu(P.p[j].epi) || P.p[j].dual) max_two_a_bn = max(max_two_a_bn, P.p[j].bn);
   }
-  // a pair CTA's accumulator is one buffer of the item's token columns: always two buffers
-  P.nacc = (max_two_a_bn > 128 && !pair) ? 1 : 2;
+  P.nacc = (max_two_a_bn > 128) ? 1 : 2;
   P.acc2_off = (max_two_a_bn > 128) ? BN : 128;
   // token rows of a stage's B slot (a pair CTA loads half of the 16-rounded tile), whole boxes
   const int64_t b_rows = pair ? cdiv(max_bn, 16) * 8 : max_bn;
   P.b_bytes = (int)cdiv(b_rows, B_BOX_ROWS) * B_BOX_BYTES;
-  const int stage_bytes = ((P.glu && !pair) ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
-  // transpose tiles sized for the widest output of the launch; in a pair SwiGLU launch the up
-  // warps' tiles carry a 16 x 32 fp32 chunk to the gate warps
+  const int stage_bytes = (P.glu ? 2 * A_BYTES : A_BYTES) + P.b_bytes;
+  // transpose tiles sized for the widest output of the launch
   P.epi_tile = 16 * 32 * 2;
   for (int j = 0; j < n_probs; ++j)
-    if (P.p[j].epi == EPI_F32 || (pair && is_glu(P.p[j].epi))) P.epi_tile = EPI_TILE_MAX;
+    if (P.p[j].epi == EPI_F32) P.epi_tile = EPI_TILE_MAX;
   const int ew = P.fp8 ? Inst<true, false, false>::EW
                        : (kc ? Inst<false, true, false>::EW
                              : (bwd ? Inst<false, false, true>::EW : Inst<false, false, false>::EW));

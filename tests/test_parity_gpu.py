@@ -476,15 +476,17 @@ for name, T in (("small_bf16", 1000), ("l535b_e64_t1368", 1368)):
 """
 
 
-def test_pair_kernels_forced():
-    """Every launch that can run as CTA pairs does (MOE_TC_PAIR=1: the SwiGLU GEMM 1 with its
-    gate/up hand-over, the grouped dual GEMM 2, the dense dual back GEMM), in a child process
+@pytest.mark.parametrize("mode", ["0", "dual", "glu"])
+def test_pair_modes_forced(mode):
+    """The tensor-core launches that run as CTA pairs by default (the SwiGLU GEMM 1 and the shared
+    experts' gate/up, the grouped dual GEMM 2, the dense dual GEMMs) run on single CTAs instead
+    (MOE_TC_PAIR=0), or only the dual ("dual") or SwiGLU ("glu") ones as pairs, in a child process
     because the switch is read once per process; outputs against the oracle, routing exact."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, MOE_TC_PAIR="1")
+    env = dict(os.environ, MOE_TC_PAIR=mode)
     r = subprocess.run([sys.executable, "-c", _PAIR_CHILD, root], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
