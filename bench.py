@@ -33,11 +33,21 @@ STAGES = ["prep", "front_gemm", "router_select", "dispatch", "expert_gemm1", "ex
           "combine", "back_gemm"]
 def launches_per_forward(shape, simt: bool) -> int:
     """This library's kernel launches in one moe_forward: the device-report reset, router
-    preparation (2), the front GEMMs (one tensor-core launch, or one CUDA-core launch per
-    problem), the router (3), dispatch (3), the expert GEMMs (2), then the combine and the
-    back GEMM (one launch when the combine runs inside the tensor-core back GEMM)."""
+    preparation (2), the front GEMMs (one tensor-core launch; two from 0.5 TFLOP of front GEMMs
+    up, when the down-projection and shared experts run as CTA pairs beside the router's launch;
+    or one CUDA-core launch per problem), the router (3), dispatch (3), the expert GEMMs (2), then
+    the combine and the back GEMM (one launch when the combine runs inside the tensor-core back
+    GEMM)."""
     tc = shape.dtype == "bf16" and not simt
-    front = 1 if tc else 2 + (1 if shape.n_shared > 0 else 0)
+    pairs = os.environ.get("MOE_TC_PAIR", "1") in ("1", "dual") if shape.n_shared == 0 else \
+        os.environ.get("MOE_TC_PAIR", "1") == "1"
+    env_split = os.environ.get("MOE_FRONT_SPLIT")
+    front_flops = 2.0 * shape.T * shape.d_model * (shape.n_experts + shape.d_latent
+                                                    + 2 * shape.n_shared * shape.d_ff_shared)
+    split = (tc and pairs and (front_flops >= 0.5e12 if env_split is None else env_split != "0")
+             and shape.d_latent % 512 == 0
+             and (shape.n_shared == 0 or shape.d_ff_shared % 256 == 0))
+    front = (2 if split else 1) if tc else 2 + (1 if shape.n_shared > 0 else 0)
     env = os.environ.get("MOE_FUSED_COMBINE")
     rows_bytes = shape.T * shape.top_k * shape.d_latent * 2
     fused = tc and shape.n_shared > 0 and (rows_bytes <= (96 << 20) if env is None else env != "0")

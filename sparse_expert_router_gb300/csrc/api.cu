@@ -37,6 +37,23 @@ size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 // Token tiles of the back GEMM (at least 128 rows each) whose combined rows a fused combine counts.
 int64_t ready_tiles(int64_t T) { return (T + 127) / 128; }
 
+// Whether the forward's front GEMMs split into a router launch (single-CTA, K-chunked) and a
+// CTA-pair launch of the down-projection and shared experts. The pair kernel reads each token tile
+// once for two weight tiles, which pays once the front GEMMs are large: the 535B layer's took
+// 0.998 -> 0.977 ms at T=8192 (1.6 TFLOP) and 9.80 -> 8.57 ms at T=65536, while on the small bf16
+// layer (T=4096, d=2048: 0.16 TFLOP) the router launch running alone cost more than the pairs
+// saved (0.121 -> 0.127 ms). So the split is taken from 0.5 TFLOP of front GEMMs up;
+// MOE_FRONT_SPLIT in the environment forces it on ("1") or off ("0").
+bool front_split_enabled(const moe_config_t& c) {
+  static const int mode = [] {
+    const char* e = getenv("MOE_FRONT_SPLIT");
+    return !e ? -1 : (e[0] == '0' ? 0 : 1);
+  }();
+  if (mode >= 0) return mode == 1;
+  const double cols = (double)c.n_experts + c.d_latent + 2.0 * c.n_shared * c.d_ff_shared;
+  return 2.0 * c.T * (double)c.d_model * cols >= 0.5e12;
+}
+
 // Whether the combine runs inside the back GEMM's launch (the shared experts' K segment first,
 // while the launch's epilogue warps combine). There the combine is latency-bound: twelve warps per
 // SM gather y_perm. It pays only while y_perm, just written by expert GEMM 2, is still in L2 (the
@@ -1137,7 +1154,14 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w, const 
                             fuse ? (int)ready_tiles(cfg->T) : 0));
   MOE_TRY_CUDA(router_prepare(ra, cfg->dtype, k.st, k.pdl));
   record(aux, 1, k.st);
-  MOE_TRY_CUDA(run_gemms(k, front, n_front));
+  // The router's k-chunked fp32 problem runs on single CTAs. When the down-projection and the
+  // shared experts can run as CTA pairs, they get a launch of their own.
+  if (k.tc && front_split_enabled(*cfg) && gemm_tc_pairs(front + 1, n_front - 1)) {
+    MOE_TRY_CUDA(run_gemms(k, front, 1));
+    MOE_TRY_CUDA(run_gemms(k, front + 1, n_front - 1));
+  } else {
+    MOE_TRY_CUDA(run_gemms(k, front, n_front));
+  }
   record(aux, 2, k.st);
   MOE_TRY_CUDA(router_select(ra, cfg->dtype, num_sms(), k.st, k.pdl));
   record(aux, 3, k.st);

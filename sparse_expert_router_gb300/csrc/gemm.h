@@ -95,6 +95,8 @@ cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl);
 cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cudaStream_t stream,
                     bool pdl);
 bool gemm_tc_supported(const GemmProblem& p);
+// Whether gemm_tc would run these problems, launched together, as CTA pairs.
+bool gemm_tc_pairs(const GemmProblem* probs, int n_probs);
 
 // Self-test of the kernels' bounded mbarrier wait (a barrier nothing arrives at).
 cudaError_t bounded_wait_selftest(void* dev_header, uint64_t limit_ns, cudaStream_t stream);

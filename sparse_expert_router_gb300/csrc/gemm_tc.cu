@@ -1513,6 +1513,24 @@ bool gemm_tc_supported(const GemmProblem& p) {
   return true;
 }
 
+bool gemm_tc_pairs(const GemmProblem* probs, int n_probs) {
+  const int pmode = pair_mode();
+  if (pmode == PAIR_NONE || n_probs < 1 || n_probs > MAX_PROBS) return false;
+  for (int j = 0; j < n_probs; ++j) {
+    const GemmProblem& g = probs[j];
+    if (!gemm_tc_supported(g) || g.w_fp8 || g.kchunk || g.a_kmajor || g.cmb_seg >= 0) return false;
+    const int Mw = (g.group == GROUP_COLS) ? g.Mg : g.M;
+    if (is_glu(g.epi)) {
+      if (g.epi != EPI_SWIGLU || Mw % (2 * BM) || g.M % (2 * BM) || pmode == PAIR_DUAL) return false;
+    } else {   // a dual item, as gemm_tc forms them
+      if (g.group == GROUP_COLS || (g.epi != EPI_STORE && g.epi != EPI_F32) ||
+          g.M % (4 * BM) || pmode == PAIR_GLU)
+        return false;
+    }
+  }
+  return true;
+}
+
 cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cudaStream_t stream,
                     bool pdl) {
   if (n_probs < 1 || n_probs > MAX_PROBS) return cudaErrorInvalidValue;

@@ -476,19 +476,22 @@ for name, T in (("small_bf16", 1000), ("l535b_e64_t1368", 1368)):
 """
 
 
-@pytest.mark.parametrize("mode", ["0", "dual", "glu"])
-def test_pair_modes_forced(mode):
+@pytest.mark.parametrize("env", [{"MOE_TC_PAIR": "0"}, {"MOE_TC_PAIR": "dual"},
+                                 {"MOE_TC_PAIR": "glu"}, {"MOE_FRONT_SPLIT": "1"}],
+                         ids=["single", "dual", "glu", "front_split"])
+def test_pair_modes_forced(env):
     """The tensor-core launches that run as CTA pairs by default (the SwiGLU GEMM 1 and the shared
     experts' gate/up, the grouped dual GEMM 2, the dense dual GEMMs) run on single CTAs instead
-    (MOE_TC_PAIR=0), or only the dual ("dual") or SwiGLU ("glu") ones as pairs, in a child process
-    because the switch is read once per process; outputs against the oracle, routing exact."""
+    (MOE_TC_PAIR=0), or only the dual ("dual") or SwiGLU ("glu") ones as pairs; or the front GEMMs
+    split into the router's launch and a pair launch on layers below the 0.5 TFLOP of front GEMMs
+    where that starts by default (MOE_FRONT_SPLIT=1). Each runs in a child process because the
+    switches are read once per process; outputs against the oracle, routing exact."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, MOE_TC_PAIR=mode)
-    r = subprocess.run([sys.executable, "-c", _PAIR_CHILD, root], env=env, cwd=root,
-                       capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "-c", _PAIR_CHILD, root], env=dict(os.environ, **env),
+                       cwd=root, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.count(" ok ") == 2, r.stdout
 
