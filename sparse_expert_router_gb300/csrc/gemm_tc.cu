@@ -54,7 +54,8 @@ using namespace tc;
 constexpr int PAIR_SMEM_BUDGET = 225 * 1024;
 constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
-constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem
+constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem beside others
+constexpr int BN_CHUNKED_MAX = 192;   // ... and at most, in a launch of k-chunked problems only
 constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
 constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte row of E4M3)
 #ifndef MOE_TC_EPI_WARPS
@@ -643,12 +644,14 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
       const TcProblem& q = P.p[it.p];
       if (KC && q.kchunk) {
         // k-chunked fp32 problem: sum the chunk accumulators in registers, in chunk order.
-        // This warp owns columns half*16 + 32*i (i < 4) of the <= 128-token tile.
+        // This warp owns columns half*16 + 32*i (i < KCW) of the <= BN_CHUNKED_MAX-token tile.
+        constexpr int KCW = BN_CHUNKED_MAX / 32;
+        static_assert(!KC || EPI_WARPS == 8, "k-chunked epilogue layout");
         int kb_total = q.seg[0].kblocks;
         const int f0 = it.m0 + quad * 32;
-        float acc[4][16];
+        float acc[KCW][16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < KCW; ++i)
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
         bool ok = true;
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
           tc_fence_after();
           const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < KCW; ++i) {
             const int c0 = half * 16 + 32 * i;
             if (c0 < it.nrows) {
               float v[16];
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
         if (!ok) break;
         const float bias = (q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < KCW; ++i) {
           const int c0 = half * 16 + 32 * i;
           if (c0 < it.nrows) {
             float v[16];
@@ -1684,6 +1687,31 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     int64_t best_cost = -1;
     // heights in whole 32-row TMA boxes: the B slot of a stage holds max_bn rows
     for (int bn = BN; bn >= 160; bn -= B_BOX_ROWS) {
+      int64_t items = 0;
+      for (int j = 0; j < n_probs; ++j) items += (int64_t)P.p[j].m_tiles * cdiv(P.p[j].rows, bn);
+      const int64_t cost = cdiv(items, sms) * bn;
+      if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_bn = bn; }
+    }
+    base = 0;
+    for (int j = 0; j < n_probs; ++j) {
+      TcProblem& q = P.p[j];
+      q.bn = best_bn;
+      q.item_base = base;
+      q.n_items = q.m_tiles * cdiv(q.rows, q.bn);
+      base += q.n_items;
+    }
+  }
+  // A launch of k-chunked problems only (the router's logits): the token tile height that
+  // fills whole waves, by the same estimate, from 128 to BN_CHUNKED_MAX rows. The router of the
+  // 535B layer at T=8192 has 3 x 64 items of 128 rows (1.26 waves on 152 SMs), or 3 x 43 of 192
+  // (one wave), each item reading its whole K of both operands.
+  bool kc_only = kc;
+  for (int j = 0; j < n_probs; ++j) kc_only = kc_only && P.p[j].kchunk > 0;
+  if (kc_only) {
+    const int64_t sms = num_sms_tc();
+    int best_bn = BN_CHUNKED;
+    int64_t best_cost = -1;
+    for (int bn = BN_CHUNKED; bn <= BN_CHUNKED_MAX; bn += B_BOX_ROWS) {
       int64_t items = 0;
       for (int j = 0; j < n_probs; ++j) items += (int64_t)P.p[j].m_tiles * cdiv(P.p[j].rows, bn);
       const int64_t cost = cdiv(items, sms) * bn;
