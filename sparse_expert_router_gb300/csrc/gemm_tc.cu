@@ -56,6 +56,7 @@ constexpr int BM = 128;        // features per tile (MMA M, tensor-memory lanes)
 constexpr int BN = MOE_TC_BN;  // max token rows per tile (MMA N)
 constexpr int BN_CHUNKED = 128;   // token rows per tile of a k-chunked problem beside others
 constexpr int BN_CHUNKED_MAX = 192;   // ... and at most, in a launch of k-chunked problems only
+constexpr int64_t DENSE_BAND_BYTES = (int64_t)32 << 20;   // activation rows per band of dense tiles
 constexpr int BK = 64;         // k per stage (one 128-byte swizzle row of bf16)
 constexpr int BK8 = 128;       // k per stage of an fp8 problem (one 128-byte row of E4M3)
 #ifndef MOE_TC_EPI_WARPS
@@ -96,6 +97,7 @@ struct TcProblem {
   int dual;                    // item = 256 features as two 128-feature tiles sharing the token tile
   int kchunk;                  // k-blocks per accumulation chunk (0 = whole K)
   int bn;                      // token rows per tile
+  int band;                    // dense problems: token tiles per band (0: all of them)
   const float* w_scale;        // fp8: per-feature weight scales [G, M] of w (and of w3)
   const float* w3_scale;
   const float* act_scale;      // fp8: quantization multiplier of the activations ([1])
@@ -185,6 +187,20 @@ struct Sched {
   int32_t* gitem;   // [G + 1]
 };
 
+// Token and feature tile of item `local` of a dense problem. Token tiles vary fastest within
+// bands of q.band of them, the bands one after another: the items in flight on the persistent
+// grid share the band's activation rows in L2 while every weight tile passes over them.
+__device__ __forceinline__ void dense_tile(const TcProblem& q, int64_t local, int64_t n_tiles,
+                                           int& n_t, int& m_t) {
+  const int64_t band = (q.band > 0 && q.band < n_tiles) ? q.band : n_tiles;
+  const int64_t per_band = band * q.m_tiles;
+  const int64_t b = local / per_band;
+  const int64_t within = local - b * per_band;
+  const int64_t bt = imin64(band, n_tiles - b * band);   // token tiles of this band
+  n_t = (int)(b * band + within % bt);
+  m_t = (int)(within / bt);
+}
+
 __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_t w) {
   Item it;
   int p = 0;
@@ -209,7 +225,7 @@ __device__ __forceinline__ Item decode(const TcParams& P, const Sched& S, int64_
   } else {
     int64_t n_tiles = cdiv(q.rows, q.bn);
     int n_t, m_t;
-    if (q.n_fastest) { n_t = (int)(local % n_tiles); m_t = (int)(local / n_tiles); }
+    if (q.n_fastest) dense_tile(q, local, n_tiles, n_t, m_t);
     else { n_t = (int)(local / q.m_tiles); m_t = (int)(local % q.m_tiles); }
     it.m0 = m_t * BM * (q.dual ? 2 : 1);
     if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
@@ -951,7 +967,8 @@ __device__ __forceinline__ Item pair_decode(const TcParams& P, const Sched& S, i
     it.nrows = (int)imin64(q.bn, (int64_t)S.ghi[g] - it.row0);
   } else {
     const int64_t n_tiles = cdiv(q.rows, q.bn);
-    const int n_t = (int)(local % n_tiles), m_t = (int)(local / n_tiles);   // token tiles fastest
+    int n_t, m_t;
+    dense_tile(q, local, n_tiles, n_t, m_t);
     it.m0 = m_t * pw;
     if (q.group == GROUP_COLS) { it.wg = it.m0 / q.Mg; it.m_w = it.m0 % q.Mg; }
     else { it.wg = 0; it.m_w = it.m0; }
@@ -1725,6 +1742,17 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
       q.n_items = q.m_tiles * cdiv(q.rows, q.bn);
       base += q.n_items;
     }
+  }
+  // Dense problems walk their token tiles in bands of about DENSE_BAND_BYTES of activation rows
+  // (all K segments), which stay in L2 while the band's weight tiles stream past them.
+  for (int j = 0; j < n_probs; ++j) {
+    TcProblem& q = P.p[j];
+    q.band = 0;
+    if (q.group == GROUP_ROWS || q.kchunk || !q.n_fastest) continue;
+    int64_t row_bytes = 0;
+    for (int s = 0; s < q.n_seg; ++s)
+      row_bytes += (int64_t)q.seg[s].kblocks * (P.fp8 ? BK8 : 2 * BK);
+    q.band = (int)imax64(1, DENSE_BAND_BYTES / ((int64_t)q.bn * row_bytes));
   }
   if (P.cmb.active) P.cmb.bn = P.p[0].bn;
   int max_bn = 0, max_two_a_bn = 0;
