@@ -745,7 +745,8 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if shape.expert_dtype == "bf16" else "bf16; expert MLP e4m3 (f32 accumulate)",
+        "dtype": ("f32" if shape.dtype == "f32" else
+                  "bf16" if shape.expert_dtype == "bf16" else "bf16; expert MLP e4m3 (f32 accumulate)"),
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, near-uniform "
                 "routing unless the workload is Zipf-skewed)",
         "config": forward_config(shape, args, world),

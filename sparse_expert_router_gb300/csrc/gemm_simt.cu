@@ -1,7 +1,8 @@
 // CUDA-core GEMM for the fp32 configuration and as the bf16 cross-check path.
 //
 // 64 x 64 output tile per 256-thread block, 4 x 4 outputs per thread, k staged 16 at a time
-// through shared memory. Every output is accumulated sequentially over k with fused
+// through shared memory, the next step's tile loaded into registers while the current one is
+// multiplied. Every output is accumulated sequentially over k with fused
 // multiply-adds, so its rounding error is bounded by gamma_K * sum_k |a_k w_k| (the router's
 // certified top-k relies on this bound).
 #include "common.cuh"
@@ -59,42 +60,68 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
   const int tx = tid % 16, ty = tid / 16;   // thread owns rows ty*4.., cols tx*4..
   float acc[4][4] = {}, acc3[4][4] = {};
 
-  for (int si = 0; si < p.n_seg; ++si) {
-    const GemmSeg& s = p.seg[si];
-    const T* act = static_cast<const T*>(s.act);
-    for (int k0 = 0; k0 < s.K; k0 += BK) {
-      // stage A: 64 rows x 16 k (4 elements per thread)
-      for (int i = tid; i < BM * BK; i += NT) {
-        int rr = i / BK, kk = i % BK;
-        int r = r0 + rr, k = k0 + kk;
-        sA[kk][rr] = (r < r1 && k < s.K) ? ld_f(act, (int64_t)r * s.K + k) : 0.0f;
-      }
-      // stage W (and W3): 16 k x 64 columns
-      for (int i = tid; i < BK * BN; i += NT) {
-        int kk = i / BN, cc = i % BN;
-        int k = k0 + kk, c = c0 + cc;
-        bool ok = (k < s.K && c < p.M);
-        sW[kk][cc] = ok ? ld_f(weight_ptr<T>(p, s, s.w, g, k, c), 0) : 0.0f;
-        if (glu) sW3[kk][cc] = ok ? ld_f(weight_ptr<T>(p, s, s.w3, g, k, c), 0) : 0.0f;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int kk = 0; kk < BK; ++kk) {
-        float a[4], w[4], w3[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = sA[kk][ty * 4 + i];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) { w[j] = sW[kk][tx * 4 + j]; w3[j] = glu ? sW3[kk][tx * 4 + j] : 0.0f; }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
-            if (glu) acc3[i][j] = fmaf(a[i], w3[j], acc3[i][j]);
-          }
-      }
-      __syncthreads();
+  // The k steps of all segments in order. Each step's tile is loaded into registers one step
+  // ahead (all of a thread's loads issued together, then stored to shared memory), so the loads
+  // of step s+1 are in flight while step s is multiplied; the accumulation order over k is that
+  // of the segments' k.
+  constexpr int A_PER = BM * BK / NT, W_PER = BK * BN / NT;
+  int n_steps = 0;
+  for (int si = 0; si < p.n_seg; ++si) n_steps += (p.seg[si].K + BK - 1) / BK;
+  float ra[A_PER], rw[W_PER], rw3[W_PER];
+  auto load_step = [&](int step) {
+    int si = 0, k0 = step * BK;   // segment si, k offset k0 within it
+    while (k0 >= ((p.seg[si].K + BK - 1) / BK) * BK) {
+      k0 -= ((p.seg[si].K + BK - 1) / BK) * BK;
+      ++si;
     }
+    const GemmSeg& sg = p.seg[si];
+    const T* act = static_cast<const T*>(sg.act);
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+      const int idx = tid + i * NT, rr = idx / BK, kk = idx % BK;
+      const int r = r0 + rr, k = k0 + kk;
+      ra[i] = (r < r1 && k < sg.K) ? ld_f(act, (int64_t)r * sg.K + k) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < W_PER; ++i) {
+      const int idx = tid + i * NT, kk = idx / BN, cc = idx % BN;
+      const int k = k0 + kk, c = c0 + cc;
+      const bool ok = (k < sg.K && c < p.M);
+      rw[i] = ok ? ld_f(weight_ptr<T>(p, sg, sg.w, g, k, c), 0) : 0.0f;
+      rw3[i] = (ok && glu) ? ld_f(weight_ptr<T>(p, sg, sg.w3, g, k, c), 0) : 0.0f;
+    }
+  };
+  if (n_steps > 0) load_step(0);
+  for (int step = 0; step < n_steps; ++step) {
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+      const int idx = tid + i * NT;
+      sA[idx % BK][idx / BK] = ra[i];
+    }
+#pragma unroll
+    for (int i = 0; i < W_PER; ++i) {
+      const int idx = tid + i * NT;
+      sW[idx / BN][idx % BN] = rw[i];
+      sW3[idx / BN][idx % BN] = rw3[i];
+    }
+    __syncthreads();
+    if (step + 1 < n_steps) load_step(step + 1);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], w[4], w3[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = sA[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { w[j] = sW[kk][tx * 4 + j]; w3[j] = glu ? sW3[kk][tx * 4 + j] : 0.0f; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+          if (glu) acc3[i][j] = fmaf(a[i], w3[j], acc3[i][j]);
+        }
+    }
+    __syncthreads();
   }
 
 #pragma unroll
