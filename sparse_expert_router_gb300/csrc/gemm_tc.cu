@@ -978,6 +978,10 @@ __device__ __forceinline__ Item pair_decode(const TcParams& P, const Sched& S, i
   return it;
 }
 
+// FP8: E4M3 weights and activations (kind::f8f6f4), a stage carrying 128 k in the same bytes;
+// the epilogue applies the activation and per-feature weight scales and, for a SwiGLU GEMM,
+// writes an E4M3 hidden and keeps its running max |value|.
+template <bool FP8>
 __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams P) {
   constexpr int EPI_WARPS = MOE_TC_EPI_WARPS;
@@ -1112,14 +1116,20 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
         const TcSeg& sg = q.seg[s];
         const CUtensorMap* m3 = gl ? &sg.a3 : &sg.a1;
         for (int kb = 0; kb < sg.kblocks; ++kb) {
-          const int k0 = kb * BK;
+          const int k0 = kb * (FP8 ? BK8 : BK);
           if (!mbar_wait(empty(stage), phase ^ 1u, &s_abort, P.hdr, 1)) { ok = false; break; }
           const uint32_t fb = mapa_shared(full(stage), 0);
           if (rank == 0) mbar_expect_tx(full(stage), bytes);
-          tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx1, k0, it.wg);
-          tma_load_3d_pair(smem_u32(sA1(stage)) + A_HALF, &sg.a1, fb, mx1 + 64, k0, it.wg);
-          tma_load_3d_pair(smem_u32(sA3(stage)), m3, fb, mx3, k0, it.wg);
-          tma_load_3d_pair(smem_u32(sA3(stage)) + A_HALF, m3, fb, mx3 + 64, k0, it.wg);
+          if constexpr (FP8) {
+            // one [128 k][128 features] box of E4M3 per weight tile
+            tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx1, k0, it.wg);
+            tma_load_3d_pair(smem_u32(sA3(stage)), m3, fb, mx3, k0, it.wg);
+          } else {
+            tma_load_3d_pair(smem_u32(sA1(stage)), &sg.a1, fb, mx1, k0, it.wg);
+            tma_load_3d_pair(smem_u32(sA1(stage)) + A_HALF, &sg.a1, fb, mx1 + 64, k0, it.wg);
+            tma_load_3d_pair(smem_u32(sA3(stage)), m3, fb, mx3, k0, it.wg);
+            tma_load_3d_pair(smem_u32(sA3(stage)) + A_HALF, m3, fb, mx3 + 64, k0, it.wg);
+          }
           for (int b = 0; b < nb; ++b)
             tma_load_2d_pair(smem_u32(sB(stage)) + b * B_BOX_BYTES, &sg.b, fb, k0,
                              (int)(my_row0 + b * B_BOX_ROWS));
@@ -1137,7 +1147,7 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
       Item it = pair_decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int n = ((it.nrows + 15) / 16) * 16;
-      const uint32_t idesc = make_idesc(n, false, false, 2 * BM);
+      const uint32_t idesc = make_idesc(n, FP8, false, 2 * BM);
       int kb_total = 0;
       for (int s2 = 0; s2 < q.n_seg; ++s2) kb_total += q.seg[s2].kblocks;
       const int buf = ev % nacc;
@@ -1152,15 +1162,28 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
         tc_fence_after();
         const uint32_t a1 = smem_u32(sA1(stage)), a3 = smem_u32(sA3(stage)),
                        b = smem_u32(sB(stage));
-        // MN-major A (LBO: the two 64-feature atoms, SBO: 8-row k groups), K-major B
+        // MN-major A (LBO: the two 64-feature atoms of bf16, SBO: 8-row k groups), K-major B;
+        // every MMA consumes 32 bytes of each 128-byte row: 16 k of bf16 or 32 k of E4M3
+        if constexpr (FP8) {
 #pragma unroll
-        for (int k16 = 0; k16 < BK / 16; ++k16) {
-          const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
-          mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd, idesc,
-                        accumulate);
-          mma_bf16_pair(d_tmem + acc2, smem_desc(a3 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd,
-                        idesc, accumulate);
-          accumulate = 1;
+          for (int k32 = 0; k32 < BK8 / 32; ++k32) {
+            const uint64_t bd = smem_desc(b + k32 * 32, 16, 1024);
+            mma_e4m3_pair(d_tmem, smem_desc(a1 + k32 * 4096u, (uint32_t)A_HALF, 1024u), bd,
+                          idesc, accumulate);
+            mma_e4m3_pair(d_tmem + acc2, smem_desc(a3 + k32 * 4096u, (uint32_t)A_HALF, 1024u),
+                          bd, idesc, accumulate);
+            accumulate = 1;
+          }
+        } else {
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t bd = smem_desc(b + k16 * 32, 16, 1024);
+            mma_bf16_pair(d_tmem, smem_desc(a1 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd,
+                          idesc, accumulate);
+            mma_bf16_pair(d_tmem + acc2, smem_desc(a3 + k16 * 2048u, (uint32_t)A_HALF, 1024u), bd,
+                          idesc, accumulate);
+            accumulate = 1;
+          }
         }
         mma_commit_pair(empty(stage), 3);         // frees the stage in both CTAs
         if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -1178,6 +1201,18 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
     unsigned char* stg = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
     float* stg_f = reinterpret_cast<float*>(stg);
     bf16* stg_h = reinterpret_cast<bf16*>(stg);
+    // 16 token rows x 32 E4M3 codes of the transpose tile (byte j * 32 + lane = token j,
+    // feature lane): lane -> (row lane / 2, 16-byte half lane % 2)
+    auto store_e4m3_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
+                               int M) {
+      const int rows_here = min(16, it.nrows - c0);
+      const int row = lane >> 1, part = lane & 1;
+      if (f0 + part * 16 < M && row < rows_here) {
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 32 + part * 16);
+        const int64_t o = (it.row0 + c0 + row) * ld + col0 + f0 + part * 16;
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + o) = val;
+      }
+    };
     auto store_bf16_tile = [&](void* out, int64_t ld, int col0, const Item& it, int c0, int f0,
                                int M) {
       const int rows_here = min(16, it.nrows - c0);
@@ -1228,15 +1263,80 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
       mbar_arrive_cluster(mapa_shared(tmem_empty(b), 0));
     };
     int ev = 0;
+    float amax = 0.0f;                                   // fp8 hidden: this thread's max |value|
     for (int64_t w = unit; w < total; w += n_units) {
       Item it = pair_decode(P, S, w);
       const TcProblem& q = P.p[it.p];
       const int buf = ev % nacc;
       const uint32_t acc_phase = (uint32_t)(ev / nacc) & 1u;
       ++ev;
+      // fp8: dequantization factor of each accumulator of this CTA's features, fp32(1 /
+      // activation scale) times the feature's weight scale in this expert (w, and w3 for the up
+      // projection), loaded before the wait for the accumulator
+      float sc1s[2] = {1.0f, 1.0f}, sc3s[2] = {1.0f, 1.0f}, osc = 1.0f;
+      if constexpr (FP8) {
+        const float da = __fdiv_rn(1.0f, *q.act_scale);
+        const bool gl = is_glu(q.epi);
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int f = (gl ? it.m0 + (int)rank * BM : it.m0 + (int)rank * 2 * BM + sub * BM) +
+                        quad * 32 + lane;
+          const bool fok = (sub == 0 || !gl) && f < q.M;
+          const int64_t fs = (int64_t)it.wg * q.M + f;
+          sc1s[sub] = fok ? __fmul_rn(da, q.w_scale[fs]) : 0.0f;
+          sc3s[sub] = (fok && q.w3_scale) ? __fmul_rn(da, q.w3_scale[fs]) : 0.0f;
+        }
+        if (q.out_fp8) osc = *q.out_scale;
+      }
       if (!mbar_wait(tmem_full(buf), acc_phase, &s_abort, P.hdr, 4)) break;
       tc_fence_after();
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+      if constexpr (FP8) {
+        if (is_glu(q.epi)) {
+          // E4M3 hidden of this CTA's 128 features: the SwiGLU of every chunk of this warp is
+          // packed into registers, the accumulators released, then the codes written out
+          constexpr int CPW = (BN / 16 + EPI_WARPS / 4 - 1) / (EPI_WARPS / 4);   // chunks per warp
+          const int f0 = it.m0 + (int)rank * BM + quad * 32;
+          const bool fok = f0 + lane < q.M;
+          const float sc1 = sc1s[0], sc3 = sc3s[0];
+          uint32_t pk[CPW][4];
+#pragma unroll
+          for (int i = 0; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+              float v[16], v3[16];
+              tmem_ld16(lane_addr + c0, v);
+              tmem_ld16(lane_addr + acc2 + c0, v3);
+              tmem_wait_ld();
+              const int valid = min(16, it.nrows - c0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float h = swiglu(__fmul_rn(v[j], sc1), __fmul_rn(v3[j], sc3));
+                if (fok && j < valid) amax = fmaxf(amax, fabsf(h));
+                v[j] = __fmul_rn(h, osc);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; j += 4)
+                pk[i][j / 4] = e4m3x2(v[j + 1], v[j]) | (e4m3x2(v[j + 3], v[j + 2]) << 16);
+            }
+          }
+          release(buf);
+          uint8_t* stg_b = reinterpret_cast<uint8_t*>(stg);
+#pragma unroll
+          for (int i = 0; i < CPW; ++i) {
+            const int c0 = half * 16 + i * 16 * (EPI_WARPS / 4);
+            if (c0 < it.nrows) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                stg_b[j * 32 + lane] = (uint8_t)((pk[i][j / 4] >> (8 * (j % 4))) & 0xFFu);
+              __syncwarp();
+              store_e4m3_tile(q.out, q.ld_out, q.out_col0, it, c0, f0, q.M);
+              __syncwarp();
+            }
+          }
+          continue;
+        }
+      }
       if (is_glu(q.epi)) {
         // bf16 hidden of this CTA's 128 features: the SwiGLU of a warp's first CPR chunks is
         // packed into registers before the accumulators are released; chunks past those (tiles
@@ -1297,6 +1397,7 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
         const int f0 = it.m0 + (int)rank * 2 * BM + sub * BM + quad * 32;
         const uint32_t la = lane_addr + (uint32_t)sub * acc2;
         const float bias = (f32out && q.bias && f0 + lane < q.M) ? q.bias[f0 + lane] : 0.0f;
+        const float sc = sub ? sc1s[1] : sc1s[0];
         for (int c0 = half * 16; c0 < it.nrows; c0 += 16 * (EPI_WARPS / 4)) {
           float v[16];
           tmem_ld16(la + c0, v);
@@ -1305,10 +1406,19 @@ __global__ void __launch_bounds__(64 + 32 * MOE_TC_EPI_WARPS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], bias);
           }
+          if constexpr (FP8) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], sc);
+          }
           store_rows(q.out, q.ld_out, q.out_col0, f32out ? 0 : 1, it, c0, f0, q.M, v);
         }
       }
       release(buf);
+    }
+    if (FP8 && P.amax) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+      if (lane == 0 && amax > 0.0f) amax_update(P.amax, amax);
     }
   }
 
@@ -1466,11 +1576,12 @@ cudaLaunchConfig_t pair_config(dim3 grid, dim3 block, size_t smem, cudaStream_t 
 // cached per device: the persistent grid of a pair launch.
 int max_pairs(void (*kern)(TcParams), dim3 block) {
   static std::mutex mu;
-  static std::map<int, int> cache;
+  static std::map<std::pair<int, void*>, int> cache;   // (device, kernel instance)
   int dev = 0;
   cudaGetDevice(&dev);
+  const std::pair<int, void*> key(dev, reinterpret_cast<void*>(kern));
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(dev);
+  auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BUDGET) ==
@@ -1480,7 +1591,7 @@ int max_pairs(void (*kern)(TcParams), dim3 block) {
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();   // a failed query leaves no error behind
-  cache[dev] = n;
+  cache[key] = n;
   return n;
 }
 
@@ -1660,12 +1771,14 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
     bwd = bwd || P.p[j].a_kmajor || P.p[j].epi == EPI_SWIGLU_SAVE || P.p[j].epi == EPI_SWIGLU_BWD;
   }
   if (kc && bwd) return cudaErrorNotSupported;
-  // CTA pairs (cta_group::2) for bf16 launches whose every item has two weight tiles
+  // CTA pairs (cta_group::2) for launches whose every item has two weight tiles: bf16, or E4M3
+  // with an E4M3 hidden out of the SwiGLU GEMM and a bf16 output of the dual one
   const int pmode = pair_mode();
-  bool pair = pmode != PAIR_NONE && !P.fp8 && !kc && !bwd && !P.cmb.active;
+  bool pair = pmode != PAIR_NONE && !kc && !bwd && !P.cmb.active;
   for (int j = 0; j < n_probs; ++j) {
     const TcProblem& q = P.p[j];
     const int Mw = (q.group == GROUP_COLS) ? q.Mg : q.M;
+    pair = pair && (P.fp8 ? (is_glu(q.epi) ? q.out_fp8 != 0 : q.out_fp8 == 0) : q.out_fp8 == 0);
     // a pair item spans 256 (SwiGLU) or 512 (dual) features, within one weight group
     pair = pair && (is_glu(q.epi) || q.dual) &&
            (q.epi == EPI_SWIGLU || q.epi == EPI_STORE || q.epi == EPI_F32) &&
@@ -1676,7 +1789,8 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
                                     : (kc ? Inst<false, true, false>::EW
                                           : (bwd ? Inst<false, false, true>::EW
                                                  : Inst<false, false, false>::EW))));
-  const int n_pairs = pair ? max_pairs(tc_gemm_pair_kernel, block) : 0;
+  const int n_pairs =
+      pair ? max_pairs(P.fp8 ? tc_gemm_pair_kernel<true> : tc_gemm_pair_kernel<false>, block) : 0;
   if (pair && n_pairs < 1) {   // no CTA pair fits: this and later launches run without pairs
     pair_disable();
     pair = false;
@@ -1785,7 +1899,7 @@ cudaError_t gemm_tc(const GemmProblem* probs, int n_probs, void* dev_header, cud
   const int G = (P.grouped >= 0) ? P.p[P.grouped].G : 0;
   const size_t smem = (size_t)P.stages * stage_bytes + 1024 +
                       epi_bytes + (size_t)(3 * G + 1) * 4;
-  auto kern = pair ? tc_gemm_pair_kernel
+  auto kern = pair ? (P.fp8 ? tc_gemm_pair_kernel<true> : tc_gemm_pair_kernel<false>)
              : P.cmb.active ? tc_gemm_kernel<false, false, false, true>
              : P.fp8 ? tc_gemm_kernel<true, false, false>
                      : (kc ? tc_gemm_kernel<false, true, false>
