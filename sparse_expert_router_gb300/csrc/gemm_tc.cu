@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(64 + 32 * Inst<FP8, KC, BWD>::EW, 1)
 // and up tiles of its 128), a dual item 512 (each CTA two 128-feature tiles). The token tile is
 // loaded once per pair instead of once per CTA: 46 KB per k-block and SM instead of 60 KB for the
 // same MMAs, where L2-to-SM ingest is what bounds the dense GEMMs.
-// bf16 forward problems only (EPI_SWIGLU, EPI_STORE, EPI_F32); no combine.
+// Forward problems (EPI_SWIGLU, EPI_STORE, EPI_F32), bf16 or E4M3 operands; no combine.
 
 // Item w of a pair launch: SwiGLU items of 256 features, dual items of 512.
 __device__ __forceinline__ Item pair_decode(const TcParams& P, const Sched& S, int64_t w) {

@@ -1104,6 +1104,16 @@ EDGE = {
     "k1_cap_fp8": (LayerShape("k1_cap_fp8", T=333, d_model=256, d_latent=128, n_experts=64,
                               top_k=1, d_ff=128, n_shared=1, d_ff_shared=256, dtype="bf16",
                               capacity=(1, 21), expert_dtype="fp8"), 0),
+    # widths at which the expert GEMMs run as CTA pairs (d_ff a multiple of 256, d_latent of
+    # 512), bf16 and fp8, with one-row and empty groups (T = 1) and ~9-row groups (E = 1024)
+    "t1_pair": (LayerShape("t1_pair", T=1, d_model=512, d_latent=512, n_experts=64, top_k=8,
+                           d_ff=256, n_shared=1, d_ff_shared=256, dtype="bf16"), 0),
+    "t1_pair_fp8": (LayerShape("t1_pair_fp8", T=1, d_model=512, d_latent=512, n_experts=64,
+                               top_k=8, d_ff=256, n_shared=1, d_ff_shared=256, dtype="bf16",
+                               expert_dtype="fp8"), 0),
+    "e1024_pair_fp8": (LayerShape("e1024_pair_fp8", T=300, d_model=512, d_latent=512,
+                                  n_experts=1024, top_k=32, d_ff=256, n_shared=0, d_ff_shared=0,
+                                  dtype="bf16", expert_dtype="fp8"), 0),
 }
 
 
@@ -1112,7 +1122,8 @@ EDGE = {
 def test_edge_case_forward(name, pdl):
     """Every token's routing, dispatch and output against the oracle at the edges the method
     allows: a single token, k = E, k = 1 with capacity 1, 1024 experts with top-32, no shared
-    experts, token counts one past a tile; the fp8 expert path at three of them."""
+    experts, token counts one past a tile; the fp8 expert path at three of them; and the CTA-pair
+    expert GEMMs (bf16 and fp8) with one-row, empty and ~9-row groups."""
     shape, flags = EDGE[name]
     cpu = make_layer_inputs(shape, "cpu")
     inp = {k: v.to(DEV) for k, v in cpu.items()}
