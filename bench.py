@@ -154,6 +154,15 @@ def weight_bytes(shape) -> int:
     return bank + scales + 2 * (d * E + 2 * d * L + 3 * d * SF) + 4 * (E + L)
 
 
+def f32_alu_peak(dev, clk) -> float:
+    """Peak of the CUDA-core fp32 GEMMs (TFLOP/s), derived from unit counts and clock: every SM's
+    128 fp32 lanes issuing one fused multiply-add (2 flops) a clock at the highest SM clock seen
+    (2,070 MHz when none was sampled): ~80.5 TFLOP/s on 152 SMs."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def tc_peak(pk, stage, which="bf16_burst") -> float:
     """Tensor-core peak (TFLOP/s) of a stage: the measured bf16 rate (burst by default: the timed
     loops here last a fraction of a second; "bf16_sustained" for the seconds-long rate under the
@@ -704,6 +713,9 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
     if fused:
         alg["back_gemm"]["bytes"] += alg.pop("combine")["bytes"]
     stages = {}
+    # GEMMs on CUDA cores (the fp32 layer, or --simt) are rated against the fp32 ALU peak
+    cuda_core = shape.dtype == "f32" or args.simt
+    alu_peak = f32_alu_peak(dev, clk) if cuda_core else None
     for s in STAGES:
         ms = stage_ms[s] / args.steps
         st = {"ms": round(ms, 4)}
@@ -716,7 +728,10 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
             tr = profiled_traffic(shape.name, s)
             if tr is not None:
                 st["traffic"] = tr
-            if f:
+            if f and cuda_core:
+                st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 2)
+                st["f32_alu_frac"] = round(st["tflop_s"] / alu_peak, 4)
+            elif f:
                 tp, tps = tc_peak(pk, alg[s]), tc_peak(pk, alg[s], "bf16_sustained")
                 st["tflop_s"] = round(f / (ms * 1e-3) / 1e12, 1)
                 st[alg[s].get("tc_peak", "bf16") + "_frac"] = round(st["tflop_s"] / tp, 3)
@@ -725,9 +740,13 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
     dom = max((s for s in STAGES if s in alg), key=lambda s: stage_ms[s])
     f, by = alg[dom]["flops"], alg[dom]["bytes"]
     ms_dom = stage_ms[dom] / args.steps
-    tp = tc_peak(pk, alg[dom])
+    tp = alu_peak if cuda_core else tc_peak(pk, alg[dom])
     t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), f / (tp * 1e12)
-    if t_hbm >= t_tc:
+    if cuda_core and t_hbm < t_tc:
+        ach = f / (ms_dom * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(ach, 2), "peak": round(tp, 1), "unit": "TFLOP/s",
+                "frac": round(ach / tp, 4)}
+    elif t_hbm >= t_tc:
         ach = by / (ms_dom * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4)}
@@ -737,10 +756,11 @@ def bench_forward(args, shape, m, world, rank, local, dev, e2e_on=None):
                 "unit": "TFLOP/s", "frac": round(ach / tp, 4),
                 "sustained_frac": round(ach / tc_peak(pk, alg[dom], "bf16_sustained"), 4)}
     roof.update({"kernel": dom, "traffic": profiled_traffic(shape.name, dom),
-                 "peak_source": pk["source"]
+                 "peak_source": ("derived: SMs x 128 fp32 lanes x 2 flops x max SM clock"
+                                 if roof["bound"] == "alu" else pk["source"]
                  + ((" (bf16 burst" + (" x 2, the nominal E4M3/bf16 ratio)"
                                        if alg[dom].get("tc_peak") == "fp8" else ")"))
-                    if roof["bound"] == "tensor" else " (HBM copy)")})
+                    if roof["bound"] == "tensor" else " (HBM copy)"))})
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
