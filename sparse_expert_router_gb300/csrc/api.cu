@@ -267,11 +267,7 @@ moe_status_t cuda_status(cudaError_t e) {
 cudaError_t run_gemms(const Call& k, GemmProblem* probs, int n) {
   if (n == 0) return cudaSuccess;
   if (k.tc) return gemm_tc(probs, n, k.hdr(), k.st, k.pdl);
-  for (int i = 0; i < n; ++i) {
-    cudaError_t e = gemm_simt(probs[i], k.st, k.pdl);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return gemm_simt(probs, n, k.st, k.pdl);   // independent problems, one launch per three
 }
 
 moe_status_t check_tc(const Call& k, const GemmProblem* probs, int n) {

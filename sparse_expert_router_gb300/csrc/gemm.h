@@ -87,8 +87,9 @@ struct GemmProblem {
   uint32_t* cmb_ready = nullptr;
 };
 
-// CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output).
-cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl);
+// CUDA-core GEMM (fp32 FMA, sequential accumulation over k for every output). The n problems
+// must be independent; up to three share one launch.
+cudaError_t gemm_simt(const GemmProblem* probs, int n, cudaStream_t stream, bool pdl);
 
 // tcgen05 GEMM (bf16 operands, fp32 accumulation in tensor memory). Up to 3 problems share
 // one persistent launch. Returns cudaErrorNotSupported when a problem does not fit its rules.

@@ -22,8 +22,21 @@ __device__ __forceinline__ const T* weight_ptr(const GemmProblem& p, const GemmS
   return w + (int64_t)k * p.M + c;
 }
 
+// Up to three independent problems per launch (the front GEMMs: router, down-projection,
+// shared gate/up), problem blockIdx.z; blocks past a problem's tiles leave at once.
+constexpr int SIMT_MAX_PROBS = 3;
+struct SimtLaunch {
+  GemmProblem p[SIMT_MAX_PROBS];
+};
+
+__host__ __device__ __forceinline__ int64_t simt_row_tiles(const GemmProblem& p) {
+  return cdiv(p.rows, BM) + (p.group == GROUP_ROWS ? p.G : 0);
+}
+
 template <typename T>
-__global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
+__global__ void __launch_bounds__(NT) simt_gemm_kernel(const __grid_constant__ SimtLaunch L) {
+  const GemmProblem& p = L.p[blockIdx.z];
+  if ((int64_t)blockIdx.x >= simt_row_tiles(p) || (int64_t)blockIdx.y * BN >= p.M) return;
   pdl_wait();
   __shared__ float sA[BK][BM + 4];
   __shared__ float sW[BK][BN];
@@ -149,17 +162,36 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const GemmProblem p) {
 
 }  // namespace
 
-cudaError_t gemm_simt(const GemmProblem& p, cudaStream_t stream, bool pdl) {
-  // fp8, transposed weights and the backward epilogues run on tensor cores only
-  if (p.w_fp8 || p.out_fp8 || p.a_kmajor || p.epi > EPI_SWIGLU) return cudaErrorNotSupported;
-  for (int s = 0; s < p.n_seg; ++s)
-    if (p.seg[s].ld && p.seg[s].ld != p.seg[s].K) return cudaErrorNotSupported;
-  if (p.rows <= 0 || p.M <= 0) return cudaSuccess;
-  int64_t tiles = cdiv(p.rows, BM) + (p.group == GROUP_ROWS ? p.G : 0);
-  dim3 grid((unsigned)tiles, (unsigned)cdiv(p.M, BN));
-  if (p.dtype == DT_BF16)
-    return launch(simt_gemm_kernel<bf16>, grid, dim3(NT), 0, stream, pdl, p);
-  return launch(simt_gemm_kernel<float>, grid, dim3(NT), 0, stream, pdl, p);
+cudaError_t gemm_simt(const GemmProblem* probs, int n, cudaStream_t stream, bool pdl) {
+  SimtLaunch L{};
+  int m = 0;
+  int64_t gx = 0, gy = 0;
+  auto flush = [&]() -> cudaError_t {
+    if (m == 0) return cudaSuccess;
+    const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)m);
+    const bool bf = L.p[0].dtype == DT_BF16;
+    cudaError_t e = bf ? launch(simt_gemm_kernel<bf16>, grid, dim3(NT), 0, stream, pdl, L)
+                       : launch(simt_gemm_kernel<float>, grid, dim3(NT), 0, stream, pdl, L);
+    m = 0;
+    gx = gy = 0;
+    return e;
+  };
+  for (int i = 0; i < n; ++i) {
+    const GemmProblem& p = probs[i];
+    // fp8, transposed weights and the backward epilogues run on tensor cores only
+    if (p.w_fp8 || p.out_fp8 || p.a_kmajor || p.epi > EPI_SWIGLU) return cudaErrorNotSupported;
+    for (int s = 0; s < p.n_seg; ++s)
+      if (p.seg[s].ld && p.seg[s].ld != p.seg[s].K) return cudaErrorNotSupported;
+    if (p.rows <= 0 || p.M <= 0) continue;
+    if (m == SIMT_MAX_PROBS || (m > 0 && p.dtype != L.p[0].dtype)) {
+      cudaError_t e = flush();
+      if (e != cudaSuccess) return e;
+    }
+    L.p[m++] = p;
+    gx = imax64(gx, simt_row_tiles(p));
+    gy = imax64(gy, cdiv(p.M, BN));
+  }
+  return flush();
 }
 
 }  // namespace moe
